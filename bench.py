@@ -1,0 +1,483 @@
+#!/usr/bin/env python3
+"""Benchmark of the NSA selection-attention forward on GB300.
+
+One step = one forward over the whole workload (every (b, m, g) row): one
+launch of the library's kernel. Default workload: B=1, M=N=65536, H=64, G=8,
+D=128, block_size=64, T=16 (block 0, the two most recent causal blocks and
+13 random earlier ones per row), fp16 inputs, seeded synthetic data.
+
+Prints ONE JSON line (rank 0):
+  value         TFLOP/s over the timed steps (4*D FLOPs per query, head and
+                visible gathered key), inputs resident in HBM, L2 flushed
+                between steps (a 512 MiB write outside the timed events);
+  gathered_gbs  gathered K/V bytes per second (whole selected blocks);
+  speedup_vs_dense_causal  time of the same build with every causal block
+                listed (T=1024, same Q/K/V) over the sparse time;
+  roofline      the kernel against max(FLOPs / fp16 tensor peak, gathered
+                bytes / HBM bandwidth) -- the gathered bytes dominate;
+  e2e           the same metric through the C ABI's host-buffer call
+                (host->device inputs, device->host O and LSE every step);
+  cpu_baseline  the CPU oracle timed on a bounded row sample, host cores;
+  clocks        nvidia-smi SM clocks and throttle reasons during the steps.
+
+``--impl reference`` times the CPU oracle instead (the only reference that
+exists for this method), on the same workload, metric and unit.
+
+Under torchrun (N > 1) every rank runs its own workload (seed + rank) on its
+own GPU -- independent problems, weak scaling, no collective on the data
+path; the time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sel-attn fwd TFLOP/s & gathered-KV GB/s (M=64k,T=16,bs=64); x vs dense causal"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="m64k_bs64")
+    ap.add_argument("--dense-steps", type=int, default=3)
+    ap.add_argument("--skip-dense", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=24576,
+                    help="rows of the CPU-oracle sample")
+    ap.add_argument("--seed", type=int, default=None)
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nsa_block_selection_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{workload}_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons (200 ms)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.gpu_id is not None:
+                cmd += ["-i", str(self.gpu_id)]
+            self.proc = subprocess.Popen(cmd, stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r.split(",") for r in self.tmp.read().strip().splitlines() if r.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_smi_id(dev):
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev.index or 0] if vis else (dev.index or 0)
+
+
+def time_steps(fn, steps, warmup, flush, barrier):
+    """Per-step CUDA-event times (ms) of fn() on the current stream; flush()
+    runs before every step outside the events."""
+    import torch
+
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    barrier()
+    st = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    wall0 = time.perf_counter()
+    for s, e in evs:
+        flush()
+        s.record(st)
+        fn()
+        e.record(st)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier()
+    return [s.elapsed_time(e) for s, e in evs], wall
+
+
+def sample_rows(w, n_rows, seed):
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    b = rng.integers(w.B, size=n_rows)
+    m = rng.integers(w.M, size=n_rows)
+    g = rng.integers(w.G, size=n_rows)
+    return b, m, g
+
+
+def cpu_oracle_sample(timer, idx, w, n_rows, seed):
+    """(TFLOP/s, info) of the oracle on a seeded sample of rows."""
+    from nsa_block_selection_gb300.metrics import count_rows
+
+    b, m, g = sample_rows(w, n_rows, seed)
+    rows = [(int(x), int(y), int(z)) for x, y, z in zip(b, m, g)]
+    flops = count_rows(idx[b, m, g], m, w.N, w.block_size, w.heads_per_group, w.D)
+    secs = timer.time_rows(rows)
+    tflops = flops / secs / 1e12
+    return tflops, {
+        "value": tflops, "unit": "TFLOP/s", "cores": timer.workers, "kind": "oracle",
+        "sample": f"{n_rows} seeded random (b,m,g) rows of {w.name} "
+                  f"({flops / 1e9:.2f} GFLOP), fp64 numpy, {timer.workers} spawn workers x "
+                  f"1 BLAS thread, {secs:.2f} s",
+        "host_cpu_count": os.cpu_count(),
+    }
+
+
+# --------------------------------------------------------------------------
+# arms
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from nsa_block_selection_gb300 import inputs as gen
+
+    w = gen.workload(args.workload)
+    seed = args.seed if args.seed is not None else gen.default_seed(w.name)
+    q, k, v, idx = gen.make_inputs(w, seed)
+    from oracle.cpu_baseline import OracleTimer, host_cores
+
+    rows_per_step = 256 * host_cores()
+    vals = []
+    info = None
+    with OracleTimer(q, k, v, idx, w.block_size, w.scale) as timer:
+        for i in range(args.warmup + args.steps):
+            tf, info = cpu_oracle_sample(timer, idx, w, rows_per_step, seed + 7 + i)
+            if i >= args.warmup:
+                vals.append(tf)
+    value = statistics.mean(vals)
+    info["value"] = value
+    rows_total = w.B * w.M * w.G
+    from nsa_block_selection_gb300.metrics import count_work
+    import torch
+
+    work = count_work(torch.from_numpy(idx), w.N, w.block_size, w.heads_per_group, w.D)
+    ms = work["flops"] / (value * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "M": w.M, "N": w.N, "H": w.H, "G": w.G,
+                   "D": w.D, "block_size": w.block_size, "T": w.T,
+                   "rows_per_step": rows_per_step, "rows_total": rows_total,
+                   "note": "ms_per_step extrapolates the sample throughput to the whole "
+                           "workload"},
+        "cpu_baseline": info,
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from nsa_block_selection_gb300 import _lib, inputs as gen, sel_attn_fwd
+    from nsa_block_selection_gb300.metrics import count_work
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+        barrier = dist.barrier
+    else:
+        dist = None
+
+        def barrier():
+            return None
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    w = gen.workload(args.workload)
+    seed = (args.seed if args.seed is not None else gen.default_seed(w.name)) + rank
+    q_np, k_np, v_np, idx_np = gen.make_inputs(w, seed)
+
+    # CPU baseline first (spawned pool, before any timing), rank 0 at N=1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        from oracle.cpu_baseline import OracleTimer
+
+        with OracleTimer(q_np, k_np, v_np, idx_np, w.block_size, w.scale) as timer:
+            _, cpu = cpu_oracle_sample(timer, idx_np, w, args.cpu_rows, seed + 99)
+
+    q = torch.from_numpy(q_np).to(dev)
+    k = torch.from_numpy(k_np).to(dev)
+    v = torch.from_numpy(v_np).to(dev)
+    idx = torch.from_numpy(idx_np).to(dev)
+    out = torch.empty((w.B, w.M, w.H, w.D), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=dev)
+    work = count_work(idx, w.N, w.block_size, w.heads_per_group, w.D)
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    def step():
+        sel_attn_fwd(q, k, v, idx, w.block_size, w.scale, out=out, lse=lse)
+
+    clocks = ClockSampler(gpu_smi_id(dev))
+    clocks.start()
+    times, wall = time_steps(step, args.steps, args.warmup, flush, barrier)
+    clk = clocks.stop()
+    t_ms = statistics.mean(times)
+    if dist is not None:
+        tt = torch.tensor([t_ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+        tot = torch.tensor([work["flops"], work["gathered_bytes"]], dtype=torch.float64)
+        dist.all_reduce(tot)
+        flops_all, bytes_all = float(tot[0]), float(tot[1])
+    else:
+        flops_all, bytes_all = float(work["flops"]), float(work["gathered_bytes"])
+    tflops = flops_all / (t_ms * 1e-3) / 1e12
+    gbs = bytes_all / (t_ms * 1e-3) / 1e9
+
+    # e2e: host buffers through the C ABI each step
+    e2e = None
+    if not args.skip_e2e:
+        e2e = run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist)
+
+    # dense-causal-equivalent run: same Q/K/V, every causal block listed
+    dense = None
+    if rank == 0 and world == 1 and not args.skip_dense:
+        dense = run_dense(w, q, k, v, out, lse, flush, args, t_ms)
+
+    peaks = load_peaks()
+    t_roof = max(work["flops"] / (peaks["bf16_tflops"] * 1e12),
+                 work["gathered_bytes"] / (peaks["hbm_gbs"] * 1e9))
+    per_launch_bytes = work["gathered_bytes"]
+    achieved = per_launch_bytes / (statistics.mean(times) * 1e-3) / 1e9
+    roofline = {
+        "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(w.name),
+        "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+        "t_roofline_ms": t_roof * 1e3,
+        "flop_frac_of_tensor_peak": (work["flops"] / (statistics.mean(times) * 1e-3))
+                                     / (peaks["bf16_tflops"] * 1e12),
+        "note": "achieved = gathered K/V bytes (whole selected blocks) / kernel time; "
+                "blocks are re-read from L2, so it can exceed HBM bandwidth",
+    }
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "M": w.M, "N": w.N, "H": w.H, "G": w.G,
+                   "D": w.D, "block_size": w.block_size, "T": w.T, "seed": seed,
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, "
+                         "outside the timed events)",
+                   "parallelism": f"independent replicas x{world}" if world > 1 else "1 GPU",
+                   "accumulate": "fp32"},
+        "gathered_gbs": gbs,
+        "flops_per_step": work["flops"], "gathered_bytes_per_step": work["gathered_bytes"],
+        "speedup_vs_dense_causal": dense["speedup"] if dense else None,
+        "dense_causal": dense,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": args.steps,
+        "wall_s_timed": wall,
+        "kernel_source_sha": kernel_source_hash(),
+        "device": torch.cuda.get_device_name(dev),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_dense(w, q, k, v, out, lse, flush, args, t_sparse_ms):
+    import torch
+
+    from nsa_block_selection_gb300 import inputs as gen, sel_attn_fwd
+    from nsa_block_selection_gb300.metrics import count_work
+
+    T = -(-w.M // w.block_size)
+    idx_d = gen.dense_causal_indices_torch(w.B, w.M, w.G, T, w.block_size, q.device)
+    work = count_work(idx_d, w.N, w.block_size, w.heads_per_group, w.D)
+
+    def step():
+        sel_attn_fwd(q, k, v, idx_d, w.block_size, w.scale, out=out, lse=lse)
+
+    times, _ = time_steps(step, max(1, args.dense_steps), 1, flush, lambda: None)
+    t = statistics.mean(times)
+    del idx_d
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name} with T={T}: every causal block listed",
+            "ms_per_step": t, "tflops": work["flops"] / (t * 1e-3) / 1e12,
+            "gathered_gbs": work["gathered_bytes"] / (t * 1e-3) / 1e9,
+            "speedup": t / t_sparse_ms, "work_ratio": None, "steps": max(1, args.dense_steps)}
+
+
+def run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist):
+    """Host (pinned) buffers in and out every step: H2D of Q/K/V/indices,
+    the forward, D2H of O and LSE, all inside the timed events."""
+    import torch
+
+    from nsa_block_selection_gb300 import sel_attn_fwd
+
+    hq = torch.from_numpy(q_np).pin_memory()
+    hk = torch.from_numpy(k_np).pin_memory()
+    hv = torch.from_numpy(v_np).pin_memory()
+    hi = torch.from_numpy(idx_np).pin_memory()
+    ho = torch.empty((w.B, w.M, w.H, w.D), dtype=torch.float32).pin_memory()
+    hl = torch.empty((w.B, w.H, w.M), dtype=torch.float32).pin_memory()
+    dq, dk, dv, di = (torch.empty_like(x, device=dev) for x in (hq, hk, hv, hi))
+    do = torch.empty(ho.shape, dtype=torch.float32, device=dev)
+    dl = torch.empty(hl.shape, dtype=torch.float32, device=dev)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        di.copy_(hi, non_blocking=True)
+        sel_attn_fwd(dq, dk, dv, di, w.block_size, w.scale, out=do, lse=dl)
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+
+    steps = max(3, args.steps // 4)
+    times, _ = time_steps(step, steps, 2, lambda: None, barrier)
+    t = statistics.mean(times)
+    if dist is not None:
+        tt = torch.tensor([t], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    flops = work["flops"] * (dist.get_world_size() if dist is not None else 1)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hi))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hl))
+    return {"value": flops / (t * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": t,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "path": "pinned host -> cudaMemcpyAsync -> nsa_sel_attn_fwd -> host"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

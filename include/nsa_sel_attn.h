@@ -1,0 +1,98 @@
+/*
+ * nsa_sel_attn.h -- C ABI of the NSA selection-attention forward library
+ * (libnsa_sel_attn.so, sm_103a).
+ *
+ * The operation is the one stated in "[wave] NSA: selection attention forward
+ * kernel":
+ *   section "Operation"    -- Q [B,M,H,D], K [B,N,G,D], V [B,N,G,D],
+ *                             block_indices [B,M,G,T] in; O_slc [B,M,H,D],
+ *                             LSE_slc [B,H,M] out; T = selected blocks/query;
+ *   section "Algorithm"    -- for query m and each selected block t, the keys
+ *                             [t*block_size, (t+1)*block_size) are gathered,
+ *                             scored against q[m] (QK^T), causally masked and
+ *                             softmaxed; V is accumulated with an online
+ *                             softmax (running max + log-sum-exp); O and LSE
+ *                             are stored;
+ *   section "Requirements" -- the heads of a GQA group share block_indices;
+ *                             online softmax across all T blocks; causal mask
+ *                             inside gathered blocks; FP16 matmuls with FP32
+ *                             accumulation; LSE returned for the backward
+ *                             pass; block_size 64 and 32.
+ *
+ * Conventions where the pages are silent (the library's contract):
+ *   - head h belongs to KV group h / (H/G) (contiguous heads per group);
+ *   - key n is visible to query m iff n <= m and n < N;
+ *   - scores are multiplied by `scale` (pass <= 0 for 1/sqrt(D));
+ *   - block_indices entries < 0 or >= ceil(N/block_size) are padding and may
+ *     sit anywhere in a row; a row must not list a block twice (a top-k
+ *     output never does; a repeated block is counted twice);
+ *   - a row with no visible key yields O = 0 and LSE = -inf;
+ *   - LSE is the natural log of sum(exp(scale * q.k)) over visible keys.
+ *
+ * Every buffer is contiguous row-major in the layout given, owned by the
+ * caller, and not retained after the call returns. Keys/values in rows that
+ * no index selects, and in the causal future of a query, are never read.
+ */
+#ifndef NSA_SEL_ATTN_H
+#define NSA_SEL_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. Values < 0 are errors; nothing was launched when an argument
+ * check fails. */
+typedef enum nsa_status {
+  NSA_OK = 0,
+  NSA_ERR_NULL = -1,        /* a required pointer is NULL                     */
+  NSA_ERR_SHAPE = -2,       /* a size is negative or the sizes are too large */
+  NSA_ERR_BLOCK_SIZE = -3,  /* block_size not in {32, 64}                     */
+  NSA_ERR_HEAD_DIM = -4,    /* D not in {64, 128}                             */
+  NSA_ERR_GROUPS = -5,      /* G <= 0, H % G != 0 or H/G != 8                 */
+  NSA_ERR_ALIGN = -6,       /* Q, K, V or O not 16-byte aligned, LSE or
+                               block_indices not 4-byte aligned               */
+  NSA_ERR_LAUNCH = -7,      /* the CUDA runtime refused the launch or a copy
+                               (no device, no sm_103a image, bad stream ...) */
+  NSA_ERR_TIMEOUT = -8      /* reserved: a bounded device-side wait gave up   */
+} nsa_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nsa_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int nsa_version(void);
+
+/*
+ * nsa_sel_attn_fwd -- selection-attention forward on the GPU.
+ *
+ *   Q              device, IEEE fp16, [B, M, H, D]
+ *   K, V           device, IEEE fp16, [B, N, G, D]
+ *   block_indices  device, int32,     [B, M, G, T]; block ids, -1 = padding
+ *   O              device, fp32,      [B, M, H, D]   (output)
+ *   LSE            device, fp32,      [B, H, M]      (output, natural log)
+ *   B, M, N, T     >= 0; an empty problem (B*M == 0) returns NSA_OK at once
+ *   H, G, D        > 0, H % G == 0, H/G == 8, D in {64, 128}
+ *   block_size     32 or 64
+ *   scale          score multiplier; <= 0 selects 1/sqrt(D)
+ *   stream         cudaStream_t to launch on (NULL = legacy default stream)
+ *
+ * Asynchronous: validates the arguments on the host, enqueues one kernel on
+ * `stream` and returns without synchronising. It allocates nothing, frees
+ * nothing and keeps no state between calls; concurrent calls on different
+ * streams are safe. Returns NSA_OK, or a negative nsa_status. Errors that
+ * surface only when the kernel runs are reported by the next CUDA call that
+ * synchronises with `stream`, as for any CUDA launch.
+ */
+int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V,
+                     const int32_t* block_indices, float* O, float* LSE,
+                     int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
+                     int64_t D, int64_t T, int block_size, float scale,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSA_SEL_ATTN_H */

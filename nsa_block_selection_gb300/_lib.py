@@ -1,0 +1,107 @@
+"""ctypes binding of ``libnsa_sel_attn.so`` (argument marshalling only).
+
+Every step of the selection-attention forward runs in the library's CUDA
+kernels; this module only checks tensor dtypes/devices, allocates outputs
+with torch and passes raw pointers, sizes and the current CUDA stream. There
+is no fallback: if the library is missing, calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "lib", "libnsa_sel_attn.so")
+
+NSA_OK = 0
+
+EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd")
+
+_lib = None
+
+
+class NsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the library (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} is missing: build it with `python -m nsa_block_selection_gb300.build` "
+            "(the CUDA library is the only implementation)")
+    lib = ctypes.CDLL(p)
+    i64, c_int, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    lib.nsa_status_string.restype = ctypes.c_char_p
+    lib.nsa_status_string.argtypes = [c_int]
+    lib.nsa_version.restype = c_int
+    lib.nsa_version.argtypes = []
+    lib.nsa_sel_attn_fwd.restype = c_int
+    lib.nsa_sel_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
+                                     c_int, ctypes.c_float, vp]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().nsa_status_string(int(status)).decode()
+
+
+def _ptr(t) -> Optional[int]:
+    return t.data_ptr() if t is not None and t.numel() > 0 else None
+
+
+def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float] = None,
+                 out=None, lse=None, stream=None):
+    """NSA selection-attention forward on the GPU.
+
+    q: fp16 [B, M, H, D]; k, v: fp16 [B, N, G, D]; block_indices: int32
+    [B, M, G, T] (-1 = padding); all contiguous on one CUDA device.
+    Returns (O fp32 [B, M, H, D], LSE fp32 [B, H, M]); ``out``/``lse`` may be
+    given preallocated. ``stream`` defaults to torch's current stream.
+    """
+    import torch
+
+    lib = load()
+    B, M, H, D = q.shape
+    Bk, N, G, Dk = k.shape
+    T = block_indices.shape[-1]
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or \
+            tuple(block_indices.shape) != (B, M, G, T):
+        raise ValueError("shape mismatch: q [B,M,H,D], k/v [B,N,G,D], "
+                         "block_indices [B,M,G,T]")
+    for name, t, dt in (("q", q, torch.float16), ("k", k, torch.float16),
+                        ("v", v, torch.float16), ("block_indices", block_indices, torch.int32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty((B, M, H, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    if out.dtype != torch.float32 or tuple(out.shape) != (B, M, H, D) or not out.is_contiguous():
+        raise ValueError("out must be contiguous fp32 [B, M, H, D]")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, M) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, H, M]")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.nsa_sel_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out),
+                              _ptr(lse), B, M, N, H, G, D, T, int(block_size), sc,
+                              ctypes.c_void_p(stream.cuda_stream))
+    if st != NSA_OK:
+        raise NsaError(st, "nsa_sel_attn_fwd")
+    return out, lse

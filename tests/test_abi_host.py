@@ -1,0 +1,90 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function the headers declare, and rejects bad arguments before touching
+CUDA."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from nsa_block_selection_gb300 import _lib
+from nsa_block_selection_gb300.build import INCLUDE
+
+# Sizes of a valid call: B, M, N, H, G, D, T, block_size
+GOOD = dict(B=1, M=128, N=128, H=16, G=2, D=128, T=4, bs=64)
+FAKE = 4096  # a 16-byte aligned non-null address that is never dereferenced
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(INCLUDE, "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(nsa_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = _lib.LIB_PATH
+    if not os.path.exists(path):
+        from nsa_block_selection_gb300.build import build
+
+        build()
+    return _lib.load()
+
+
+def call(lib, q=FAKE, k=FAKE, v=FAKE, idx=FAKE, o=FAKE, lse=FAKE, scale=0.0, **over):
+    a = dict(GOOD)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return lib.nsa_sel_attn_fwd(vp(q), vp(k), vp(v), vp(idx), vp(o), vp(lse), a["B"], a["M"],
+                                a["N"], a["H"], a["G"], a["D"], a["T"], a["bs"], scale, None)
+
+
+def test_exports_match_header(lib):
+    names = declared_functions()
+    assert set(names) >= {"nsa_sel_attn_fwd", "nsa_status_string", "nsa_version"}
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(_lib.EXPORTS) <= set(names)
+
+
+def test_status_strings(lib):
+    for code in range(0, -9, -1):
+        s = lib.nsa_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.nsa_status_string(-99).decode() == "unknown status"
+    assert lib.nsa_version() >= 100
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(B=-1), -2), (dict(M=-3), -2), (dict(N=-1), -2), (dict(T=-1), -2),
+    (dict(H=0), -2), (dict(G=0), -2), (dict(D=0), -2),
+    (dict(H=12, G=2), -5), (dict(H=16, G=4), -5), (dict(H=15, G=2), -5),
+    (dict(D=96), -4), (dict(D=256), -4),
+    (dict(bs=16), -3), (dict(bs=128), -3), (dict(bs=0), -3),
+    (dict(M=1 << 31), -2), (dict(N=1 << 40), -2),
+])
+def test_bad_sizes(lib, over, status):
+    assert call(lib, **over) == status
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "idx", "o", "lse"])
+def test_null_pointers(lib, which):
+    assert call(lib, **{which: None}) == -1
+
+
+@pytest.mark.parametrize("which,addr", [("q", FAKE + 8), ("k", FAKE + 2), ("v", FAKE + 4),
+                                        ("o", FAKE + 4), ("lse", FAKE + 2), ("idx", FAKE + 1)])
+def test_misaligned(lib, which, addr):
+    assert call(lib, **{which: addr}) == -6
+
+
+@pytest.mark.parametrize("over", [dict(B=0), dict(M=0), dict(B=0, M=0)])
+def test_empty_problem_is_a_no_op(lib, over):
+    # returns before any CUDA call, so it runs without a GPU; pointers unused
+    assert call(lib, q=None, k=None, v=None, idx=None, o=None, lse=None, **over) == 0
