@@ -21,6 +21,7 @@ m64k_bs64   1 65536 64    8 128 64  16 1.0 {0, c-1, c} + 13 random from [1, c-1)
 m32k_bs32   2 32768 32    4 128 32  32 1.5 {0, c-1, c} + 29 random from [1, c-1)
 dense_m16k  1 16384 64    8 128 64 256 1.0 every block of [0, c]
 dense_m64k  1 65536 64    8 128 64 1024 1.0 every block of [0, c]
+m16k_bs64   1 16384 64    8 128 64  16 1.0 as m64k_bs64 (profiling size)
 =========== = ===== ===== == = === == ==== ===== ==================================
 
 Here c = floor(m / bs) is the query's own (diagonal) block. A row whose
@@ -91,6 +92,9 @@ WORKLOADS = {
                            "all_causal"),
     "dense_m64k": Workload("dense_m64k", 1, 65536, 65536, 64, 8, 128, 64, 1024, 1.0,
                            "all_causal"),
+    # m64k_bs64 cut to 16k queries: same row rule, ~0.9 GB on the device
+    "m16k_bs64": Workload("m16k_bs64", 1, 16384, 16384, 64, 8, 128, 64, 16, 1.0,
+                          "first_two_local"),
 }
 
 # Order of the parity workloads; position i seeds with 20260000 + i.
