@@ -30,8 +30,9 @@
  *   - LSE is the natural log of sum(exp(scale * q.k)) over visible keys.
  *
  * Every buffer is contiguous row-major in the layout given, owned by the
- * caller, and not retained after the call returns. Keys/values in rows that
- * no index selects, and in the causal future of a query, are never read.
+ * caller, and not retained after the call returns. Key/value rows that no
+ * index selects are never read; rows after a query inside its own 16-key
+ * tile may be read but never reach the output (whatever they hold).
  */
 #ifndef NSA_SEL_ATTN_H
 #define NSA_SEL_ATTN_H
@@ -55,7 +56,8 @@ typedef enum nsa_status {
                                block_indices not 4-byte aligned               */
   NSA_ERR_LAUNCH = -7,      /* the CUDA runtime refused the launch or a copy
                                (no device, no sm_103a image, bad stream ...) */
-  NSA_ERR_TIMEOUT = -8      /* reserved: a bounded device-side wait gave up   */
+  NSA_ERR_TIMEOUT = -8      /* a bounded device-side wait gave up (reported by
+                               nsa_sync_status)                               */
 } nsa_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -79,8 +81,10 @@ int nsa_version(void);
  *   stream         cudaStream_t to launch on (NULL = legacy default stream)
  *
  * Asynchronous: validates the arguments on the host, enqueues one kernel on
- * `stream` and returns without synchronising. It allocates nothing, frees
- * nothing and keeps no state between calls; concurrent calls on different
+ * `stream` and returns without synchronising. K and V are fetched with TMA
+ * through tensor maps encoded on the host for each call. It allocates
+ * nothing, frees nothing and keeps no state between calls (the per-device
+ * status word of nsa_sync_status aside); concurrent calls on different
  * streams are safe. Returns NSA_OK, or a negative nsa_status. Errors that
  * surface only when the kernel runs are reported by the next CUDA call that
  * synchronises with `stream`, as for any CUDA launch.
@@ -90,6 +94,29 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V,
                      int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                      int64_t D, int64_t T, int block_size, float scale,
                      void* stream);
+
+/*
+ * nsa_sync_status -- wait for `stream`, then read and clear the device status
+ * word of the current device.
+ *
+ * Every device-side wait of this library's kernels is bounded (1 s). A warp
+ * whose wait gives up records it in a per-device status word, lets its own
+ * copies in flight land, and returns without writing its outputs. This call
+ * returns NSA_ERR_TIMEOUT if that happened in any launch since the last call,
+ * NSA_ERR_LAUNCH if synchronising the stream reports a CUDA error, NSA_OK
+ * otherwise. It synchronises; it allocates nothing.
+ */
+int nsa_sync_status(void* stream);
+
+/*
+ * nsa_selftest_wait_timeout -- test hook for the bounded waits.
+ *
+ * Launches one warp on `stream` that waits on a barrier nothing will ever
+ * complete; after `limit_ns` (1e3 .. 2e9) it gives up and sets the status
+ * word, so the next nsa_sync_status() returns NSA_ERR_TIMEOUT. Touches no
+ * other memory. Returns NSA_ERR_SHAPE for a limit out of range.
+ */
+int nsa_selftest_wait_timeout(int64_t limit_ns, void* stream);
 
 #ifdef __cplusplus
 }

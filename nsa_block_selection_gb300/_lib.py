@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(PKG, "lib", "libnsa_sel_attn.so")
 
 NSA_OK = 0
 
-EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd")
+EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sync_status",
+           "nsa_selftest_wait_timeout")
 
 _lib = None
 
@@ -48,6 +49,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_fwd.restype = c_int
     lib.nsa_sel_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
                                      c_int, ctypes.c_float, vp]
+    lib.nsa_sync_status.restype = c_int
+    lib.nsa_sync_status.argtypes = [vp]
+    lib.nsa_selftest_wait_timeout.restype = c_int
+    lib.nsa_selftest_wait_timeout.argtypes = [i64, vp]
     if path is None:
         _lib = lib
     return lib
@@ -105,3 +110,22 @@ def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float]
     if st != NSA_OK:
         raise NsaError(st, "nsa_sel_attn_fwd")
     return out, lse
+
+
+def sync_status(stream=None) -> int:
+    """Wait for ``stream`` (default: torch's current stream) and return the
+    library's device status (NSA_OK, or -8 after a timed-out device wait)."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return load().nsa_sync_status(ctypes.c_void_p(stream.cuda_stream))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    """Launch the self-test kernel whose wait can only time out."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return load().nsa_selftest_wait_timeout(int(limit_ns), ctypes.c_void_p(stream.cuda_stream))

@@ -6,25 +6,35 @@
 // block_indices[b, m, g, :] selects, causally masked; O [B,M,H,D] and the
 // natural-log LSE [B,H,M] are written.
 //
-// Kernel shape (one warp per (b, m, g) work unit):
+// Kernel shape (one warp per (b, m, g) work unit, warps independent):
 //  * the warp walks its index row and streams the selected keys in tiles of
-//    16 keys (K tile + V tile, 2 x 16 x D fp16) through a private ring of
-//    NSTAGE shared-memory stages filled with 16-byte cp.async copies; key rows
-//    past the query's last visible key are zero-filled and never read;
+//    16 keys through a private ring of NSTAGE shared-memory stages; lane 0
+//    fills a stage with TMA bulk-tensor copies (K tile + V tile, 128-byte
+//    swizzled rows) that complete on the stage's mbarrier;
 //  * S^T = K Q^T on the tensor cores (mma.sync m16n8k16, fp16 in, fp32 acc):
 //    16 keys x 8 heads, so the group's 8 heads are exactly the MMA's N;
-//  * scores are scaled into the log2 domain, causally masked, and folded into
-//    a running (max, sum) per head; the probabilities are rounded to fp16,
-//    transposed in registers (movmatrix) into the B operand of
-//    O^T += V^T P^T, whose A operand comes from ldmatrix.trans;
+//  * the running max is kept in raw score units; probabilities are
+//    exp2(s * scale*log2(e) - max * scale*log2(e)) (one FMA + ex2), and the
+//    O accumulator is rescaled only when some head's max grows;
+//  * P is rounded to fp16, transposed in registers (movmatrix) into the B
+//    operand of O^T += V^T P^T, whose A operand comes from ldmatrix.trans;
 //  * the epilogue normalises O, writes it as fp32 and writes LSE.
-// Shared-memory rows are XOR-swizzled in 16-byte units so every ldmatrix
-// phase touches 8 distinct bank groups.
+// Keys past the query's last visible key (causal edge, or n >= N) are masked
+// by select; V rows there are zeroed in shared memory before the PV product,
+// so whatever those rows hold never reaches the output. Rows n >= N are
+// outside the tensor map and arrive as zeros.
+//
+// Every mbarrier wait is bounded (1 s of %globaltimer). On timeout the warp
+// sets bit 0 of the device status word, waits (bounded) for its own copies in
+// flight, and returns without writing its outputs; nsa_sync_status() reports
+// it as NSA_ERR_TIMEOUT.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "nsa_sel_attn.h"
 #include "ptx.cuh"
@@ -33,33 +43,49 @@
 #define NSA_WARPS 4
 #endif
 #ifndef NSA_STAGES
-#define NSA_STAGES 3
+#define NSA_STAGES 2
 #endif
+
+__device__ unsigned int g_nsa_device_status = 0u;
 
 namespace nsa {
 
 constexpr int kHeadsPerGroup = 8;
 constexpr int kTileKeys = 16;
+constexpr int kBoxCols = 64;                   // d columns per TMA box: 128-byte rows
+constexpr int kBoxBytes = kTileKeys * 128;     // one box: 16 keys x 64 d x fp16
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr unsigned kFull = 0xffffffffu;
 
 struct Problem {
   const __half* Q;
-  const __half* K;
-  const __half* V;
   const int32_t* idx;
   float* O;
   float* LSE;
-  int64_t B, M, N, H, G, T;
+  int64_t M, N, H, G, T;
   int64_t units;  // B * G * M
   int bs;
   int nblk;       // ceil(N / bs)
   float sl2;      // scale * log2(e)
 };
 
-__device__ __forceinline__ float fast_exp2(float x) {
+__device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
+
+// Bounded wait on an mbarrier phase; false after `limit_ns` without it.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void report_timeout() { atomicOr(&g_nsa_device_status, 1u); }
 
 // Warp-uniform walk over the 16-key tiles one index row selects, in the
 // order the row lists its blocks. Padding (< 0 or >= nblk) and blocks that
@@ -94,13 +120,13 @@ struct TileWalk {
         const int j = win + (threadIdx.x & 31);
         const int t = (j < T) ? __ldg(row + j) : -1;
         const bool ok = t >= 0 && t < nblk && t * bs <= lastkey;
-        mask = __ballot_sync(0xffffffffu, ok);
+        mask = __ballot_sync(kFull, ok);
         lane_val = t;
         win += 32;
       }
       const int src = __ffs(mask) - 1;
       mask &= mask - 1u;
-      const int t = __shfl_sync(0xffffffffu, lane_val, src);
+      const int t = __shfl_sync(kFull, lane_val, src);
       n0 = t * bs;
       nend = min(n0 + bs, lastkey + 1);
     }
@@ -111,22 +137,22 @@ struct TileWalk {
 };
 
 template <int D, int WARPS, int NSTAGE>
-struct WarpKernelCfg {
-  static constexpr int kRowBytes = D * 2;
-  static constexpr int kPiecesPerRow = D / 8;  // 16-byte pieces
-  static constexpr int kTileBytes = kTileKeys * kRowBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
+struct Cfg {
+  static constexpr int kBoxes = D / kBoxCols;          // TMA boxes per tile
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;  // K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kWarpBytes = NSTAGE * kStageBytes;
-  static constexpr int kSmemBytes = WARPS * kWarpBytes;
-  static constexpr int kCopiesPerLane = kTileKeys * kPiecesPerRow / 32;
+  static constexpr int kBarOffset = WARPS * kWarpBytes;
+  static constexpr int kSmemBytes = kBarOffset + WARPS * NSTAGE * 8 + 1024;  // + align slack
   static constexpr int kSteps = D / 16;
 };
 
 template <int D, int WARPS, int NSTAGE>
 __global__ void __launch_bounds__(WARPS * 32)
-    sel_attn_fwd_warp_kernel(const Problem p) {
-  using C = WarpKernelCfg<D, WARPS, NSTAGE>;
-  extern __shared__ __align__(128) uint8_t smem[];
+    sel_attn_fwd_kernel(const Problem p, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV) {
+  using C = Cfg<D, WARPS, NSTAGE>;
+  extern __shared__ uint8_t smem_raw[];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -134,14 +160,26 @@ __global__ void __launch_bounds__(WARPS * 32)
   if (unit >= p.units) return;
   const int64_t m = unit % p.M;
   const int64_t bg = unit / p.M;
-  const int64_t g = bg % p.G;
-  const int64_t b = bg / p.G;
+  const int g = static_cast<int>(bg % p.G);
+  const int b = static_cast<int>(bg / p.G);
   const int gid = lane >> 2;  // MMA group id (row within an 8-row slab)
   const int tig = lane & 3;   // thread in group
 
-  const uint32_t wsm = smem_u32(smem) + warp * C::kWarpBytes;
-  const int64_t hbase = g * kHeadsPerGroup;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t stages = base + warp * C::kWarpBytes;
+  const uint32_t bars = base + C::kBarOffset + warp * NSTAGE * 8;
 
+  if (lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+#pragma unroll
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(bars + 8 * s, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+
+  const int64_t hbase = static_cast<int64_t>(g) * kHeadsPerGroup;
   // Q^T as the B operand of S^T = K Q^T: head gid, dims 16k + 2tig (+1, +8, +9).
   uint32_t qf[C::kSteps][2];
   {
@@ -155,25 +193,19 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
   const int32_t* irow = p.idx + ((b * p.M + m) * p.G + g) * p.T;
-  const int64_t kv_stride = p.G * D;  // elements between consecutive keys
-  const __half* kb = p.K + (b * p.N * p.G + g) * D;
-  const __half* vb = p.V + (b * p.N * p.G + g) * D;
   const uint64_t keep = l2_policy_evict_last();
 
   auto issue = [&](int slot, int n0) {
-    const uint32_t sk = wsm + slot * C::kStageBytes;
-    const uint32_t sv = sk + C::kTileBytes;
+    if (lane == 0) {
+      const uint32_t bar = bars + 8 * slot;
+      const uint32_t sk = stages + slot * C::kStageBytes;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, C::kStageBytes);
 #pragma unroll
-    for (int i = 0; i < C::kCopiesPerLane; ++i) {
-      const int piece = i * 32 + lane;
-      const int r = piece / C::kPiecesPerRow;
-      const int c = piece % C::kPiecesPerRow;
-      const int n = n0 + r;
-      const bool ok = n <= lastkey;
-      const int64_t off = static_cast<int64_t>(ok ? n : 0) * kv_stride + c * 8;
-      const uint32_t so = r * C::kRowBytes + ((c ^ (r & 7)) << 4);
-      cp_async_16_hint(sk + so, kb + off, ok ? 16 : 0, keep);
-      cp_async_16_hint(sv + so, vb + off, ok ? 16 : 0, keep);
+      for (int h = 0; h < C::kBoxes; ++h) {
+        tma_load_4d(sk + h * kBoxBytes, &tmK, bar, h * kBoxCols, g, n0, b, keep);
+        tma_load_4d(sk + C::kTileBytes + h * kBoxBytes, &tmV, bar, h * kBoxCols, g, n0, b, keep);
+      }
     }
   };
 
@@ -183,89 +215,103 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   int issued = 0;
 #pragma unroll
-  for (int s = 0; s < NSTAGE - 1; ++s) {
+  for (int s = 0; s < NSTAGE; ++s) {
     int n0;
     if (prod.next(n0)) {
-      issue(issued % NSTAGE, n0);
+      issue(s, n0);
       ++issued;
     }
-    cp_async_commit();
   }
 
   float acc[C::kSteps][4];
 #pragma unroll
   for (int i = 0; i < C::kSteps; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float mrun0 = -INFINITY, mrun1 = -INFINITY;  // heads 2tig, 2tig+1 (log2 domain)
+  float mrun0 = -INFINITY, mrun1 = -INFINITY;  // running max of raw scores, heads 2tig, 2tig+1
+  float neg0 = 0.f, neg1 = 0.f;                // -max * scale * log2(e) (0 while empty)
   float l0 = 0.f, l1 = 0.f;                    // this lane's share of the row sums
+  const float sl2 = p.sl2;
 
   // ldmatrix row addresses: K tiles (row-major A), V tiles (transposed A).
-  const int ka_row = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const uint32_t ka = (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
   const int ka_hi = lane >> 4;
-  const int va_row = (lane & 7) + (lane >> 4) * 8;
+  const uint32_t va = (lane & 7) * 128 + ((lane & 16) ? 8 * 128 : 0);
   const int va_hi = (lane >> 3) & 1;
-  const int sw = lane & 7;  // row & 7 for both
+  const int sw = lane & 7;  // key row & 7 for both
 
   int consumed = 0;
+  bool failed = false;
   int n0;
   while (cons.next(n0)) {
-    {
-      int nn;
-      if (prod.next(nn)) {
-        issue(issued % NSTAGE, nn);
-        ++issued;
-      }
-      cp_async_commit();
-    }
-    cp_async_wait<NSTAGE - 1>();
-    __syncwarp();
-
-    const uint32_t sk = wsm + (consumed % NSTAGE) * C::kStageBytes;
+    const int slot = consumed % NSTAGE;
+    const uint32_t sk = stages + slot * C::kStageBytes;
     const uint32_t sv = sk + C::kTileBytes;
+    const bool ok = wait_phase(bars + 8 * slot, (consumed / NSTAGE) & 1, kWaitLimitNs);
+    if (!__all_sync(kFull, ok)) {
+      failed = true;
+      break;
+    }
+    const bool edge = n0 + kTileKeys - 1 > lastkey;  // warp-uniform
+    if (edge) {
+      // zero the V rows past the last visible key (they may hold anything)
+#pragma unroll
+      for (int e = lane; e < kTileKeys * (D / 8); e += 32) {
+        const int r = e / (D / 8), c = e % (D / 8);
+        if (n0 + r > lastkey)
+          st_shared_zero16(sv + (c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
 
-    // S^T (16 keys x 8 heads) = K_tile Q^T
+    // S^T (16 keys x 8 heads) = K_tile Q^T, raw dot products
     float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < C::kSteps; ++k) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4(sk + ka_row * C::kRowBytes + (((2 * k + ka_hi) ^ sw) << 4), a0, a1, a2, a3);
+      ldsm_x4(sk + (k >> 2) * kBoxBytes + ka + ((((k & 3) * 2 + ka_hi) ^ sw) << 4), a0, a1, a2,
+              a3);
       mma_16816(s, a0, a1, a2, a3, qf[k][0], qf[k][1]);
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) s[j] *= p.sl2;
-    if (n0 + kTileKeys - 1 > lastkey) {  // causal edge or end of keys
+    if (edge) {
       if (n0 + gid > lastkey) s[0] = s[1] = -INFINITY;
       if (n0 + gid + 8 > lastkey) s[2] = s[3] = -INFINITY;
     }
 
-    // online softmax, per head
+    // online softmax per head; rescale only when a max grows
     float mx0 = fmaxf(s[0], s[2]);
     float mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
     }
-    const float mn0 = fmaxf(mrun0, mx0);
-    const float mn1 = fmaxf(mrun1, mx1);
-    const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
-    const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-    const float al0 = fast_exp2(mrun0 - mu0);
-    const float al1 = fast_exp2(mrun1 - mu1);
-    const float p0 = fast_exp2(s[0] - mu0);
-    const float p1 = fast_exp2(s[1] - mu1);
-    const float p2 = fast_exp2(s[2] - mu0);
-    const float p3 = fast_exp2(s[3] - mu1);
-    l0 = l0 * al0 + (p0 + p2);
-    l1 = l1 * al1 + (p1 + p3);
-    mrun0 = mn0;
-    mrun1 = mn1;
+    if (__any_sync(kFull, (mx0 > mrun0) || (mx1 > mrun1))) {
+      const float mn0 = fmaxf(mrun0, mx0);
+      const float mn1 = fmaxf(mrun1, mx1);
+      const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+      const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+      const float al0 = ex2((mrun0 - mu0) * sl2);
+      const float al1 = ex2((mrun1 - mu1) * sl2);
+      mrun0 = mn0;
+      mrun1 = mn1;
+      neg0 = -mu0 * sl2;
+      neg1 = -mu1 * sl2;
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
-    for (int i = 0; i < C::kSteps; ++i) {
-      acc[i][0] *= al0;
-      acc[i][1] *= al1;
-      acc[i][2] *= al0;
-      acc[i][3] *= al1;
+      for (int i = 0; i < C::kSteps; ++i) {
+        acc[i][0] *= al0;
+        acc[i][1] *= al1;
+        acc[i][2] *= al0;
+        acc[i][3] *= al1;
+      }
     }
+    const float p0 = ex2(fmaf(s[0], sl2, neg0));
+    const float p1 = ex2(fmaf(s[1], sl2, neg1));
+    const float p2 = ex2(fmaf(s[2], sl2, neg0));
+    const float p3 = ex2(fmaf(s[3], sl2, neg1));
+    l0 += p0 + p2;
+    l1 += p1 + p3;
 
     // P^T as the B operand: (keys 2tig.., head gid) from (key gid, heads 2tig..)
     const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
@@ -275,19 +321,34 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
     for (int i = 0; i < C::kSteps; ++i) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(sv + va_row * C::kRowBytes + (((2 * i + va_hi) ^ sw) << 4), a0, a1, a2, a3);
+      ldsm_x4_t(sv + (i >> 2) * kBoxBytes + va + ((((i & 3) * 2 + va_hi) ^ sw) << 4), a0, a1,
+                a2, a3);
       mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
     }
     ++consumed;
     __syncwarp();
+    {
+      int nn;
+      if (prod.next(nn)) {
+        issue(slot, nn);
+        ++issued;
+      }
+    }
   }
-  cp_async_wait<0>();
+
+  if (failed) {
+    // copies still in flight target this warp's stages: let them land first
+    if (lane == 0) report_timeout();
+    for (int j = consumed; j < issued; ++j)
+      wait_phase(bars + 8 * (j % NSTAGE), (j / NSTAGE) & 1, kWaitLimitNs);
+    return;
+  }
 
   // epilogue: finish the row sums, normalise, store O (fp32) and LSE
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    l0 += __shfl_xor_sync(kFull, l0, off);
+    l1 += __shfl_xor_sync(kFull, l1, off);
   }
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
   const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
@@ -302,22 +363,83 @@ __global__ void __launch_bounds__(WARPS * 32)
   if (gid == 0) {
     constexpr float kLn2 = 0.69314718055994530942f;
     float* L = p.LSE + (b * p.H + hbase + 2 * tig) * p.M + m;
-    L[0] = l0 > 0.f ? (mrun0 + log2f(l0)) * kLn2 : -INFINITY;
-    L[p.M] = l1 > 0.f ? (mrun1 + log2f(l1)) * kLn2 : -INFINITY;
+    L[0] = l0 > 0.f ? (mrun0 * sl2 + __log2f(l0)) * kLn2 : -INFINITY;
+    L[p.M] = l1 > 0.f ? (mrun1 * sl2 + __log2f(l1)) * kLn2 : -INFINITY;
   }
 }
 
+// A one-warp kernel whose mbarrier never completes: exercises the bounded
+// wait and the status word without touching any other memory.
+__global__ void selftest_timeout_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t a = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(a, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = wait_phase(a, 0, limit_ns);
+  if (!__all_sync(kFull, ok) && threadIdx.x == 0) report_timeout();
+}
+
+// ---- host side ---------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// K or V [B, N, G, D] fp16 as a 4-D map (d, g, n, b); box = 64 d x 1 x 16 keys x 1.
+static bool encode_kv_map(CUtensorMap* tm, const void* ptr, int64_t B, int64_t N, int64_t G,
+                          int64_t D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(G),
+                              static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D * 2),
+                                 static_cast<cuuint64_t>(G * D * 2),
+                                 static_cast<cuuint64_t>(N * G * D * 2)};
+  const cuuint32_t box[4] = {kBoxCols, 1, kTileKeys, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
-static int launch_warp_kernel(const Problem& p, cudaStream_t stream) {
+static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
+                      cudaStream_t stream) {
   constexpr int W = NSA_WARPS;
   constexpr int S = NSA_STAGES;
-  using C = WarpKernelCfg<D, W, S>;
-  auto kern = sel_attn_fwd_warp_kernel<D, W, S>;
+  using C = Cfg<D, W, S>;
+  CUtensorMap tk, tv;
+  if (p.N > 0) {
+    if (!encode_kv_map(&tk, K, B, p.N, p.G, D) || !encode_kv_map(&tv, V, B, p.N, p.G, D))
+      return NSA_ERR_LAUNCH;
+  } else {
+    memset(&tk, 0, sizeof(tk));  // no key: no tile is ever loaded
+    memset(&tv, 0, sizeof(tv));
+  }
+  auto kern = sel_attn_fwd_kernel<D, W, S>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return NSA_ERR_LAUNCH;
   const int64_t blocks = (p.units + W - 1) / W;
-  kern<<<static_cast<unsigned>(blocks), W * 32, C::kSmemBytes, stream>>>(p);
+  kern<<<static_cast<unsigned>(blocks), W * 32, C::kSmemBytes, stream>>>(p, tk, tv);
   return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
@@ -340,7 +462,7 @@ const char* nsa_status_string(int status) {
   }
 }
 
-int nsa_version(void) { return 100; }
+int nsa_version(void) { return 200; }
 
 int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* block_indices,
                      float* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
@@ -350,9 +472,9 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t*
   if (H % G != 0 || H / G != kHeadsPerGroup) return NSA_ERR_GROUPS;
   if (D != 64 && D != 128) return NSA_ERR_HEAD_DIM;
   if (block_size != 32 && block_size != 64) return NSA_ERR_BLOCK_SIZE;
-  // 32-bit key and index arithmetic inside the kernel; grid of B*G*M warps
+  // 32-bit key / coordinate arithmetic inside the kernel; grid of B*G*M warps
   const int64_t lim = (int64_t(1) << 31) - 1024;
-  if (M > lim || N > lim || T > lim || G > lim) return NSA_ERR_SHAPE;
+  if (M > lim || N > lim || T > lim || G > lim || B > lim) return NSA_ERR_SHAPE;
   if (B > 0 && M > 0 && B * G > lim / M) return NSA_ERR_SHAPE;
   if (B == 0 || M == 0) return NSA_OK;
   if (!Q || !O || !LSE) return NSA_ERR_NULL;
@@ -367,12 +489,9 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t*
 
   Problem p;
   p.Q = static_cast<const __half*>(Q);
-  p.K = static_cast<const __half*>(K);
-  p.V = static_cast<const __half*>(V);
   p.idx = block_indices;
   p.O = O;
   p.LSE = LSE;
-  p.B = B;
   p.M = M;
   p.N = N;
   p.H = H;
@@ -384,7 +503,29 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t*
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   p.sl2 = sc * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return D == 64 ? launch_warp_kernel<64>(p, st) : launch_warp_kernel<128>(p, st);
+  return D == 64 ? launch_fwd<64>(p, K, V, B, st) : launch_fwd<128>(p, K, V, B, st);
+}
+
+int nsa_sync_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NSA_ERR_LAUNCH;
+  unsigned int v = 0u;
+  if (cudaMemcpyFromSymbol(&v, g_nsa_device_status, sizeof(v)) != cudaSuccess)
+    return NSA_ERR_LAUNCH;
+  if (v != 0u) {
+    const unsigned int zero = 0u;
+    if (cudaMemcpyToSymbol(g_nsa_device_status, &zero, sizeof(zero)) != cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    return NSA_ERR_TIMEOUT;
+  }
+  return NSA_OK;
+}
+
+int nsa_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+  if (limit_ns < 1000 || limit_ns > 2000000000) return NSA_ERR_SHAPE;
+  nsa::selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint64_t>(limit_ns));
+  return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
 }  // extern "C"
