@@ -8,14 +8,17 @@
 //
 // Kernel shape (one warp per (b, m, g) work unit, warps independent):
 //  * the warp walks its index row and streams the selected keys in tiles of
-//    16 keys through a private ring of NSTAGE shared-memory stages; lane 0
-//    fills a stage with TMA bulk-tensor copies (K tile + V tile, 128-byte
-//    swizzled rows) that complete on the stage's mbarrier;
+//    16 keys through a private ring of NSLOT shared-memory slots, K tile and
+//    V tile of a 16-key tile in consecutive slots; lane 0 fills a slot with
+//    TMA bulk-tensor copies (128-byte swizzled rows) that complete on the
+//    slot's mbarrier, and refills it as soon as the tile in it is used;
 //  * S^T = K Q^T on the tensor cores (mma.sync m16n8k16, fp16 in, fp32 acc):
-//    16 keys x 8 heads, so the group's 8 heads are exactly the MMA's N;
-//  * the running max is kept in raw score units; probabilities are
-//    exp2(s * scale*log2(e) - max * scale*log2(e)) (one FMA + ex2), and the
-//    O accumulator is rescaled only when some head's max grows;
+//    16 keys x 8 heads, so the group's 8 heads are exactly the MMA's N; the
+//    k-steps run as two independent MMA chains;
+//  * scores are scaled into the log2 domain; probabilities are
+//    exp2(x - ref) with a per-head reference that only moves when a score
+//    exceeds it by more than 8 (so the max reduction and the O rescale run
+//    on few tiles);
 //  * P is rounded to fp16, transposed in registers (movmatrix) into the B
 //    operand of O^T += V^T P^T, whose A operand comes from ldmatrix.trans;
 //  * the epilogue normalises O, writes it as fp32 and writes LSE.
@@ -42,8 +45,11 @@
 #ifndef NSA_WARPS
 #define NSA_WARPS 4
 #endif
-#ifndef NSA_STAGES
-#define NSA_STAGES 2
+#ifndef NSA_SLOTS
+#define NSA_SLOTS 3
+#endif
+#ifndef NSA_GROUP_INTERLEAVE
+#define NSA_GROUP_INTERLEAVE 1
 #endif
 
 __device__ unsigned int g_nsa_device_status = 0u;
@@ -64,6 +70,7 @@ struct Problem {
   float* LSE;
   int64_t M, N, H, G, T;
   int64_t units;  // B * G * M
+  int gi;         // KV groups interleaved in the unit order (divides G)
   int bs;
   int nblk;       // ceil(N / bs)
   float sl2;      // scale * log2(e)
@@ -136,44 +143,54 @@ struct TileWalk {
   }
 };
 
-template <int D, int WARPS, int NSTAGE>
+template <int D, int WARPS, int NSLOT>
 struct Cfg {
-  static constexpr int kBoxes = D / kBoxCols;          // TMA boxes per tile
-  static constexpr int kTileBytes = kBoxes * kBoxBytes;  // K (or V) tile
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kWarpBytes = NSTAGE * kStageBytes;
+  static constexpr int kBoxes = D / kBoxCols;            // TMA boxes per tile
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one K (or V) tile = one slot
+  static constexpr int kWarpBytes = NSLOT * kTileBytes;
   static constexpr int kBarOffset = WARPS * kWarpBytes;
-  static constexpr int kSmemBytes = kBarOffset + WARPS * NSTAGE * 8 + 1024;  // + align slack
+  static constexpr int kSmemBytes = kBarOffset + WARPS * NSLOT * 8 + 1024;  // + align slack
   static constexpr int kSteps = D / 16;
 };
 
-template <int D, int WARPS, int NSTAGE>
+// Raise the running max only when a scaled score exceeds it by more than
+// 2^8: probabilities stay <= 256 (exact in the sums, fine for fp16) and the
+// shuffle reduction and O rescale run on few tiles. LSE and O use the same
+// reference, so the result does not depend on it.
+constexpr float kMaxSlack = 8.0f;
+
+template <int D, int WARPS, int NSLOT>
 __global__ void __launch_bounds__(WARPS * 32)
     sel_attn_fwd_kernel(const Problem p, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
-  using C = Cfg<D, WARPS, NSTAGE>;
+  using C = Cfg<D, WARPS, NSLOT>;
+  static_assert(NSLOT >= 2, "need at least two slots");
   extern __shared__ uint8_t smem_raw[];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
   if (unit >= p.units) return;
-  const int64_t m = unit % p.M;
-  const int64_t bg = unit / p.M;
-  const int g = static_cast<int>(bg % p.G);
-  const int b = static_cast<int>(bg / p.G);
+  // unit -> (b, g_hi, m, g_lo): gi groups interleaved, m next, then groups
+  const int g_lo = static_cast<int>(unit % p.gi);
+  const int64_t r1 = unit / p.gi;
+  const int64_t m = r1 % p.M;
+  const int64_t r2 = r1 / p.M;
+  const int g_hi = static_cast<int>(r2 % (p.G / p.gi));
+  const int b = static_cast<int>(r2 / (p.G / p.gi));
+  const int g = g_hi * p.gi + g_lo;
   const int gid = lane >> 2;  // MMA group id (row within an 8-row slab)
   const int tig = lane & 3;   // thread in group
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t stages = base + warp * C::kWarpBytes;
-  const uint32_t bars = base + C::kBarOffset + warp * NSTAGE * 8;
+  const uint32_t slots = base + warp * C::kWarpBytes;
+  const uint32_t bars = base + C::kBarOffset + warp * NSLOT * 8;
 
   if (lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
 #pragma unroll
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(bars + 8 * s, 1);
+    for (int s = 0; s < NSLOT; ++s) mbar_init(bars + 8 * s, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -195,40 +212,51 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int32_t* irow = p.idx + ((b * p.M + m) * p.G + g) * p.T;
   const uint64_t keep = l2_policy_evict_last();
 
-  auto issue = [&](int slot, int n0) {
-    if (lane == 0) {
-      const uint32_t bar = bars + 8 * slot;
-      const uint32_t sk = stages + slot * C::kStageBytes;
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, C::kStageBytes);
-#pragma unroll
-      for (int h = 0; h < C::kBoxes; ++h) {
-        tma_load_4d(sk + h * kBoxBytes, &tmK, bar, h * kBoxCols, g, n0, b, keep);
-        tma_load_4d(sk + C::kTileBytes + h * kBoxBytes, &tmV, bar, h * kBoxCols, g, n0, b, keep);
-      }
-    }
-  };
-
+  // Loads alternate K tile, V tile of the same 16 keys; load j uses slot
+  // j % NSLOT and completes phase (j / NSLOT) & 1 of that slot's barrier.
   TileWalk prod, cons;
   prod.init(irow, static_cast<int>(p.T), p.nblk, p.bs, lastkey);
   cons.init(irow, static_cast<int>(p.T), p.nblk, p.bs, lastkey);
-
-  int issued = 0;
-#pragma unroll
-  for (int s = 0; s < NSTAGE; ++s) {
+  int nload = 0;
+  int pend_n0 = 0;
+  bool prod_done = false;
+  auto issue_next = [&]() {
     int n0;
-    if (prod.next(n0)) {
-      issue(s, n0);
-      ++issued;
+    if (nload & 1) {
+      n0 = pend_n0;
+    } else {
+      if (prod_done || !prod.next(n0)) {
+        prod_done = true;
+        return;
+      }
+      pend_n0 = n0;
     }
-  }
+    const int slot = nload % NSLOT;
+    if (lane == 0) {
+      const uint32_t bar = bars + 8 * slot;
+      const uint32_t dst = slots + slot * C::kTileBytes;
+      const CUtensorMap* tm = (nload & 1) ? &tmV : &tmK;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+      for (int h = 0; h < C::kBoxes; ++h)
+        tma_load_4d(dst + h * kBoxBytes, tm, bar, h * kBoxCols, g, n0, b, keep);
+    }
+    ++nload;
+  };
+  auto wait_load = [&](int j) {
+    return wait_phase(bars + 8 * (j % NSLOT), (j / NSLOT) & 1, kWaitLimitNs);
+  };
+
+#pragma unroll
+  for (int s = 0; s < NSLOT; ++s) issue_next();
 
   float acc[C::kSteps][4];
 #pragma unroll
   for (int i = 0; i < C::kSteps; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float mrun0 = -INFINITY, mrun1 = -INFINITY;  // running max of raw scores, heads 2tig, 2tig+1
-  float neg0 = 0.f, neg1 = 0.f;                // -max * scale * log2(e) (0 while empty)
-  float l0 = 0.f, l1 = 0.f;                    // this lane's share of the row sums
+  float m2a = -INFINITY, m2b = -INFINITY;  // reference max, scaled (x = s * sl2), heads 2tig, 2tig+1
+  float nega = 0.f, negb = 0.f;            // -reference (0 while a head has seen nothing)
+  float la = 0.f, lb = 0.f;                // this lane's share of the row sums
   const float sl2 = p.sl2;
 
   // ldmatrix row addresses: K tiles (row-major A), V tiles (transposed A).
@@ -238,19 +266,84 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int va_hi = (lane >> 3) & 1;
   const int sw = lane & 7;  // key row & 7 for both
 
-  int consumed = 0;
-  bool failed = false;
+  int tile = 0;
+  int pending = -1;  // first load not known to have landed, after a timeout
   int n0;
   while (cons.next(n0)) {
-    const int slot = consumed % NSTAGE;
-    const uint32_t sk = stages + slot * C::kStageBytes;
-    const uint32_t sv = sk + C::kTileBytes;
-    const bool ok = wait_phase(bars + 8 * slot, (consumed / NSTAGE) & 1, kWaitLimitNs);
-    if (!__all_sync(kFull, ok)) {
-      failed = true;
+    const int jk = 2 * tile, jv = 2 * tile + 1;
+    const uint32_t sk = slots + (jk % NSLOT) * C::kTileBytes;
+    const uint32_t sv = slots + (jv % NSLOT) * C::kTileBytes;
+    if (!__all_sync(kFull, wait_load(jk))) {
+      pending = jk;
       break;
     }
+    // S^T (16 keys x 8 heads) = K_tile Q^T, raw dot products, two MMA chains
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < C::kSteps; k += 2) {
+      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+      ldsm_x4(sk + (k >> 2) * kBoxBytes + ka + ((((k & 3) * 2 + ka_hi) ^ sw) << 4), a0, a1, a2,
+              a3);
+      ldsm_x4(sk + ((k + 1) >> 2) * kBoxBytes + ka + (((((k + 1) & 3) * 2 + ka_hi) ^ sw) << 4),
+              b0, b1, b2, b3);
+      mma_16816(s, a0, a1, a2, a3, qf[k][0], qf[k][1]);
+      mma_16816(t, b0, b1, b2, b3, qf[k + 1][0], qf[k + 1][1]);
+    }
+    __syncwarp();
+    issue_next();  // the K slot is free
+
+    float x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = (s[j] + t[j]) * sl2;
     const bool edge = n0 + kTileKeys - 1 > lastkey;  // warp-uniform
+    if (edge) {
+      if (n0 + gid > lastkey) x[0] = x[1] = -INFINITY;
+      if (n0 + gid + 8 > lastkey) x[2] = x[3] = -INFINITY;
+    }
+    // online softmax per head: move the reference only on a large excess
+    float mxa = fmaxf(x[0], x[2]);
+    float mxb = fmaxf(x[1], x[3]);
+    if (__any_sync(kFull, (mxa > m2a + kMaxSlack) || (mxb > m2b + kMaxSlack))) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mxa = fmaxf(mxa, __shfl_xor_sync(kFull, mxa, off));
+        mxb = fmaxf(mxb, __shfl_xor_sync(kFull, mxb, off));
+      }
+      const float mna = fmaxf(m2a, mxa);
+      const float mnb = fmaxf(m2b, mxb);
+      const float ua = (mna == -INFINITY) ? 0.f : mna;
+      const float ub = (mnb == -INFINITY) ? 0.f : mnb;
+      const float ala = ex2(m2a - ua);
+      const float alb = ex2(m2b - ub);
+      m2a = mna;
+      m2b = mnb;
+      nega = -ua;
+      negb = -ub;
+      la *= ala;
+      lb *= alb;
+#pragma unroll
+      for (int i = 0; i < C::kSteps; ++i) {
+        acc[i][0] *= ala;
+        acc[i][1] *= alb;
+        acc[i][2] *= ala;
+        acc[i][3] *= alb;
+      }
+    }
+    const float p0 = ex2(x[0] + nega);
+    const float p1 = ex2(x[1] + negb);
+    const float p2 = ex2(x[2] + nega);
+    const float p3 = ex2(x[3] + negb);
+    la += p0 + p2;
+    lb += p1 + p3;
+    // P^T as the B operand: (keys 2tig.., head gid) from (key gid, heads 2tig..)
+    const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
+    const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
+
+    if (!__all_sync(kFull, wait_load(jv))) {
+      pending = jv;
+      break;
+    }
     if (edge) {
       // zero the V rows past the last visible key (they may hold anything)
 #pragma unroll
@@ -262,61 +355,6 @@ __global__ void __launch_bounds__(WARPS * 32)
       fence_proxy_async_smem();
       __syncwarp();
     }
-
-    // S^T (16 keys x 8 heads) = K_tile Q^T, raw dot products
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int k = 0; k < C::kSteps; ++k) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(sk + (k >> 2) * kBoxBytes + ka + ((((k & 3) * 2 + ka_hi) ^ sw) << 4), a0, a1, a2,
-              a3);
-      mma_16816(s, a0, a1, a2, a3, qf[k][0], qf[k][1]);
-    }
-    if (edge) {
-      if (n0 + gid > lastkey) s[0] = s[1] = -INFINITY;
-      if (n0 + gid + 8 > lastkey) s[2] = s[3] = -INFINITY;
-    }
-
-    // online softmax per head; rescale only when a max grows
-    float mx0 = fmaxf(s[0], s[2]);
-    float mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-    }
-    if (__any_sync(kFull, (mx0 > mrun0) || (mx1 > mrun1))) {
-      const float mn0 = fmaxf(mrun0, mx0);
-      const float mn1 = fmaxf(mrun1, mx1);
-      const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
-      const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-      const float al0 = ex2((mrun0 - mu0) * sl2);
-      const float al1 = ex2((mrun1 - mu1) * sl2);
-      mrun0 = mn0;
-      mrun1 = mn1;
-      neg0 = -mu0 * sl2;
-      neg1 = -mu1 * sl2;
-      l0 *= al0;
-      l1 *= al1;
-#pragma unroll
-      for (int i = 0; i < C::kSteps; ++i) {
-        acc[i][0] *= al0;
-        acc[i][1] *= al1;
-        acc[i][2] *= al0;
-        acc[i][3] *= al1;
-      }
-    }
-    const float p0 = ex2(fmaf(s[0], sl2, neg0));
-    const float p1 = ex2(fmaf(s[1], sl2, neg1));
-    const float p2 = ex2(fmaf(s[2], sl2, neg0));
-    const float p3 = ex2(fmaf(s[3], sl2, neg1));
-    l0 += p0 + p2;
-    l1 += p1 + p3;
-
-    // P^T as the B operand: (keys 2tig.., head gid) from (key gid, heads 2tig..)
-    const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
-    const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
-
     // O^T (D x 8 heads) += V_tile^T P^T
 #pragma unroll
     for (int i = 0; i < C::kSteps; ++i) {
@@ -325,46 +363,39 @@ __global__ void __launch_bounds__(WARPS * 32)
                 a2, a3);
       mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
     }
-    ++consumed;
     __syncwarp();
-    {
-      int nn;
-      if (prod.next(nn)) {
-        issue(slot, nn);
-        ++issued;
-      }
-    }
+    issue_next();  // the V slot is free
+    ++tile;
   }
 
-  if (failed) {
-    // copies still in flight target this warp's stages: let them land first
+  if (pending >= 0) {
+    // copies still in flight target this warp's slots: let them land first
     if (lane == 0) report_timeout();
-    for (int j = consumed; j < issued; ++j)
-      wait_phase(bars + 8 * (j % NSTAGE), (j / NSTAGE) & 1, kWaitLimitNs);
+    for (int j = pending; j < nload; ++j) wait_load(j);
     return;
   }
 
   // epilogue: finish the row sums, normalise, store O (fp32) and LSE
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(kFull, l0, off);
-    l1 += __shfl_xor_sync(kFull, l1, off);
+    la += __shfl_xor_sync(kFull, la, off);
+    lb += __shfl_xor_sync(kFull, lb, off);
   }
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-  const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  const float inva = la > 0.f ? 1.f / la : 0.f;
+  const float invb = lb > 0.f ? 1.f / lb : 0.f;
   float* o = p.O + ((b * p.M + m) * p.H + hbase + 2 * tig) * D + gid;
 #pragma unroll
   for (int i = 0; i < C::kSteps; ++i) {
-    o[16 * i] = acc[i][0] * inv0;
-    o[D + 16 * i] = acc[i][1] * inv1;
-    o[16 * i + 8] = acc[i][2] * inv0;
-    o[D + 16 * i + 8] = acc[i][3] * inv1;
+    o[16 * i] = acc[i][0] * inva;
+    o[D + 16 * i] = acc[i][1] * invb;
+    o[16 * i + 8] = acc[i][2] * inva;
+    o[D + 16 * i + 8] = acc[i][3] * invb;
   }
   if (gid == 0) {
     constexpr float kLn2 = 0.69314718055994530942f;
     float* L = p.LSE + (b * p.H + hbase + 2 * tig) * p.M + m;
-    L[0] = l0 > 0.f ? (mrun0 * sl2 + __log2f(l0)) * kLn2 : -INFINITY;
-    L[p.M] = l1 > 0.f ? (mrun1 * sl2 + __log2f(l1)) * kLn2 : -INFINITY;
+    L[0] = la > 0.f ? (m2a + __log2f(la)) * kLn2 : -INFINITY;
+    L[p.M] = lb > 0.f ? (m2b + __log2f(lb)) * kLn2 : -INFINITY;
   }
 }
 
@@ -424,7 +455,7 @@ template <int D>
 static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
                       cudaStream_t stream) {
   constexpr int W = NSA_WARPS;
-  constexpr int S = NSA_STAGES;
+  constexpr int S = NSA_SLOTS;
   using C = Cfg<D, W, S>;
   CUtensorMap tk, tv;
   if (p.N > 0) {
@@ -498,6 +529,7 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t*
   p.G = G;
   p.T = T;
   p.units = B * G * M;
+  p.gi = (G % NSA_GROUP_INTERLEAVE == 0) ? NSA_GROUP_INTERLEAVE : 1;
   p.bs = block_size;
   p.nblk = static_cast<int>((N + block_size - 1) / block_size);
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
