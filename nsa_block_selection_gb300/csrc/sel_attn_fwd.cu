@@ -8,10 +8,10 @@
 //
 // Kernel shape (one warp per (b, m, g) work unit, warps independent):
 //  * the warp walks its index row and streams the selected keys in tiles of
-//    16 keys through a private ring of NSLOT shared-memory slots, K tile and
-//    V tile of a 16-key tile in consecutive slots; lane 0 fills a slot with
-//    TMA bulk-tensor copies (128-byte swizzled rows) that complete on the
-//    slot's mbarrier, and refills it as soon as the tile in it is used;
+//    16 keys through two private shared-memory slots (K tile, V tile); lane 0
+//    fills a slot with TMA bulk-tensor copies (128-byte swizzled rows) that
+//    complete on the slot's mbarrier, and refills it with the next tile's K
+//    (or V) as soon as QK^T (or PV) has read it;
 //  * S^T = K Q^T on the tensor cores (mma.sync m16n8k16, fp16 in, fp32 acc):
 //    16 keys x 8 heads, so the group's 8 heads are exactly the MMA's N; the
 //    k-steps run as two independent MMA chains;
@@ -45,8 +45,8 @@
 #ifndef NSA_WARPS
 #define NSA_WARPS 4
 #endif
-#ifndef NSA_SLOTS
-#define NSA_SLOTS 3
+#ifndef NSA_MIN_BLOCKS
+#define NSA_MIN_BLOCKS 4
 #endif
 #ifndef NSA_GROUP_INTERLEAVE
 #define NSA_GROUP_INTERLEAVE 1
@@ -143,13 +143,13 @@ struct TileWalk {
   }
 };
 
-template <int D, int WARPS, int NSLOT>
+template <int D, int WARPS>
 struct Cfg {
   static constexpr int kBoxes = D / kBoxCols;            // TMA boxes per tile
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one K (or V) tile = one slot
-  static constexpr int kWarpBytes = NSLOT * kTileBytes;
+  static constexpr int kWarpBytes = 2 * kTileBytes;      // slot 0: K, slot 1: V
   static constexpr int kBarOffset = WARPS * kWarpBytes;
-  static constexpr int kSmemBytes = kBarOffset + WARPS * NSLOT * 8 + 1024;  // + align slack
+  static constexpr int kSmemBytes = kBarOffset + WARPS * 2 * 8 + 1024;  // + align slack
   static constexpr int kSteps = D / 16;
 };
 
@@ -159,12 +159,11 @@ struct Cfg {
 // reference, so the result does not depend on it.
 constexpr float kMaxSlack = 8.0f;
 
-template <int D, int WARPS, int NSLOT>
-__global__ void __launch_bounds__(WARPS * 32)
+template <int D, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     sel_attn_fwd_kernel(const Problem p, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
-  using C = Cfg<D, WARPS, NSLOT>;
-  static_assert(NSLOT >= 2, "need at least two slots");
+  using C = Cfg<D, WARPS>;
   extern __shared__ uint8_t smem_raw[];
 
   const int warp = threadIdx.x >> 5;
@@ -184,13 +183,13 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t slots = base + warp * C::kWarpBytes;
-  const uint32_t bars = base + C::kBarOffset + warp * NSLOT * 8;
+  const uint32_t bars = base + C::kBarOffset + warp * 2 * 8;
 
   if (lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-#pragma unroll
-    for (int s = 0; s < NSLOT; ++s) mbar_init(bars + 8 * s, 1);
+    mbar_init(bars, 1);
+    mbar_init(bars + 8, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -212,44 +211,31 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int32_t* irow = p.idx + ((b * p.M + m) * p.G + g) * p.T;
   const uint64_t keep = l2_policy_evict_last();
 
-  // Loads alternate K tile, V tile of the same 16 keys; load j uses slot
-  // j % NSLOT and completes phase (j / NSLOT) & 1 of that slot's barrier.
-  TileWalk prod, cons;
-  prod.init(irow, static_cast<int>(p.T), p.nblk, p.bs, lastkey);
-  cons.init(irow, static_cast<int>(p.T), p.nblk, p.bs, lastkey);
-  int nload = 0;
-  int pend_n0 = 0;
-  bool prod_done = false;
-  auto issue_next = [&]() {
-    int n0;
-    if (nload & 1) {
-      n0 = pend_n0;
-    } else {
-      if (prod_done || !prod.next(n0)) {
-        prod_done = true;
-        return;
-      }
-      pend_n0 = n0;
-    }
-    const int slot = nload % NSLOT;
+  // Two slots: slot 0 holds the K tile, slot 1 the V tile of the same 16
+  // keys. The K tile of the next 16 keys is requested as soon as QK^T has
+  // read slot 0, its V tile as soon as PV has read slot 1; both barriers
+  // complete once per tile, so the phase parity is the tile count's low bit.
+  const uint32_t sk = slots;
+  const uint32_t sv = slots + C::kTileBytes;
+  const uint32_t bar_k = bars, bar_v = bars + 8;
+  auto issue = [&](uint32_t dst, uint32_t bar, const CUtensorMap* tm, int n0) {
     if (lane == 0) {
-      const uint32_t bar = bars + 8 * slot;
-      const uint32_t dst = slots + slot * C::kTileBytes;
-      const CUtensorMap* tm = (nload & 1) ? &tmV : &tmK;
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
       for (int h = 0; h < C::kBoxes; ++h)
         tma_load_4d(dst + h * kBoxBytes, tm, bar, h * kBoxCols, g, n0, b, keep);
     }
-    ++nload;
-  };
-  auto wait_load = [&](int j) {
-    return wait_phase(bars + 8 * (j % NSLOT), (j / NSLOT) & 1, kWaitLimitNs);
   };
 
-#pragma unroll
-  for (int s = 0; s < NSLOT; ++s) issue_next();
+  TileWalk walk;
+  walk.init(irow, static_cast<int>(p.T), p.nblk, p.bs, lastkey);
+  int n_next = 0;
+  bool have = walk.next(n_next);
+  if (have) {
+    issue(sk, bar_k, &tmK, n_next);
+    issue(sv, bar_v, &tmV, n_next);
+  }
 
   float acc[C::kSteps][4];
 #pragma unroll
@@ -260,21 +246,18 @@ __global__ void __launch_bounds__(WARPS * 32)
   const float sl2 = p.sl2;
 
   // ldmatrix row addresses: K tiles (row-major A), V tiles (transposed A).
-  const uint32_t ka = (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
+  const uint32_t ka = sk + (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
   const int ka_hi = lane >> 4;
-  const uint32_t va = (lane & 7) * 128 + ((lane & 16) ? 8 * 128 : 0);
+  const uint32_t va = sv + (lane & 7) * 128 + ((lane & 16) ? 8 * 128 : 0);
   const int va_hi = (lane >> 3) & 1;
   const int sw = lane & 7;  // key row & 7 for both
 
-  int tile = 0;
-  int pending = -1;  // first load not known to have landed, after a timeout
-  int n0;
-  while (cons.next(n0)) {
-    const int jk = 2 * tile, jv = 2 * tile + 1;
-    const uint32_t sk = slots + (jk % NSLOT) * C::kTileBytes;
-    const uint32_t sv = slots + (jv % NSLOT) * C::kTileBytes;
-    if (!__all_sync(kFull, wait_load(jk))) {
-      pending = jk;
+  uint32_t phase = 0;
+  int timed_out = 0;  // 1: K tile missing, 2: V tile missing
+  while (have) {
+    const int n0 = n_next;
+    if (!__all_sync(kFull, wait_phase(bar_k, phase, kWaitLimitNs))) {
+      timed_out = 1;
       break;
     }
     // S^T (16 keys x 8 heads) = K_tile Q^T, raw dot products, two MMA chains
@@ -283,15 +266,15 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
     for (int k = 0; k < C::kSteps; k += 2) {
       uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-      ldsm_x4(sk + (k >> 2) * kBoxBytes + ka + ((((k & 3) * 2 + ka_hi) ^ sw) << 4), a0, a1, a2,
-              a3);
-      ldsm_x4(sk + ((k + 1) >> 2) * kBoxBytes + ka + (((((k + 1) & 3) * 2 + ka_hi) ^ sw) << 4),
-              b0, b1, b2, b3);
+      ldsm_x4(ka + (k >> 2) * kBoxBytes + ((((k & 3) * 2 + ka_hi) ^ sw) << 4), a0, a1, a2, a3);
+      ldsm_x4(ka + ((k + 1) >> 2) * kBoxBytes + (((((k + 1) & 3) * 2 + ka_hi) ^ sw) << 4), b0,
+              b1, b2, b3);
       mma_16816(s, a0, a1, a2, a3, qf[k][0], qf[k][1]);
       mma_16816(t, b0, b1, b2, b3, qf[k + 1][0], qf[k + 1][1]);
     }
     __syncwarp();
-    issue_next();  // the K slot is free
+    have = walk.next(n_next);
+    if (have) issue(sk, bar_k, &tmK, n_next);  // slot 0 is free
 
     float x[4];
 #pragma unroll
@@ -340,8 +323,8 @@ __global__ void __launch_bounds__(WARPS * 32)
     const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
     const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
 
-    if (!__all_sync(kFull, wait_load(jv))) {
-      pending = jv;
+    if (!__all_sync(kFull, wait_phase(bar_v, phase, kWaitLimitNs))) {
+      timed_out = 2;
       break;
     }
     if (edge) {
@@ -359,19 +342,24 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
     for (int i = 0; i < C::kSteps; ++i) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(sv + (i >> 2) * kBoxBytes + va + ((((i & 3) * 2 + va_hi) ^ sw) << 4), a0, a1,
-                a2, a3);
+      ldsm_x4_t(va + (i >> 2) * kBoxBytes + ((((i & 3) * 2 + va_hi) ^ sw) << 4), a0, a1, a2, a3);
       mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
     }
     __syncwarp();
-    issue_next();  // the V slot is free
-    ++tile;
+    if (have) issue(sv, bar_v, &tmV, n_next);  // slot 1 is free
+    phase ^= 1u;
   }
 
-  if (pending >= 0) {
+  if (timed_out) {
     // copies still in flight target this warp's slots: let them land first
     if (lane == 0) report_timeout();
-    for (int j = pending; j < nload; ++j) wait_load(j);
+    if (timed_out == 1) {
+      wait_phase(bar_k, phase, kWaitLimitNs);
+      wait_phase(bar_v, phase, kWaitLimitNs);
+    } else {
+      if (have) wait_phase(bar_k, phase ^ 1u, kWaitLimitNs);
+      wait_phase(bar_v, phase, kWaitLimitNs);
+    }
     return;
   }
 
@@ -455,8 +443,7 @@ template <int D>
 static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
                       cudaStream_t stream) {
   constexpr int W = NSA_WARPS;
-  constexpr int S = NSA_SLOTS;
-  using C = Cfg<D, W, S>;
+  using C = Cfg<D, W>;
   CUtensorMap tk, tv;
   if (p.N > 0) {
     if (!encode_kv_map(&tk, K, B, p.N, p.G, D) || !encode_kv_map(&tv, V, B, p.N, p.G, D))
@@ -465,7 +452,7 @@ static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
     memset(&tk, 0, sizeof(tk));  // no key: no tile is ever loaded
     memset(&tv, 0, sizeof(tv));
   }
-  auto kern = sel_attn_fwd_kernel<D, W, S>;
+  auto kern = sel_attn_fwd_kernel<D, W>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return NSA_ERR_LAUNCH;
