@@ -15,8 +15,9 @@ Prints ONE JSON line (rank 0):
                 listed (T=1024, same Q/K/V) over the sparse time;
   roofline      the kernel against max(FLOPs / fp16 tensor peak, gathered
                 bytes / HBM bandwidth) -- the gathered bytes dominate;
-  e2e           the same metric through the C ABI's host-buffer call
-                (host->device inputs, device->host O and LSE every step);
+  e2e           the same metric through the C ABI's host-buffer entry point
+                (pinned host inputs uploaded and O / LSE downloaded every step,
+                chunked so copies overlap the kernels);
   cpu_baseline  the CPU oracle timed on a bounded row sample, host cores;
   clocks        nvidia-smi SM clocks and throttle reasons during the steps.
 
@@ -62,6 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=24576,
                     help="rows of the CPU-oracle sample")
     ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--chunk-m", type=int, default=0,
+                    help="queries per chunk of the host-buffer pipeline (0: default)")
     return ap.parse_args(argv)
 
 
@@ -432,11 +435,13 @@ def run_dense(w, q, k, v, out, lse, flush, args, t_sparse_ms):
 
 
 def run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist):
-    """Host (pinned) buffers in and out every step: H2D of Q/K/V/indices,
-    the forward, D2H of O and LSE, all inside the timed events."""
+    """Host (pinned) buffers in and out every step through the C ABI's host
+    entry point: chunked uploads of Q / indices / visible K-V rows, the
+    forward, downloads of O and LSE, overlapped on three streams, all inside
+    the timed events."""
     import torch
 
-    from nsa_block_selection_gb300 import sel_attn_fwd
+    from nsa_block_selection_gb300 import _lib
 
     hq = torch.from_numpy(q_np).pin_memory()
     hk = torch.from_numpy(k_np).pin_memory()
@@ -444,18 +449,13 @@ def run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist):
     hi = torch.from_numpy(idx_np).pin_memory()
     ho = torch.empty((w.B, w.M, w.H, w.D), dtype=torch.float32).pin_memory()
     hl = torch.empty((w.B, w.H, w.M), dtype=torch.float32).pin_memory()
-    dq, dk, dv, di = (torch.empty_like(x, device=dev) for x in (hq, hk, hv, hi))
-    do = torch.empty(ho.shape, dtype=torch.float32, device=dev)
-    dl = torch.empty(hl.shape, dtype=torch.float32, device=dev)
+    need = _lib.host_workspace_bytes(w.B, w.M, w.N, w.H, w.G, w.D, w.T, w.block_size,
+                                     args.chunk_m)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
 
     def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        di.copy_(hi, non_blocking=True)
-        sel_attn_fwd(dq, dk, dv, di, w.block_size, w.scale, out=do, lse=dl)
-        ho.copy_(do, non_blocking=True)
-        hl.copy_(dl, non_blocking=True)
+        _lib.sel_attn_fwd_host(hq, hk, hv, hi, w.block_size, w.scale, out=ho, lse=hl,
+                               chunk_m=args.chunk_m, workspace=ws, device=dev, sync=False)
 
     steps = max(3, args.steps // 4)
     times, _ = time_steps(step, steps, 2, lambda: None, barrier)
@@ -469,7 +469,9 @@ def run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist):
     d2h = sum(x.numel() * x.element_size() for x in (ho, hl))
     return {"value": flops / (t * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": t,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "path": "pinned host -> cudaMemcpyAsync -> nsa_sel_attn_fwd -> host"}
+            "workspace_bytes": need,
+            "path": "pinned host -> nsa_sel_attn_fwd_host (chunked H2D / forward / D2H "
+                    "pipeline) -> pinned host"}
 
 
 def main(argv=None):

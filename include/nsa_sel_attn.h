@@ -56,8 +56,9 @@ typedef enum nsa_status {
                                block_indices not 4-byte aligned               */
   NSA_ERR_LAUNCH = -7,      /* the CUDA runtime refused the launch or a copy
                                (no device, no sm_103a image, bad stream ...) */
-  NSA_ERR_TIMEOUT = -8      /* a bounded device-side wait gave up (reported by
+  NSA_ERR_TIMEOUT = -8,     /* a bounded device-side wait gave up (reported by
                                nsa_sync_status)                               */
+  NSA_ERR_WORKSPACE = -9    /* workspace NULL or smaller than required        */
 } nsa_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -94,6 +95,49 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V,
                      int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                      int64_t D, int64_t T, int block_size, float scale,
                      void* stream);
+
+/*
+ * nsa_sel_attn_fwd_host_workspace_bytes -- device workspace that
+ * nsa_sel_attn_fwd_host needs for these sizes and query chunk length
+ * (chunk_m <= 0 selects the default). Returns the byte count, or a negative
+ * nsa_status for invalid sizes. Pure host arithmetic; no CUDA call.
+ */
+int64_t nsa_sel_attn_fwd_host_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_t H,
+                                              int64_t G, int64_t D, int64_t T, int block_size,
+                                              int64_t chunk_m);
+
+/*
+ * nsa_sel_attn_fwd_host -- the same forward with HOST buffers in and out.
+ *
+ *   Q, K, V, block_indices   host memory, layouts as in nsa_sel_attn_fwd
+ *   O, LSE                   host memory, written
+ *   workspace                device memory of at least
+ *                            nsa_sel_attn_fwd_host_workspace_bytes(...) bytes,
+ *                            256-byte aligned, owned by the caller
+ *   chunk_m                  queries per pipeline chunk (<= 0: default,
+ *                            about M/8 rounded up to a multiple of 64)
+ *   stream                   caller's stream; the kernels run on it
+ *
+ * The queries are processed in chunks of chunk_m positions. For each chunk
+ * the call enqueues, on an internal upload stream, the copies of its Q rows,
+ * its index rows and the K/V rows it can see (keys below the chunk's end,
+ * each copied once); the kernel on `stream`; and on an internal download
+ * stream, the copies of its O rows and LSE columns. Chunk buffers are double
+ * buffered in the workspace, so uploads, kernels and downloads of adjacent
+ * chunks overlap. Copies overlap only if the host buffers are page-locked
+ * (pinned); with pageable memory they are correct but serial.
+ *
+ * Returns after enqueueing; `stream` is made to wait for every copy, so the
+ * outputs are complete once `stream` is synchronised. Results are
+ * bit-identical to nsa_sel_attn_fwd on the same inputs. It allocates no
+ * memory (the internal streams and events are created and released by the
+ * call). Errors: as nsa_sel_attn_fwd, plus NSA_ERR_WORKSPACE.
+ */
+int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
+                          const int32_t* block_indices, float* O, float* LSE, int64_t B,
+                          int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                          int block_size, float scale, void* workspace,
+                          int64_t workspace_bytes, int64_t chunk_m, void* stream);
 
 /*
  * nsa_sync_status -- wait for `stream`, then read and clear the device status

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(PKG, "lib", "libnsa_sel_attn.so")
 NSA_OK = 0
 
 EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sync_status",
-           "nsa_selftest_wait_timeout")
+           "nsa_selftest_wait_timeout", "nsa_sel_attn_fwd_host_workspace_bytes",
+           "nsa_sel_attn_fwd_host")
 
 _lib = None
 
@@ -53,6 +54,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sync_status.argtypes = [vp]
     lib.nsa_selftest_wait_timeout.restype = c_int
     lib.nsa_selftest_wait_timeout.argtypes = [i64, vp]
+    lib.nsa_sel_attn_fwd_host_workspace_bytes.restype = i64
+    lib.nsa_sel_attn_fwd_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64, i64,
+                                                          c_int, i64]
+    lib.nsa_sel_attn_fwd_host.restype = c_int
+    lib.nsa_sel_attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                          i64, c_int, ctypes.c_float, vp, i64, i64, vp]
     if path is None:
         _lib = lib
     return lib
@@ -78,21 +85,7 @@ def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float]
     import torch
 
     lib = load()
-    B, M, H, D = q.shape
-    Bk, N, G, Dk = k.shape
-    T = block_indices.shape[-1]
-    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or \
-            tuple(block_indices.shape) != (B, M, G, T):
-        raise ValueError("shape mismatch: q [B,M,H,D], k/v [B,N,G,D], "
-                         "block_indices [B,M,G,T]")
-    for name, t, dt in (("q", q, torch.float16), ("k", k, torch.float16),
-                        ("v", v, torch.float16), ("block_indices", block_indices, torch.int32)):
-        if t.dtype != dt:
-            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
-        if not t.is_cuda:
-            raise ValueError(f"{name} must be a CUDA tensor")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
+    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=True)
     if out is None:
         out = torch.empty((B, M, H, D), dtype=torch.float32, device=q.device)
     if lse is None:
@@ -109,6 +102,77 @@ def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float]
                               ctypes.c_void_p(stream.cuda_stream))
     if st != NSA_OK:
         raise NsaError(st, "nsa_sel_attn_fwd")
+    return out, lse
+
+
+def _check_common(q, k, v, block_indices, device_expected: bool):
+    import torch
+
+    B, M, H, D = q.shape
+    Bk, N, G, Dk = k.shape
+    T = block_indices.shape[-1]
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or \
+            tuple(block_indices.shape) != (B, M, G, T):
+        raise ValueError("shape mismatch: q [B,M,H,D], k/v [B,N,G,D], "
+                         "block_indices [B,M,G,T]")
+    for name, t, dt in (("q", q, torch.float16), ("k", k, torch.float16),
+                        ("v", v, torch.float16), ("block_indices", block_indices, torch.int32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if t.is_cuda != device_expected:
+            raise ValueError(f"{name} must be a {'CUDA' if device_expected else 'CPU'} tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    return B, M, N, H, G, D, T
+
+
+def host_workspace_bytes(B, M, N, H, G, D, T, block_size, chunk_m=0) -> int:
+    n = load().nsa_sel_attn_fwd_host_workspace_bytes(B, M, N, H, G, D, T, int(block_size),
+                                                     int(chunk_m))
+    if n < 0:
+        raise NsaError(int(n), "nsa_sel_attn_fwd_host_workspace_bytes")
+    return int(n)
+
+
+def sel_attn_fwd_host(q, k, v, block_indices, block_size: int, scale: Optional[float] = None,
+                      out=None, lse=None, chunk_m: int = 0, workspace=None, device=None,
+                      stream=None, sync: bool = True):
+    """Forward with host (CPU) tensors in and out, through the library's
+    pipelined host entry point (pin the tensors for overlapped copies).
+
+    Returns (O, LSE) as CPU fp32 tensors. ``workspace`` is a CUDA uint8
+    tensor of at least :func:`host_workspace_bytes`; one is allocated when
+    omitted. With ``sync=False`` the call returns once everything is
+    enqueued on ``stream``.
+    """
+    import torch
+
+    lib = load()
+    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=False)
+    device = torch.device(device) if device is not None else torch.device("cuda",
+                                                                        torch.cuda.current_device())
+    need = host_workspace_bytes(B, M, N, H, G, D, T, block_size, chunk_m)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    if out is None:
+        out = torch.empty((B, M, H, D), dtype=torch.float32, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, H, M), dtype=torch.float32, pin_memory=True)
+    if out.is_cuda or lse.is_cuda or out.dtype != torch.float32 or lse.dtype != torch.float32:
+        raise ValueError("out and lse must be fp32 CPU tensors")
+    if tuple(out.shape) != (B, M, H, D) or tuple(lse.shape) != (B, H, M):
+        raise ValueError("out must be [B, M, H, D] and lse [B, H, M]")
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.nsa_sel_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out),
+                                   _ptr(lse), B, M, N, H, G, D, T, int(block_size), sc,
+                                   workspace.data_ptr(), workspace.numel(), int(chunk_m),
+                                   ctypes.c_void_p(stream.cuda_stream))
+    if st != NSA_OK:
+        raise NsaError(st, "nsa_sel_attn_fwd_host")
+    if sync:
+        stream.synchronize()
     return out, lse
 
 

@@ -41,6 +41,7 @@
 
 #include "nsa_sel_attn.h"
 #include "ptx.cuh"
+#include "sel_attn_fwd.cuh"
 
 #ifndef NSA_WARPS
 #define NSA_WARPS 4
@@ -69,6 +70,7 @@ struct Problem {
   float* O;
   float* LSE;
   int64_t M, N, H, G, T;
+  int64_t m_off;  // query position of row 0 (a chunk of a longer sequence)
   int64_t units;  // B * G * M
   int gi;         // KV groups interleaved in the unit order (divides G)
   int bs;
@@ -207,7 +209,8 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     }
   }
 
-  const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
+  const int64_t mpos = m + p.m_off;  // the query's position in the key sequence
+  const int lastkey = static_cast<int>(mpos < p.N - 1 ? mpos : p.N - 1);
   const int32_t* irow = p.idx + ((b * p.M + m) * p.G + g) * p.T;
   const uint64_t keep = l2_policy_evict_last();
 
@@ -463,29 +466,10 @@ static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
 
 }  // namespace nsa
 
-extern "C" {
+namespace nsa {
 
-const char* nsa_status_string(int status) {
-  switch (status) {
-    case NSA_OK: return "ok";
-    case NSA_ERR_NULL: return "null pointer";
-    case NSA_ERR_SHAPE: return "invalid shape";
-    case NSA_ERR_BLOCK_SIZE: return "block_size must be 32 or 64";
-    case NSA_ERR_HEAD_DIM: return "head dim D must be 64 or 128";
-    case NSA_ERR_GROUPS: return "H must be 8 * G (8 query heads per KV group)";
-    case NSA_ERR_ALIGN: return "misaligned pointer";
-    case NSA_ERR_LAUNCH: return "CUDA launch failed";
-    case NSA_ERR_TIMEOUT: return "device wait timed out";
-    default: return "unknown status";
-  }
-}
-
-int nsa_version(void) { return 200; }
-
-int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* block_indices,
-                     float* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
-                     int64_t D, int64_t T, int block_size, float scale, void* stream) {
-  using namespace nsa;
+int check_sizes(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                int block_size) {
   if (B < 0 || M < 0 || N < 0 || T < 0 || H <= 0 || G <= 0 || D <= 0) return NSA_ERR_SHAPE;
   if (H % G != 0 || H / G != kHeadsPerGroup) return NSA_ERR_GROUPS;
   if (D != 64 && D != 128) return NSA_ERR_HEAD_DIM;
@@ -494,6 +478,16 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t*
   const int64_t lim = (int64_t(1) << 31) - 1024;
   if (M > lim || N > lim || T > lim || G > lim || B > lim) return NSA_ERR_SHAPE;
   if (B > 0 && M > 0 && B * G > lim / M) return NSA_ERR_SHAPE;
+  return NSA_OK;
+}
+
+int launch_forward(const void* Q, const void* K, const void* V, const int32_t* block_indices,
+                   float* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
+                   int64_t D, int64_t T, int64_t m_off, int block_size, float scale,
+                   cudaStream_t st) {
+  const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
+  if (chk != NSA_OK) return chk;
+  if (m_off < 0 || m_off > ((int64_t(1) << 31) - 1024) - M) return NSA_ERR_SHAPE;
   if (B == 0 || M == 0) return NSA_OK;
   if (!Q || !O || !LSE) return NSA_ERR_NULL;
   if (N > 0 && (!K || !V)) return NSA_ERR_NULL;
@@ -515,14 +509,43 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t*
   p.H = H;
   p.G = G;
   p.T = T;
+  p.m_off = m_off;
   p.units = B * G * M;
   p.gi = (G % NSA_GROUP_INTERLEAVE == 0) ? NSA_GROUP_INTERLEAVE : 1;
   p.bs = block_size;
   p.nblk = static_cast<int>((N + block_size - 1) / block_size);
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   p.sl2 = sc * 1.4426950408889634f;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   return D == 64 ? launch_fwd<64>(p, K, V, B, st) : launch_fwd<128>(p, K, V, B, st);
+}
+
+}  // namespace nsa
+
+extern "C" {
+
+const char* nsa_status_string(int status) {
+  switch (status) {
+    case NSA_OK: return "ok";
+    case NSA_ERR_NULL: return "null pointer";
+    case NSA_ERR_SHAPE: return "invalid shape";
+    case NSA_ERR_BLOCK_SIZE: return "block_size must be 32 or 64";
+    case NSA_ERR_HEAD_DIM: return "head dim D must be 64 or 128";
+    case NSA_ERR_GROUPS: return "H must be 8 * G (8 query heads per KV group)";
+    case NSA_ERR_ALIGN: return "misaligned pointer";
+    case NSA_ERR_LAUNCH: return "CUDA launch failed";
+    case NSA_ERR_TIMEOUT: return "device wait timed out";
+    case NSA_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int nsa_version(void) { return 200; }
+
+int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* block_indices,
+                     float* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
+                     int64_t D, int64_t T, int block_size, float scale, void* stream) {
+  return nsa::launch_forward(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T, 0, block_size,
+                             scale, static_cast<cudaStream_t>(stream));
 }
 
 int nsa_sync_status(void* stream) {

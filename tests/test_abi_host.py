@@ -88,3 +88,39 @@ def test_misaligned(lib, which, addr):
 def test_empty_problem_is_a_no_op(lib, over):
     # returns before any CUDA call, so it runs without a GPU; pointers unused
     assert call(lib, q=None, k=None, v=None, idx=None, o=None, lse=None, **over) == 0
+
+
+def test_host_workspace_bytes(lib):
+    f = lib.nsa_sel_attn_fwd_host_workspace_bytes
+    n = f(1, 65536, 65536, 64, 8, 128, 16, 64, 8192)
+    kv = 2 * 65536 * 8 * 128 * 2
+    per_slot = 8192 * 64 * 128 * 2 + 8192 * 8 * 16 * 4 + 8192 * 64 * 128 * 4 + 64 * 8192 * 4
+    assert n == kv + 2 * per_slot
+    assert f(1, 65536, 65536, 64, 8, 128, 16, 64, 0) == n  # default chunk = M/8
+    assert f(1, 100, 100, 16, 2, 64, 4, 32, 1000) > 0       # chunk clipped to M
+    assert f(1, 100, 100, 16, 2, 64, 4, 48, 0) == -3
+    assert f(1, 100, 100, 12, 2, 64, 4, 32, 0) == -5
+
+
+def call_host(lib, q=FAKE, k=FAKE, v=FAKE, idx=FAKE, o=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 40,
+              chunk=0, **over):
+    a = dict(GOOD)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return lib.nsa_sel_attn_fwd_host(vp(q), vp(k), vp(v), vp(idx), vp(o), vp(lse), a["B"], a["M"],
+                                     a["N"], a["H"], a["G"], a["D"], a["T"], a["bs"], 0.0, vp(ws),
+                                     ws_bytes, chunk, None)
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "idx", "o", "lse"])
+def test_host_null_pointers(lib, which):
+    assert call_host(lib, **{which: None}) == -1
+
+
+def test_host_workspace_checks(lib):
+    need = lib.nsa_sel_attn_fwd_host_workspace_bytes(1, 128, 128, 16, 2, 128, 4, 64, 0)
+    assert call_host(lib, ws=None) == -9
+    assert call_host(lib, ws_bytes=need - 1) == -9
+    assert call_host(lib, ws=FAKE + 16, ws_bytes=need) == -6
+    assert call_host(lib, bs=16) == -3
+    assert call_host(lib, B=0, q=None, k=None, v=None, idx=None, o=None, lse=None, ws=None) == 0

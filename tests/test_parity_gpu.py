@@ -195,3 +195,31 @@ def test_bounded_wait_reports_timeout():
     O, L = run_cuda(q, k, v, idx, 32)
     check_all_rows(q, k, v, idx, 32, O, L, what="after timeout")
     assert _lib.sync_status() == 0
+
+
+@pytest.mark.parametrize("B,M,N,T,bs,chunk", [
+    (1, 1000, 1000, 5, 64, 0), (2, 777, 777, 4, 32, 100), (2, 600, 450, 6, 64, 64),
+    (1, 300, 520, 3, 32, 1000), (1, 256, 256, 0, 32, 64)])
+def test_host_entry_matches_device_entry(B, M, N, T, bs, chunk):
+    """Host buffers through the chunked pipeline == device entry, bit for bit."""
+    import torch
+
+    from nsa_block_selection_gb300 import _lib
+
+    q, k, v, idx = _small(B, M, N, 16, 2, 128, bs, max(T, 1), "first_two_local", seed=M + T)
+    if T == 0:
+        idx = np.zeros((B, M, 2, 0), np.int32)
+    else:
+        nb = -(-N // bs)
+        idx = np.where(idx < nb, idx, -1).astype(np.int32)  # M > N: ids past N are padding
+    O_d, L_d = run_cuda(q, k, v, idx, bs)
+    pin = [torch.from_numpy(x).pin_memory() for x in (q, k, v, idx)]
+    O_h, L_h = _lib.sel_attn_fwd_host(*pin, bs, chunk_m=chunk)
+    assert torch.equal(O_h, O_d.cpu()) and torch.equal(L_h, L_d.cpu())
+    # pageable host memory is also accepted
+    O_p, L_p = _lib.sel_attn_fwd_host(*[torch.from_numpy(x) for x in (q, k, v, idx)], bs,
+                                      out=torch.empty_like(O_h), lse=torch.empty_like(L_h),
+                                      chunk_m=chunk)
+    assert torch.equal(O_p, O_d.cpu()) and torch.equal(L_p, L_d.cpu())
+    if T:
+        check_all_rows(q, k, v, idx, bs, O_d, L_d, what="host entry")
