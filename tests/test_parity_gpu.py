@@ -206,7 +206,8 @@ def test_host_entry_matches_device_entry(B, M, N, T, bs, chunk):
 
     from nsa_block_selection_gb300 import _lib
 
-    q, k, v, idx = _small(B, M, N, 16, 2, 128, bs, max(T, 1), "first_two_local", seed=M + T)
+    rule = "first_two_local" if T >= 3 else "local"
+    q, k, v, idx = _small(B, M, N, 16, 2, 128, bs, max(T, 1), rule, seed=M + T)
     if T == 0:
         idx = np.zeros((B, M, 2, 0), np.int32)
     else:
