@@ -40,7 +40,7 @@ struct HostPlan {
 };
 
 int64_t default_chunk(int64_t M) {
-  int64_t c = (M + 7) / 8;
+  int64_t c = (M + 31) / 32;
   c = (c + 63) / 64 * 64;
   if (c < 64) c = 64;
   return c < M ? c : M;

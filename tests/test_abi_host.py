@@ -96,7 +96,8 @@ def test_host_workspace_bytes(lib):
     kv = 2 * 65536 * 8 * 128 * 2
     per_slot = 8192 * 64 * 128 * 2 + 8192 * 8 * 16 * 4 + 8192 * 64 * 128 * 4 + 64 * 8192 * 4
     assert n == kv + 2 * per_slot
-    assert f(1, 65536, 65536, 64, 8, 128, 16, 64, 0) == n  # default chunk = M/8
+    per_slot2 = 2048 * 64 * 128 * 2 + 2048 * 8 * 16 * 4 + 2048 * 64 * 128 * 4 + 64 * 2048 * 4
+    assert f(1, 65536, 65536, 64, 8, 128, 16, 64, 0) == kv + 2 * per_slot2  # default: M/32
     assert f(1, 100, 100, 16, 2, 64, 4, 32, 1000) > 0       # chunk clipped to M
     assert f(1, 100, 100, 16, 2, 64, 4, 48, 0) == -3
     assert f(1, 100, 100, 12, 2, 64, 4, 32, 0) == -5
