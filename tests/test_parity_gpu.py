@@ -224,3 +224,18 @@ def test_host_entry_matches_device_entry(B, M, N, T, bs, chunk):
     assert torch.equal(O_p, O_d.cpu()) and torch.equal(L_p, L_d.cpu())
     if T:
         check_all_rows(q, k, v, idx, bs, O_d, L_d, what="host entry")
+
+
+@pytest.mark.parametrize("M,bs,T,perm", [(2047, 32, 64, False), (1531, 64, 24, True),
+                                          (13, 32, 1, False)])
+def test_cta_shared_blocks(M, bs, T, perm):
+    """Consecutive queries list many common blocks (every causal block), more
+    than one CTA shares, in rows longer than 32 entries, with a partial last
+    CTA; optionally each row permuted."""
+    q, k, v, _ = _small(1, M, M, 8, 1, 128, bs, 1, "local", seed=M + bs)
+    idx = gen.dense_causal_indices(1, M, 1, -(-M // bs), bs)
+    idx = np.ascontiguousarray(idx[..., :T])  # the first T causal blocks
+    if perm:
+        idx = np.random.default_rng(1).permuted(idx, axis=-1).copy()
+    O, L = run_cuda(q, k, v, idx, bs)
+    check_all_rows(q, k, v, idx, bs, O, L, what=f"shared M{M} bs{bs} T{T}")
