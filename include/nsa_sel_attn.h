@@ -114,8 +114,8 @@ int64_t nsa_sel_attn_fwd_host_workspace_bytes(int64_t B, int64_t M, int64_t N, i
  *   workspace                device memory of at least
  *                            nsa_sel_attn_fwd_host_workspace_bytes(...) bytes,
  *                            256-byte aligned, owned by the caller
- *   chunk_m                  queries per pipeline chunk (<= 0: default,
- *                            about M/32 rounded up to a multiple of 64)
+ *   chunk_m                  queries per pipeline chunk, rounded up to a
+ *                            multiple of 64 (<= 0: default, about M/32)
  *   stream                   caller's stream; the kernels run on it
  *
  * The queries are processed in chunks of chunk_m positions. For each chunk

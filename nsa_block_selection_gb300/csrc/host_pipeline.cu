@@ -49,7 +49,10 @@ int64_t default_chunk(int64_t M) {
 HostPlan make_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
                    int64_t chunk_m) {
   HostPlan pl;
-  pl.chunk = chunk_m > 0 ? (chunk_m < M ? chunk_m : M) : default_chunk(M);
+  // chunks start at multiples of 64 positions, so a chunk's kernel groups its
+  // queries exactly as a single launch over all M would (bit-identical output)
+  const int64_t c64 = chunk_m > 0 ? (chunk_m + 63) / 64 * 64 : 0;
+  pl.chunk = c64 > 0 ? (c64 < M ? c64 : M) : default_chunk(M);
   if (pl.chunk < 1) pl.chunk = 1;
   pl.nchunks = M > 0 ? (M + pl.chunk - 1) / pl.chunk : 0;
   const size_t kv = align_up(static_cast<size_t>(B * N * G * D) * 2);

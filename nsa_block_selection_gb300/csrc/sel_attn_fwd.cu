@@ -6,15 +6,8 @@
 // block_indices[b, m, g, :] selects, causally masked; O [B,M,H,D] and the
 // natural-log LSE [B,H,M] are written.
 //
-// Kernel shape (a CTA takes WARPS consecutive queries of one (b, g); one warp
-// per query):
-//  * the CTA first finds the blocks every one of its rows selects; the tiles
-//    of those blocks that all its queries see in full are loaded once into
-//    CTA-shared slots (TMA, full/empty mbarriers, warp 0 produces) and used by
-//    every warp -- the selected sets of neighbouring queries overlap (e.g. the
-//    first and the most recent blocks), and those bytes then leave L2 once
-//    per CTA instead of once per query;
-//  * each warp walks its index row and streams its other keys in tiles of
+// Kernel shape (one warp per (b, m, g) work unit, warps independent):
+//  * the warp walks its index row and streams the selected keys in tiles of
 //    16 keys through two private shared-memory slots (K tile, V tile); lane 0
 //    fills a slot with TMA bulk-tensor copies (128-byte swizzled rows) that
 //    complete on the slot's mbarrier, and refills it with the next tile's K
@@ -51,10 +44,10 @@
 #include "sel_attn_fwd.cuh"
 
 #ifndef NSA_WARPS
-#define NSA_WARPS 8
+#define NSA_WARPS 4
 #endif
 #ifndef NSA_MIN_BLOCKS
-#define NSA_MIN_BLOCKS 2
+#define NSA_MIN_BLOCKS 4
 #endif
 
 __device__ unsigned int g_nsa_device_status = 0u;
@@ -100,29 +93,24 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64
 __device__ __forceinline__ void report_timeout() { atomicOr(&g_nsa_device_status, 1u); }
 
 // Warp-uniform walk over the 16-key tiles one index row selects, in the
-// order the row lists its blocks. Padding (< 0 or >= nblk), blocks that start
-// after the last visible key, tiles of a block that start after it, and the
-// leading tiles of CTA-shared blocks (processed from the shared slots) are
-// skipped.
+// order the row lists its blocks. Padding (< 0 or >= nblk) and blocks that
+// start after the last visible key are skipped, as are tiles of a block that
+// start after it.
 struct TileWalk {
   const int32_t* row;
   int T, nblk, bs, lastkey;
-  int sh_block;   // this lane's entry of the CTA's shared-block list (-1: none)
-  int sh_limit;   // tiles of a shared block ending at or before it are shared
   int win;        // start of the next 32-entry window
   unsigned mask;  // lanes of the current window still to visit
   int lane_val;   // this lane's entry of the current window
   int n0, nend;   // next tile start, end of the visible keys of the block
 
-  __device__ __forceinline__ void init(const int32_t* r, int T_, int nblk_, int bs_, int lastkey_,
-                                       int sh_block_, int sh_limit_) {
+  __device__ __forceinline__ void init(const int32_t* r, int T_, int nblk_, int bs_,
+                                       int lastkey_) {
     row = r;
     T = T_;
     nblk = nblk_;
     bs = bs_;
     lastkey = lastkey_;
-    sh_block = sh_block_;
-    sh_limit = sh_limit_;
     win = 0;
     mask = 0u;
     lane_val = -1;
@@ -146,10 +134,6 @@ struct TileWalk {
       const int t = __shfl_sync(kFull, lane_val, src);
       n0 = t * bs;
       nend = min(n0 + bs, lastkey + 1);
-      if (__ballot_sync(kFull, sh_block == t) != 0u) {
-        const int shared_tiles = min((sh_limit + 1 - n0) / kTileKeys, bs / kTileKeys);
-        n0 += shared_tiles * kTileKeys;
-      }
     }
     out = n0;
     n0 += kTileKeys;
@@ -157,21 +141,13 @@ struct TileWalk {
   }
 };
 
-constexpr int kMaxShared = 8;       // CTA-shared blocks at most
-constexpr int kMaxSharedTiles = 32; // their 16-key tiles (8 blocks x 64 keys)
-
 template <int D, int WARPS>
 struct Cfg {
   static constexpr int kBoxes = D / kBoxCols;            // TMA boxes per tile
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one K (or V) tile = one slot
-  static constexpr int kWarpBytes = 2 * kTileBytes;      // private slots: K, V
-  static constexpr int kSharedOffset = WARPS * kWarpBytes;  // shared slots: K0 V0 K1 V1
-  static constexpr int kBarOffset = kSharedOffset + 4 * kTileBytes;
-  // barriers: 2 per warp, 4 shared "full", 4 shared "empty"
-  static constexpr int kMetaOffset = kBarOffset + (2 * WARPS + 8) * 8;
-  // rows[WARPS][32], shared tile starts, shared blocks, counts
-  static constexpr int kMetaInts = WARPS * 32 + kMaxSharedTiles + kMaxShared + 2;
-  static constexpr int kSmemBytes = kMetaOffset + kMetaInts * 4 + 1024;  // + align slack
+  static constexpr int kWarpBytes = 2 * kTileBytes;      // slot 0: K, slot 1: V
+  static constexpr int kBarOffset = WARPS * kWarpBytes;
+  static constexpr int kSmemBytes = kBarOffset + WARPS * 2 * 8 + 1024;  // + align slack
   static constexpr int kSteps = D / 16;
 };
 
@@ -190,132 +166,29 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // CTA -> (b, g, WARPS consecutive queries); warp -> one query
-  const int64_t mtiles = (p.M + WARPS - 1) / WARPS;
-  const int64_t bg = blockIdx.x / mtiles;
-  const int64_t m0 = (blockIdx.x % mtiles) * WARPS;
+  const int64_t unit = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
+  if (unit >= p.units) return;
+  // unit -> (b, g, m), m fastest: the warps in flight share one group's K/V
+  const int64_t m = unit % p.M;
+  const int64_t bg = unit / p.M;
   const int g = static_cast<int>(bg % p.G);
   const int b = static_cast<int>(bg / p.G);
-  const int nw = static_cast<int>(p.M - m0 < WARPS ? p.M - m0 : WARPS);  // active warps
-  const bool active = warp < nw;
-  const int64_t m = m0 + warp;
   const int gid = lane >> 2;  // MMA group id (row within an 8-row slab)
   const int tig = lane & 3;   // thread in group
 
-  const uint32_t sbase = smem_u32(smem_raw);
-  const uint32_t base = (sbase + 1023u) & ~1023u;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t slots = base + warp * C::kWarpBytes;
-  const uint32_t shslots = base + C::kSharedOffset;
-  const uint32_t bars = base + C::kBarOffset + warp * 16;
-  const uint32_t shfull = base + C::kBarOffset + WARPS * 16;
-  const uint32_t shempty = shfull + 32;
-  int* rows = reinterpret_cast<int*>(smem_raw + (base - sbase) + C::kMetaOffset);
-  int* sh_tiles = rows + WARPS * 32;
-  int* sh_blocks = sh_tiles + kMaxSharedTiles;
-  int* sh_count = sh_blocks + kMaxShared;
+  const uint32_t bars = base + C::kBarOffset + warp * 2 * 8;
 
   if (lane == 0) {
-    if (warp == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        mbar_init(shfull + 8 * s, 1);
-        mbar_init(shempty + 8 * s, nw);
-      }
-    }
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
     mbar_init(bars, 1);
     mbar_init(bars + 8, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-
-  const int64_t mpos = m + p.m_off;  // the query's position in the key sequence
-  const int lastkey = static_cast<int>(mpos < p.N - 1 ? mpos : p.N - 1);
-  const int64_t mpos0 = m0 + p.m_off;  // the CTA's first (smallest) position
-  const int min_last = static_cast<int>(mpos0 < p.N - 1 ? mpos0 : p.N - 1);
-  const int32_t* irow = p.idx + ((b * p.M + (active ? m : m0)) * p.G + g) * p.T;
-  const uint64_t keep = l2_policy_evict_last();
-
-  auto tma_tile = [&](uint32_t dst, uint32_t bar, const CUtensorMap* tm, int n0) {
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, C::kTileBytes);
-#pragma unroll
-    for (int h = 0; h < C::kBoxes; ++h)
-      tma_load_4d(dst + h * kBoxBytes, tm, bar, h * kBoxCols, g, n0, b, keep);
-  };
-
-  // ---- blocks every query of the CTA selects: publish first index windows
-  {
-    int t = -1;
-    if (active && lane < p.T) {
-      t = __ldg(irow + lane);
-      if (!(t >= 0 && t < p.nblk && t * p.bs <= lastkey)) t = -1;
-    }
-    rows[warp * 32 + lane] = t;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // a block is shared if every active row lists it in its first window and
-    // at least its first tile is visible to the CTA's first query
-    const int cand = rows[lane];
-    bool ok = cand >= 0 && cand * p.bs + kTileKeys - 1 <= min_last;
-    for (int i = 0; i < lane; ++i) ok = ok && rows[i] != cand;  // first occurrence
-    for (int w = 1; w < nw; ++w) {
-      bool found = false;
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i) found = found || rows[w * 32 + i] == cand;
-      ok = ok && found;
-    }
-    const unsigned bal = __ballot_sync(kFull, ok);
-    const int pos = __popc(bal & ((1u << lane) - 1u));
-    const bool kept = ok && pos < kMaxShared;
-    int ntile = 0;
-    if (kept) {
-      sh_blocks[pos] = cand;
-      ntile = min((min_last + 1 - cand * p.bs) / kTileKeys, p.bs / kTileKeys);
-    }
-    int incl = ntile;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(kFull, incl, off);
-      if (lane >= off) incl += v;
-    }
-    for (int i = 0; i < ntile; ++i) sh_tiles[incl - ntile + i] = cand * p.bs + i * kTileKeys;
-    const int ntot = __shfl_sync(kFull, incl, 31);
-    if (lane == 0) {
-      sh_count[0] = min(__popc(bal), kMaxShared);
-      sh_count[1] = ntot;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      for (int j = 0; j < 2 && j < ntot; ++j) {
-        tma_tile(shslots + (2 * j) * C::kTileBytes, shfull + 8 * (2 * j), &tmK, sh_tiles[j]);
-        tma_tile(shslots + (2 * j + 1) * C::kTileBytes, shfull + 8 * (2 * j + 1), &tmV,
-                 sh_tiles[j]);
-      }
-    }
-  }
-  __syncthreads();
-  if (!active) return;
-  const int n_sh_tiles = sh_count[1];
-  const int sh_block = lane < sh_count[0] ? sh_blocks[lane] : -1;
-
-  // ---- private slots: slot 0 K tile, slot 1 V tile of the same 16 keys. The
-  // K tile of the next 16 keys is requested as soon as QK^T has read slot 0,
-  // its V tile as soon as PV has read slot 1; both barriers complete once per
-  // tile, so the phase parity is the private tile count's low bit.
-  const uint32_t sk = slots;
-  const uint32_t sv = slots + C::kTileBytes;
-  const uint32_t bar_k = bars, bar_v = bars + 8;
-  TileWalk walk;
-  walk.init(irow, static_cast<int>(p.T), p.nblk, p.bs, lastkey, sh_block, min_last);
-  int n_next = 0;
-  bool have = walk.next(n_next);
-  if (have && lane == 0) {
-    tma_tile(sk, bar_k, &tmK, n_next);
-    tma_tile(sv, bar_v, &tmV, n_next);
-  }
+  __syncwarp();
 
   const int64_t hbase = static_cast<int64_t>(g) * kHeadsPerGroup;
   // Q^T as the B operand of S^T = K Q^T: head gid, dims 16k + 2tig (+1, +8, +9).
@@ -329,6 +202,37 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     }
   }
 
+  const int64_t mpos = m + p.m_off;  // the query's position in the key sequence
+  const int lastkey = static_cast<int>(mpos < p.N - 1 ? mpos : p.N - 1);
+  const int32_t* irow = p.idx + ((b * p.M + m) * p.G + g) * p.T;
+  const uint64_t keep = l2_policy_evict_last();
+
+  // Two slots: slot 0 holds the K tile, slot 1 the V tile of the same 16
+  // keys. The K tile of the next 16 keys is requested as soon as QK^T has
+  // read slot 0, its V tile as soon as PV has read slot 1; both barriers
+  // complete once per tile, so the phase parity is the tile count's low bit.
+  const uint32_t sk = slots;
+  const uint32_t sv = slots + C::kTileBytes;
+  const uint32_t bar_k = bars, bar_v = bars + 8;
+  auto issue = [&](uint32_t dst, uint32_t bar, const CUtensorMap* tm, int n0) {
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+      for (int h = 0; h < C::kBoxes; ++h)
+        tma_load_4d(dst + h * kBoxBytes, tm, bar, h * kBoxCols, g, n0, b, keep);
+    }
+  };
+
+  TileWalk walk;
+  walk.init(irow, static_cast<int>(p.T), p.nblk, p.bs, lastkey);
+  int n_next = 0;
+  bool have = walk.next(n_next);
+  if (have) {
+    issue(sk, bar_k, &tmK, n_next);
+    issue(sv, bar_v, &tmV, n_next);
+  }
+
   float acc[C::kSteps][4];
 #pragma unroll
   for (int i = 0; i < C::kSteps; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -337,34 +241,46 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   float la = 0.f, lb = 0.f;                // this lane's share of the row sums
   const float sl2 = p.sl2;
 
-  // ldmatrix row offsets in a slot: K tiles (row-major A), V tiles (transposed A)
-  const uint32_t ka = (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
+  // ldmatrix row addresses: K tiles (row-major A), V tiles (transposed A).
+  const uint32_t ka = sk + (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
   const int ka_hi = lane >> 4;
-  const uint32_t va = (lane & 7) * 128 + ((lane & 16) ? 8 * 128 : 0);
+  const uint32_t va = sv + (lane & 7) * 128 + ((lane & 16) ? 8 * 128 : 0);
   const int va_hi = (lane >> 3) & 1;
   const int sw = lane & 7;  // key row & 7 for both
 
-  // x = (K_tile Q^T) * scale * log2(e): 16 keys x 8 heads, two MMA chains
-  auto qk = [&](uint32_t kslot, float (&x)[4]) {
+  uint32_t phase = 0;
+  int timed_out = 0;  // 1: K tile missing, 2: V tile missing
+  while (have) {
+    const int n0 = n_next;
+    if (!__all_sync(kFull, wait_phase(bar_k, phase, kWaitLimitNs))) {
+      timed_out = 1;
+      break;
+    }
+    // S^T (16 keys x 8 heads) = K_tile Q^T, raw dot products, two MMA chains
     float s[4] = {0.f, 0.f, 0.f, 0.f};
     float t[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < C::kSteps; k += 2) {
       uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-      ldsm_x4(kslot + ka + (k >> 2) * kBoxBytes + ((((k & 3) * 2 + ka_hi) ^ sw) << 4), a0, a1,
-              a2, a3);
-      ldsm_x4(kslot + ka + ((k + 1) >> 2) * kBoxBytes +
-                  (((((k + 1) & 3) * 2 + ka_hi) ^ sw) << 4),
-              b0, b1, b2, b3);
+      ldsm_x4(ka + (k >> 2) * kBoxBytes + ((((k & 3) * 2 + ka_hi) ^ sw) << 4), a0, a1, a2, a3);
+      ldsm_x4(ka + ((k + 1) >> 2) * kBoxBytes + (((((k + 1) & 3) * 2 + ka_hi) ^ sw) << 4), b0,
+              b1, b2, b3);
       mma_16816(s, a0, a1, a2, a3, qf[k][0], qf[k][1]);
       mma_16816(t, b0, b1, b2, b3, qf[k + 1][0], qf[k + 1][1]);
     }
+    __syncwarp();
+    have = walk.next(n_next);
+    if (have) issue(sk, bar_k, &tmK, n_next);  // slot 0 is free
+
+    float x[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) x[j] = (s[j] + t[j]) * sl2;
-  };
-  // online softmax per head (reference moves only on a large excess); returns
-  // P^T as the B operand: (keys 2tig.., head gid) from (key gid, heads 2tig..)
-  auto softmax = [&](const float (&x)[4], uint32_t& pb0, uint32_t& pb1) {
+    const bool edge = n0 + kTileKeys - 1 > lastkey;  // warp-uniform
+    if (edge) {
+      if (n0 + gid > lastkey) x[0] = x[1] = -INFINITY;
+      if (n0 + gid + 8 > lastkey) x[2] = x[3] = -INFINITY;
+    }
+    // online softmax per head: move the reference only on a large excess
     float mxa = fmaxf(x[0], x[2]);
     float mxb = fmaxf(x[1], x[3]);
     if (__any_sync(kFull, (mxa > m2a + kMaxSlack) || (mxb > m2b + kMaxSlack))) {
@@ -399,89 +315,12 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     const float p3 = ex2(x[3] + negb);
     la += p0 + p2;
     lb += p1 + p3;
-    pb0 = movmatrix_t(pack_half2(p0, p1));
-    pb1 = movmatrix_t(pack_half2(p2, p3));
-  };
-  // O^T (D x 8 heads) += V_tile^T P^T
-  auto pv = [&](uint32_t vslot, uint32_t pb0, uint32_t pb1) {
-#pragma unroll
-    for (int i = 0; i < C::kSteps; ++i) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(vslot + va + (i >> 2) * kBoxBytes + ((((i & 3) * 2 + va_hi) ^ sw) << 4), a0, a1,
-                a2, a3);
-      mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
-    }
-  };
+    // P^T as the B operand: (keys 2tig.., head gid) from (key gid, heads 2tig..)
+    const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
+    const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
 
-  int fail = 0;      // 0: ok; 1: private K missing; 2: private V missing; 3: shared
-  int sh_done = 0;   // shared tiles this warp has finished
-  int shk_issued = n_sh_tiles < 2 ? n_sh_tiles : 2;  // shared K / V tiles warp 0 has requested
-  int shv_issued = shk_issued;
-  uint32_t phase = 0;
-
-  // ---- tiles every query of the CTA sees in full, from the shared slots
-  for (int j = 0; j < n_sh_tiles; ++j) {
-    const int st = j & 1;
-    const uint32_t ph = (j >> 1) & 1;
-    const uint32_t kslot = shslots + (2 * st) * C::kTileBytes;
-    const uint32_t vslot = kslot + C::kTileBytes;
-    if (!__all_sync(kFull, wait_phase(shfull + 8 * (2 * st), ph, kWaitLimitNs))) {
-      fail = 3;
-      break;
-    }
-    float x[4];
-    qk(kslot, x);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(shempty + 8 * (2 * st));
-    if (warp == 0 && j + 2 < n_sh_tiles) {
-      if (!__all_sync(kFull, wait_phase(shempty + 8 * (2 * st), ph, kWaitLimitNs))) {
-        fail = 3;
-        break;
-      }
-      if (lane == 0) tma_tile(kslot, shfull + 8 * (2 * st), &tmK, sh_tiles[j + 2]);
-      shk_issued = j + 3;
-    }
-    uint32_t pb0, pb1;
-    softmax(x, pb0, pb1);
-    if (!__all_sync(kFull, wait_phase(shfull + 8 * (2 * st + 1), ph, kWaitLimitNs))) {
-      fail = 3;
-      break;
-    }
-    pv(vslot, pb0, pb1);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(shempty + 8 * (2 * st + 1));
-    if (warp == 0 && j + 2 < n_sh_tiles) {
-      if (!__all_sync(kFull, wait_phase(shempty + 8 * (2 * st + 1), ph, kWaitLimitNs))) {
-        fail = 3;
-        break;
-      }
-      if (lane == 0) tma_tile(vslot, shfull + 8 * (2 * st + 1), &tmV, sh_tiles[j + 2]);
-      shv_issued = j + 3;
-    }
-    sh_done = j + 1;
-  }
-
-  // ---- this query's other tiles, from the private slots
-  while (have && fail == 0) {
-    const int n0 = n_next;
-    if (!__all_sync(kFull, wait_phase(bar_k, phase, kWaitLimitNs))) {
-      fail = 1;
-      break;
-    }
-    float x[4];
-    qk(sk, x);
-    __syncwarp();
-    have = walk.next(n_next);
-    if (have && lane == 0) tma_tile(sk, bar_k, &tmK, n_next);  // slot 0 is free
-    const bool edge = n0 + kTileKeys - 1 > lastkey;  // warp-uniform
-    if (edge) {
-      if (n0 + gid > lastkey) x[0] = x[1] = -INFINITY;
-      if (n0 + gid + 8 > lastkey) x[2] = x[3] = -INFINITY;
-    }
-    uint32_t pb0, pb1;
-    softmax(x, pb0, pb1);
     if (!__all_sync(kFull, wait_phase(bar_v, phase, kWaitLimitNs))) {
-      fail = 2;
+      timed_out = 2;
       break;
     }
     if (edge) {
@@ -495,28 +334,22 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
       fence_proxy_async_smem();
       __syncwarp();
     }
-    pv(sv, pb0, pb1);
+    // O^T (D x 8 heads) += V_tile^T P^T
+#pragma unroll
+    for (int i = 0; i < C::kSteps; ++i) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(va + (i >> 2) * kBoxBytes + ((((i & 3) * 2 + va_hi) ^ sw) << 4), a0, a1, a2, a3);
+      mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
+    }
     __syncwarp();
-    if (have && lane == 0) tma_tile(sv, bar_v, &tmV, n_next);  // slot 1 is free
+    if (have) issue(sv, bar_v, &tmV, n_next);  // slot 1 is free
     phase ^= 1u;
   }
 
-  if (fail) {
-    // let the copies still in flight into this warp's (and, for warp 0, the
-    // shared) slots land before the CTA can exit
+  if (timed_out) {
+    // copies still in flight target this warp's slots: let them land first
     if (lane == 0) report_timeout();
-    if (fail == 3) {
-      if (have) {  // the first private tile was requested before the shared phase
-        wait_phase(bar_k, 0, kWaitLimitNs);
-        wait_phase(bar_v, 0, kWaitLimitNs);
-      }
-      if (warp == 0) {
-        for (int j = sh_done; j < shk_issued; ++j)
-          wait_phase(shfull + 8 * (2 * (j & 1)), (j >> 1) & 1, kWaitLimitNs);
-        for (int j = sh_done; j < shv_issued; ++j)
-          wait_phase(shfull + 8 * (2 * (j & 1) + 1), (j >> 1) & 1, kWaitLimitNs);
-      }
-    } else if (fail == 1) {
+    if (timed_out == 1) {
       wait_phase(bar_k, phase, kWaitLimitNs);
       wait_phase(bar_v, phase, kWaitLimitNs);
     } else {
@@ -526,7 +359,7 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     return;
   }
 
-  // ---- epilogue: finish the row sums, normalise, store O (fp32) and LSE
+  // epilogue: finish the row sums, normalise, store O (fp32) and LSE
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     la += __shfl_xor_sync(kFull, la, off);
@@ -619,7 +452,7 @@ static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return NSA_ERR_LAUNCH;
-  const int64_t blocks = (p.units / p.M) * ((p.M + W - 1) / W);
+  const int64_t blocks = (p.units + W - 1) / W;
   kern<<<static_cast<unsigned>(blocks), W * 32, C::kSmemBytes, stream>>>(p, tk, tv);
   return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
