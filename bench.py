@@ -185,6 +185,20 @@ def gpu_smi_id(dev):
         return vis.split(",")[dev.index or 0] if vis else (dev.index or 0)
 
 
+def reduce_over_ranks(t_ms, flops, nbytes, dist=None):
+    """Whole-job figures: the slowest rank's time, the work summed over ranks
+    (independent problems per rank; one scalar all-reduce, no data path)."""
+    if dist is None:
+        return float(t_ms), float(flops), float(nbytes)
+    import torch
+
+    tt = torch.tensor([float(t_ms)], dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    tot = torch.tensor([float(flops), float(nbytes)], dtype=torch.float64)
+    dist.all_reduce(tot)
+    return float(tt.item()), float(tot[0]), float(tot[1])
+
+
 def time_steps(fn, steps, warmup, flush, barrier):
     """Per-step CUDA-event times (ms) of fn() on the current stream; flush()
     runs before every step outside the events."""
@@ -341,16 +355,8 @@ def run_ours(args):
     clocks.start()
     times, wall = time_steps(step, args.steps, args.warmup, flush, barrier)
     clk = clocks.stop()
-    t_ms = statistics.mean(times)
-    if dist is not None:
-        tt = torch.tensor([t_ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
-        tot = torch.tensor([work["flops"], work["gathered_bytes"]], dtype=torch.float64)
-        dist.all_reduce(tot)
-        flops_all, bytes_all = float(tot[0]), float(tot[1])
-    else:
-        flops_all, bytes_all = float(work["flops"]), float(work["gathered_bytes"])
+    t_ms, flops_all, bytes_all = reduce_over_ranks(statistics.mean(times), work["flops"],
+                                                   work["gathered_bytes"], dist)
     tflops = flops_all / (t_ms * 1e-3) / 1e12
     gbs = bytes_all / (t_ms * 1e-3) / 1e9
 
@@ -461,12 +467,7 @@ def run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist):
     times, _ = time_steps(step, steps, 2, lambda: None, barrier)
     # host-memory bandwidth is shared with other tenants of the machine: the
     # median step is the figure, the mean is reported beside it
-    t = statistics.median(times)
-    if dist is not None:
-        tt = torch.tensor([t], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
-    flops = work["flops"] * (dist.get_world_size() if dist is not None else 1)
+    t, flops, _ = reduce_over_ranks(statistics.median(times), work["flops"], 0, dist)
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hi))
     d2h = sum(x.numel() * x.element_size() for x in (ho, hl))
     return {"value": flops / (t * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": t,
