@@ -67,6 +67,8 @@ __all__ = [
     "sel_attn_row",
     "sel_attn_rows",
     "sel_attn_fwd",
+    "softmax_grad_terms",
+    "sel_attn_bwd",
 ]
 
 
@@ -257,3 +259,53 @@ def sel_attn_fwd(Q, K, V, idx, block_size: int, scale: Optional[float] = None,
                 O[b, m, heads] = o
                 L[b, heads, m] = lse
     return O, L
+
+
+# --------------------------------------------------------------------------
+# Backward (gradients of the forward above)
+# --------------------------------------------------------------------------
+#
+# The issue's "Requirements" section returns LSE because the backward pass
+# needs it. The gradient of the definition above, per (b, m, g) row and head
+# h, with p_n = exp(s_n - LSE), dP_n = dO . v_n and
+# delta = sum_n p_n dP_n (= dO . O):
+#
+#   dV[n] += p_n dO                  dS_n = p_n (dP_n - delta)
+#   dQ    += scale sum_n dS_n k_n    dK[n] += scale dS_n q
+#
+# summed over every (m, h) whose visible set contains key n.
+
+def softmax_grad_terms(s: np.ndarray, lse: np.ndarray, v: np.ndarray, do: np.ndarray):
+    """p, dS for one row: s [H', n], lse [H'], v [n, D], do [H', D]."""
+    p = np.exp(s - lse[:, None])
+    dp = do @ v.T
+    delta = (p * dp).sum(axis=1)
+    return p, p * (dp - delta[:, None])
+
+
+def sel_attn_bwd(Q, K, V, idx, dO, block_size: int, scale: Optional[float] = None):
+    """Gradients dQ [B,M,H,D], dK [B,N,G,D], dV [B,N,G,D] (float64) of the
+    forward for the upstream gradient dO [B,M,H,D] (LSE is recomputed)."""
+    B, M, H, D = Q.shape
+    N, G = K.shape[1], K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dQ = np.zeros((B, M, H, D))
+    dK = np.zeros((B, N, G, D))
+    dV = np.zeros((B, N, G, D))
+    for b in range(B):
+        for m in range(M):
+            for g in range(G):
+                heads, q, Kg, Vg = _row_operands(Q, K, V, b, m, g, H, G)
+                n = visible_keys(idx[b, m, g], m, N, block_size)
+                if n.size == 0:
+                    continue
+                k = np.asarray(Kg[n], dtype=np.float64)
+                v = np.asarray(Vg[n], dtype=np.float64)
+                do = np.asarray(dO[b, m, heads], dtype=np.float64)
+                s = scores(q, k, scale)
+                p, ds = softmax_grad_terms(s, logsumexp_rows(s), v, do)
+                dQ[b, m, heads] = scale * (ds @ k)
+                dK[b, n, g] += scale * (ds.T @ q)
+                dV[b, n, g] += p.T @ do
+    return dQ, dK, dV

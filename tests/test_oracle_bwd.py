@@ -1,0 +1,66 @@
+"""The oracle's backward against its pins, and planted mistakes (no GPU)."""
+
+import numpy as np
+import pytest
+
+import oracle.sel_attn as S
+from _pins_bwd import BPINS
+
+
+@pytest.mark.parametrize("pin", BPINS, ids=[p.__name__ for p in BPINS])
+def test_bwd_pin(pin):
+    pin(S)
+
+
+_orig_terms = S.softmax_grad_terms
+
+
+def _no_delta(s, lse, v, do):
+    p = np.exp(s - lse[:, None])
+    return p, p * (do @ v.T)
+
+
+def _delta_sign(s, lse, v, do):
+    p = np.exp(s - lse[:, None])
+    dp = do @ v.T
+    return p, p * (dp + (p * dp).sum(axis=1)[:, None])
+
+
+def _p_unnormalised(s, lse, v, do):
+    p, ds = _orig_terms(s, lse, v, do)
+    return np.exp(s), ds
+
+
+def _dp_transposed_values(s, lse, v, do):
+    return _orig_terms(s, lse, v[::-1], do)
+
+
+def _ds_missing_p(s, lse, v, do):
+    p = np.exp(s - lse[:, None])
+    dp = do @ v.T
+    return p, dp - (p * dp).sum(axis=1)[:, None]
+
+
+BMUTANTS = {
+    "delta_dropped": ("softmax_grad_terms", _no_delta),
+    "delta_sign": ("softmax_grad_terms", _delta_sign),
+    "p_unnormalised": ("softmax_grad_terms", _p_unnormalised),
+    "dp_values_misaligned": ("softmax_grad_terms", _dp_transposed_values),
+    "ds_without_p": ("softmax_grad_terms", _ds_missing_p),
+    "causal_strict": ("causal_visible", lambda n, m: n < m),
+    "scale_dropped": ("scores", lambda q, k, scale: q @ k.T),
+    "group_is_h_mod_G": ("head_group", lambda h, H, G: h % G),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BMUTANTS))
+def test_bwd_mutant_is_caught(name, monkeypatch):
+    attr, fn = BMUTANTS[name]
+    monkeypatch.setattr(S, attr, fn)
+    failed = []
+    for pin in BPINS:
+        try:
+            pin(S)
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            failed.append(pin.__name__)
+    assert failed, f"backward mutant {name} passed every pin"
