@@ -140,6 +140,45 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
                           int64_t workspace_bytes, int64_t chunk_m, void* stream);
 
 /*
+ * nsa_sel_attn_bwd_workspace_bytes -- device workspace nsa_sel_attn_bwd
+ * needs: delta [B,H,M] fp32, the per-(b, g, block) query lists (at most
+ * B*M*G*T entries) and their counts and offsets. Negative nsa_status for
+ * invalid sizes (B*M*G*T must stay below 2^31). Pure host arithmetic.
+ */
+int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_t H,
+                                         int64_t G, int64_t D, int64_t T, int block_size);
+
+/*
+ * nsa_sel_attn_bwd -- gradients of nsa_sel_attn_fwd (the section
+ * "Requirements" returns LSE for this pass).
+ *
+ *   Q, K, V, block_indices   as for the forward (device)
+ *   O, LSE                   the forward's outputs (device, fp32)
+ *   dO                       upstream gradient of O, fp32 [B, M, H, D]
+ *   dQ                       fp32 [B, M, H, D]   (written)
+ *   dK, dV                   fp32 [B, N, G, D]   (written; zeroed first)
+ *   workspace                device memory of at least
+ *                            nsa_sel_attn_bwd_workspace_bytes() bytes,
+ *                            256-byte aligned
+ *
+ * With p = exp(scale q.k - LSE), dP = dO.v and delta = dO.O per row and head:
+ * dS = p (dP - delta), dQ = scale sum dS k, dK += scale dS q, dV += p dO over
+ * every visible (query, head, key). Three stages on `stream`: a query-major
+ * kernel for dQ (and delta); a transposed index listing, per (b, g, block),
+ * the queries that selected it; a key-major kernel that loads each block
+ * once per chunk of its list and adds its dK / dV partial sums with fp32
+ * atomics. dQ is deterministic; dK / dV sum in an order set by atomics
+ * (equal within rounding from run to run). Asynchronous, allocates nothing;
+ * errors as nsa_sel_attn_fwd plus NSA_ERR_WORKSPACE. Pointers must be
+ * 16-byte aligned (LSE and block_indices 4-byte).
+ */
+int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V,
+                     const int32_t* block_indices, const float* O, const float* LSE,
+                     const float* dO, float* dQ, float* dK, float* dV, int64_t B, int64_t M,
+                     int64_t N, int64_t H, int64_t G, int64_t D, int64_t T, int block_size,
+                     float scale, void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
  * nsa_sync_status -- wait for `stream`, then read and clear the device status
  * word of the current device.
  *

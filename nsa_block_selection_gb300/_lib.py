@@ -20,7 +20,7 @@ NSA_OK = 0
 
 EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sync_status",
            "nsa_selftest_wait_timeout", "nsa_sel_attn_fwd_host_workspace_bytes",
-           "nsa_sel_attn_fwd_host")
+           "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd")
 
 _lib = None
 
@@ -57,6 +57,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_fwd_host_workspace_bytes.restype = i64
     lib.nsa_sel_attn_fwd_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64, i64,
                                                           c_int, i64]
+    lib.nsa_sel_attn_bwd_workspace_bytes.restype = i64
+    lib.nsa_sel_attn_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64, i64, c_int]
+    lib.nsa_sel_attn_bwd.restype = c_int
+    lib.nsa_sel_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
+                                     i64, i64, i64, c_int, ctypes.c_float, vp, i64, vp]
     lib.nsa_sel_attn_fwd_host.restype = c_int
     lib.nsa_sel_attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                           i64, c_int, ctypes.c_float, vp, i64, i64, vp]
@@ -174,6 +179,50 @@ def sel_attn_fwd_host(q, k, v, block_indices, block_size: int, scale: Optional[f
     if sync:
         stream.synchronize()
     return out, lse
+
+
+def bwd_workspace_bytes(B, M, N, H, G, D, T, block_size) -> int:
+    n = load().nsa_sel_attn_bwd_workspace_bytes(B, M, N, H, G, D, T, int(block_size))
+    if n < 0:
+        raise NsaError(int(n), "nsa_sel_attn_bwd_workspace_bytes")
+    return int(n)
+
+
+def sel_attn_bwd(q, k, v, block_indices, o, lse, do, block_size: int,
+                 scale: Optional[float] = None, dq=None, dk=None, dv=None, workspace=None,
+                 stream=None):
+    """Gradients of :func:`sel_attn_fwd`: returns (dQ, dK, dV) fp32 CUDA tensors.
+
+    ``o`` and ``lse`` are the forward's outputs, ``do`` the fp32 upstream
+    gradient [B, M, H, D]. ``workspace`` (CUDA uint8) is allocated when
+    omitted.
+    """
+    import torch
+
+    lib = load()
+    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=True)
+    for name, t, shape in (("o", o, (B, M, H, D)), ("lse", lse, (B, H, M)),
+                           ("do", do, (B, M, H, D))):
+        if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous() \
+                or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of shape {shape}")
+    dev = q.device
+    dq = torch.empty((B, M, H, D), dtype=torch.float32, device=dev) if dq is None else dq
+    dk = torch.empty((B, N, G, D), dtype=torch.float32, device=dev) if dk is None else dk
+    dv = torch.empty((B, N, G, D), dtype=torch.float32, device=dev) if dv is None else dv
+    need = bwd_workspace_bytes(B, M, N, H, G, D, T, block_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.nsa_sel_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(o), _ptr(lse),
+                              _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, M, N, H, G, D, T,
+                              int(block_size), sc, workspace.data_ptr(), workspace.numel(),
+                              ctypes.c_void_p(stream.cuda_stream))
+    if st != NSA_OK:
+        raise NsaError(st, "nsa_sel_attn_bwd")
+    return dq, dk, dv
 
 
 def sync_status(stream=None) -> int:

@@ -1,0 +1,712 @@
+// NSA selection-attention backward for sm_103a: dQ, dK, dV from dO.
+//
+// The forward ("[wave] NSA: selection attention forward kernel", sections
+// "Operation" / "Algorithm") returns LSE because the backward needs it
+// (section "Requirements"). Per (b, m, g) row and head h, over its visible
+// keys n, with p_n = exp(scale q.k_n - LSE), dP_n = dO . v_n and
+// delta = dO . O:
+//   dS_n = p_n (dP_n - delta);  dQ = scale sum_n dS_n k_n;
+//   dK[n] += scale dS_n q;      dV[n] += p_n dO.
+//
+// Three stages, all on the caller's stream:
+//  1. query-major kernel (one warp per (b, m, g), same TMA tile gather as the
+//     forward): recomputes S^T = K Q^T, P, dP^T = V dO^T and dS on the tensor
+//     cores (mma.sync m16n8k16, fp16 operands, fp32 accumulate) and
+//     accumulates dQ^T += K^T dS^T in registers; it also writes delta.
+//  2. transposed index: for every (b, g, block) the list of queries whose row
+//     selects it (count with atomics, one-CTA scan, fill with atomics). The
+//     order inside a list follows atomic order.
+//  3. key-major kernel: one CTA per chunk of <= kQueriesPerChunk queries of a
+//     list. Its bs/16 warps each own 16 keys of the block (loaded once by TMA)
+//     and, for each query of the chunk, recompute S^T, P, dP^T, dS and
+//     accumulate dV += P^T dO and dK += dS^T Q with mma.sync m16n8k8 (the C
+//     layout of S^T is already the A layout of that MMA); the partial sums
+//     are added into dK / dV (fp32, zeroed first) with float2 atomics.
+// Masked keys get exact zero weights by select (never multiplied through),
+// and K/V rows past a query's last visible key are zeroed in shared memory
+// before they enter a product in stage 1.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "nsa_sel_attn.h"
+#include "ptx.cuh"
+#include "sel_attn_fwd.cuh"
+
+namespace nsa {
+
+constexpr int kQueriesPerChunk = 256;
+
+struct BwdProblem {
+  const __half* Q;
+  const int32_t* idx;
+  const float* O;
+  const float* LSE;
+  const float* dO;
+  float* dQ;
+  float* dK;
+  float* dV;
+  float* delta;        // [B, H, M]
+  const int* offs;     // [L + 1] list starts (L = B * G * nblk)
+  const int* choffs;   // [L + 1] chunk starts
+  const int* lists;    // query ids, list by list
+  int64_t B, M, N, H, G, T;
+  int64_t units;       // B * G * M
+  int bs, nblk, L;
+  float sl2;           // scale * log2(e)
+  float scale;
+};
+
+// fp32 pair -> fp16x2 (round to nearest even)
+__device__ __forceinline__ uint32_t ld_f32x2_as_half2(const float* p) {
+  const float2 v = __ldg(reinterpret_cast<const float2*>(p));
+  return pack_half2(v.x, v.y);
+}
+
+// ---------------------------------------------------------------------------
+// Stage 1: dQ (query-major)
+// ---------------------------------------------------------------------------
+
+template <int D, int WARPS>
+struct DqCfg {
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kWarpBytes = 3 * kTileBytes;  // K slot 0, K slot 1, V slot
+  static constexpr int kBarOffset = WARPS * kWarpBytes;
+  static constexpr int kSmemBytes = kBarOffset + WARPS * 3 * 8 + 1024;
+  static constexpr int kSteps = D / 16;
+};
+
+template <int D, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 3)
+    sel_attn_bwd_dq_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV) {
+  using C = DqCfg<D, WARPS>;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
+  if (unit >= p.units) return;
+  const int64_t m = unit % p.M;
+  const int64_t bg = unit / p.M;
+  const int g = static_cast<int>(bg % p.G);
+  const int b = static_cast<int>(bg / p.G);
+  const int gid = lane >> 2;
+  const int tig = lane & 3;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t slots = base + warp * C::kWarpBytes;  // K0, K1, V
+  const uint32_t bars = base + C::kBarOffset + warp * 24;
+  if (lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    mbar_init(bars, 1);
+    mbar_init(bars + 8, 1);
+    mbar_init(bars + 16, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+
+  const int64_t hbase = static_cast<int64_t>(g) * kHeadsPerGroup;
+  const int64_t row = (b * p.M + m) * p.H + hbase;  // first head of the group
+  // Q^T and dO^T as B operands (head gid, dims 16k + 2tig (+1, +8, +9));
+  // delta of head gid from the same dO elements against O (fp32)
+  uint32_t qf[C::kSteps][2], df[C::kSteps][2];
+  float dpart = 0.f;
+  {
+    const __half* q = p.Q + (row + gid) * D + 2 * tig;
+    const float* dob = p.dO + (row + gid) * D + 2 * tig;
+    const float* ob = p.O + (row + gid) * D + 2 * tig;
+#pragma unroll
+    for (int k = 0; k < C::kSteps; ++k) {
+      qf[k][0] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k));
+      qf[k][1] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k + 8));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float2 d2 = __ldg(reinterpret_cast<const float2*>(dob + 16 * k + 8 * h));
+        const float2 o2 = __ldg(reinterpret_cast<const float2*>(ob + 16 * k + 8 * h));
+        df[k][h] = pack_half2(d2.x, d2.y);
+        dpart = fmaf(d2.x, o2.x, fmaf(d2.y, o2.y, dpart));
+      }
+    }
+  }
+  dpart += __shfl_xor_sync(kFull, dpart, 1);
+  dpart += __shfl_xor_sync(kFull, dpart, 2);  // delta of head gid
+  if (tig == 0) p.delta[(b * p.H + hbase + gid) * p.M + m] = dpart;
+  const float dla = __shfl_sync(kFull, dpart, (2 * tig) * 4);      // head 2tig
+  const float dlb = __shfl_sync(kFull, dpart, (2 * tig + 1) * 4);  // head 2tig+1
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float lsa = p.LSE[(b * p.H + hbase + 2 * tig) * p.M + m] * kLog2e;
+  const float lsb = p.LSE[(b * p.H + hbase + 2 * tig + 1) * p.M + m] * kLog2e;
+
+  const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
+  const int32_t* irow = p.idx + ((b * p.M + m) * p.G + g) * p.T;
+  const uint64_t keep = l2_policy_evict_last();
+  auto tma_tile = [&](uint32_t dst, uint32_t bar, const CUtensorMap* tm, int n0) {
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+    for (int h = 0; h < C::kBoxes; ++h)
+      tma_load_4d(dst + h * kBoxBytes, tm, bar, h * kBoxCols, g, n0, b, keep);
+  };
+  const uint32_t sv = slots + 2 * C::kTileBytes;
+  const uint32_t bar_v = bars + 16;
+
+  TileWalk walk;
+  walk.init(irow, static_cast<int>(p.T), p.nblk, p.bs, lastkey);
+  int nA = 0, nB = 0;
+  bool hA = walk.next(nA);
+  bool hB = hA && walk.next(nB);
+  if (lane == 0) {
+    if (hA) {
+      tma_tile(slots, bars, &tmK, nA);
+      tma_tile(sv, bar_v, &tmV, nA);
+    }
+    if (hB) tma_tile(slots + C::kTileBytes, bars + 8, &tmK, nB);
+  }
+
+  float acc[C::kSteps][4];
+#pragma unroll
+  for (int i = 0; i < C::kSteps; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  const float sl2 = p.sl2;
+  const uint32_t ka = (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
+  const int ka_hi = lane >> 4;
+  const uint32_t ta = (lane & 7) * 128 + ((lane & 16) ? 8 * 128 : 0);
+  const int ta_hi = (lane >> 3) & 1;
+  const int sw = lane & 7;
+
+  // x^T (16 keys x 8 heads) = X_tile B with B given as fragments (two chains)
+  auto rows_times = [&](uint32_t slot, const uint32_t(&bf)[C::kSteps][2], float (&x)[4]) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < C::kSteps; k += 2) {
+      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+      ldsm_x4(slot + ka + (k >> 2) * kBoxBytes + ((((k & 3) * 2 + ka_hi) ^ sw) << 4), a0, a1,
+              a2, a3);
+      ldsm_x4(slot + ka + ((k + 1) >> 2) * kBoxBytes +
+                  (((((k + 1) & 3) * 2 + ka_hi) ^ sw) << 4),
+              b0, b1, b2, b3);
+      mma_16816(s, a0, a1, a2, a3, bf[k][0], bf[k][1]);
+      mma_16816(t, b0, b1, b2, b3, bf[k + 1][0], bf[k + 1][1]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = s[j] + t[j];
+  };
+
+  int i = 0;
+  int fail = 0;  // 1: K of tile i missing, 2: V of tile i missing
+  while (hA) {
+    const int n0 = nA;
+    const int ks = i & 1;
+    const uint32_t sk = slots + ks * C::kTileBytes;
+    if (!__all_sync(kFull, wait_phase(bars + 8 * ks, (i >> 1) & 1, kWaitLimitNs))) {
+      fail = 1;
+      break;
+    }
+    float x[4];
+    rows_times(sk, qf, x);
+    if (!__all_sync(kFull, wait_phase(bar_v, i & 1, kWaitLimitNs))) {
+      fail = 2;
+      break;
+    }
+    const bool edge = n0 + kTileKeys - 1 > lastkey;
+    if (edge) {
+      // zero K and V rows past the last visible key: both enter products
+#pragma unroll
+      for (int e = lane; e < 2 * kTileKeys * (D / 8); e += 32) {
+        const int r = (e >> 1) / (D / 8), c = (e >> 1) % (D / 8);
+        if (n0 + r > lastkey)
+          st_shared_zero16(((e & 1) ? sv : sk) + (c >> 3) * kBoxBytes + r * 128 +
+                           (((c & 7) ^ (r & 7)) << 4));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (n0 + gid > lastkey) x[0] = x[1] = -INFINITY;
+      if (n0 + gid + 8 > lastkey) x[2] = x[3] = -INFINITY;
+    }
+    float dp[4];
+    rows_times(sv, df, dp);
+    __syncwarp();
+    if (hB && lane == 0) tma_tile(sv, bar_v, &tmV, nB);  // V slot is free
+    // P = exp(s*scale - LSE), dS = P (dP - delta); masked keys: exactly 0
+    float ds[4];
+    ds[0] = x[0] == -INFINITY ? 0.f : ex2(fmaf(x[0], sl2, -lsa)) * (dp[0] - dla);
+    ds[1] = x[1] == -INFINITY ? 0.f : ex2(fmaf(x[1], sl2, -lsb)) * (dp[1] - dlb);
+    ds[2] = x[2] == -INFINITY ? 0.f : ex2(fmaf(x[2], sl2, -lsa)) * (dp[2] - dla);
+    ds[3] = x[3] == -INFINITY ? 0.f : ex2(fmaf(x[3], sl2, -lsb)) * (dp[3] - dlb);
+    const uint32_t db0 = movmatrix_t(pack_half2(ds[0], ds[1]));
+    const uint32_t db1 = movmatrix_t(pack_half2(ds[2], ds[3]));
+    // dQ^T (D x 8 heads) += K_tile^T dS^T
+#pragma unroll
+    for (int d = 0; d < C::kSteps; ++d) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(sk + ta + (d >> 2) * kBoxBytes + ((((d & 3) * 2 + ta_hi) ^ sw) << 4), a0, a1, a2,
+                a3);
+      mma_16816(acc[d], a0, a1, a2, a3, db0, db1);
+    }
+    __syncwarp();
+    int nC = 0;
+    const bool hC = hB && walk.next(nC);
+    if (hC && lane == 0) tma_tile(sk, bars + 8 * ks, &tmK, nC);  // this K slot is free
+    nA = nB;
+    hA = hB;
+    nB = nC;
+    hB = hC;
+    ++i;
+  }
+  if (fail) {
+    if (lane == 0) report_timeout();
+    if (fail == 1) wait_phase(bars + 8 * (i & 1), (i >> 1) & 1, kWaitLimitNs);
+    wait_phase(bar_v, i & 1, kWaitLimitNs);
+    if (hB) wait_phase(bars + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1, kWaitLimitNs);
+    return;
+  }
+  float* o = p.dQ + (row + 2 * tig) * D + gid;
+#pragma unroll
+  for (int d = 0; d < C::kSteps; ++d) {
+    o[16 * d] = acc[d][0] * p.scale;
+    o[D + 16 * d] = acc[d][1] * p.scale;
+    o[16 * d + 8] = acc[d][2] * p.scale;
+    o[D + 16 * d + 8] = acc[d][3] * p.scale;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 2: transposed index (who selected each (b, g, block))
+// ---------------------------------------------------------------------------
+
+// Entry e of block_indices -> the list it belongs to, or -1 (padding, out of
+// range, or wholly in the query's future).
+__device__ __forceinline__ int entry_list(const BwdProblem& p, int64_t e, int64_t* m_out) {
+  const int64_t r = e / p.T;  // (b * M + m) * G + g
+  const int g = static_cast<int>(r % p.G);
+  const int64_t bm = r / p.G;
+  const int64_t m = bm % p.M;
+  const int64_t b = bm / p.M;
+  const int t = __ldg(p.idx + e);
+  const int64_t lastkey = m < p.N - 1 ? m : p.N - 1;
+  *m_out = m;
+  if (t < 0 || t >= p.nblk || static_cast<int64_t>(t) * p.bs > lastkey) return -1;
+  return static_cast<int>((b * p.G + g) * p.nblk + t);
+}
+
+__global__ void csr_count_kernel(const BwdProblem p, int* count) {
+  const int64_t total = p.B * p.M * p.G * p.T;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int64_t m;
+    const int l = entry_list(p, e, &m);
+    if (l >= 0) atomicAdd(count + l, 1);
+  }
+}
+
+// Exclusive scans of count[] and of ceil(count / chunk) over L lists, one CTA
+// of 1024 threads walking the array in tiles; offs[L] and choffs[L] get totals.
+__global__ void __launch_bounds__(1024) csr_scan_kernel(const int* count, int* offs, int* choffs,
+                                                        int L, int chunk) {
+  __shared__ int wsum[2][32];
+  __shared__ int carry[2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry[0] = carry[1] = 0;
+  __syncthreads();
+  for (int base = 0; base < L; base += 1024) {
+    const int i = base + threadIdx.x;
+    const int c = i < L ? count[i] : 0;
+    const int k = (c + chunk - 1) / chunk;
+    int sc = c, sk = k;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(kFull, sc, off), bb = __shfl_up_sync(kFull, sk, off);
+      if (lane >= off) {
+        sc += a;
+        sk += bb;
+      }
+    }
+    if (lane == 31) {
+      wsum[0][warp] = sc;
+      wsum[1][warp] = sk;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int a = wsum[0][lane], bb = wsum[1][lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int x = __shfl_up_sync(kFull, a, off), y = __shfl_up_sync(kFull, bb, off);
+        if (lane >= off) {
+          a += x;
+          bb += y;
+        }
+      }
+      wsum[0][lane] = a;
+      wsum[1][lane] = bb;
+    }
+    __syncthreads();
+    const int pc = carry[0] + (warp ? wsum[0][warp - 1] : 0) + sc - c;
+    const int pk = carry[1] + (warp ? wsum[1][warp - 1] : 0) + sk - k;
+    if (i < L) {
+      offs[i] = pc;
+      choffs[i] = pk;
+    }
+    __syncthreads();
+    if (threadIdx.x == 1023) {
+      carry[0] = pc + c;
+      carry[1] = pk + k;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    offs[L] = carry[0];
+    choffs[L] = carry[1];
+  }
+}
+
+__global__ void csr_fill_kernel(const BwdProblem p, int* cursor, int* lists) {
+  const int64_t total = p.B * p.M * p.G * p.T;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int64_t m;
+    const int l = entry_list(p, e, &m);
+    if (l >= 0) lists[p.offs[l] + atomicAdd(cursor + l, 1)] = static_cast<int>(m);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 3: dK, dV (key-major)
+// ---------------------------------------------------------------------------
+
+template <int D, int KT>
+struct DkvCfg {
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr int kBoxBytesBlk = KT * kTileKeys * 128;  // one box of bs rows
+  static constexpr int kBlockBytes = kBoxes * kBoxBytesBlk;  // K (or V) block
+  static constexpr int kSmemBytes = 2 * kBlockBytes + 8 + 1024;
+  static constexpr int kSteps = D / 16;
+  static constexpr int kNTiles = D / 8;
+};
+
+template <int D, int KT>
+__global__ void __launch_bounds__(KT * 32)
+    sel_attn_bwd_dkv_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV) {
+  using C = DkvCfg<D, KT>;
+  extern __shared__ uint8_t smem_raw[];
+  const int c = blockIdx.x;
+  if (c >= p.choffs[p.L]) return;
+  // list l with choffs[l] <= c < choffs[l + 1]
+  int lo = 0, hi = p.L;  // invariant: choffs[lo] <= c < choffs[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.choffs[mid] <= c)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int l = lo;
+  const int q0 = p.offs[l] + (c - p.choffs[l]) * kQueriesPerChunk;
+  const int q1 = min(q0 + kQueriesPerChunk, p.offs[l + 1]);
+  const int t = l % p.nblk;
+  const int bg = l / p.nblk;
+  const int g = bg % static_cast<int>(p.G);
+  const int b = bg / static_cast<int>(p.G);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2;
+  const int tig = lane & 3;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sK = base, sV = base + C::kBlockBytes;
+  const uint32_t bar = base + 2 * C::kBlockBytes;
+  const int n_blk = t * p.bs;  // first key of the block
+  if (threadIdx.x == 0) {
+    const uint64_t keep = l2_policy_evict_last();
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, 2 * C::kBlockBytes);
+#pragma unroll
+    for (int h = 0; h < C::kBoxes; ++h) {
+      tma_load_4d(sK + h * C::kBoxBytesBlk, &tmK, bar, h * kBoxCols, g, n_blk, b, keep);
+      tma_load_4d(sV + h * C::kBoxBytesBlk, &tmV, bar, h * kBoxCols, g, n_blk, b, keep);
+    }
+  }
+  __syncthreads();
+  if (!__all_sync(kFull, wait_phase(bar, 0, kWaitLimitNs))) {
+    // the load never landed; wait (bounded) once more so it cannot land later
+    if (lane == 0 && warp == 0) report_timeout();
+    wait_phase(bar, 0, kWaitLimitNs);
+    return;
+  }
+
+  const int nw0 = n_blk + warp * kTileKeys;  // this warp's first key
+  const uint32_t wK = sK + warp * kTileKeys * 128, wV = sV + warp * kTileKeys * 128;
+  const uint32_t ka = (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
+  const int ka_hi = lane >> 4;
+  const int sw = lane & 7;
+  const float sl2 = p.sl2;
+  constexpr float kLog2e = 1.4426950408889634f;
+
+  float dk[C::kNTiles][4], dv[C::kNTiles][4];
+#pragma unroll
+  for (int j = 0; j < C::kNTiles; ++j)
+    dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = dv[j][0] = dv[j][1] = dv[j][2] = dv[j][3] = 0.f;
+
+  for (int qi = q0; qi < q1; ++qi) {
+    const int m = __ldg(p.lists + qi);
+    const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
+    if (nw0 > lastkey) continue;  // all of this warp's keys are in the future
+    const int64_t hbase = static_cast<int64_t>(g) * kHeadsPerGroup;
+    const int64_t row = (b * p.M + m) * p.H + hbase;
+    uint32_t qf[C::kSteps][2], df[C::kSteps][2];
+    {
+      const __half* q = p.Q + (row + gid) * D + 2 * tig;
+      const float* dob = p.dO + (row + gid) * D + 2 * tig;
+#pragma unroll
+      for (int k = 0; k < C::kSteps; ++k) {
+        qf[k][0] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k));
+        qf[k][1] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k + 8));
+        df[k][0] = ld_f32x2_as_half2(dob + 16 * k);
+        df[k][1] = ld_f32x2_as_half2(dob + 16 * k + 8);
+      }
+    }
+    const float lsa = __ldg(p.LSE + (b * p.H + hbase + 2 * tig) * p.M + m) * kLog2e;
+    const float lsb = __ldg(p.LSE + (b * p.H + hbase + 2 * tig + 1) * p.M + m) * kLog2e;
+    const float dla = __ldg(p.delta + (b * p.H + hbase + 2 * tig) * p.M + m);
+    const float dlb = __ldg(p.delta + (b * p.H + hbase + 2 * tig + 1) * p.M + m);
+
+    // S^T and dP^T (16 keys x 8 heads) for this warp's keys
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, dp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < C::kSteps; ++k) {
+      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+      const uint32_t off = (k >> 2) * C::kBoxBytesBlk + ((((k & 3) * 2 + ka_hi) ^ sw) << 4);
+      ldsm_x4(wK + ka + off, a0, a1, a2, a3);
+      ldsm_x4(wV + ka + off, b0, b1, b2, b3);
+      mma_16816(s, a0, a1, a2, a3, qf[k][0], qf[k][1]);
+      mma_16816(dp, b0, b1, b2, b3, df[k][0], df[k][1]);
+    }
+    const bool va = nw0 + gid <= lastkey, vb = nw0 + gid + 8 <= lastkey;
+    float pr[4], ds[4];
+    pr[0] = va ? ex2(fmaf(s[0], sl2, -lsa)) : 0.f;
+    pr[1] = va ? ex2(fmaf(s[1], sl2, -lsb)) : 0.f;
+    pr[2] = vb ? ex2(fmaf(s[2], sl2, -lsa)) : 0.f;
+    pr[3] = vb ? ex2(fmaf(s[3], sl2, -lsb)) : 0.f;
+    ds[0] = va ? pr[0] * (dp[0] - dla) : 0.f;
+    ds[1] = va ? pr[1] * (dp[1] - dlb) : 0.f;
+    ds[2] = vb ? pr[2] * (dp[2] - dla) : 0.f;
+    ds[3] = vb ? pr[3] * (dp[3] - dlb) : 0.f;
+    // A operands (16 keys x 8 heads): the C layout of S^T is the A layout of
+    // m16n8k8
+    const uint32_t pa0 = pack_half2(pr[0], pr[1]), pa1 = pack_half2(pr[2], pr[3]);
+    const uint32_t sa0 = pack_half2(ds[0], ds[1]), sa1 = pack_half2(ds[2], ds[3]);
+    // dV (16 keys x D) += P^T dO ; dK (16 keys x D) += dS^T Q ; B operands
+    // (heads x 8 dims) are the transposes of the dO / Q fragments
+#pragma unroll
+    for (int k = 0; k < C::kSteps; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = 2 * k + h;
+        mma_1688(dv[j], pa0, pa1, movmatrix_t(df[k][h]));
+        mma_1688(dk[j], sa0, sa1, movmatrix_t(qf[k][h]));
+      }
+    }
+  }
+
+  // add this chunk's partial sums into dK / dV (rows past N are not written)
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int n = nw0 + gid + 8 * r;
+    if (n >= p.N) continue;
+    float* dkr = p.dK + ((b * p.N + n) * p.G + g) * D + 2 * tig;
+    float* dvr = p.dV + ((b * p.N + n) * p.G + g) * D + 2 * tig;
+#pragma unroll
+    for (int j = 0; j < C::kNTiles; ++j) {
+      atomicAdd(reinterpret_cast<float2*>(dkr + 8 * j),
+                make_float2(dk[j][2 * r] * p.scale, dk[j][2 * r + 1] * p.scale));
+      atomicAdd(reinterpret_cast<float2*>(dvr + 8 * j), make_float2(dv[j][2 * r], dv[j][2 * r + 1]));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host
+// ---------------------------------------------------------------------------
+
+struct BwdPlan {
+  size_t off_delta, off_count, off_cursor, off_offs, off_choffs, off_lists, total;
+  int64_t L, entries;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t T,
+                        int bs) {
+  BwdPlan pl;
+  const int64_t nblk = (N + bs - 1) / bs;
+  pl.L = B * G * nblk;
+  pl.entries = B * M * G * T;
+  size_t at = 0;
+  pl.off_delta = at;
+  at += align256(static_cast<size_t>(B * H * M) * 4);
+  pl.off_count = at;
+  at += align256(static_cast<size_t>(pl.L) * 4);
+  pl.off_cursor = at;
+  at += align256(static_cast<size_t>(pl.L) * 4);
+  pl.off_offs = at;
+  at += align256(static_cast<size_t>(pl.L + 1) * 4);
+  pl.off_choffs = at;
+  at += align256(static_cast<size_t>(pl.L + 1) * 4);
+  pl.off_lists = at;
+  at += align256(static_cast<size_t>(pl.entries) * 4);
+  pl.total = at;
+  return pl;
+}
+
+template <int D>
+static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
+                      const BwdPlan& pl, cudaStream_t st) {
+  constexpr int W = 4;
+  using Cq = DqCfg<D, W>;
+  int* count = reinterpret_cast<int*>(ws + pl.off_count);
+  int* cursor = reinterpret_cast<int*>(ws + pl.off_cursor);
+  int* offs = reinterpret_cast<int*>(ws + pl.off_offs);
+  int* choffs = reinterpret_cast<int*>(ws + pl.off_choffs);
+  int* lists = reinterpret_cast<int*>(ws + pl.off_lists);
+  p.delta = reinterpret_cast<float*>(ws + pl.off_delta);
+  p.offs = offs;
+  p.choffs = choffs;
+  p.lists = lists;
+  const int64_t B = p.units / (p.M * p.G);
+  if (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
+      cudaMemsetAsync(p.dV, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
+      cudaMemsetAsync(count, 0, static_cast<size_t>(pl.L) * 4, st) != cudaSuccess ||
+      cudaMemsetAsync(cursor, 0, static_cast<size_t>(pl.L) * 4, st) != cudaSuccess)
+    return NSA_ERR_LAUNCH;
+
+  CUtensorMap tk, tv, tkb, tvb;
+  const bool have_keys = p.N > 0;
+  if (have_keys) {
+    if (!encode_kv_map(&tk, K, B, p.N, p.G, D) || !encode_kv_map(&tv, V, B, p.N, p.G, D) ||
+        !encode_kv_map(&tkb, K, B, p.N, p.G, D, p.bs) ||
+        !encode_kv_map(&tvb, V, B, p.N, p.G, D, p.bs))
+      return NSA_ERR_LAUNCH;
+  } else {
+    memset(&tk, 0, sizeof(tk));
+    memset(&tv, 0, sizeof(tv));
+    memset(&tkb, 0, sizeof(tkb));
+    memset(&tvb, 0, sizeof(tvb));
+  }
+
+  // stage 1: dQ and delta
+  auto kq = sel_attn_bwd_dq_kernel<D, W>;
+  if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, Cq::kSmemBytes) !=
+      cudaSuccess)
+    return NSA_ERR_LAUNCH;
+  kq<<<static_cast<unsigned>((p.units + W - 1) / W), W * 32, Cq::kSmemBytes, st>>>(p, tk, tv);
+  if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
+  if (!have_keys || p.T == 0) return NSA_OK;  // dK = dV = 0
+
+  // stage 2: transposed index
+  const int64_t grid_e = (pl.entries + 255) / 256 < 152 * 64 ? (pl.entries + 255) / 256 : 152 * 64;
+  csr_count_kernel<<<static_cast<unsigned>(grid_e), 256, 0, st>>>(p, count);
+  csr_scan_kernel<<<1, 1024, 0, st>>>(count, offs, choffs, static_cast<int>(pl.L),
+                                      kQueriesPerChunk);
+  csr_fill_kernel<<<static_cast<unsigned>(grid_e), 256, 0, st>>>(p, cursor, lists);
+  if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
+
+  // stage 3: dK, dV; grid bound: sum over lists of ceil(count / chunk)
+  const int64_t chunks = (pl.entries + kQueriesPerChunk - 1) / kQueriesPerChunk + pl.L;
+  if (p.bs == 64) {
+    using Ck = DkvCfg<D, 4>;
+    auto kk = sel_attn_bwd_dkv_kernel<D, 4>;
+    if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, Ck::kSmemBytes) !=
+        cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    kk<<<static_cast<unsigned>(chunks), 4 * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb);
+  } else {
+    using Ck = DkvCfg<D, 2>;
+    auto kk = sel_attn_bwd_dkv_kernel<D, 2>;
+    if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, Ck::kSmemBytes) !=
+        cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    kk<<<static_cast<unsigned>(chunks), 2 * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb);
+  }
+  return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
+}
+
+int bwd_read_and_clear_status(unsigned int* value) { return read_and_clear_status(value); }
+
+}  // namespace nsa
+
+extern "C" {
+
+int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
+                                         int64_t D, int64_t T, int block_size) {
+  const int chk = nsa::check_sizes(B, M, N, H, G, D, T, block_size);
+  if (chk != NSA_OK) return chk;
+  if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
+  return static_cast<int64_t>(nsa::bwd_plan(B, M, N, H, G, T, block_size).total);
+}
+
+int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* block_indices,
+                     const float* O, const float* LSE, const float* dO, float* dQ, float* dK,
+                     float* dV, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
+                     int64_t T, int block_size, float scale, void* workspace,
+                     int64_t workspace_bytes, void* stream) {
+  using namespace nsa;
+  const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
+  if (chk != NSA_OK) return chk;
+  if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
+  const BwdPlan pl = bwd_plan(B, M, N, H, G, T, block_size);
+  if (pl.L > (int64_t(1) << 31) - 2) return NSA_ERR_SHAPE;
+  if (B == 0 || (M == 0 && N == 0)) return NSA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (M == 0) {  // no query: every key gradient is zero
+    if (!dK || !dV) return NSA_ERR_NULL;
+    if (cudaMemsetAsync(dK, 0, static_cast<size_t>(B * N * G * D) * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(dV, 0, static_cast<size_t>(B * N * G * D) * 4, st) != cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    return NSA_OK;
+  }
+  if (!Q || !O || !LSE || !dO || !dQ) return NSA_ERR_NULL;
+  if (N > 0 && (!K || !V || !dK || !dV)) return NSA_ERR_NULL;
+  if (T > 0 && !block_indices) return NSA_ERR_NULL;
+  if (!workspace || workspace_bytes < static_cast<int64_t>(pl.total)) return NSA_ERR_WORKSPACE;
+  auto mis = [](const void* ptr, uintptr_t a) {
+    return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+  };
+  if (mis(Q, 16) || mis(K, 16) || mis(V, 16) || mis(O, 16) || mis(dO, 16) || mis(dQ, 16) ||
+      mis(dK, 16) || mis(dV, 16) || mis(LSE, 4) || mis(block_indices, 4) || mis(workspace, 256))
+    return NSA_ERR_ALIGN;
+
+  BwdProblem p;
+  p.Q = static_cast<const __half*>(Q);
+  p.idx = block_indices;
+  p.O = O;
+  p.LSE = LSE;
+  p.dO = dO;
+  p.dQ = dQ;
+  p.dK = dK;
+  p.dV = dV;
+  p.M = M;
+  p.N = N;
+  p.H = H;
+  p.G = G;
+  p.T = T;
+  p.B = B;
+  p.units = B * G * M;
+  p.bs = block_size;
+  p.nblk = static_cast<int>((N + block_size - 1) / block_size);
+  p.L = static_cast<int>(pl.L);
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  p.sl2 = p.scale * 1.4426950408889634f;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return D == 64 ? launch_bwd<64>(p, K, V, ws, pl, st) : launch_bwd<128>(p, K, V, ws, pl, st);
+}
+
+}  // extern "C"

@@ -39,6 +39,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "common.cuh"
 #include "nsa_sel_attn.h"
 #include "ptx.cuh"
 #include "sel_attn_fwd.cuh"
@@ -50,16 +51,7 @@
 #define NSA_MIN_BLOCKS 4
 #endif
 
-__device__ unsigned int g_nsa_device_status = 0u;
-
 namespace nsa {
-
-constexpr int kHeadsPerGroup = 8;
-constexpr int kTileKeys = 16;
-constexpr int kBoxCols = 64;                   // d columns per TMA box: 128-byte rows
-constexpr int kBoxBytes = kTileKeys * 128;     // one box: 16 keys x 64 d x fp16
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr unsigned kFull = 0xffffffffu;
 
 struct Problem {
   const __half* Q;
@@ -72,73 +64,6 @@ struct Problem {
   int bs;
   int nblk;       // ceil(N / bs)
   float sl2;      // scale * log2(e)
-};
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Bounded wait on an mbarrier phase; false after `limit_ns` without it.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ void report_timeout() { atomicOr(&g_nsa_device_status, 1u); }
-
-// Warp-uniform walk over the 16-key tiles one index row selects, in the
-// order the row lists its blocks. Padding (< 0 or >= nblk) and blocks that
-// start after the last visible key are skipped, as are tiles of a block that
-// start after it.
-struct TileWalk {
-  const int32_t* row;
-  int T, nblk, bs, lastkey;
-  int win;        // start of the next 32-entry window
-  unsigned mask;  // lanes of the current window still to visit
-  int lane_val;   // this lane's entry of the current window
-  int n0, nend;   // next tile start, end of the visible keys of the block
-
-  __device__ __forceinline__ void init(const int32_t* r, int T_, int nblk_, int bs_,
-                                       int lastkey_) {
-    row = r;
-    T = T_;
-    nblk = nblk_;
-    bs = bs_;
-    lastkey = lastkey_;
-    win = 0;
-    mask = 0u;
-    lane_val = -1;
-    n0 = 0;
-    nend = 0;
-  }
-
-  __device__ __forceinline__ bool next(int& out) {
-    while (n0 >= nend) {
-      while (mask == 0u) {
-        if (win >= T) return false;
-        const int j = win + (threadIdx.x & 31);
-        const int t = (j < T) ? __ldg(row + j) : -1;
-        const bool ok = t >= 0 && t < nblk && t * bs <= lastkey;
-        mask = __ballot_sync(kFull, ok);
-        lane_val = t;
-        win += 32;
-      }
-      const int src = __ffs(mask) - 1;
-      mask &= mask - 1u;
-      const int t = __shfl_sync(kFull, lane_val, src);
-      n0 = t * bs;
-      nend = min(n0 + bs, lastkey + 1);
-    }
-    out = n0;
-    n0 += kTileKeys;
-    return true;
-  }
 };
 
 template <int D, int WARPS>
@@ -399,42 +324,6 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns) {
 
 // ---- host side ---------------------------------------------------------------
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// K or V [B, N, G, D] fp16 as a 4-D map (d, g, n, b); box = 64 d x 1 x 16 keys x 1.
-static bool encode_kv_map(CUtensorMap* tm, const void* ptr, int64_t B, int64_t N, int64_t G,
-                          int64_t D) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(G),
-                              static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D * 2),
-                                 static_cast<cuuint64_t>(G * D * 2),
-                                 static_cast<cuuint64_t>(N * G * D * 2)};
-  const cuuint32_t box[4] = {kBoxCols, 1, kTileKeys, 1};
-  const cuuint32_t estride[4] = {1, 1, 1, 1};
-  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
-             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
                       cudaStream_t stream) {
@@ -543,16 +432,10 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t*
 int nsa_sync_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return NSA_ERR_LAUNCH;
-  unsigned int v = 0u;
-  if (cudaMemcpyFromSymbol(&v, g_nsa_device_status, sizeof(v)) != cudaSuccess)
-    return NSA_ERR_LAUNCH;
-  if (v != 0u) {
-    const unsigned int zero = 0u;
-    if (cudaMemcpyToSymbol(g_nsa_device_status, &zero, sizeof(zero)) != cudaSuccess)
-      return NSA_ERR_LAUNCH;
-    return NSA_ERR_TIMEOUT;
-  }
-  return NSA_OK;
+  unsigned int fwd = 0u, bwd = 0u;
+  if (nsa::read_and_clear_status(&fwd) != NSA_OK) return NSA_ERR_LAUNCH;
+  if (nsa::bwd_read_and_clear_status(&bwd) != NSA_OK) return NSA_ERR_LAUNCH;
+  return (fwd | bwd) ? NSA_ERR_TIMEOUT : NSA_OK;
 }
 
 int nsa_selftest_wait_timeout(int64_t limit_ns, void* stream) {

@@ -20,4 +20,7 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
                    int64_t D, int64_t T, int64_t m_off, int block_size, float scale,
                    cudaStream_t st);
 
+// Reads and clears the status word of the backward kernels' translation unit.
+int bwd_read_and_clear_status(unsigned int* value);
+
 }  // namespace nsa

@@ -283,9 +283,19 @@ def softmax_grad_terms(s: np.ndarray, lse: np.ndarray, v: np.ndarray, do: np.nda
     return p, p * (dp - delta[:, None])
 
 
-def sel_attn_bwd(Q, K, V, idx, dO, block_size: int, scale: Optional[float] = None):
+def _fp16(x: np.ndarray) -> np.ndarray:
+    return x.astype(np.float16).astype(np.float64)
+
+
+def sel_attn_bwd(Q, K, V, idx, dO, block_size: int, scale: Optional[float] = None,
+                 emulate_kernel_rounding: bool = False):
     """Gradients dQ [B,M,H,D], dK [B,N,G,D], dV [B,N,G,D] (float64) of the
-    forward for the upstream gradient dO [B,M,H,D] (LSE is recomputed)."""
+    forward for the upstream gradient dO [B,M,H,D] (LSE is recomputed).
+
+    ``emulate_kernel_rounding=True`` rounds to fp16 the operands that enter
+    fp16 matrix products on the GPU (dO, P for dV, dS for dQ and dK), all
+    else in float64: it measures what fp16 operands alone cost, the yardstick
+    of the GPU parity tolerance."""
     B, M, H, D = Q.shape
     N, G = K.shape[1], K.shape[2]
     if scale is None:
@@ -304,7 +314,15 @@ def sel_attn_bwd(Q, K, V, idx, dO, block_size: int, scale: Optional[float] = Non
                 v = np.asarray(Vg[n], dtype=np.float64)
                 do = np.asarray(dO[b, m, heads], dtype=np.float64)
                 s = scores(q, k, scale)
-                p, ds = softmax_grad_terms(s, logsumexp_rows(s), v, do)
+                if emulate_kernel_rounding:
+                    lse = logsumexp_rows(s)
+                    p = np.exp(s - lse[:, None])
+                    dp = _fp16(do) @ v.T
+                    delta = (do * attend(s, lse, v)).sum(axis=1)
+                    ds = _fp16(p * (dp - delta[:, None]))
+                    p, do = _fp16(p), _fp16(do)
+                else:
+                    p, ds = softmax_grad_terms(s, logsumexp_rows(s), v, do)
                 dQ[b, m, heads] = scale * (ds @ k)
                 dK[b, n, g] += scale * (ds.T @ q)
                 dV[b, n, g] += p.T @ do

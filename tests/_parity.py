@@ -91,3 +91,14 @@ def sample_rows(B, M, G, bs, seed, n_random=4096):
         for g in range(G):
             rows.add((b, int(m), g))
     return sorted(rows)
+
+
+def small_inputs(B, M, N, H, G, D, bs, T, rule, seed, sigma=1.0):
+    """Seeded inputs for a small problem; index rows from the workload rules
+    (rows for M > N may name blocks past N: they are padding)."""
+    from nsa_block_selection_gb300 import inputs as gen
+
+    w = gen.Workload("small", B, M, N, H, G, D, bs, T, sigma, rule)
+    q, k, v = gen.make_qkv(w, seed)
+    idx = gen.make_block_indices(w.replace(N=min(M, N)) if M <= N else w, seed)
+    return q, k, v, idx

@@ -1,0 +1,88 @@
+"""Backward (dQ, dK, dV) on the GPU vs the fp64 oracle.
+
+Tolerance: per tensor, max |GPU - exact| <= 4 * max |emulated - exact| +
+1e-5 * max |exact|, where "emulated" is the oracle with fp16 operands exactly
+where the kernels use them (dO, P, dS) and float64 elsewhere: the kernels
+may cost at most a small multiple of what fp16 operands alone cost.
+"""
+
+import numpy as np
+import pytest
+
+import oracle.sel_attn as oracle
+from _parity import small_inputs, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu(cuda_lib):
+    import torch
+
+    assert torch.cuda.is_available()
+
+
+def _run(q, k, v, idx, dO, bs, scale=None):
+    import torch
+
+    from nsa_block_selection_gb300 import sel_attn_fwd
+    from nsa_block_selection_gb300._lib import sel_attn_bwd
+
+    tq, tk, tv, ti, tdo = to_dev(q, k, v, idx, dO)
+    O, L = sel_attn_fwd(tq, tk, tv, ti, bs, scale)
+    grads = sel_attn_bwd(tq, tk, tv, ti, O, L, tdo, bs, scale)
+    torch.cuda.synchronize()
+    return [g.cpu().numpy().astype(np.float64) for g in grads]
+
+
+def _check(got, q, k, v, idx, dO, bs, scale=None, what=""):
+    exact = oracle.sel_attn_bwd(q, k, v, idx, dO, bs, scale)
+    emul = oracle.sel_attn_bwd(q, k, v, idx, dO, bs, scale, emulate_kernel_rounding=True)
+    for name, g, ex, em in zip(("dQ", "dK", "dV"), got, exact, emul):
+        err = np.abs(g - ex).max() if g.size else 0.0
+        err_em = np.abs(em - ex).max() if g.size else 0.0
+        top = np.abs(ex).max() if g.size else 0.0
+        assert np.isfinite(g).all(), f"{what} {name}: non-finite"
+        assert err <= 4 * err_em + 1e-5 * top, \
+            f"{what} {name}: err {err:.3e} vs emulated {err_em:.3e} (max {top:.3e})"
+
+
+@pytest.mark.parametrize("B,M,N,D,bs,T,rule", [
+    (2, 700, 700, 128, 64, 5, "first_two_local"),
+    (1, 900, 900, 64, 32, 4, "local"),
+    (1, 500, 500, 128, 32, 6, "first_local"),
+    (1, 300, 520, 128, 64, 3, "local"),
+    (1, 520, 300, 64, 64, 3, "local"),
+    (1, 640, 640, 128, 64, 10, "all_causal"),
+])
+def test_bwd_matches_oracle(B, M, N, D, bs, T, rule):
+    q, k, v, idx = small_inputs(B, M, N, 16, 2, D, bs, T, rule, seed=M + T)
+    dO = np.random.default_rng(M).standard_normal(q.shape).astype(np.float32)
+    got = _run(q, k, v, idx, dO, bs)
+    _check(got, q, k, v, idx, dO, bs, what=f"M{M} N{N} D{D} bs{bs}")
+
+
+def test_bwd_padding_out_of_range_future_and_empty_rows():
+    q, k, v, idx = small_inputs(1, 400, 400, 16, 2, 128, 64, 6, "first_two_local", seed=9)
+    rng = np.random.default_rng(10)
+    idx = rng.permuted(idx, axis=-1).copy()
+    pads = idx < 0
+    idx[pads] = rng.choice(np.array([-1, -3, 7, 1 << 29], np.int32), size=int(pads.sum()))
+    idx[0, 5:9] = -1  # empty rows
+    dO = rng.standard_normal(q.shape).astype(np.float32)
+    got = _run(q, k, v, idx, dO, 64, scale=0.1)
+    _check(got, q, k, v, idx, dO, 64, scale=0.1, what="padding")
+    assert np.all(got[0][0, 5:9] == 0)  # dQ of empty rows
+
+
+@pytest.mark.parametrize("T,N", [(0, 256), (3, 0)])
+def test_bwd_degenerate(T, N):
+    import torch
+
+    q, k, v, idx = small_inputs(1, 256, 256, 8, 1, 64, 32, 3, "local", seed=11)
+    if T == 0:
+        idx = np.zeros((1, 256, 1, 0), np.int32)
+    k, v = k[:, :N].copy(), v[:, :N].copy()
+    dO = np.ones(q.shape, np.float32)
+    dq, dk, dv = _run(q, k, v, idx, dO, 32)
+    assert np.all(dq == 0) and np.all(dk == 0) and np.all(dv == 0)

@@ -64,3 +64,16 @@ def test_bwd_mutant_is_caught(name, monkeypatch):
         except (AssertionError, ValueError, IndexError, FloatingPointError):
             failed.append(pin.__name__)
     assert failed, f"backward mutant {name} passed every pin"
+
+
+def test_bwd_rounding_emulation_is_close():
+    """fp16 operands (dO, P, dS) move the exact gradients only slightly."""
+    from nsa_block_selection_gb300 import inputs as gen
+
+    w = gen.Workload("t", 1, 96, 96, 8, 1, 32, 16, 4, 1.0, "first_two_local")
+    q, k, v, idx = gen.make_inputs(w, 3)
+    dO = np.random.default_rng(4).standard_normal(q.shape)
+    exact = S.sel_attn_bwd(q, k, v, idx, dO, 16)
+    emul = S.sel_attn_bwd(q, k, v, idx, dO, 16, emulate_kernel_rounding=True)
+    for a, b in zip(exact, emul):
+        assert np.abs(a - b).max() <= 5e-3 * np.abs(a).max()
