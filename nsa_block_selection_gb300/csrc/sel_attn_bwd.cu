@@ -582,10 +582,11 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   p.choffs = choffs;
   p.lists = lists;
   const int64_t B = p.units / (p.M * p.G);
-  if (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
-      cudaMemsetAsync(p.dV, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
-      cudaMemsetAsync(count, 0, static_cast<size_t>(pl.L) * 4, st) != cudaSuccess ||
-      cudaMemsetAsync(cursor, 0, static_cast<size_t>(pl.L) * 4, st) != cudaSuccess)
+  if (p.N > 0 &&
+      (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
+       cudaMemsetAsync(p.dV, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
+       cudaMemsetAsync(count, 0, static_cast<size_t>(pl.L) * 4, st) != cudaSuccess ||
+       cudaMemsetAsync(cursor, 0, static_cast<size_t>(pl.L) * 4, st) != cudaSuccess))
     return NSA_ERR_LAUNCH;
 
   CUtensorMap tk, tv, tkb, tvb;
