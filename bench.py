@@ -60,6 +60,7 @@ def parse_args(argv=None):
     ap.add_argument("--skip-dense", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-bwd", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=24576,
                     help="rows of the CPU-oracle sample")
     ap.add_argument("--seed", type=int, default=None)
@@ -365,6 +366,11 @@ def run_ours(args):
     if not args.skip_e2e:
         e2e = run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist)
 
+    # backward (dQ, dK, dV) on the same inputs, after the timed forward
+    backward = None
+    if rank == 0 and world == 1 and not args.skip_bwd:
+        backward = run_backward(w, q, k, v, idx, out, lse, work, flush, args)
+
     # dense-causal-equivalent run: same Q/K/V, every causal block listed
     dense = None
     if rank == 0 and world == 1 and not args.skip_dense:
@@ -402,6 +408,7 @@ def run_ours(args):
         "flops_per_step": work["flops"], "gathered_bytes_per_step": work["gathered_bytes"],
         "speedup_vs_dense_causal": dense["speedup"] if dense else None,
         "dense_causal": dense,
+        "backward": backward,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -415,6 +422,39 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def run_backward(w, q, k, v, idx, out, lse, work, flush, args):
+    """nsa_sel_attn_bwd on the forward's outputs and a seeded fp32 dO.
+    FLOPs: 10*D per (query, head, visible key) -- QK^T, dP, dQ, dK, dV."""
+    import torch
+
+    from nsa_block_selection_gb300 import _lib
+
+    gen = torch.Generator(device=q.device).manual_seed(1234)
+    do = torch.randn(out.shape, generator=gen, device=q.device, dtype=torch.float32)
+    need = _lib.bwd_workspace_bytes(w.B, w.M, w.N, w.H, w.G, w.D, w.T, w.block_size)
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(out)
+    dk = torch.empty((w.B, w.N, w.G, w.D), dtype=torch.float32, device=q.device)
+    dv = torch.empty_like(dk)
+
+    def step():
+        _lib.sel_attn_bwd(q, k, v, idx, out, lse, do, w.block_size, w.scale, dq=dq, dk=dk,
+                          dv=dv, workspace=ws)
+
+    steps = max(3, args.steps // 6)
+    times, _ = time_steps(step, steps, 2, flush, lambda: None)
+    t = statistics.mean(times)
+    flops = work["flops"] // 4 * 10
+    res = {"ms_per_step": t, "tflops": flops / (t * 1e-3) / 1e12, "flops_per_step": flops,
+           "gathered_gbs_dq_stage": work["gathered_bytes"] / (t * 1e-3) / 1e9,
+           "workspace_bytes": need, "steps": steps,
+           "kernels": "dQ (query-major), index transpose (count, scan, fill), dK/dV "
+                      "(key-major, float2 atomics)"}
+    del ws, do, dq, dk, dv
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_dense(w, q, k, v, out, lse, flush, args, t_sparse_ms):

@@ -69,6 +69,8 @@ __all__ = [
     "sel_attn_fwd",
     "softmax_grad_terms",
     "sel_attn_bwd",
+    "sel_attn_bwd_dq_rows",
+    "sel_attn_bwd_block",
 ]
 
 
@@ -327,3 +329,52 @@ def sel_attn_bwd(Q, K, V, idx, dO, block_size: int, scale: Optional[float] = Non
                 dK[b, n, g] += scale * (ds.T @ q)
                 dV[b, n, g] += p.T @ do
     return dQ, dK, dV
+
+
+def sel_attn_bwd_dq_rows(Q, K, V, idx, dO, rows, block_size: int,
+                         scale: Optional[float] = None) -> np.ndarray:
+    """dQ [R, H/G, D] of the listed (b, m, g) rows (each row's dQ depends on
+    that row only)."""
+    B, M, H, D = Q.shape
+    N, G = K.shape[1], K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.zeros((len(rows), H // G, D))
+    for r, (b, m, g) in enumerate(rows):
+        heads, q, Kg, Vg = _row_operands(Q, K, V, b, m, g, H, G)
+        n = visible_keys(idx[b, m, g], m, N, block_size)
+        if n.size == 0:
+            continue
+        k = np.asarray(Kg[n], dtype=np.float64)
+        v = np.asarray(Vg[n], dtype=np.float64)
+        s = scores(q, k, scale)
+        _, ds = softmax_grad_terms(s, logsumexp_rows(s), v,
+                                   np.asarray(dO[b, m, heads], dtype=np.float64))
+        out[r] = scale * (ds @ k)
+    return out
+
+
+def sel_attn_bwd_block(Q, K, V, idx, dO, b: int, g: int, t: int, block_size: int,
+                       scale: Optional[float] = None):
+    """dK, dV rows [keys of block t, D] of (b, g): contributions of every row
+    of group g that selects block t."""
+    B, M, H, D = Q.shape
+    N, G = K.shape[1], K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    keys = block_keys(t, block_size, N)
+    dK = np.zeros((keys.size, D))
+    dV = np.zeros((keys.size, D))
+    for m in np.nonzero((np.asarray(idx[b, :, g]) == t).any(axis=-1))[0]:
+        m = int(m)
+        heads, q, Kg, Vg = _row_operands(Q, K, V, b, m, g, H, G)
+        n = visible_keys(idx[b, m, g], m, N, block_size)
+        k = np.asarray(Kg[n], dtype=np.float64)
+        v = np.asarray(Vg[n], dtype=np.float64)
+        s = scores(q, k, scale)
+        p, ds = softmax_grad_terms(s, logsumexp_rows(s), v,
+                                   np.asarray(dO[b, m, heads], dtype=np.float64))
+        sel = (n >= keys[0]) & (n <= keys[-1])
+        dK[n[sel] - keys[0]] += scale * (ds[:, sel].T @ q)
+        dV[n[sel] - keys[0]] += p[:, sel].T @ np.asarray(dO[b, m, heads], dtype=np.float64)
+    return dK, dV

@@ -86,3 +86,40 @@ def test_bwd_degenerate(T, N):
     dO = np.ones(q.shape, np.float32)
     dq, dk, dv = _run(q, k, v, idx, dO, 32)
     assert np.all(dq == 0) and np.all(dk == 0) and np.all(dv == 0)
+
+
+@pytest.mark.parametrize("name", ["m64k_bs64", "m32k_bs32"])
+def test_bwd_full_size(name):
+    """Full-size workloads: dQ on sampled rows and dK/dV of sampled blocks vs
+    the oracle; dV column sums equal the summed upstream gradient of every
+    non-empty row and dK column sums vanish (exact identities)."""
+    import torch
+
+    from nsa_block_selection_gb300 import inputs as gen
+    from _parity import sample_rows
+
+    w = gen.workload(name)
+    q, k, v, idx = gen.make_inputs(w)
+    dO = np.random.default_rng(1).standard_normal(q.shape, dtype=np.float32)
+    dq, dk, dv = _run(q, k, v, idx, dO, w.block_size)
+    hpg = w.H // w.G
+    # dQ, sampled rows
+    rows = sample_rows(w.B, w.M, w.G, w.block_size, seed=7, n_random=512)
+    ex = oracle.sel_attn_bwd_dq_rows(q, k, v, idx, dO, rows, w.block_size)
+    got = np.stack([dq[b, m, g * hpg:(g + 1) * hpg] for b, m, g in rows])
+    err = np.abs(got - ex).max()
+    assert err <= 2e-3 * np.abs(ex).max(), f"dQ sampled rows: {err:.3e}"
+    # dK / dV of sampled blocks (the first, a middle, the last)
+    nblk = -(-w.N // w.block_size)
+    for b, g, t in ((0, 0, 1), (w.B - 1, w.G - 1, nblk // 2), (0, w.G // 2, nblk - 1)):
+        ek, ev = oracle.sel_attn_bwd_block(q, k, v, idx, dO, b, g, t, w.block_size)
+        sl = slice(t * w.block_size, min((t + 1) * w.block_size, w.N))
+        for nm, gg, ee in (("dK", dk[b, sl, g], ek), ("dV", dv[b, sl, g], ev)):
+            e = np.abs(gg - ee).max()
+            assert e <= 2e-3 * max(np.abs(ee).max(), 1e-30), f"{nm} block {t}: {e:.3e}"
+    # identities over all keys
+    nonempty = (idx >= 0).any(-1)  # every row lists its own block here
+    assert nonempty.all()
+    want = dO.astype(np.float64).reshape(w.B, w.M, w.G, hpg, w.D).sum(axis=(1, 3))
+    np.testing.assert_allclose(dv.sum(axis=1), want, rtol=1e-4, atol=1e-3 * np.abs(want).max())
+    assert np.abs(dk.sum(axis=1)).max() <= 1e-4 * np.abs(dk).sum(axis=1).max()

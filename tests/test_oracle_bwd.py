@@ -77,3 +77,20 @@ def test_bwd_rounding_emulation_is_close():
     emul = S.sel_attn_bwd(q, k, v, idx, dO, 16, emulate_kernel_rounding=True)
     for a, b in zip(exact, emul):
         assert np.abs(a - b).max() <= 5e-3 * np.abs(a).max()
+
+
+def test_bwd_restricted_helpers_agree_with_full():
+    """dQ of chosen rows and dK/dV of one block equal the full backward."""
+    from nsa_block_selection_gb300 import inputs as gen
+
+    w = gen.Workload("t", 2, 80, 80, 8, 2, 16, 8, 5, 1.0, "first_two_local")
+    q, k, v, idx = gen.make_inputs(w, 5)
+    dO = np.random.default_rng(6).standard_normal(q.shape)
+    dQ, dK, dV = S.sel_attn_bwd(q, k, v, idx, dO, 8)
+    rows = [(1, 79, 0), (0, 3, 1), (1, 40, 1)]
+    got = S.sel_attn_bwd_dq_rows(q, k, v, idx, dO, rows, 8)
+    for r, (b, m, g) in enumerate(rows):
+        np.testing.assert_allclose(got[r], dQ[b, m, 4 * g:4 * g + 4], atol=1e-12)
+    bk, bv = S.sel_attn_bwd_block(q, k, v, idx, dO, 1, 1, 3, 8)
+    np.testing.assert_allclose(bk, dK[1, 24:32, 1], atol=1e-12)
+    np.testing.assert_allclose(bv, dV[1, 24:32, 1], atol=1e-12)
