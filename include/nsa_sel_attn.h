@@ -58,7 +58,9 @@ typedef enum nsa_status {
                                (no device, no sm_103a image, bad stream ...) */
   NSA_ERR_TIMEOUT = -8,     /* a bounded device-side wait gave up (reported by
                                nsa_sync_status)                               */
-  NSA_ERR_WORKSPACE = -9    /* workspace NULL or smaller than required        */
+  NSA_ERR_WORKSPACE = -9,   /* workspace NULL or smaller than required        */
+  NSA_ERR_SCRATCH = -10     /* problem needs more scratch than the fixed
+                               buffer of nsa_sel_attn_bwd_noalloc (64 MiB)    */
 } nsa_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -177,6 +179,35 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V,
                      const float* dO, float* dQ, float* dK, float* dV, int64_t B, int64_t M,
                      int64_t N, int64_t H, int64_t G, int64_t D, int64_t T, int block_size,
                      float scale, void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * nsa_sel_attn_bwd_noalloc -- nsa_sel_attn_bwd for callers that cannot
+ * allocate device memory. The pages have no counterpart to this entry point.
+ *
+ * Some callers may not allocate at all: a plugin inside a host application
+ * that owns every device allocation through its own pool and hands plugins
+ * no allocator, or a service that reserves all of its memory at start-up and
+ * forbids allocation while it serves. They still pass every input and
+ * output; the scratch the backward needs (delta, the per-block query lists
+ * and their offsets) comes from a fixed 64 MiB array inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ * Arguments, layouts and results are those of nsa_sel_attn_bwd without the
+ * workspace. A problem whose scratch (nsa_sel_attn_bwd_workspace_bytes)
+ * exceeds 64 MiB is rejected with NSA_ERR_SCRATCH before anything is
+ * launched. The call allocates and frees nothing. The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * Every call uses the same array and finds the previous call's contents in
+ * it; the parts that must start at zero are cleared on the call's stream.
+ * Calls whose work overlaps on the GPU (on different streams, or from
+ * different threads on one device) race on the array: serialise them.
+ */
+int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
+                             const int32_t* block_indices, const float* O, const float* LSE,
+                             const float* dO, float* dQ, float* dK, float* dV, int64_t B,
+                             int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                             int block_size, float scale, void* stream);
 
 /*
  * nsa_sync_status -- wait for `stream`, then read and clear the device status

@@ -20,7 +20,8 @@ NSA_OK = 0
 
 EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sync_status",
            "nsa_selftest_wait_timeout", "nsa_sel_attn_fwd_host_workspace_bytes",
-           "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd")
+           "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd",
+           "nsa_sel_attn_bwd_noalloc")
 
 _lib = None
 
@@ -62,6 +63,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_bwd.restype = c_int
     lib.nsa_sel_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                      i64, i64, i64, c_int, ctypes.c_float, vp, i64, vp]
+    lib.nsa_sel_attn_bwd_noalloc.restype = c_int
+    lib.nsa_sel_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64,
+                                             i64, i64, i64, i64, i64, c_int, ctypes.c_float, vp]
     lib.nsa_sel_attn_fwd_host.restype = c_int
     lib.nsa_sel_attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                           i64, c_int, ctypes.c_float, vp, i64, i64, vp]

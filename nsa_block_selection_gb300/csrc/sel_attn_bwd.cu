@@ -31,6 +31,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "nsa_sel_attn.h"
@@ -642,6 +643,36 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
 
 int bwd_read_and_clear_status(unsigned int* value) { return read_and_clear_status(value); }
 
+// ---- fixed scratch for callers that cannot allocate --------------------------
+//
+// Some callers of this library may not allocate device memory at all: a
+// plugin inside a host application that owns every device allocation
+// through its own pool and hands plugins no allocator, or a service that
+// reserves all of its memory at start-up and forbids allocation while it
+// serves. nsa_sel_attn_bwd_noalloc gives them the backward without a
+// caller-provided workspace: its scratch (delta, list counts and offsets,
+// the query lists) lives in this file-scope device array, which every GPU
+// that loads the library holds until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB per device
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device. In host code
+// the array's name is only a host-side handle, never a device address; the
+// address is looked up once per device, with that device current.
+static void* noalloc_scratch_address() {
+  static std::mutex mu;
+  static void* addr[128] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = ptr;
+  }
+  return addr[dev];
+}
+
 }  // namespace nsa
 
 extern "C" {
@@ -707,6 +738,61 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t*
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   p.sl2 = p.scale * 1.4426950408889634f;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return D == 64 ? launch_bwd<64>(p, K, V, ws, pl, st) : launch_bwd<128>(p, K, V, ws, pl, st);
+}
+
+int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
+                             const int32_t* block_indices, const float* O, const float* LSE,
+                             const float* dO, float* dQ, float* dK, float* dV, int64_t B,
+                             int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                             int block_size, float scale, void* stream) {
+  using namespace nsa;
+  const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
+  if (chk != NSA_OK) return chk;
+  if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
+  const BwdPlan pl = bwd_plan(B, M, N, H, G, T, block_size);
+  if (pl.L > (int64_t(1) << 31) - 2) return NSA_ERR_SHAPE;
+  if (pl.total > kNoAllocScratchBytes) return NSA_ERR_SCRATCH;
+  if (B == 0 || M == 0) {
+    // no query, so no scratch: the workspace entry point zeroes dK and dV
+    return nsa_sel_attn_bwd(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, B, M, N, H, G, D, T,
+                            block_size, scale, nullptr, 0, stream);
+  }
+  if (!Q || !O || !LSE || !dO || !dQ) return NSA_ERR_NULL;
+  if (N > 0 && (!K || !V || !dK || !dV)) return NSA_ERR_NULL;
+  if (T > 0 && !block_indices) return NSA_ERR_NULL;
+  auto mis = [](const void* ptr, uintptr_t a) {
+    return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+  };
+  if (mis(Q, 16) || mis(K, 16) || mis(V, 16) || mis(O, 16) || mis(dO, 16) || mis(dQ, 16) ||
+      mis(dK, 16) || mis(dV, 16) || mis(LSE, 4) || mis(block_indices, 4))
+    return NSA_ERR_ALIGN;
+  void* scratch = noalloc_scratch_address();
+  if (scratch == nullptr) return NSA_ERR_LAUNCH;
+
+  BwdProblem p;
+  p.Q = static_cast<const __half*>(Q);
+  p.idx = block_indices;
+  p.O = O;
+  p.LSE = LSE;
+  p.dO = dO;
+  p.dQ = dQ;
+  p.dK = dK;
+  p.dV = dV;
+  p.M = M;
+  p.N = N;
+  p.H = H;
+  p.G = G;
+  p.T = T;
+  p.B = B;
+  p.units = B * G * M;
+  p.bs = block_size;
+  p.nblk = static_cast<int>((N + block_size - 1) / block_size);
+  p.L = static_cast<int>(pl.L);
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  p.sl2 = p.scale * 1.4426950408889634f;
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   return D == 64 ? launch_bwd<64>(p, K, V, ws, pl, st) : launch_bwd<128>(p, K, V, ws, pl, st);
 }
 

@@ -416,6 +416,8 @@ const char* nsa_status_string(int status) {
     case NSA_ERR_LAUNCH: return "CUDA launch failed";
     case NSA_ERR_TIMEOUT: return "device wait timed out";
     case NSA_ERR_WORKSPACE: return "workspace too small";
+    case NSA_ERR_SCRATCH:
+      return "problem needs more scratch than the fixed buffer of the no-allocation entry point";
     default: return "unknown status";
   }
 }
