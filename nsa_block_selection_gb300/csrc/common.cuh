@@ -142,4 +142,19 @@ static inline bool encode_kv_map(CUtensorMap* tm, const void* ptr, int64_t B, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A row-major fp16 matrix [rows, D] as a 2-D map; box = 64 columns x `rows_per_box`
+// rows, 128-byte swizzle (used for the 8 head rows of one (b, m, g)).
+static inline bool encode_rows_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t D,
+                                   int rows_per_box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D * 2)};
+  const cuuint32_t box[2] = {kBoxCols, static_cast<cuuint32_t>(rows_per_box)};
+  const cuuint32_t estride[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace nsa

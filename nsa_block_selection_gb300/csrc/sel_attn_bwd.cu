@@ -32,6 +32,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "nsa_sel_attn.h"
@@ -51,7 +52,8 @@ struct BwdProblem {
   float* dQ;
   float* dK;
   float* dV;
-  float* delta;        // [B, H, M]
+  __half* dO16;        // [B, M, H, D] fp16 copy of dO (stage 1 -> stage 3)
+  float* rec;          // [B * M * G][16]: LSE * log2(e) of the 8 heads, then delta
   const int* offs;     // [L + 1] list starts (L = B * G * nblk)
   const int* choffs;   // [L + 1] chunk starts
   const int* lists;    // query ids, list by list
@@ -138,12 +140,25 @@ __global__ void __launch_bounds__(WARPS * 32, 3)
   }
   dpart += __shfl_xor_sync(kFull, dpart, 1);
   dpart += __shfl_xor_sync(kFull, dpart, 2);  // delta of head gid
-  if (tig == 0) p.delta[(b * p.H + hbase + gid) * p.M + m] = dpart;
   const float dla = __shfl_sync(kFull, dpart, (2 * tig) * 4);      // head 2tig
   const float dlb = __shfl_sync(kFull, dpart, (2 * tig + 1) * 4);  // head 2tig+1
   constexpr float kLog2e = 1.4426950408889634f;
   const float lsa = p.LSE[(b * p.H + hbase + 2 * tig) * p.M + m] * kLog2e;
   const float lsb = p.LSE[(b * p.H + hbase + 2 * tig + 1) * p.M + m] * kLog2e;
+  {
+    // for stage 3: dO as fp16 rows, and one 64-byte record per (b, m, g)
+    uint32_t* d16 = reinterpret_cast<uint32_t*>(p.dO16 + (row + gid) * D + 2 * tig);
+#pragma unroll
+    for (int k = 0; k < C::kSteps; ++k) {
+      d16[8 * k] = df[k][0];
+      d16[8 * k + 4] = df[k][1];
+    }
+    if (tig == 0) {
+      float* rec = p.rec + ((b * p.M + m) * p.G + g) * 16;
+      rec[gid] = p.LSE[(b * p.H + hbase + gid) * p.M + m] * kLog2e;
+      rec[8 + gid] = dpart;
+    }
+  }
 
   const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
   const int32_t* irow = p.idx + ((b * p.M + m) * p.G + g) * p.T;
@@ -383,18 +398,28 @@ __global__ void csr_fill_kernel(const BwdProblem p, int* cursor, int* lists) {
 
 template <int D, int KT>
 struct DkvCfg {
+  static constexpr int kWarps = 2 * KT;                       // (16-key tile, half of D)
   static constexpr int kBoxes = D / kBoxCols;
-  static constexpr int kBoxBytesBlk = KT * kTileKeys * 128;  // one box of bs rows
-  static constexpr int kBlockBytes = kBoxes * kBoxBytesBlk;  // K (or V) block
-  static constexpr int kSmemBytes = 2 * kBlockBytes + 8 + 1024;
+  static constexpr int kBoxBytesBlk = KT * kTileKeys * 128;   // one box of bs rows
+  static constexpr int kBlockBytes = kBoxes * kBoxBytesBlk;   // K (or V) block
+  static constexpr int kRowBox = 8 * 128;                     // 8 head rows x 64 dims
+  static constexpr int kRecOffset = 2 * kBoxes * kRowBox;     // after the Q and dO boxes
+  static constexpr int kStageBytes = kRecOffset + 1024;       // record, keeps 1 KB alignment
+  static constexpr int kStageTx = kRecOffset + 64;            // bytes each stage receives
+  static constexpr int kStages = 4;
+  static constexpr int kStageOffset = 2 * kBlockBytes;
+  static constexpr int kBarOffset = kStageOffset + kStages * kStageBytes;
+  static constexpr int kSmemBytes = kBarOffset + (1 + 2 * kStages) * 8 + 1024;
   static constexpr int kSteps = D / 16;
-  static constexpr int kNTiles = D / 8;
+  static constexpr int kHalfTiles = D / 16;                   // 8-dim n-tiles per half of D
 };
 
 template <int D, int KT>
-__global__ void __launch_bounds__(KT * 32)
+__global__ void __launch_bounds__(2 * KT * 32, 1)
     sel_attn_bwd_dkv_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
-                            const __grid_constant__ CUtensorMap tmV) {
+                            const __grid_constant__ CUtensorMap tmV,
+                            const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmD) {
   using C = DkvCfg<D, KT>;
   extern __shared__ uint8_t smem_raw[];
   const int c = blockIdx.x;
@@ -410,112 +435,176 @@ __global__ void __launch_bounds__(KT * 32)
   }
   const int l = lo;
   const int q0 = p.offs[l] + (c - p.choffs[l]) * kQueriesPerChunk;
-  const int q1 = min(q0 + kQueriesPerChunk, p.offs[l + 1]);
+  const int nq = min(q0 + kQueriesPerChunk, p.offs[l + 1]) - q0;
   const int t = l % p.nblk;
   const int bg = l / p.nblk;
   const int g = bg % static_cast<int>(p.G);
   const int b = bg / static_cast<int>(p.G);
+  const int64_t hbase = static_cast<int64_t>(g) * kHeadsPerGroup;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int kt = warp >> 1;  // 16-key tile of the block
+  const int dh = warp & 1;   // half of D this warp accumulates
   const int gid = lane >> 2;
   const int tig = lane & 3;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sK = base, sV = base + C::kBlockBytes;
-  const uint32_t bar = base + 2 * C::kBlockBytes;
+  const uint32_t stages = base + C::kStageOffset;
+  const uint32_t bar_blk = base + C::kBarOffset;
+  const uint32_t full = bar_blk + 8, empty = full + 8 * C::kStages;
   const int n_blk = t * p.bs;  // first key of the block
-  if (threadIdx.x == 0) {
-    const uint64_t keep = l2_policy_evict_last();
-    mbar_init(bar, 1);
-    fence_mbar_init();
+  const float* stage_rec = reinterpret_cast<const float*>(smem_raw + (base - smem_u32(smem_raw)) +
+                                                          C::kStageOffset + C::kRecOffset);
+
+  // query i of the chunk -> stage i % kStages (its Q and dO head rows, record)
+  auto issue_query = [&](int i) {
+    const int s = i % C::kStages;
+    const uint32_t st = stages + s * C::kStageBytes;
+    const int m = __ldg(p.lists + q0 + i);
+    const int qrow = static_cast<int>((b * p.M + m) * p.H + hbase);
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, 2 * C::kBlockBytes);
+    mbar_arrive_expect_tx(full + 8 * s, C::kStageTx);
 #pragma unroll
     for (int h = 0; h < C::kBoxes; ++h) {
-      tma_load_4d(sK + h * C::kBoxBytesBlk, &tmK, bar, h * kBoxCols, g, n_blk, b, keep);
-      tma_load_4d(sV + h * C::kBoxBytesBlk, &tmV, bar, h * kBoxCols, g, n_blk, b, keep);
+      tma_load_2d(st + h * C::kRowBox, &tmQ, full + 8 * s, h * kBoxCols, qrow);
+      tma_load_2d(st + (C::kBoxes + h) * C::kRowBox, &tmD, full + 8 * s, h * kBoxCols, qrow);
     }
+    bulk_load(st + C::kRecOffset, p.rec + ((b * p.M + m) * p.G + g) * 16, 64, full + 8 * s);
+  };
+
+  if (threadIdx.x == 0) {
+    const uint64_t keep = l2_policy_evict_last();
+    mbar_init(bar_blk, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full + 8 * s, 1);
+      mbar_init(empty + 8 * s, C::kWarps);
+    }
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar_blk, 2 * C::kBlockBytes);
+#pragma unroll
+    for (int h = 0; h < C::kBoxes; ++h) {
+      tma_load_4d(sK + h * C::kBoxBytesBlk, &tmK, bar_blk, h * kBoxCols, g, n_blk, b, keep);
+      tma_load_4d(sV + h * C::kBoxBytesBlk, &tmV, bar_blk, h * kBoxCols, g, n_blk, b, keep);
+    }
+    for (int i = 0; i < nq && i < C::kStages; ++i) issue_query(i);
   }
   __syncthreads();
-  if (!__all_sync(kFull, wait_phase(bar, 0, kWaitLimitNs))) {
-    // the load never landed; wait (bounded) once more so it cannot land later
-    if (lane == 0 && warp == 0) report_timeout();
-    wait_phase(bar, 0, kWaitLimitNs);
-    return;
+  int issued = nq < C::kStages ? nq : C::kStages;  // meaningful in thread 0 only
+  bool ok = __all_sync(kFull, wait_phase(bar_blk, 0, kWaitLimitNs));
+
+  // this warp's 16 keys of K and V as cached A fragments (all of D)
+  const int nw0 = n_blk + kt * kTileKeys;
+  uint32_t kf[C::kSteps][4], vf[C::kSteps][4];
+  if (ok) {
+    const uint32_t ka = (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
+    const int ka_hi = lane >> 4;
+    const int sw = lane & 7;
+#pragma unroll
+    for (int k = 0; k < C::kSteps; ++k) {
+      const uint32_t off = kt * kTileKeys * 128 + ka + (k >> 2) * C::kBoxBytesBlk +
+                           ((((k & 3) * 2 + ka_hi) ^ sw) << 4);
+      ldsm_x4(sK + off, kf[k][0], kf[k][1], kf[k][2], kf[k][3]);
+      ldsm_x4(sV + off, vf[k][0], vf[k][1], vf[k][2], vf[k][3]);
+    }
   }
-
-  const int nw0 = n_blk + warp * kTileKeys;  // this warp's first key
-  const uint32_t wK = sK + warp * kTileKeys * 128, wV = sV + warp * kTileKeys * 128;
-  const uint32_t ka = (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
-  const int ka_hi = lane >> 4;
-  const int sw = lane & 7;
   const float sl2 = p.sl2;
-  constexpr float kLog2e = 1.4426950408889634f;
-
-  float dk[C::kNTiles][4], dv[C::kNTiles][4];
+  float dk[C::kHalfTiles][4], dv[C::kHalfTiles][4];
 #pragma unroll
-  for (int j = 0; j < C::kNTiles; ++j)
+  for (int j = 0; j < C::kHalfTiles; ++j)
     dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = dv[j][0] = dv[j][1] = dv[j][2] = dv[j][3] = 0.f;
+  // ldmatrix of a stage's head rows: tile = lane >> 3, row = head lane & 7
+  const int qrow_l = lane & 7;
+  const int qtile = lane >> 3;
 
-  for (int qi = q0; qi < q1; ++qi) {
-    const int m = __ldg(p.lists + qi);
+  int i = 0;
+  for (; ok && i < nq; ++i) {
+    const int s = i % C::kStages;
+    const uint32_t ph = (i / C::kStages) & 1;
+    const uint32_t st = stages + s * C::kStageBytes;
+    if (!__all_sync(kFull, wait_phase(full + 8 * s, ph, kWaitLimitNs))) {
+      ok = false;
+      break;
+    }
+    const int m = __ldg(p.lists + q0 + i);
     const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
-    if (nw0 > lastkey) continue;  // all of this warp's keys are in the future
-    const int64_t hbase = static_cast<int64_t>(g) * kHeadsPerGroup;
-    const int64_t row = (b * p.M + m) * p.H + hbase;
-    uint32_t qf[C::kSteps][2], df[C::kSteps][2];
-    {
-      const __half* q = p.Q + (row + gid) * D + 2 * tig;
-      const float* dob = p.dO + (row + gid) * D + 2 * tig;
+    if (nw0 <= lastkey) {  // else all of this warp's keys are in the query's future
+      uint32_t qf[C::kSteps][2], df[C::kSteps][2];
 #pragma unroll
-      for (int k = 0; k < C::kSteps; ++k) {
-        qf[k][0] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k));
-        qf[k][1] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k + 8));
-        df[k][0] = ld_f32x2_as_half2(dob + 16 * k);
-        df[k][1] = ld_f32x2_as_half2(dob + 16 * k + 8);
+      for (int k = 0; k < C::kSteps; k += 2) {
+        const int cc = 2 * k + qtile;  // 16-byte column chunk of D
+        const uint32_t off = (cc >> 3) * C::kRowBox + qrow_l * 128 + (((cc & 7) ^ qrow_l) << 4);
+        ldsm_x4(st + off, qf[k][0], qf[k][1], qf[k + 1][0], qf[k + 1][1]);
+        ldsm_x4(st + C::kBoxes * C::kRowBox + off, df[k][0], df[k][1], df[k + 1][0],
+                df[k + 1][1]);
       }
-    }
-    const float lsa = __ldg(p.LSE + (b * p.H + hbase + 2 * tig) * p.M + m) * kLog2e;
-    const float lsb = __ldg(p.LSE + (b * p.H + hbase + 2 * tig + 1) * p.M + m) * kLog2e;
-    const float dla = __ldg(p.delta + (b * p.H + hbase + 2 * tig) * p.M + m);
-    const float dlb = __ldg(p.delta + (b * p.H + hbase + 2 * tig + 1) * p.M + m);
-
-    // S^T and dP^T (16 keys x 8 heads) for this warp's keys
-    float s[4] = {0.f, 0.f, 0.f, 0.f}, dp[4] = {0.f, 0.f, 0.f, 0.f};
+      const float* rec = stage_rec + s * (C::kStageBytes / 4);
+      const float lsa = rec[2 * tig], lsb = rec[2 * tig + 1];
+      const float dla = rec[8 + 2 * tig], dlb = rec[8 + 2 * tig + 1];
+      // S^T and dP^T (16 keys x 8 heads), two chains each
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < C::kSteps; ++k) {
-      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-      const uint32_t off = (k >> 2) * C::kBoxBytesBlk + ((((k & 3) * 2 + ka_hi) ^ sw) << 4);
-      ldsm_x4(wK + ka + off, a0, a1, a2, a3);
-      ldsm_x4(wV + ka + off, b0, b1, b2, b3);
-      mma_16816(s, a0, a1, a2, a3, qf[k][0], qf[k][1]);
-      mma_16816(dp, b0, b1, b2, b3, df[k][0], df[k][1]);
-    }
-    const bool va = nw0 + gid <= lastkey, vb = nw0 + gid + 8 <= lastkey;
-    float pr[4], ds[4];
-    pr[0] = va ? ex2(fmaf(s[0], sl2, -lsa)) : 0.f;
-    pr[1] = va ? ex2(fmaf(s[1], sl2, -lsb)) : 0.f;
-    pr[2] = vb ? ex2(fmaf(s[2], sl2, -lsa)) : 0.f;
-    pr[3] = vb ? ex2(fmaf(s[3], sl2, -lsb)) : 0.f;
-    ds[0] = va ? pr[0] * (dp[0] - dla) : 0.f;
-    ds[1] = va ? pr[1] * (dp[1] - dlb) : 0.f;
-    ds[2] = vb ? pr[2] * (dp[2] - dla) : 0.f;
-    ds[3] = vb ? pr[3] * (dp[3] - dlb) : 0.f;
-    // A operands (16 keys x 8 heads): the C layout of S^T is the A layout of
-    // m16n8k8
-    const uint32_t pa0 = pack_half2(pr[0], pr[1]), pa1 = pack_half2(pr[2], pr[3]);
-    const uint32_t sa0 = pack_half2(ds[0], ds[1]), sa1 = pack_half2(ds[2], ds[3]);
-    // dV (16 keys x D) += P^T dO ; dK (16 keys x D) += dS^T Q ; B operands
-    // (heads x 8 dims) are the transposes of the dO / Q fragments
-#pragma unroll
-    for (int k = 0; k < C::kSteps; ++k) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int j = 2 * k + h;
-        mma_1688(dv[j], pa0, pa1, movmatrix_t(df[k][h]));
-        mma_1688(dk[j], sa0, sa1, movmatrix_t(qf[k][h]));
+      for (int k = 0; k < C::kSteps; k += 2) {
+        mma_16816(s0, kf[k][0], kf[k][1], kf[k][2], kf[k][3], qf[k][0], qf[k][1]);
+        mma_16816(d0, vf[k][0], vf[k][1], vf[k][2], vf[k][3], df[k][0], df[k][1]);
+        mma_16816(s1, kf[k + 1][0], kf[k + 1][1], kf[k + 1][2], kf[k + 1][3], qf[k + 1][0],
+                  qf[k + 1][1]);
+        mma_16816(d1, vf[k + 1][0], vf[k + 1][1], vf[k + 1][2], vf[k + 1][3], df[k + 1][0],
+                  df[k + 1][1]);
       }
+      const bool va = nw0 + gid <= lastkey, vb = nw0 + gid + 8 <= lastkey;
+      float pr[4], ds[4];
+      pr[0] = va ? ex2(fmaf(s0[0] + s1[0], sl2, -lsa)) : 0.f;
+      pr[1] = va ? ex2(fmaf(s0[1] + s1[1], sl2, -lsb)) : 0.f;
+      pr[2] = vb ? ex2(fmaf(s0[2] + s1[2], sl2, -lsa)) : 0.f;
+      pr[3] = vb ? ex2(fmaf(s0[3] + s1[3], sl2, -lsb)) : 0.f;
+      ds[0] = va ? pr[0] * (d0[0] + d1[0] - dla) : 0.f;
+      ds[1] = va ? pr[1] * (d0[1] + d1[1] - dlb) : 0.f;
+      ds[2] = vb ? pr[2] * (d0[2] + d1[2] - dla) : 0.f;
+      ds[3] = vb ? pr[3] * (d0[3] + d1[3] - dlb) : 0.f;
+      // A operands (16 keys x 8 heads): the C layout of S^T is the A layout of
+      // m16n8k8; B operands (8 heads x 8 dims) are transposed Q / dO fragments
+      const uint32_t pa0 = pack_half2(pr[0], pr[1]), pa1 = pack_half2(pr[2], pr[3]);
+      const uint32_t sa0 = pack_half2(ds[0], ds[1]), sa1 = pack_half2(ds[2], ds[3]);
+      // this warp's half of D (branch on the warp-uniform half so that every
+      // fragment index is a compile-time constant)
+      auto accumulate = [&](auto half) {
+        constexpr int h0 = decltype(half)::value * C::kHalfTiles;
+#pragma unroll
+        for (int jj = 0; jj < C::kHalfTiles; ++jj) {
+          const int j = h0 + jj;  // 8-dim tile of D
+          mma_1688(dv[jj], pa0, pa1, movmatrix_t(df[j >> 1][j & 1]));
+          mma_1688(dk[jj], sa0, sa1, movmatrix_t(qf[j >> 1][j & 1]));
+        }
+      };
+      if (dh == 0)
+        accumulate(std::integral_constant<int, 0>{});
+      else
+        accumulate(std::integral_constant<int, 1>{});
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + 8 * s);
+    if (warp == 0 && i + C::kStages < nq) {
+      // refill this stage once every warp is done with it
+      if (!__all_sync(kFull, wait_phase(empty + 8 * s, ph, kWaitLimitNs))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) issue_query(i + C::kStages);
+      issued = i + C::kStages + 1;
+    }
+  }
+  if (!ok) {
+    // let every copy this CTA requested land before it can exit
+    if (lane == 0) report_timeout();
+    if (threadIdx.x == 0) {
+      wait_phase(bar_blk, 0, kWaitLimitNs);
+      for (int j = i; j < issued; ++j)
+        wait_phase(full + 8 * (j % C::kStages), (j / C::kStages) & 1, kWaitLimitNs);
+    }
+    return;
   }
 
   // add this chunk's partial sums into dK / dV (rows past N are not written)
@@ -523,13 +612,14 @@ __global__ void __launch_bounds__(KT * 32)
   for (int r = 0; r < 2; ++r) {
     const int n = nw0 + gid + 8 * r;
     if (n >= p.N) continue;
-    float* dkr = p.dK + ((b * p.N + n) * p.G + g) * D + 2 * tig;
-    float* dvr = p.dV + ((b * p.N + n) * p.G + g) * D + 2 * tig;
+    float* dkr = p.dK + ((b * p.N + n) * p.G + g) * D + dh * (D / 2) + 2 * tig;
+    float* dvr = p.dV + ((b * p.N + n) * p.G + g) * D + dh * (D / 2) + 2 * tig;
 #pragma unroll
-    for (int j = 0; j < C::kNTiles; ++j) {
-      atomicAdd(reinterpret_cast<float2*>(dkr + 8 * j),
-                make_float2(dk[j][2 * r] * p.scale, dk[j][2 * r + 1] * p.scale));
-      atomicAdd(reinterpret_cast<float2*>(dvr + 8 * j), make_float2(dv[j][2 * r], dv[j][2 * r + 1]));
+    for (int jj = 0; jj < C::kHalfTiles; ++jj) {
+      atomicAdd(reinterpret_cast<float2*>(dkr + 8 * jj),
+                make_float2(dk[jj][2 * r] * p.scale, dk[jj][2 * r + 1] * p.scale));
+      atomicAdd(reinterpret_cast<float2*>(dvr + 8 * jj),
+                make_float2(dv[jj][2 * r], dv[jj][2 * r + 1]));
     }
   }
 }
@@ -539,21 +629,23 @@ __global__ void __launch_bounds__(KT * 32)
 // ---------------------------------------------------------------------------
 
 struct BwdPlan {
-  size_t off_delta, off_count, off_cursor, off_offs, off_choffs, off_lists, total;
+  size_t off_do16, off_rec, off_count, off_cursor, off_offs, off_choffs, off_lists, total;
   int64_t L, entries;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t T,
-                        int bs) {
+static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
+                        int64_t T, int bs) {
   BwdPlan pl;
   const int64_t nblk = (N + bs - 1) / bs;
   pl.L = B * G * nblk;
   pl.entries = B * M * G * T;
   size_t at = 0;
-  pl.off_delta = at;
-  at += align256(static_cast<size_t>(B * H * M) * 4);
+  pl.off_do16 = at;
+  at += align256(static_cast<size_t>(B * M * H * D) * 2);
+  pl.off_rec = at;
+  at += align256(static_cast<size_t>(B * M * G) * 64);
   pl.off_count = at;
   at += align256(static_cast<size_t>(pl.L) * 4);
   pl.off_cursor = at;
@@ -578,7 +670,8 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   int* offs = reinterpret_cast<int*>(ws + pl.off_offs);
   int* choffs = reinterpret_cast<int*>(ws + pl.off_choffs);
   int* lists = reinterpret_cast<int*>(ws + pl.off_lists);
-  p.delta = reinterpret_cast<float*>(ws + pl.off_delta);
+  p.dO16 = reinterpret_cast<__half*>(ws + pl.off_do16);
+  p.rec = reinterpret_cast<float*>(ws + pl.off_rec);
   p.offs = offs;
   p.choffs = choffs;
   p.lists = lists;
@@ -622,6 +715,10 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
 
   // stage 3: dK, dV; grid bound: sum over lists of ceil(count / chunk)
+  CUtensorMap tq, tdo;
+  if (!encode_rows_map(&tq, p.Q, B * p.M * p.H, D, kHeadsPerGroup) ||
+      !encode_rows_map(&tdo, p.dO16, B * p.M * p.H, D, kHeadsPerGroup))
+    return NSA_ERR_LAUNCH;
   const int64_t chunks = (pl.entries + kQueriesPerChunk - 1) / kQueriesPerChunk + pl.L;
   if (p.bs == 64) {
     using Ck = DkvCfg<D, 4>;
@@ -629,14 +726,16 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, Ck::kSmemBytes) !=
         cudaSuccess)
       return NSA_ERR_LAUNCH;
-    kk<<<static_cast<unsigned>(chunks), 4 * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb);
+    kk<<<static_cast<unsigned>(chunks), Ck::kWarps * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb, tq,
+                                                                             tdo);
   } else {
     using Ck = DkvCfg<D, 2>;
     auto kk = sel_attn_bwd_dkv_kernel<D, 2>;
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, Ck::kSmemBytes) !=
         cudaSuccess)
       return NSA_ERR_LAUNCH;
-    kk<<<static_cast<unsigned>(chunks), 2 * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb);
+    kk<<<static_cast<unsigned>(chunks), Ck::kWarps * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb, tq,
+                                                                             tdo);
   }
   return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
@@ -682,7 +781,7 @@ int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_
   const int chk = nsa::check_sizes(B, M, N, H, G, D, T, block_size);
   if (chk != NSA_OK) return chk;
   if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
-  return static_cast<int64_t>(nsa::bwd_plan(B, M, N, H, G, T, block_size).total);
+  return static_cast<int64_t>(nsa::bwd_plan(B, M, N, H, G, D, T, block_size).total);
 }
 
 int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* block_indices,
@@ -694,7 +793,7 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t*
   const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
   if (chk != NSA_OK) return chk;
   if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
-  const BwdPlan pl = bwd_plan(B, M, N, H, G, T, block_size);
+  const BwdPlan pl = bwd_plan(B, M, N, H, G, D, T, block_size);
   if (pl.L > (int64_t(1) << 31) - 2) return NSA_ERR_SHAPE;
   if (B == 0 || (M == 0 && N == 0)) return NSA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -750,7 +849,7 @@ int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
   const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
   if (chk != NSA_OK) return chk;
   if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
-  const BwdPlan pl = bwd_plan(B, M, N, H, G, T, block_size);
+  const BwdPlan pl = bwd_plan(B, M, N, H, G, D, T, block_size);
   if (pl.L > (int64_t(1) << 31) - 2) return NSA_ERR_SHAPE;
   if (pl.total > kNoAllocScratchBytes) return NSA_ERR_SCRATCH;
   if (B == 0 || M == 0) {
