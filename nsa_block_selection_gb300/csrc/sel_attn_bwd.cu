@@ -406,10 +406,13 @@ struct DkvCfg {
   static constexpr int kRecOffset = 2 * kBoxes * kRowBox;     // after the Q and dO boxes
   static constexpr int kStageBytes = kRecOffset + 1024;       // record, keeps 1 KB alignment
   static constexpr int kStageTx = kRecOffset + 64;            // bytes each stage receives
-  static constexpr int kStages = 4;
+  // queries in flight: their Q / dO rows sit at random places in memory, so
+  // the ring must cover a DRAM round trip of several query iterations
+  static constexpr int kStages = 16;
   static constexpr int kStageOffset = 2 * kBlockBytes;
   static constexpr int kBarOffset = kStageOffset + kStages * kStageBytes;
-  static constexpr int kSmemBytes = kBarOffset + (1 + 2 * kStages) * 8 + 1024;
+  static constexpr int kListOffset = kBarOffset + (1 + 2 * kStages) * 8;
+  static constexpr int kSmemBytes = kListOffset + kQueriesPerChunk * 4 + 1024;
   static constexpr int kSteps = D / 16;
   static constexpr int kHalfTiles = D / 16;                   // 8-dim n-tiles per half of D
 };
@@ -457,11 +460,12 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
   const float* stage_rec = reinterpret_cast<const float*>(smem_raw + (base - smem_u32(smem_raw)) +
                                                           C::kStageOffset + C::kRecOffset);
 
+  int* qlist = reinterpret_cast<int*>(smem_raw + (base - smem_u32(smem_raw)) + C::kListOffset);
   // query i of the chunk -> stage i % kStages (its Q and dO head rows, record)
   auto issue_query = [&](int i) {
     const int s = i % C::kStages;
     const uint32_t st = stages + s * C::kStageBytes;
-    const int m = __ldg(p.lists + q0 + i);
+    const int m = qlist[i];
     const int qrow = static_cast<int>((b * p.M + m) * p.H + hbase);
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(full + 8 * s, C::kStageTx);
@@ -473,6 +477,7 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
     bulk_load(st + C::kRecOffset, p.rec + ((b * p.M + m) * p.G + g) * 16, 64, full + 8 * s);
   };
 
+  for (int j = threadIdx.x; j < nq; j += blockDim.x) qlist[j] = __ldg(p.lists + q0 + j);
   if (threadIdx.x == 0) {
     const uint64_t keep = l2_policy_evict_last();
     mbar_init(bar_blk, 1);
@@ -488,10 +493,11 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
       tma_load_4d(sK + h * C::kBoxBytesBlk, &tmK, bar_blk, h * kBoxCols, g, n_blk, b, keep);
       tma_load_4d(sV + h * C::kBoxBytesBlk, &tmV, bar_blk, h * kBoxCols, g, n_blk, b, keep);
     }
-    for (int i = 0; i < nq && i < C::kStages; ++i) issue_query(i);
   }
-  __syncthreads();
-  int issued = nq < C::kStages ? nq : C::kStages;  // meaningful in thread 0 only
+  __syncthreads();  // barriers initialised, query list in shared memory
+  if (threadIdx.x == 0)
+    for (int i = 0; i < nq && i < C::kStages; ++i) issue_query(i);
+  int issued = nq < C::kStages ? nq : C::kStages;  // meaningful in warp 0 only
   bool ok = __all_sync(kFull, wait_phase(bar_blk, 0, kWaitLimitNs));
 
   // this warp's 16 keys of K and V as cached A fragments (all of D)
@@ -518,90 +524,114 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
   const int qrow_l = lane & 7;
   const int qtile = lane >> 3;
 
-  int i = 0;
-  for (; ok && i < nq; ++i) {
+  using Frag = uint32_t[C::kSteps][2];
+  // Query i's Q / dO fragments, record and position into registers; the stage
+  // is released right away (and warp 0 refills it) so that the next query's
+  // copy overlaps this one's arithmetic.
+  auto fetch = [&](int i, Frag& qf, Frag& df, float (&rc)[4], int& m) -> bool {
     const int s = i % C::kStages;
     const uint32_t ph = (i / C::kStages) & 1;
     const uint32_t st = stages + s * C::kStageBytes;
-    if (!__all_sync(kFull, wait_phase(full + 8 * s, ph, kWaitLimitNs))) {
-      ok = false;
-      break;
+    if (!__all_sync(kFull, wait_phase(full + 8 * s, ph, kWaitLimitNs))) return false;
+#pragma unroll
+    for (int k = 0; k < C::kSteps; k += 2) {
+      const int cc = 2 * k + qtile;  // 16-byte column chunk of D
+      const uint32_t off = (cc >> 3) * C::kRowBox + qrow_l * 128 + (((cc & 7) ^ qrow_l) << 4);
+      ldsm_x4(st + off, qf[k][0], qf[k][1], qf[k + 1][0], qf[k + 1][1]);
+      ldsm_x4(st + C::kBoxes * C::kRowBox + off, df[k][0], df[k][1], df[k + 1][0], df[k + 1][1]);
     }
-    const int m = __ldg(p.lists + q0 + i);
-    const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
-    if (nw0 <= lastkey) {  // else all of this warp's keys are in the query's future
-      uint32_t qf[C::kSteps][2], df[C::kSteps][2];
-#pragma unroll
-      for (int k = 0; k < C::kSteps; k += 2) {
-        const int cc = 2 * k + qtile;  // 16-byte column chunk of D
-        const uint32_t off = (cc >> 3) * C::kRowBox + qrow_l * 128 + (((cc & 7) ^ qrow_l) << 4);
-        ldsm_x4(st + off, qf[k][0], qf[k][1], qf[k + 1][0], qf[k + 1][1]);
-        ldsm_x4(st + C::kBoxes * C::kRowBox + off, df[k][0], df[k][1], df[k + 1][0],
-                df[k + 1][1]);
-      }
-      const float* rec = stage_rec + s * (C::kStageBytes / 4);
-      const float lsa = rec[2 * tig], lsb = rec[2 * tig + 1];
-      const float dla = rec[8 + 2 * tig], dlb = rec[8 + 2 * tig + 1];
-      // S^T and dP^T (16 keys x 8 heads), two chains each
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int k = 0; k < C::kSteps; k += 2) {
-        mma_16816(s0, kf[k][0], kf[k][1], kf[k][2], kf[k][3], qf[k][0], qf[k][1]);
-        mma_16816(d0, vf[k][0], vf[k][1], vf[k][2], vf[k][3], df[k][0], df[k][1]);
-        mma_16816(s1, kf[k + 1][0], kf[k + 1][1], kf[k + 1][2], kf[k + 1][3], qf[k + 1][0],
-                  qf[k + 1][1]);
-        mma_16816(d1, vf[k + 1][0], vf[k + 1][1], vf[k + 1][2], vf[k + 1][3], df[k + 1][0],
-                  df[k + 1][1]);
-      }
-      const bool va = nw0 + gid <= lastkey, vb = nw0 + gid + 8 <= lastkey;
-      float pr[4], ds[4];
-      pr[0] = va ? ex2(fmaf(s0[0] + s1[0], sl2, -lsa)) : 0.f;
-      pr[1] = va ? ex2(fmaf(s0[1] + s1[1], sl2, -lsb)) : 0.f;
-      pr[2] = vb ? ex2(fmaf(s0[2] + s1[2], sl2, -lsa)) : 0.f;
-      pr[3] = vb ? ex2(fmaf(s0[3] + s1[3], sl2, -lsb)) : 0.f;
-      ds[0] = va ? pr[0] * (d0[0] + d1[0] - dla) : 0.f;
-      ds[1] = va ? pr[1] * (d0[1] + d1[1] - dlb) : 0.f;
-      ds[2] = vb ? pr[2] * (d0[2] + d1[2] - dla) : 0.f;
-      ds[3] = vb ? pr[3] * (d0[3] + d1[3] - dlb) : 0.f;
-      // A operands (16 keys x 8 heads): the C layout of S^T is the A layout of
-      // m16n8k8; B operands (8 heads x 8 dims) are transposed Q / dO fragments
-      const uint32_t pa0 = pack_half2(pr[0], pr[1]), pa1 = pack_half2(pr[2], pr[3]);
-      const uint32_t sa0 = pack_half2(ds[0], ds[1]), sa1 = pack_half2(ds[2], ds[3]);
-      // this warp's half of D (branch on the warp-uniform half so that every
-      // fragment index is a compile-time constant)
-      auto accumulate = [&](auto half) {
-        constexpr int h0 = decltype(half)::value * C::kHalfTiles;
-#pragma unroll
-        for (int jj = 0; jj < C::kHalfTiles; ++jj) {
-          const int j = h0 + jj;  // 8-dim tile of D
-          mma_1688(dv[jj], pa0, pa1, movmatrix_t(df[j >> 1][j & 1]));
-          mma_1688(dk[jj], sa0, sa1, movmatrix_t(qf[j >> 1][j & 1]));
-        }
-      };
-      if (dh == 0)
-        accumulate(std::integral_constant<int, 0>{});
-      else
-        accumulate(std::integral_constant<int, 1>{});
-    }
+    const float* rec = stage_rec + s * (C::kStageBytes / 4);
+    rc[0] = rec[2 * tig];
+    rc[1] = rec[2 * tig + 1];
+    rc[2] = rec[8 + 2 * tig];
+    rc[3] = rec[8 + 2 * tig + 1];
+    m = qlist[i];
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + 8 * s);
     if (warp == 0 && i + C::kStages < nq) {
-      // refill this stage once every warp is done with it
-      if (!__all_sync(kFull, wait_phase(empty + 8 * s, ph, kWaitLimitNs))) {
-        ok = false;
-        break;
-      }
+      // refill the stage once every warp has taken its copy
+      if (!__all_sync(kFull, wait_phase(empty + 8 * s, ph, kWaitLimitNs))) return false;
       if (lane == 0) issue_query(i + C::kStages);
       issued = i + C::kStages + 1;
     }
+    return true;
+  };
+
+  auto compute = [&](const Frag& qf, const Frag& df, const float (&rc)[4], int m) {
+    const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
+    if (nw0 > lastkey) return;  // all of this warp's keys are in the query's future
+    // S^T and dP^T (16 keys x 8 heads), two chains each
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < C::kSteps; k += 2) {
+      mma_16816(s0, kf[k][0], kf[k][1], kf[k][2], kf[k][3], qf[k][0], qf[k][1]);
+      mma_16816(d0, vf[k][0], vf[k][1], vf[k][2], vf[k][3], df[k][0], df[k][1]);
+      mma_16816(s1, kf[k + 1][0], kf[k + 1][1], kf[k + 1][2], kf[k + 1][3], qf[k + 1][0],
+                qf[k + 1][1]);
+      mma_16816(d1, vf[k + 1][0], vf[k + 1][1], vf[k + 1][2], vf[k + 1][3], df[k + 1][0],
+                df[k + 1][1]);
+    }
+    const bool va = nw0 + gid <= lastkey, vb = nw0 + gid + 8 <= lastkey;
+    float pr[4], ds[4];
+    pr[0] = va ? ex2(fmaf(s0[0] + s1[0], sl2, -rc[0])) : 0.f;
+    pr[1] = va ? ex2(fmaf(s0[1] + s1[1], sl2, -rc[1])) : 0.f;
+    pr[2] = vb ? ex2(fmaf(s0[2] + s1[2], sl2, -rc[0])) : 0.f;
+    pr[3] = vb ? ex2(fmaf(s0[3] + s1[3], sl2, -rc[1])) : 0.f;
+    ds[0] = va ? pr[0] * (d0[0] + d1[0] - rc[2]) : 0.f;
+    ds[1] = va ? pr[1] * (d0[1] + d1[1] - rc[3]) : 0.f;
+    ds[2] = vb ? pr[2] * (d0[2] + d1[2] - rc[2]) : 0.f;
+    ds[3] = vb ? pr[3] * (d0[3] + d1[3] - rc[3]) : 0.f;
+    // A operands (16 keys x 8 heads): the C layout of S^T is the A layout of
+    // m16n8k8; B operands (8 heads x 8 dims) are transposed Q / dO fragments
+    const uint32_t pa0 = pack_half2(pr[0], pr[1]), pa1 = pack_half2(pr[2], pr[3]);
+    const uint32_t sa0 = pack_half2(ds[0], ds[1]), sa1 = pack_half2(ds[2], ds[3]);
+    // this warp's half of D (branch on the warp-uniform half so that every
+    // fragment index is a compile-time constant)
+    auto accumulate = [&](auto half) {
+      constexpr int h0 = decltype(half)::value * C::kHalfTiles;
+#pragma unroll
+      for (int jj = 0; jj < C::kHalfTiles; ++jj) {
+        const int j = h0 + jj;  // 8-dim tile of D
+        mma_1688(dv[jj], pa0, pa1, movmatrix_t(df[j >> 1][j & 1]));
+        mma_1688(dk[jj], sa0, sa1, movmatrix_t(qf[j >> 1][j & 1]));
+      }
+    };
+    if (dh == 0)
+      accumulate(std::integral_constant<int, 0>{});
+    else
+      accumulate(std::integral_constant<int, 1>{});
+  };
+
+  // queries alternate between two register sets (A, B): query i+1 is fetched
+  // before query i is computed
+  uint32_t qa[C::kSteps][2], da[C::kSteps][2], qb[C::kSteps][2], db[C::kSteps][2];
+  float ra[4], rb[4];
+  int ma = 0, mb = 0;
+  int i = 0;         // next query to compute
+  int failed_at = -1;
+  if (ok && nq > 0 && !fetch(0, qa, da, ra, ma)) failed_at = 0;
+  if (!ok) failed_at = 0;
+  while (failed_at < 0 && i < nq) {
+    if (i + 1 < nq && !fetch(i + 1, qb, db, rb, mb)) {
+      failed_at = i + 1;
+      break;
+    }
+    compute(qa, da, ra, ma);
+    if (++i >= nq) break;
+    if (i + 1 < nq && !fetch(i + 1, qa, da, ra, ma)) {
+      failed_at = i + 1;
+      break;
+    }
+    compute(qb, db, rb, mb);
+    ++i;
   }
-  if (!ok) {
+  if (failed_at >= 0) {
     // let every copy this CTA requested land before it can exit
     if (lane == 0) report_timeout();
     if (threadIdx.x == 0) {
       wait_phase(bar_blk, 0, kWaitLimitNs);
-      for (int j = i; j < issued; ++j)
+      for (int j = failed_at; j < issued; ++j)
         wait_phase(full + 8 * (j % C::kStages), (j / C::kStages) & 1, kWaitLimitNs);
     }
     return;
