@@ -51,7 +51,7 @@ typedef enum nsa_status {
   NSA_ERR_SHAPE = -2,       /* a size is negative or the sizes are too large */
   NSA_ERR_BLOCK_SIZE = -3,  /* block_size not in {32, 64}                     */
   NSA_ERR_HEAD_DIM = -4,    /* D not in {64, 128}                             */
-  NSA_ERR_GROUPS = -5,      /* G <= 0, H % G != 0 or H/G != 8                 */
+  NSA_ERR_GROUPS = -5,      /* H % G != 0, or H/G > 8 and not a multiple of 8 */
   NSA_ERR_ALIGN = -6,       /* Q, K, V or O not 16-byte aligned, LSE or
                                block_indices not 4-byte aligned               */
   NSA_ERR_LAUNCH = -7,      /* the CUDA runtime refused the launch or a copy
@@ -78,7 +78,10 @@ int nsa_version(void);
  *   O              device, fp32,      [B, M, H, D]   (output)
  *   LSE            device, fp32,      [B, H, M]      (output, natural log)
  *   B, M, N, T     >= 0; an empty problem (B*M == 0) returns NSA_OK at once
- *   H, G, D        > 0, H % G == 0, H/G == 8, D in {64, 128}
+ *   H, G, D        > 0, H % G == 0, D in {64, 128}; H/G (query heads per
+ *                  KV group) is 1..8, or a multiple of 8 -- a warp serves up to
+ *                  8 heads of a group: fewer are padded, more are split into
+ *                  sub-groups of 8 that share the group's K/V and index row
  *   block_size     32 or 64
  *   scale          score multiplier; <= 0 selects 1/sqrt(D)
  *   stream         cudaStream_t to launch on (NULL = legacy default stream)

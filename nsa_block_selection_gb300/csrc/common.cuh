@@ -15,7 +15,15 @@
 
 namespace nsa {
 
+// Query heads one warp serves (the N of its MMAs). A KV group with fewer
+// heads pads the rest; a group with more (a multiple of 8) is split into
+// sub-groups of 8 that share the group's K/V and index row.
 constexpr int kHeadsPerGroup = 8;
+
+// Sub-groups of 8 heads for `hpg` heads per KV group (1 when hpg <= 8).
+__host__ __device__ inline int head_subgroups(int64_t hpg) {
+  return static_cast<int>((hpg + kHeadsPerGroup - 1) / kHeadsPerGroup);
+}
 constexpr int kTileKeys = 16;
 constexpr int kBoxCols = 64;                   // d columns per TMA box: 128-byte rows
 constexpr int kBoxBytes = kTileKeys * 128;     // one box: 16 keys x 64 d x fp16

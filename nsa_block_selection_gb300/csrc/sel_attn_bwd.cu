@@ -53,12 +53,13 @@ struct BwdProblem {
   float* dK;
   float* dV;
   __half* dO16;        // [B, M, H, D] fp16 copy of dO (stage 1 -> stage 3)
-  float* rec;          // [B * M * G][16]: LSE * log2(e) of the 8 heads, then delta
+  float* rec;          // [B * M * G * nsub][16]: LSE * log2(e) of 8 heads, then delta
   const int* offs;     // [L + 1] list starts (L = B * G * nblk)
   const int* choffs;   // [L + 1] chunk starts
   const int* lists;    // query ids, list by list
   int64_t B, M, N, H, G, T;
-  int64_t units;       // B * G * M
+  int64_t units;       // B * G * nsub * M
+  int hpg, nsub;       // heads per KV group, sub-groups of 8 heads
   int bs, nblk, L;
   float sl2;           // scale * log2(e)
   float scale;
@@ -95,11 +96,16 @@ __global__ void __launch_bounds__(WARPS * 32, 3)
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
   if (unit >= p.units) return;
   const int64_t m = unit % p.M;
-  const int64_t bg = unit / p.M;
+  const int64_t r = unit / p.M;
+  const int sub = static_cast<int>(r % p.nsub);
+  const int64_t bg = r / p.nsub;
   const int g = static_cast<int>(bg % p.G);
   const int b = static_cast<int>(bg / p.G);
   const int gid = lane >> 2;
   const int tig = lane & 3;
+  // heads hbase + j, j < hw; MMA columns j >= hw are padding
+  const int hw = p.hpg - sub * kHeadsPerGroup < kHeadsPerGroup ? p.hpg - sub * kHeadsPerGroup
+                                                                : kHeadsPerGroup;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t slots = base + warp * C::kWarpBytes;  // K0, K1, V
@@ -115,24 +121,28 @@ __global__ void __launch_bounds__(WARPS * 32, 3)
   }
   __syncwarp();
 
-  const int64_t hbase = static_cast<int64_t>(g) * kHeadsPerGroup;
-  const int64_t row = (b * p.M + m) * p.H + hbase;  // first head of the group
+  const int64_t hbase = static_cast<int64_t>(g) * p.hpg + sub * kHeadsPerGroup;
+  const int64_t row = (b * p.M + m) * p.H + hbase;  // first head of this warp
   // Q^T and dO^T as B operands (head gid, dims 16k + 2tig (+1, +8, +9));
-  // delta of head gid from the same dO elements against O (fp32)
+  // delta of head gid from the same dO elements against O (fp32); padding
+  // columns are zero
   uint32_t qf[C::kSteps][2], df[C::kSteps][2];
   float dpart = 0.f;
   {
+    const bool real = gid < hw;
     const __half* q = p.Q + (row + gid) * D + 2 * tig;
     const float* dob = p.dO + (row + gid) * D + 2 * tig;
     const float* ob = p.O + (row + gid) * D + 2 * tig;
 #pragma unroll
     for (int k = 0; k < C::kSteps; ++k) {
-      qf[k][0] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k));
-      qf[k][1] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k + 8));
+      qf[k][0] = real ? __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k)) : 0u;
+      qf[k][1] = real ? __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k + 8)) : 0u;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float2 d2 = __ldg(reinterpret_cast<const float2*>(dob + 16 * k + 8 * h));
-        const float2 o2 = __ldg(reinterpret_cast<const float2*>(ob + 16 * k + 8 * h));
+        const float2 d2 =
+            real ? __ldg(reinterpret_cast<const float2*>(dob + 16 * k + 8 * h)) : float2{0.f, 0.f};
+        const float2 o2 =
+            real ? __ldg(reinterpret_cast<const float2*>(ob + 16 * k + 8 * h)) : float2{0.f, 0.f};
         df[k][h] = pack_half2(d2.x, d2.y);
         dpart = fmaf(d2.x, o2.x, fmaf(d2.y, o2.y, dpart));
       }
@@ -143,19 +153,24 @@ __global__ void __launch_bounds__(WARPS * 32, 3)
   const float dla = __shfl_sync(kFull, dpart, (2 * tig) * 4);      // head 2tig
   const float dlb = __shfl_sync(kFull, dpart, (2 * tig + 1) * 4);  // head 2tig+1
   constexpr float kLog2e = 1.4426950408889634f;
-  const float lsa = p.LSE[(b * p.H + hbase + 2 * tig) * p.M + m] * kLog2e;
-  const float lsb = p.LSE[(b * p.H + hbase + 2 * tig + 1) * p.M + m] * kLog2e;
+  // padding columns: LSE = +inf makes their probabilities exactly 0
+  const float lsa =
+      2 * tig < hw ? p.LSE[(b * p.H + hbase + 2 * tig) * p.M + m] * kLog2e : INFINITY;
+  const float lsb =
+      2 * tig + 1 < hw ? p.LSE[(b * p.H + hbase + 2 * tig + 1) * p.M + m] * kLog2e : INFINITY;
   {
-    // for stage 3: dO as fp16 rows, and one 64-byte record per (b, m, g)
-    uint32_t* d16 = reinterpret_cast<uint32_t*>(p.dO16 + (row + gid) * D + 2 * tig);
+    // for stage 3: dO as fp16 rows, and one 64-byte record per (b, m, g, sub)
+    if (gid < hw) {
+      uint32_t* d16 = reinterpret_cast<uint32_t*>(p.dO16 + (row + gid) * D + 2 * tig);
 #pragma unroll
-    for (int k = 0; k < C::kSteps; ++k) {
-      d16[8 * k] = df[k][0];
-      d16[8 * k + 4] = df[k][1];
+      for (int k = 0; k < C::kSteps; ++k) {
+        d16[8 * k] = df[k][0];
+        d16[8 * k + 4] = df[k][1];
+      }
     }
     if (tig == 0) {
-      float* rec = p.rec + ((b * p.M + m) * p.G + g) * 16;
-      rec[gid] = p.LSE[(b * p.H + hbase + gid) * p.M + m] * kLog2e;
+      float* rec = p.rec + (((b * p.M + m) * p.G + g) * p.nsub + sub) * 16;
+      rec[gid] = gid < hw ? p.LSE[(b * p.H + hbase + gid) * p.M + m] * kLog2e : INFINITY;
       rec[8 + gid] = dpart;
     }
   }
@@ -284,12 +299,17 @@ __global__ void __launch_bounds__(WARPS * 32, 3)
     return;
   }
   float* o = p.dQ + (row + 2 * tig) * D + gid;
+  const bool ha = 2 * tig < hw, hb = 2 * tig + 1 < hw;
 #pragma unroll
   for (int d = 0; d < C::kSteps; ++d) {
-    o[16 * d] = acc[d][0] * p.scale;
-    o[D + 16 * d] = acc[d][1] * p.scale;
-    o[16 * d + 8] = acc[d][2] * p.scale;
-    o[D + 16 * d + 8] = acc[d][3] * p.scale;
+    if (ha) {
+      o[16 * d] = acc[d][0] * p.scale;
+      o[16 * d + 8] = acc[d][2] * p.scale;
+    }
+    if (hb) {
+      o[D + 16 * d] = acc[d][1] * p.scale;
+      o[D + 16 * d + 8] = acc[d][3] * p.scale;
+    }
   }
 }
 
@@ -405,7 +425,6 @@ struct DkvCfg {
   static constexpr int kRowBox = 8 * 128;                     // 8 head rows x 64 dims
   static constexpr int kRecOffset = 2 * kBoxes * kRowBox;     // after the Q and dO boxes
   static constexpr int kStageBytes = kRecOffset + 1024;       // record, keeps 1 KB alignment
-  static constexpr int kStageTx = kRecOffset + 64;            // bytes each stage receives
   // queries in flight: their Q / dO rows sit at random places in memory, so
   // the ring must cover a DRAM round trip of several query iterations
   static constexpr int kStages = 16;
@@ -439,11 +458,13 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
   const int l = lo;
   const int q0 = p.offs[l] + (c - p.choffs[l]) * kQueriesPerChunk;
   const int nq = min(q0 + kQueriesPerChunk, p.offs[l + 1]) - q0;
+  const int nitems = nq * p.nsub;  // (query, sub-group of 8 heads) pairs
   const int t = l % p.nblk;
   const int bg = l / p.nblk;
   const int g = bg % static_cast<int>(p.G);
   const int b = bg / static_cast<int>(p.G);
-  const int64_t hbase = static_cast<int64_t>(g) * kHeadsPerGroup;
+  const int64_t hgroup = static_cast<int64_t>(g) * p.hpg;  // first head of the group
+  const int hw0 = p.hpg < kHeadsPerGroup ? p.hpg : kHeadsPerGroup;  // head rows per item
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -461,23 +482,36 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
                                                           C::kStageOffset + C::kRecOffset);
 
   int* qlist = reinterpret_cast<int*>(smem_raw + (base - smem_u32(smem_raw)) + C::kListOffset);
-  // query i of the chunk -> stage i % kStages (its Q and dO head rows, record)
+  // item i of the chunk -> stage i % kStages (its Q and dO head rows, record)
   auto issue_query = [&](int i) {
     const int s = i % C::kStages;
     const uint32_t st = stages + s * C::kStageBytes;
-    const int m = qlist[i];
-    const int qrow = static_cast<int>((b * p.M + m) * p.H + hbase);
+    const int m = qlist[i / p.nsub];
+    const int sub = i % p.nsub;
+    const int qrow = static_cast<int>((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup);
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(full + 8 * s, C::kStageTx);
+    mbar_arrive_expect_tx(full + 8 * s, 2 * C::kBoxes * hw0 * 128 + 64);
 #pragma unroll
     for (int h = 0; h < C::kBoxes; ++h) {
       tma_load_2d(st + h * C::kRowBox, &tmQ, full + 8 * s, h * kBoxCols, qrow);
       tma_load_2d(st + (C::kBoxes + h) * C::kRowBox, &tmD, full + 8 * s, h * kBoxCols, qrow);
     }
-    bulk_load(st + C::kRecOffset, p.rec + ((b * p.M + m) * p.G + g) * 16, 64, full + 8 * s);
+    bulk_load(st + C::kRecOffset, p.rec + (((b * p.M + m) * p.G + g) * p.nsub + sub) * 16, 64,
+              full + 8 * s);
   };
 
   for (int j = threadIdx.x; j < nq; j += blockDim.x) qlist[j] = __ldg(p.lists + q0 + j);
+  if (hw0 < kHeadsPerGroup) {
+    // head rows the copies never write (groups of fewer than 8 heads): zero,
+    // so the padding columns multiply zeros
+    const int per_stage = 2 * C::kBoxes * (kHeadsPerGroup - hw0) * 8;  // 16-byte pieces
+    for (int e = threadIdx.x; e < C::kStages * per_stage; e += blockDim.x) {
+      const int s = e / per_stage, r = e % per_stage;
+      const int box = r / ((kHeadsPerGroup - hw0) * 8);
+      const int row = hw0 + (r / 8) % (kHeadsPerGroup - hw0);
+      st_shared_zero16(stages + s * C::kStageBytes + box * C::kRowBox + row * 128 + (r % 8) * 16);
+    }
+  }
   if (threadIdx.x == 0) {
     const uint64_t keep = l2_policy_evict_last();
     mbar_init(bar_blk, 1);
@@ -496,8 +530,8 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
   }
   __syncthreads();  // barriers initialised, query list in shared memory
   if (threadIdx.x == 0)
-    for (int i = 0; i < nq && i < C::kStages; ++i) issue_query(i);
-  int issued = nq < C::kStages ? nq : C::kStages;  // meaningful in warp 0 only
+    for (int i = 0; i < nitems && i < C::kStages; ++i) issue_query(i);
+  int issued = nitems < C::kStages ? nitems : C::kStages;  // meaningful in warp 0 only
   bool ok = __all_sync(kFull, wait_phase(bar_blk, 0, kWaitLimitNs));
 
   // this warp's 16 keys of K and V as cached A fragments (all of D)
@@ -545,10 +579,10 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
     rc[1] = rec[2 * tig + 1];
     rc[2] = rec[8 + 2 * tig];
     rc[3] = rec[8 + 2 * tig + 1];
-    m = qlist[i];
+    m = qlist[i / p.nsub];
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + 8 * s);
-    if (warp == 0 && i + C::kStages < nq) {
+    if (warp == 0 && i + C::kStages < nitems) {
       // refill the stage once every warp has taken its copy
       if (!__all_sync(kFull, wait_phase(empty + 8 * s, ph, kWaitLimitNs))) return false;
       if (lane == 0) issue_query(i + C::kStages);
@@ -610,16 +644,16 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
   int ma = 0, mb = 0;
   int i = 0;         // next query to compute
   int failed_at = -1;
-  if (ok && nq > 0 && !fetch(0, qa, da, ra, ma)) failed_at = 0;
+  if (ok && nitems > 0 && !fetch(0, qa, da, ra, ma)) failed_at = 0;
   if (!ok) failed_at = 0;
-  while (failed_at < 0 && i < nq) {
-    if (i + 1 < nq && !fetch(i + 1, qb, db, rb, mb)) {
+  while (failed_at < 0 && i < nitems) {
+    if (i + 1 < nitems && !fetch(i + 1, qb, db, rb, mb)) {
       failed_at = i + 1;
       break;
     }
     compute(qa, da, ra, ma);
-    if (++i >= nq) break;
-    if (i + 1 < nq && !fetch(i + 1, qa, da, ra, ma)) {
+    if (++i >= nitems) break;
+    if (i + 1 < nitems && !fetch(i + 1, qa, da, ra, ma)) {
       failed_at = i + 1;
       break;
     }
@@ -668,6 +702,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
                         int64_t T, int bs) {
   BwdPlan pl;
+  const int64_t nsub = G > 0 ? head_subgroups(H / G) : 1;
   const int64_t nblk = (N + bs - 1) / bs;
   pl.L = B * G * nblk;
   pl.entries = B * M * G * T;
@@ -675,7 +710,7 @@ static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, i
   pl.off_do16 = at;
   at += align256(static_cast<size_t>(B * M * H * D) * 2);
   pl.off_rec = at;
-  at += align256(static_cast<size_t>(B * M * G) * 64);
+  at += align256(static_cast<size_t>(B * M * G * nsub) * 64);
   pl.off_count = at;
   at += align256(static_cast<size_t>(pl.L) * 4);
   pl.off_cursor = at;
@@ -705,7 +740,7 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   p.offs = offs;
   p.choffs = choffs;
   p.lists = lists;
-  const int64_t B = p.units / (p.M * p.G);
+  const int64_t B = p.units / (p.M * p.G * p.nsub);
   if (p.N > 0 &&
       (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
        cudaMemsetAsync(p.dV, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
@@ -746,8 +781,9 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
 
   // stage 3: dK, dV; grid bound: sum over lists of ceil(count / chunk)
   CUtensorMap tq, tdo;
-  if (!encode_rows_map(&tq, p.Q, B * p.M * p.H, D, kHeadsPerGroup) ||
-      !encode_rows_map(&tdo, p.dO16, B * p.M * p.H, D, kHeadsPerGroup))
+  const int hw0 = p.hpg < kHeadsPerGroup ? p.hpg : kHeadsPerGroup;
+  if (!encode_rows_map(&tq, p.Q, B * p.M * p.H, D, hw0) ||
+      !encode_rows_map(&tdo, p.dO16, B * p.M * p.H, D, hw0))
     return NSA_ERR_LAUNCH;
   const int64_t chunks = (pl.entries + kQueriesPerChunk - 1) / kQueriesPerChunk + pl.L;
   if (p.bs == 64) {
@@ -860,7 +896,9 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t*
   p.G = G;
   p.T = T;
   p.B = B;
-  p.units = B * G * M;
+  p.hpg = static_cast<int>(H / G);
+  p.nsub = head_subgroups(p.hpg);
+  p.units = B * G * p.nsub * M;
   p.bs = block_size;
   p.nblk = static_cast<int>((N + block_size - 1) / block_size);
   p.L = static_cast<int>(pl.L);
@@ -914,7 +952,9 @@ int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
   p.G = G;
   p.T = T;
   p.B = B;
-  p.units = B * G * M;
+  p.hpg = static_cast<int>(H / G);
+  p.nsub = head_subgroups(p.hpg);
+  p.units = B * G * p.nsub * M;
   p.bs = block_size;
   p.nblk = static_cast<int>((N + block_size - 1) / block_size);
   p.L = static_cast<int>(pl.L);

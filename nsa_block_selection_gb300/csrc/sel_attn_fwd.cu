@@ -60,7 +60,9 @@ struct Problem {
   float* LSE;
   int64_t M, N, H, G, T;
   int64_t m_off;  // query position of row 0 (a chunk of a longer sequence)
-  int64_t units;  // B * G * M
+  int64_t units;  // B * G * nsub * M
+  int hpg;        // query heads per KV group
+  int nsub;       // sub-groups of 8 heads per KV group
   int bs;
   int nblk;       // ceil(N / bs)
   float sl2;      // scale * log2(e)
@@ -93,11 +95,17 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   const int lane = threadIdx.x & 31;
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
   if (unit >= p.units) return;
-  // unit -> (b, g, m), m fastest: the warps in flight share one group's K/V
+  // unit -> (b, g, sub-group, m), m fastest: the warps in flight share one
+  // group's K/V
   const int64_t m = unit % p.M;
-  const int64_t bg = unit / p.M;
+  const int64_t r = unit / p.M;
+  const int sub = static_cast<int>(r % p.nsub);
+  const int64_t bg = r / p.nsub;
   const int g = static_cast<int>(bg % p.G);
   const int b = static_cast<int>(bg / p.G);
+  // heads of this warp: hbase + j for j < hw (MMA columns j >= hw are padding)
+  const int hw = p.hpg - sub * kHeadsPerGroup < kHeadsPerGroup ? p.hpg - sub * kHeadsPerGroup
+                                                                : kHeadsPerGroup;
   const int gid = lane >> 2;  // MMA group id (row within an 8-row slab)
   const int tig = lane & 3;   // thread in group
 
@@ -115,15 +123,16 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   }
   __syncwarp();
 
-  const int64_t hbase = static_cast<int64_t>(g) * kHeadsPerGroup;
-  // Q^T as the B operand of S^T = K Q^T: head gid, dims 16k + 2tig (+1, +8, +9).
+  const int64_t hbase = static_cast<int64_t>(g) * p.hpg + sub * kHeadsPerGroup;
+  // Q^T as the B operand of S^T = K Q^T: head gid, dims 16k + 2tig (+1, +8, +9);
+  // zero for padding columns
   uint32_t qf[C::kSteps][2];
   {
     const __half* q = p.Q + ((b * p.M + m) * p.H + hbase + gid) * D + 2 * tig;
 #pragma unroll
     for (int k = 0; k < C::kSteps; ++k) {
-      qf[k][0] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k));
-      qf[k][1] = __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k + 8));
+      qf[k][0] = gid < hw ? __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k)) : 0u;
+      qf[k][1] = gid < hw ? __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k + 8)) : 0u;
     }
   }
 
@@ -293,18 +302,23 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   const float inva = la > 0.f ? 1.f / la : 0.f;
   const float invb = lb > 0.f ? 1.f / lb : 0.f;
   float* o = p.O + ((b * p.M + m) * p.H + hbase + 2 * tig) * D + gid;
+  const bool ha = 2 * tig < hw, hb = 2 * tig + 1 < hw;  // real heads, not padding
 #pragma unroll
   for (int i = 0; i < C::kSteps; ++i) {
-    o[16 * i] = acc[i][0] * inva;
-    o[D + 16 * i] = acc[i][1] * invb;
-    o[16 * i + 8] = acc[i][2] * inva;
-    o[D + 16 * i + 8] = acc[i][3] * invb;
+    if (ha) {
+      o[16 * i] = acc[i][0] * inva;
+      o[16 * i + 8] = acc[i][2] * inva;
+    }
+    if (hb) {
+      o[D + 16 * i] = acc[i][1] * invb;
+      o[D + 16 * i + 8] = acc[i][3] * invb;
+    }
   }
   if (gid == 0) {
     constexpr float kLn2 = 0.69314718055994530942f;
     float* L = p.LSE + (b * p.H + hbase + 2 * tig) * p.M + m;
-    L[0] = la > 0.f ? (m2a + __log2f(la)) * kLn2 : -INFINITY;
-    L[p.M] = lb > 0.f ? (m2b + __log2f(lb)) * kLn2 : -INFINITY;
+    if (ha) L[0] = la > 0.f ? (m2a + __log2f(la)) * kLn2 : -INFINITY;
+    if (hb) L[p.M] = lb > 0.f ? (m2b + __log2f(lb)) * kLn2 : -INFINITY;
   }
 }
 
@@ -353,13 +367,17 @@ namespace nsa {
 int check_sizes(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
                 int block_size) {
   if (B < 0 || M < 0 || N < 0 || T < 0 || H <= 0 || G <= 0 || D <= 0) return NSA_ERR_SHAPE;
-  if (H % G != 0 || H / G != kHeadsPerGroup) return NSA_ERR_GROUPS;
+  // heads per group: up to 8 (padded), or a multiple of 8 (sub-groups)
+  if (H % G != 0) return NSA_ERR_GROUPS;
+  const int64_t hpg = H / G;
+  if (hpg > kHeadsPerGroup && hpg % kHeadsPerGroup != 0) return NSA_ERR_GROUPS;
   if (D != 64 && D != 128) return NSA_ERR_HEAD_DIM;
   if (block_size != 32 && block_size != 64) return NSA_ERR_BLOCK_SIZE;
-  // 32-bit key / coordinate arithmetic inside the kernel; grid of B*G*M warps
+  // 32-bit key / coordinate arithmetic inside the kernel; grid of
+  // B*G*(sub-groups)*M warps; 2-D tensor maps over B*M*H head rows
   const int64_t lim = (int64_t(1) << 31) - 1024;
-  if (M > lim || N > lim || T > lim || G > lim || B > lim) return NSA_ERR_SHAPE;
-  if (B > 0 && M > 0 && B * G > lim / M) return NSA_ERR_SHAPE;
+  if (M > lim || N > lim || T > lim || H > lim || B > lim) return NSA_ERR_SHAPE;
+  if (B > 0 && M > 0 && B * H > lim / M) return NSA_ERR_SHAPE;
   return NSA_OK;
 }
 
@@ -392,7 +410,9 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
   p.G = G;
   p.T = T;
   p.m_off = m_off;
-  p.units = B * G * M;
+  p.hpg = static_cast<int>(H / G);
+  p.nsub = head_subgroups(p.hpg);
+  p.units = B * G * p.nsub * M;
   p.bs = block_size;
   p.nblk = static_cast<int>((N + block_size - 1) / block_size);
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
@@ -411,7 +431,8 @@ const char* nsa_status_string(int status) {
     case NSA_ERR_SHAPE: return "invalid shape";
     case NSA_ERR_BLOCK_SIZE: return "block_size must be 32 or 64";
     case NSA_ERR_HEAD_DIM: return "head dim D must be 64 or 128";
-    case NSA_ERR_GROUPS: return "H must be 8 * G (8 query heads per KV group)";
+    case NSA_ERR_GROUPS:
+      return "H must be a multiple of G, with H/G <= 8 or a multiple of 8";
     case NSA_ERR_ALIGN: return "misaligned pointer";
     case NSA_ERR_LAUNCH: return "CUDA launch failed";
     case NSA_ERR_TIMEOUT: return "device wait timed out";

@@ -64,7 +64,7 @@ def test_status_strings(lib):
 @pytest.mark.parametrize("over,status", [
     (dict(B=-1), -2), (dict(M=-3), -2), (dict(N=-1), -2), (dict(T=-1), -2),
     (dict(H=0), -2), (dict(G=0), -2), (dict(D=0), -2),
-    (dict(H=12, G=2), -5), (dict(H=16, G=4), -5), (dict(H=15, G=2), -5),
+    (dict(H=24, G=2), -5), (dict(H=20, G=2), -5), (dict(H=15, G=2), -5),
     (dict(D=96), -4), (dict(D=256), -4),
     (dict(bs=16), -3), (dict(bs=128), -3), (dict(bs=0), -3),
     (dict(M=1 << 31), -2), (dict(N=1 << 40), -2),
@@ -100,7 +100,7 @@ def test_host_workspace_bytes(lib):
     assert f(1, 65536, 65536, 64, 8, 128, 16, 64, 0) == kv + 2 * per_slot2  # default: M/32
     assert f(1, 100, 100, 16, 2, 64, 4, 32, 1000) > 0       # chunk clipped to M
     assert f(1, 100, 100, 16, 2, 64, 4, 48, 0) == -3
-    assert f(1, 100, 100, 12, 2, 64, 4, 32, 0) == -5
+    assert f(1, 100, 100, 24, 2, 64, 4, 32, 0) == -5  # 12 heads per group
 
 
 def call_host(lib, q=FAKE, k=FAKE, v=FAKE, idx=FAKE, o=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 40,
@@ -125,3 +125,10 @@ def test_host_workspace_checks(lib):
     assert call_host(lib, ws=FAKE + 16, ws_bytes=need) == -6
     assert call_host(lib, bs=16) == -3
     assert call_host(lib, B=0, q=None, k=None, v=None, idx=None, o=None, lse=None, ws=None) == 0
+
+
+@pytest.mark.parametrize("H,G", [(16, 16), (16, 8), (12, 4), (16, 2), (64, 4), (96, 3)])
+def test_heads_per_group_accepted(lib, H, G):
+    # 1..8 heads per group, or a multiple of 8: the size checks pass (the
+    # empty problem then returns before any CUDA call)
+    assert call(lib, q=None, k=None, v=None, idx=None, o=None, lse=None, B=0, H=H, G=G) == 0

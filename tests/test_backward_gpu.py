@@ -123,3 +123,12 @@ def test_bwd_full_size(name):
     want = dO.astype(np.float64).reshape(w.B, w.M, w.G, hpg, w.D).sum(axis=(1, 3))
     np.testing.assert_allclose(dv.sum(axis=1), want, rtol=1e-4, atol=1e-3 * np.abs(want).max())
     assert np.abs(dk.sum(axis=1)).max() <= 1e-4 * np.abs(dk).sum(axis=1).max()
+
+
+@pytest.mark.parametrize("H,G,bs", [(4, 4, 64), (6, 2, 32), (16, 4, 64), (32, 2, 32)])
+def test_bwd_heads_per_group(H, G, bs):
+    """1, 3, 4 and 16 query heads per KV group."""
+    q, k, v, idx = small_inputs(1, 500, 500, H, G, 128, bs, 5, "first_two_local", seed=H + G)
+    dO = np.random.default_rng(H).standard_normal(q.shape).astype(np.float32)
+    got = _run(q, k, v, idx, dO, bs)
+    _check(got, q, k, v, idx, dO, bs, what=f"H{H} G{G}")

@@ -239,3 +239,19 @@ def test_cta_shared_blocks(M, bs, T, perm):
         idx = np.random.default_rng(1).permuted(idx, axis=-1).copy()
     O, L = run_cuda(q, k, v, idx, bs)
     check_all_rows(q, k, v, idx, bs, O, L, what=f"shared M{M} bs{bs} T{T}")
+
+
+@pytest.mark.parametrize("H,G", [(4, 4), (8, 4), (6, 2), (16, 4), (32, 2)])
+def test_heads_per_group(H, G):
+    """1, 2, 3, 4 and 16 query heads per KV group (padded or split into
+    sub-groups of 8), forward through the device and host entry points."""
+    import torch
+
+    from nsa_block_selection_gb300 import _lib
+
+    q, k, v, idx = _small(2, 600, 600, H, G, 128, 64, 5, "first_two_local", seed=H * 10 + G)
+    O, L = run_cuda(q, k, v, idx, 64)
+    check_all_rows(q, k, v, idx, 64, O, L, what=f"H{H} G{G}")
+    pin = [torch.from_numpy(x).pin_memory() for x in (q, k, v, idx)]
+    O_h, L_h = _lib.sel_attn_fwd_host(*pin, 64, chunk_m=128)
+    assert torch.equal(O_h, O.cpu()) and torch.equal(L_h, L.cpu())
