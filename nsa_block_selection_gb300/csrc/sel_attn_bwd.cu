@@ -436,7 +436,9 @@ struct DkvCfg {
   static constexpr int kHalfTiles = D / 16;                   // 8-dim n-tiles per half of D
 };
 
-template <int D, int KT>
+// SPLIT: the group has more than 8 heads (items are (query, sub-group) pairs);
+// otherwise one item per query.
+template <int D, int KT, bool SPLIT>
 __global__ void __launch_bounds__(2 * KT * 32, 1)
     sel_attn_bwd_dkv_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
@@ -458,7 +460,8 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
   const int l = lo;
   const int q0 = p.offs[l] + (c - p.choffs[l]) * kQueriesPerChunk;
   const int nq = min(q0 + kQueriesPerChunk, p.offs[l + 1]) - q0;
-  const int nitems = nq * p.nsub;  // (query, sub-group of 8 heads) pairs
+  const int nsub = SPLIT ? p.nsub : 1;
+  const int nitems = nq * nsub;  // (query, sub-group of 8 heads) pairs
   const int t = l % p.nblk;
   const int bg = l / p.nblk;
   const int g = bg % static_cast<int>(p.G);
@@ -486,8 +489,8 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
   auto issue_query = [&](int i) {
     const int s = i % C::kStages;
     const uint32_t st = stages + s * C::kStageBytes;
-    const int m = qlist[i / p.nsub];
-    const int sub = i % p.nsub;
+    const int m = qlist[SPLIT ? i / nsub : i];
+    const int sub = SPLIT ? i % nsub : 0;
     const int qrow = static_cast<int>((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup);
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(full + 8 * s, 2 * C::kBoxes * hw0 * 128 + 64);
@@ -496,7 +499,7 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
       tma_load_2d(st + h * C::kRowBox, &tmQ, full + 8 * s, h * kBoxCols, qrow);
       tma_load_2d(st + (C::kBoxes + h) * C::kRowBox, &tmD, full + 8 * s, h * kBoxCols, qrow);
     }
-    bulk_load(st + C::kRecOffset, p.rec + (((b * p.M + m) * p.G + g) * p.nsub + sub) * 16, 64,
+    bulk_load(st + C::kRecOffset, p.rec + (((b * p.M + m) * p.G + g) * nsub + sub) * 16, 64,
               full + 8 * s);
   };
 
@@ -579,7 +582,7 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
     rc[1] = rec[2 * tig + 1];
     rc[2] = rec[8 + 2 * tig];
     rc[3] = rec[8 + 2 * tig + 1];
-    m = qlist[i / p.nsub];
+    m = qlist[SPLIT ? i / nsub : i];
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + 8 * s);
     if (warp == 0 && i + C::kStages < nitems) {
@@ -786,23 +789,28 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
       !encode_rows_map(&tdo, p.dO16, B * p.M * p.H, D, hw0))
     return NSA_ERR_LAUNCH;
   const int64_t chunks = (pl.entries + kQueriesPerChunk - 1) / kQueriesPerChunk + pl.L;
-  if (p.bs == 64) {
-    using Ck = DkvCfg<D, 4>;
-    auto kk = sel_attn_bwd_dkv_kernel<D, 4>;
+  auto run = [&](auto kt, auto split) -> int {
+    constexpr int KT = decltype(kt)::value;
+    using Ck = DkvCfg<D, KT>;
+    auto kk = sel_attn_bwd_dkv_kernel<D, KT, decltype(split)::value>;
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, Ck::kSmemBytes) !=
         cudaSuccess)
       return NSA_ERR_LAUNCH;
     kk<<<static_cast<unsigned>(chunks), Ck::kWarps * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb, tq,
                                                                              tdo);
-  } else {
-    using Ck = DkvCfg<D, 2>;
-    auto kk = sel_attn_bwd_dkv_kernel<D, 2>;
-    if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, Ck::kSmemBytes) !=
-        cudaSuccess)
-      return NSA_ERR_LAUNCH;
-    kk<<<static_cast<unsigned>(chunks), Ck::kWarps * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb, tq,
-                                                                             tdo);
-  }
+    return NSA_OK;
+  };
+  using I2 = std::integral_constant<int, 2>;
+  using I4 = std::integral_constant<int, 4>;
+  using Yes = std::true_type;
+  using No = std::false_type;
+  const bool split = p.nsub > 1;
+  int rc;
+  if (p.bs == 64)
+    rc = split ? run(I4{}, Yes{}) : run(I4{}, No{});
+  else
+    rc = split ? run(I2{}, Yes{}) : run(I2{}, No{});
+  if (rc != NSA_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
