@@ -121,12 +121,15 @@ int64_t nsa_sel_attn_fwd_host_workspace_bytes(int64_t B, int64_t M, int64_t N, i
  *                            256-byte aligned, owned by the caller
  *   chunk_m                  queries per pipeline chunk, rounded up to a
  *                            multiple of 64 (<= 0: default, about M/32)
- *   stream                   caller's stream; the kernels run on it
+ *   stream                   caller's stream: the call's work starts after
+ *                            the work already queued on it, and it waits for
+ *                            all of the call's work
  *
  * The queries are processed in chunks of chunk_m positions. For each chunk
  * the call enqueues, on an internal upload stream, the copies of its Q rows,
  * its index rows and the K/V rows it can see (keys below the chunk's end,
- * each copied once); the kernel on `stream`; and on an internal download
+ * each copied once); the kernel (even chunks on `stream`, odd chunks on an
+ * internal second compute stream); and on an internal download
  * stream, the copies of its O rows and LSE columns. Chunk buffers are double
  * buffered in the workspace, so uploads, kernels and downloads of adjacent
  * chunks overlap. Copies overlap only if the host buffers are page-locked

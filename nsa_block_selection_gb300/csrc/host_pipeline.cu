@@ -4,8 +4,9 @@
 // slot c % 2 of the caller's device workspace:
 //   upload stream   : K/V rows [kv_done, min(N, end_c)) (each key row once),
 //                     Q rows and index rows of the chunk          -> event up[c%2]
-//   caller's stream : forward kernel over the chunk (query positions start
-//                     at the chunk's first position)              -> event fw[c%2]
+//   compute streams : forward kernel over the chunk (query positions start
+//                     at the chunk's first position); even chunks on the
+//                     caller's stream, odd chunks on a second one  -> event fw[c%2]
 //   download stream : O rows and LSE columns of the chunk         -> event dn[c%2]
 // Slot reuse is ordered by events: the upload of chunk c waits fw of chunk
 // c-2 (its Q/index slot has been read), the kernel of chunk c waits dn of
@@ -82,7 +83,7 @@ HostPlan make_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_
 // Streams and events of one call; released (deferred by CUDA until their
 // work completes) when the call returns.
 struct CallResources {
-  cudaStream_t up = nullptr, dn = nullptr;
+  cudaStream_t up = nullptr, dn = nullptr, fw2 = nullptr;
   cudaEvent_t start = nullptr, up_ev[2] = {nullptr, nullptr}, fw_ev[2] = {nullptr, nullptr},
               dn_ev[2] = {nullptr, nullptr};
   bool ok = true;
@@ -90,6 +91,7 @@ struct CallResources {
   CallResources() {
     ok = cudaStreamCreateWithFlags(&up, cudaStreamNonBlocking) == cudaSuccess &&
          cudaStreamCreateWithFlags(&dn, cudaStreamNonBlocking) == cudaSuccess &&
+         cudaStreamCreateWithFlags(&fw2, cudaStreamNonBlocking) == cudaSuccess &&
          cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess;
     for (int s = 0; s < 2 && ok; ++s)
       ok = cudaEventCreateWithFlags(&up_ev[s], cudaEventDisableTiming) == cudaSuccess &&
@@ -105,6 +107,7 @@ struct CallResources {
     if (start) cudaEventDestroy(start);
     if (up) cudaStreamDestroy(up);
     if (dn) cudaStreamDestroy(dn);
+    if (fw2) cudaStreamDestroy(fw2);
   }
 };
 
@@ -163,7 +166,8 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
 
   bool ok = cudaEventRecord(r.start, st) == cudaSuccess &&
             cudaStreamWaitEvent(r.up, r.start, 0) == cudaSuccess &&
-            cudaStreamWaitEvent(r.dn, r.start, 0) == cudaSuccess;
+            cudaStreamWaitEvent(r.dn, r.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(r.fw2, r.start, 0) == cudaSuccess;
   int64_t kv_done = 0;
   for (int64_t c = 0; c < pl.nchunks && ok; ++c) {
     const int s = static_cast<int>(c & 1);
@@ -194,15 +198,18 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
                         cudaMemcpyHostToDevice, r.up);
     ok = ok && cudaEventRecord(r.up_ev[s], r.up) == cudaSuccess;
 
-    // forward on the caller's stream
-    ok = ok && cudaStreamWaitEvent(st, r.up_ev[s], 0) == cudaSuccess;
-    if (c >= 2) ok = ok && cudaStreamWaitEvent(st, r.dn_ev[s], 0) == cudaSuccess;
+    // forward: chunks are independent (disjoint queries), so even chunks run
+    // on the caller's stream and odd ones on a second stream, letting one
+    // kernel's last wave overlap the next kernel
+    cudaStream_t fs = s == 0 ? st : r.fw2;
+    ok = ok && cudaStreamWaitEvent(fs, r.up_ev[s], 0) == cudaSuccess;
+    if (c >= 2) ok = ok && cudaStreamWaitEvent(fs, r.dn_ev[s], 0) == cudaSuccess;
     if (!ok) break;
     const int rc = launch_forward(dQ, N > 0 ? dK : nullptr, N > 0 ? dV : nullptr,
                                   T > 0 ? reinterpret_cast<const int32_t*>(dI) : nullptr, dO,
-                                  dL, B, mc, N, H, G, D, T, m0, block_size, scale, st);
+                                  dL, B, mc, N, H, G, D, T, m0, block_size, scale, fs);
     if (rc != NSA_OK) return rc;
-    ok = cudaEventRecord(r.fw_ev[s], st) == cudaSuccess;
+    ok = cudaEventRecord(r.fw_ev[s], fs) == cudaSuccess;
 
     // download: O rows [m0, m0+mc) of every batch, LSE columns of every (b, h)
     ok = ok && cudaStreamWaitEvent(r.dn, r.fw_ev[s], 0) == cudaSuccess;
