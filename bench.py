@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-bwd", action="store_true")
+    ap.add_argument("--skip-variants", action="store_true",
+                    help="skip timing the bf16-input and 16-bit-O forward variants")
     ap.add_argument("--cpu-rows", type=int, default=24576,
                     help="rows of the CPU-oracle sample")
     ap.add_argument("--seed", type=int, default=None)
@@ -92,13 +94,16 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
+FWD_KERNEL_SOURCES = ("common.cuh", "ptx.cuh", "sel_attn_fwd.cu", "sel_attn_fwd.cuh")
+
+
 def kernel_source_hash():
+    """Hash of the files the forward kernel is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nsa_block_selection_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in FWD_KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -371,6 +376,11 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.skip_bwd:
         backward = run_backward(w, q, k, v, idx, out, lse, work, flush, args)
 
+    # element-type variants of the forward on the same workload
+    variants = None
+    if rank == 0 and world == 1 and not args.skip_variants:
+        variants = run_variants(w, q, k, v, idx, work, flush, args)
+
     # dense-causal-equivalent run: same Q/K/V, every causal block listed
     dense = None
     if rank == 0 and world == 1 and not args.skip_dense:
@@ -409,6 +419,7 @@ def run_ours(args):
         "speedup_vs_dense_causal": dense["speedup"] if dense else None,
         "dense_causal": dense,
         "backward": backward,
+        "variants": variants,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -422,6 +433,36 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def run_variants(w, q, k, v, idx, work, flush, args):
+    """The forward with bf16 Q/K/V and/or a 16-bit O (nsa_sel_attn_fwd_ex),
+    timed like the headline run on the same index tensor (Q/K/V converted on
+    the device; the timing does not depend on the values)."""
+    import torch
+
+    from nsa_block_selection_gb300 import sel_attn_fwd
+
+    res = {}
+    steps = max(3, args.steps // 6)
+    lse = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=q.device)
+    for qkv, odt in (("bf16", "f32"), ("f16", "f16"), ("bf16", "bf16")):
+        dt = torch.bfloat16 if qkv == "bf16" else torch.float16
+        ot = torch.float32 if odt == "f32" else dt
+        tq, tk, tv = (x.to(dt) for x in (q, k, v))
+        out = torch.empty((w.B, w.M, w.H, w.D), dtype=ot, device=q.device)
+
+        def step():
+            sel_attn_fwd(tq, tk, tv, idx, w.block_size, w.scale, out=out, lse=lse)
+
+        times, _ = time_steps(step, steps, 3, flush, lambda: None)
+        t = statistics.mean(times)
+        res[f"{qkv}_in_{odt}_out"] = {"ms_per_step": t,
+                                      "tflops": work["flops"] / (t * 1e-3) / 1e12,
+                                      "steps": steps}
+        del tq, tk, tv, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_backward(w, q, k, v, idx, out, lse, work, flush, args):

@@ -59,9 +59,18 @@ typedef enum nsa_status {
   NSA_ERR_TIMEOUT = -8,     /* a bounded device-side wait gave up (reported by
                                nsa_sync_status)                               */
   NSA_ERR_WORKSPACE = -9,   /* workspace NULL or smaller than required        */
-  NSA_ERR_SCRATCH = -10     /* problem needs more scratch than the fixed
+  NSA_ERR_SCRATCH = -10,    /* problem needs more scratch than the fixed
                                buffer of nsa_sel_attn_bwd_noalloc (64 MiB)    */
+  NSA_ERR_DTYPE = -11       /* element type combination not supported by
+                               nsa_sel_attn_fwd_ex                            */
 } nsa_status;
+
+/* Element types of nsa_sel_attn_fwd_ex. */
+typedef enum nsa_dtype {
+  NSA_F16 = 0,   /* IEEE binary16                                  */
+  NSA_BF16 = 1,  /* bfloat16 (the upper 16 bits of an IEEE binary32) */
+  NSA_F32 = 2    /* IEEE binary32                                  */
+} nsa_dtype;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nsa_status_string(int status);
@@ -100,6 +109,28 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V,
                      int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                      int64_t D, int64_t T, int block_size, float scale,
                      void* stream);
+
+/*
+ * nsa_sel_attn_fwd_ex -- nsa_sel_attn_fwd with a choice of element types.
+ *
+ *   qkv_dtype  NSA_F16 or NSA_BF16: the type of Q, K and V (all three alike)
+ *   o_dtype    NSA_F32, or qkv_dtype: the type O is written in
+ *
+ * Every other argument, layout, check and property is that of
+ * nsa_sel_attn_fwd; LSE stays fp32. nsa_sel_attn_fwd is this call with
+ * (NSA_F16, NSA_F32). With bf16 inputs both products run as bf16 MMAs with
+ * fp32 accumulation, so the probabilities are rounded to bf16 (8 significant
+ * bits) before the PV product -- the bf16 reading of the "FP16 matmuls, FP32
+ * accumulation" requirement ("[wave] NSA: selection attention forward
+ * kernel", section "Requirements"). Scores, running max and row sums are
+ * fp32 in every combination; a 16-bit O is the fp32 result rounded to
+ * nearest even. Any other combination returns NSA_ERR_DTYPE before launch.
+ */
+int nsa_sel_attn_fwd_ex(const void* Q, const void* K, const void* V,
+                        const int32_t* block_indices, void* O, float* LSE,
+                        int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
+                        int64_t D, int64_t T, int block_size, float scale,
+                        int qkv_dtype, int o_dtype, void* stream);
 
 /*
  * nsa_sel_attn_fwd_host_workspace_bytes -- device workspace that

@@ -17,8 +17,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "lib", "libnsa_sel_attn.so")
 
 NSA_OK = 0
+NSA_F16, NSA_BF16, NSA_F32 = 0, 1, 2
 
-EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sync_status",
+EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sel_attn_fwd_ex",
+           "nsa_sync_status",
            "nsa_selftest_wait_timeout", "nsa_sel_attn_fwd_host_workspace_bytes",
            "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd",
            "nsa_sel_attn_bwd_noalloc")
@@ -51,6 +53,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_fwd.restype = c_int
     lib.nsa_sel_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
                                      c_int, ctypes.c_float, vp]
+    lib.nsa_sel_attn_fwd_ex.restype = c_int
+    lib.nsa_sel_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                        i64, c_int, ctypes.c_float, c_int, c_int, vp]
     lib.nsa_sync_status.restype = c_int
     lib.nsa_sync_status.argtypes = [vp]
     lib.nsa_selftest_wait_timeout.restype = c_int
@@ -82,40 +87,62 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr() if t is not None and t.numel() > 0 else None
 
 
+def _dtype_code(dt) -> int:
+    import torch
+
+    return {torch.float16: NSA_F16, torch.bfloat16: NSA_BF16, torch.float32: NSA_F32}[dt]
+
+
 def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float] = None,
-                 out=None, lse=None, stream=None):
+                 out=None, lse=None, stream=None, out_dtype=None):
     """NSA selection-attention forward on the GPU.
 
-    q: fp16 [B, M, H, D]; k, v: fp16 [B, N, G, D]; block_indices: int32
-    [B, M, G, T] (-1 = padding); all contiguous on one CUDA device.
-    Returns (O fp32 [B, M, H, D], LSE fp32 [B, H, M]); ``out``/``lse`` may be
-    given preallocated. ``stream`` defaults to torch's current stream.
+    q: fp16 or bf16 [B, M, H, D]; k, v: [B, N, G, D] of q's dtype;
+    block_indices: int32 [B, M, G, T] (-1 = padding); all contiguous on one
+    CUDA device. Returns (O [B, M, H, D], LSE fp32 [B, H, M]). O is fp32
+    unless ``out_dtype`` (or a preallocated ``out``) is q's dtype.
+    ``stream`` defaults to torch's current stream.
     """
     import torch
 
     lib = load()
-    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=True)
+    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=True,
+                                        qkv_dtypes=(torch.float16, torch.bfloat16))
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.float32
+    if out_dtype not in (torch.float32, q.dtype):
+        raise TypeError(f"O must be fp32 or {q.dtype}, got {out_dtype}")
     if out is None:
-        out = torch.empty((B, M, H, D), dtype=torch.float32, device=q.device)
+        out = torch.empty((B, M, H, D), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
-    if out.dtype != torch.float32 or tuple(out.shape) != (B, M, H, D) or not out.is_contiguous():
-        raise ValueError("out must be contiguous fp32 [B, M, H, D]")
+    if out.dtype != out_dtype or tuple(out.shape) != (B, M, H, D) or not out.is_contiguous():
+        raise ValueError(f"out must be contiguous {out_dtype} [B, M, H, D]")
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, M) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous fp32 [B, H, M]")
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
-    st = lib.nsa_sel_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out),
-                              _ptr(lse), B, M, N, H, G, D, T, int(block_size), sc,
-                              ctypes.c_void_p(stream.cuda_stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out), _ptr(lse), B, M, N, H,
+            G, D, T, int(block_size), sc)
+    if q.dtype == torch.float16 and out.dtype == torch.float32:
+        st = lib.nsa_sel_attn_fwd(*args, ctypes.c_void_p(stream.cuda_stream))
+        what = "nsa_sel_attn_fwd"
+    else:
+        st = lib.nsa_sel_attn_fwd_ex(*args, _dtype_code(q.dtype), _dtype_code(out.dtype),
+                                     ctypes.c_void_p(stream.cuda_stream))
+        what = "nsa_sel_attn_fwd_ex"
     if st != NSA_OK:
-        raise NsaError(st, "nsa_sel_attn_fwd")
+        raise NsaError(st, what)
     return out, lse
 
 
-def _check_common(q, k, v, block_indices, device_expected: bool):
+def _check_common(q, k, v, block_indices, device_expected: bool, qkv_dtypes=None):
     import torch
+
+    qkv_dtypes = qkv_dtypes or (torch.float16,)
+    if q.dtype not in qkv_dtypes:
+        raise TypeError(f"q must be one of {qkv_dtypes}, got {q.dtype}")
 
     B, M, H, D = q.shape
     Bk, N, G, Dk = k.shape
@@ -124,10 +151,12 @@ def _check_common(q, k, v, block_indices, device_expected: bool):
             tuple(block_indices.shape) != (B, M, G, T):
         raise ValueError("shape mismatch: q [B,M,H,D], k/v [B,N,G,D], "
                          "block_indices [B,M,G,T]")
-    for name, t, dt in (("q", q, torch.float16), ("k", k, torch.float16),
-                        ("v", v, torch.float16), ("block_indices", block_indices, torch.int32)):
+    named = (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype),
+             ("block_indices", block_indices, torch.int32))
+    for name, t, dt in named:
         if t.dtype != dt:
             raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+    for name, t, _ in named:
         if t.is_cuda != device_expected:
             raise ValueError(f"{name} must be a {'CUDA' if device_expected else 'CPU'} tensor")
         if not t.is_contiguous():

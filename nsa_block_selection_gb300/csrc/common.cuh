@@ -135,7 +135,8 @@ static inline EncodeTiledFn encode_fn() {
 
 // K or V [B, N, G, D] fp16 as a 4-D map (d, g, n, b); box = 64 d x 1 x rows x 1.
 static inline bool encode_kv_map(CUtensorMap* tm, const void* ptr, int64_t B, int64_t N,
-                                 int64_t G, int64_t D, int rows = kTileKeys) {
+                                 int64_t G, int64_t D, int rows = kTileKeys,
+                                 CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(G),
@@ -145,7 +146,7 @@ static inline bool encode_kv_map(CUtensorMap* tm, const void* ptr, int64_t B, in
                                  static_cast<cuuint64_t>(N * G * D * 2)};
   const cuuint32_t box[4] = {kBoxCols, 1, static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
-  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+  return enc(tm, dt, 4, const_cast<void*>(ptr), dims, strides, box,
              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

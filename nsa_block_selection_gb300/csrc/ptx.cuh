@@ -96,6 +96,42 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats rounded to nearest-even bf16, lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 16-bit operand type of the attention MMAs: fp16 or bf16 (A and B alike).
+template <bool BF16>
+__device__ __forceinline__ void mma_16816_t(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (BF16)
+    mma_16816_bf16(d, a0, a1, a2, a3, b0, b1);
+  else
+    mma_16816(d, a0, a1, a2, a3, b0, b1);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2_t(float lo, float hi) {
+  if constexpr (BF16)
+    return pack_bf162(lo, hi);
+  else
+    return pack_half2(lo, hi);
+}
+
 }  // namespace nsa
 
 namespace nsa {

@@ -54,9 +54,9 @@
 namespace nsa {
 
 struct Problem {
-  const __half* Q;
+  const uint16_t* Q;  // fp16 or bf16
   const int32_t* idx;
-  float* O;
+  void* O;            // fp32, or the inputs' 16-bit type
   float* LSE;
   int64_t M, N, H, G, T;
   int64_t m_off;  // query position of row 0 (a chunk of a longer sequence)
@@ -84,7 +84,9 @@ struct Cfg {
 // reference, so the result does not depend on it.
 constexpr float kMaxSlack = 8.0f;
 
-template <int D, int WARPS>
+// BF16: Q/K/V are bf16 (else fp16); P is rounded to the same type for the PV
+// product. O16: O is written in that 16-bit type (else fp32).
+template <int D, int WARPS, bool BF16, bool O16>
 __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     sel_attn_fwd_kernel(const Problem p, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   // zero for padding columns
   uint32_t qf[C::kSteps][2];
   {
-    const __half* q = p.Q + ((b * p.M + m) * p.H + hbase + gid) * D + 2 * tig;
+    const uint16_t* q = p.Q + ((b * p.M + m) * p.H + hbase + gid) * D + 2 * tig;
 #pragma unroll
     for (int k = 0; k < C::kSteps; ++k) {
       qf[k][0] = gid < hw ? __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k)) : 0u;
@@ -199,8 +201,8 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
       ldsm_x4(ka + (k >> 2) * kBoxBytes + ((((k & 3) * 2 + ka_hi) ^ sw) << 4), a0, a1, a2, a3);
       ldsm_x4(ka + ((k + 1) >> 2) * kBoxBytes + (((((k + 1) & 3) * 2 + ka_hi) ^ sw) << 4), b0,
               b1, b2, b3);
-      mma_16816(s, a0, a1, a2, a3, qf[k][0], qf[k][1]);
-      mma_16816(t, b0, b1, b2, b3, qf[k + 1][0], qf[k + 1][1]);
+      mma_16816_t<BF16>(s, a0, a1, a2, a3, qf[k][0], qf[k][1]);
+      mma_16816_t<BF16>(t, b0, b1, b2, b3, qf[k + 1][0], qf[k + 1][1]);
     }
     __syncwarp();
     have = walk.next(n_next);
@@ -250,8 +252,8 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     la += p0 + p2;
     lb += p1 + p3;
     // P^T as the B operand: (keys 2tig.., head gid) from (key gid, heads 2tig..)
-    const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
-    const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
+    const uint32_t pb0 = movmatrix_t(pack2_t<BF16>(p0, p1));
+    const uint32_t pb1 = movmatrix_t(pack2_t<BF16>(p2, p3));
 
     if (!__all_sync(kFull, wait_phase(bar_v, phase, kWaitLimitNs))) {
       timed_out = 2;
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     for (int i = 0; i < C::kSteps; ++i) {
       uint32_t a0, a1, a2, a3;
       ldsm_x4_t(va + (i >> 2) * kBoxBytes + ((((i & 3) * 2 + va_hi) ^ sw) << 4), a0, a1, a2, a3);
-      mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
+      mma_16816_t<BF16>(acc[i], a0, a1, a2, a3, pb0, pb1);
     }
     __syncwarp();
     if (have) issue(sv, bar_v, &tmV, n_next);  // slot 1 is free
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     return;
   }
 
-  // epilogue: finish the row sums, normalise, store O (fp32) and LSE
+  // epilogue: finish the row sums, normalise, store O and LSE
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     la += __shfl_xor_sync(kFull, la, off);
@@ -301,20 +303,38 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   }
   const float inva = la > 0.f ? 1.f / la : 0.f;
   const float invb = lb > 0.f ? 1.f / lb : 0.f;
-  float* o = p.O + ((b * p.M + m) * p.H + hbase + 2 * tig) * D + gid;
-  const bool ha = 2 * tig < hw, hb = 2 * tig + 1 < hw;  // real heads, not padding
+  if constexpr (O16) {
+    // round, then transpose each 8x8 (dim x head) quarter in registers so a
+    // lane holds two adjacent dims of head gid: one 4-byte store per pair
+    uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.O) +
+                                              ((b * p.M + m) * p.H + hbase + gid) * D) +
+                  tig;
 #pragma unroll
-  for (int i = 0; i < C::kSteps; ++i) {
-    if (ha) {
-      o[16 * i] = acc[i][0] * inva;
-      o[16 * i + 8] = acc[i][2] * inva;
+    for (int i = 0; i < C::kSteps; ++i) {
+      const uint32_t lo = movmatrix_t(pack2_t<BF16>(acc[i][0] * inva, acc[i][1] * invb));
+      const uint32_t hi = movmatrix_t(pack2_t<BF16>(acc[i][2] * inva, acc[i][3] * invb));
+      if (gid < hw) {
+        o[8 * i] = lo;
+        o[8 * i + 4] = hi;
+      }
     }
-    if (hb) {
-      o[D + 16 * i] = acc[i][1] * invb;
-      o[D + 16 * i + 8] = acc[i][3] * invb;
+  } else {
+    const bool ha = 2 * tig < hw, hb = 2 * tig + 1 < hw;  // real heads, not padding
+    float* o = static_cast<float*>(p.O) + ((b * p.M + m) * p.H + hbase + 2 * tig) * D + gid;
+#pragma unroll
+    for (int i = 0; i < C::kSteps; ++i) {
+      if (ha) {
+        o[16 * i] = acc[i][0] * inva;
+        o[16 * i + 8] = acc[i][2] * inva;
+      }
+      if (hb) {
+        o[D + 16 * i] = acc[i][1] * invb;
+        o[D + 16 * i + 8] = acc[i][3] * invb;
+      }
     }
   }
   if (gid == 0) {
+    const bool ha = 2 * tig < hw, hb = 2 * tig + 1 < hw;
     constexpr float kLn2 = 0.69314718055994530942f;
     float* L = p.LSE + (b * p.H + hbase + 2 * tig) * p.M + m;
     if (ha) L[0] = la > 0.f ? (m2a + __log2f(la)) * kLn2 : -INFINITY;
@@ -338,20 +358,23 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns) {
 
 // ---- host side ---------------------------------------------------------------
 
-template <int D>
+template <int D, bool BF16, bool O16>
 static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
                       cudaStream_t stream) {
   constexpr int W = NSA_WARPS;
   using C = Cfg<D, W>;
+  constexpr CUtensorMapDataType dt =
+      BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tk, tv;
   if (p.N > 0) {
-    if (!encode_kv_map(&tk, K, B, p.N, p.G, D) || !encode_kv_map(&tv, V, B, p.N, p.G, D))
+    if (!encode_kv_map(&tk, K, B, p.N, p.G, D, kTileKeys, dt) ||
+        !encode_kv_map(&tv, V, B, p.N, p.G, D, kTileKeys, dt))
       return NSA_ERR_LAUNCH;
   } else {
     memset(&tk, 0, sizeof(tk));  // no key: no tile is ever loaded
     memset(&tv, 0, sizeof(tv));
   }
-  auto kern = sel_attn_fwd_kernel<D, W>;
+  auto kern = sel_attn_fwd_kernel<D, W, BF16, O16>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return NSA_ERR_LAUNCH;
@@ -382,11 +405,14 @@ int check_sizes(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D
 }
 
 int launch_forward(const void* Q, const void* K, const void* V, const int32_t* block_indices,
-                   float* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
+                   void* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                    int64_t D, int64_t T, int64_t m_off, int block_size, float scale,
-                   cudaStream_t st) {
+                   int qkv_dtype, int o_dtype, cudaStream_t st) {
   const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
   if (chk != NSA_OK) return chk;
+  if ((qkv_dtype != NSA_F16 && qkv_dtype != NSA_BF16) ||
+      (o_dtype != NSA_F32 && o_dtype != qkv_dtype))
+    return NSA_ERR_DTYPE;
   if (m_off < 0 || m_off > ((int64_t(1) << 31) - 1024) - M) return NSA_ERR_SHAPE;
   if (B == 0 || M == 0) return NSA_OK;
   if (!Q || !O || !LSE) return NSA_ERR_NULL;
@@ -400,7 +426,7 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
     return NSA_ERR_ALIGN;
 
   Problem p;
-  p.Q = static_cast<const __half*>(Q);
+  p.Q = static_cast<const uint16_t*>(Q);
   p.idx = block_indices;
   p.O = O;
   p.LSE = LSE;
@@ -417,7 +443,17 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
   p.nblk = static_cast<int>((N + block_size - 1) / block_size);
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   p.sl2 = sc * 1.4426950408889634f;
-  return D == 64 ? launch_fwd<64>(p, K, V, B, st) : launch_fwd<128>(p, K, V, B, st);
+  const bool bf = qkv_dtype == NSA_BF16, o16 = o_dtype != NSA_F32;
+  if (D == 64) {
+    if (bf) return o16 ? launch_fwd<64, true, true>(p, K, V, B, st)
+                       : launch_fwd<64, true, false>(p, K, V, B, st);
+    return o16 ? launch_fwd<64, false, true>(p, K, V, B, st)
+               : launch_fwd<64, false, false>(p, K, V, B, st);
+  }
+  if (bf) return o16 ? launch_fwd<128, true, true>(p, K, V, B, st)
+                     : launch_fwd<128, true, false>(p, K, V, B, st);
+  return o16 ? launch_fwd<128, false, true>(p, K, V, B, st)
+             : launch_fwd<128, false, false>(p, K, V, B, st);
 }
 
 }  // namespace nsa
@@ -439,6 +475,8 @@ const char* nsa_status_string(int status) {
     case NSA_ERR_WORKSPACE: return "workspace too small";
     case NSA_ERR_SCRATCH:
       return "problem needs more scratch than the fixed buffer of the no-allocation entry point";
+    case NSA_ERR_DTYPE:
+      return "unsupported dtype: Q/K/V fp16 or bf16; O fp32 or the type of Q/K/V";
     default: return "unknown status";
   }
 }
@@ -449,7 +487,15 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t*
                      float* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                      int64_t D, int64_t T, int block_size, float scale, void* stream) {
   return nsa::launch_forward(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T, 0, block_size,
-                             scale, static_cast<cudaStream_t>(stream));
+                             scale, NSA_F16, NSA_F32, static_cast<cudaStream_t>(stream));
+}
+
+int nsa_sel_attn_fwd_ex(const void* Q, const void* K, const void* V,
+                        const int32_t* block_indices, void* O, float* LSE, int64_t B, int64_t M,
+                        int64_t N, int64_t H, int64_t G, int64_t D, int64_t T, int block_size,
+                        float scale, int qkv_dtype, int o_dtype, void* stream) {
+  return nsa::launch_forward(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T, 0, block_size,
+                             scale, qkv_dtype, o_dtype, static_cast<cudaStream_t>(stream));
 }
 
 int nsa_sync_status(void* stream) {

@@ -15,10 +15,12 @@ int check_sizes(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D
 // Validates and launches the forward over query rows [0, M) of Q / indices /
 // O / LSE, whose positions in the key sequence are m_off .. m_off + M - 1.
 // K and V hold the whole key sequence [B, N, G, D]; LSE is [B, H, M].
+// qkv_dtype / o_dtype are nsa_dtype values (Q/K/V fp16 or bf16; O fp32 or
+// the 16-bit type of Q/K/V).
 int launch_forward(const void* Q, const void* K, const void* V, const int32_t* block_indices,
-                   float* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
+                   void* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                    int64_t D, int64_t T, int64_t m_off, int block_size, float scale,
-                   cudaStream_t st);
+                   int qkv_dtype, int o_dtype, cudaStream_t st);
 
 // Reads and clears the status word of the backward kernels' translation unit.
 int bwd_read_and_clear_status(unsigned int* value);

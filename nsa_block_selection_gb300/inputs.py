@@ -115,14 +115,23 @@ _CHUNK = 1 << 22  # elements per independently seeded stream
 
 
 def _normal_fp16(seed: int, tensor_id: int, shape, sigma: float) -> np.ndarray:
-    """normal(0, sigma) draws rounded to fp16, filled in fixed-size chunks.
+    return _normal(seed, tensor_id, shape, sigma, np.float16)
+
+
+def _normal_f32(seed: int, tensor_id: int, shape, sigma: float) -> np.ndarray:
+    return _normal(seed, tensor_id, shape, sigma, np.float32)
+
+
+def _normal(seed: int, tensor_id: int, shape, sigma: float, dtype) -> np.ndarray:
+    """normal(0, sigma) float32 draws stored as ``dtype`` (float16: rounded to
+    nearest even), filled in fixed-size chunks.
 
     Chunk i uses ``PCG64(SeedSequence([seed, tensor_id]).spawn(...)[i])``, so
     the values depend only on (seed, tensor_id, shape), never on how many
     threads fill them.
     """
     n = int(np.prod(shape))
-    out = np.empty(n, dtype=np.float16)
+    out = np.empty(n, dtype=dtype)
     nchunks = (n + _CHUNK - 1) // _CHUNK
     children = np.random.SeedSequence([seed, tensor_id]).spawn(nchunks)
 
@@ -146,13 +155,27 @@ def _normal_fp16(seed: int, tensor_id: int, shape, sigma: float) -> np.ndarray:
     return out.reshape(shape)
 
 
-def make_qkv(w: Workload, seed: int):
-    """Q [B,M,H,D], K and V [B,N,G,D] as float16, normal(0, sigma) then RNE."""
-    return (
-        _normal_fp16(seed, 0, (w.B, w.M, w.H, w.D), w.sigma),
-        _normal_fp16(seed, 1, (w.B, w.N, w.G, w.D), w.sigma),
-        _normal_fp16(seed, 2, (w.B, w.N, w.G, w.D), w.sigma),
-    )
+def make_qkv(w: Workload, seed: int, dtype: str = "f16"):
+    """Q [B,M,H,D], K and V [B,N,G,D], normal(0, sigma) then RNE.
+
+    dtype "f16": float16 arrays. dtype "bf16": float32 arrays whose values
+    are bfloat16 numbers (the same float32 draws rounded to nearest-even
+    bfloat16 by torch), ready for ``torch.from_numpy(a).bfloat16()``.
+    """
+    if dtype == "f16":
+        return (
+            _normal_fp16(seed, 0, (w.B, w.M, w.H, w.D), w.sigma),
+            _normal_fp16(seed, 1, (w.B, w.N, w.G, w.D), w.sigma),
+            _normal_fp16(seed, 2, (w.B, w.N, w.G, w.D), w.sigma),
+        )
+    if dtype != "bf16":
+        raise ValueError(dtype)
+    import torch
+
+    return tuple(
+        torch.from_numpy(_normal_f32(seed, i, shape, w.sigma)).bfloat16().float().numpy()
+        for i, shape in enumerate([(w.B, w.M, w.H, w.D), (w.B, w.N, w.G, w.D),
+                                   (w.B, w.N, w.G, w.D)]))
 
 
 def _floyd_subsets(rng: np.random.Generator, pool: np.ndarray, k: int) -> np.ndarray:

@@ -37,10 +37,11 @@ Two routes compute the same numbers:
 * ``route="online"``: the block loop in the order the row lists the blocks,
   carrying a running max, a running sum and a running weighted V sum (the
   online softmax named in the Algorithm and Requirements sections).
-  ``emulate_kernel_rounding=True`` carries the running sums in float32 and
-  rounds the probabilities to fp16 for the V product only (the "FP16
-  matmuls, FP32 accumulation" requirement), to measure how much of the
-  parity tolerance that rounding uses.
+  ``emulate_kernel_rounding=True`` (or ``"f16"``) carries the running sums in
+  float32 and rounds the probabilities to fp16 for the V product only (the
+  "FP16 matmuls, FP32 accumulation" requirement), to measure how much of the
+  parity tolerance that rounding uses; ``"bf16"`` rounds them to bfloat16
+  instead (the same requirement read for bf16 operands).
 
 Every step is pinned by tests (textbook attention through a library routine,
 closed forms, hand-worked cases, order invariance, planted mistakes); no
@@ -64,6 +65,7 @@ __all__ = [
     "scores",
     "logsumexp_rows",
     "attend",
+    "round_bf16",
     "sel_attn_row",
     "sel_attn_rows",
     "sel_attn_fwd",
@@ -168,6 +170,26 @@ def _route_set(q, Kg, Vg, idx_row, m, N, bs, scale):
     return attend(s, lse, v), lse
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Nearest bfloat16 of float32 values (ties to even), as float32.
+
+    bfloat16 is the upper half of an IEEE binary32: rounding adds half a unit
+    of the dropped 16 bits (minus one when the kept part is even, so that
+    exact ties go to the even neighbour) and clears them. Finite inputs only.
+    """
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16 << 16
+    return u.astype(np.uint32).view(np.float32)
+
+
+def _round_p(p: np.ndarray, how) -> np.ndarray:
+    if how == "bf16":
+        return round_bf16(p)
+    if how is True or how == "f16":
+        return p.astype(np.float16).astype(np.float32)
+    raise ValueError(f"unknown rounding {how!r}")
+
+
 def _route_online(q, Kg, Vg, idx_row, m, N, bs, scale, emulate_kernel_rounding):
     hpg, D = q.shape
     acc_t = np.float32 if emulate_kernel_rounding else np.float64
@@ -189,7 +211,7 @@ def _route_online(q, Kg, Vg, idx_row, m, N, bs, scale, emulate_kernel_rounding):
             p = p.astype(np.float32)
             alpha = alpha.astype(np.float32)
             run_sum = run_sum * alpha + p.sum(axis=1, dtype=np.float32)
-            p16 = p.astype(np.float16).astype(np.float32)
+            p16 = _round_p(p, emulate_kernel_rounding)
             acc = acc * alpha[:, None] + (p16 @ v.astype(np.float32)).astype(np.float32)
         else:
             run_sum = run_sum * alpha + p.sum(axis=1)

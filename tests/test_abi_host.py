@@ -54,7 +54,7 @@ def test_exports_match_header(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, -9, -1):
+    for code in range(0, -12, -1):
         s = lib.nsa_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.nsa_status_string(-99).decode() == "unknown status"
@@ -132,3 +132,42 @@ def test_heads_per_group_accepted(lib, H, G):
     # 1..8 heads per group, or a multiple of 8: the size checks pass (the
     # empty problem then returns before any CUDA call)
     assert call(lib, q=None, k=None, v=None, idx=None, o=None, lse=None, B=0, H=H, G=G) == 0
+
+
+def call_ex(lib, qkv_dtype, o_dtype, q=FAKE, k=FAKE, v=FAKE, idx=FAKE, o=FAKE, lse=FAKE, **over):
+    a = dict(GOOD)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return lib.nsa_sel_attn_fwd_ex(vp(q), vp(k), vp(v), vp(idx), vp(o), vp(lse), a["B"], a["M"],
+                                   a["N"], a["H"], a["G"], a["D"], a["T"], a["bs"], 0.0,
+                                   qkv_dtype, o_dtype, None)
+
+
+@pytest.mark.parametrize("qkv,o,status", [
+    (_lib.NSA_F16, _lib.NSA_F32, 0), (_lib.NSA_BF16, _lib.NSA_F32, 0),
+    (_lib.NSA_F16, _lib.NSA_F16, 0), (_lib.NSA_BF16, _lib.NSA_BF16, 0),
+    (_lib.NSA_F16, _lib.NSA_BF16, -11), (_lib.NSA_BF16, _lib.NSA_F16, -11),
+    (_lib.NSA_F32, _lib.NSA_F32, -11), (3, _lib.NSA_F32, -11), (_lib.NSA_F16, -1, -11),
+])
+def test_ex_dtype_combinations(lib, qkv, o, status):
+    # the dtype check runs after the size checks and before the empty-problem
+    # return, so an empty problem shows it without any CUDA call
+    assert call_ex(lib, qkv, o, q=None, k=None, v=None, idx=None, o=None, lse=None, B=0) == status
+
+
+def test_ex_shares_the_size_checks(lib):
+    assert call_ex(lib, _lib.NSA_BF16, _lib.NSA_BF16, bs=16) == -3
+    assert call_ex(lib, _lib.NSA_BF16, _lib.NSA_F32, D=96) == -4
+    assert call_ex(lib, _lib.NSA_F16, _lib.NSA_F16, o=None) == -1
+    assert call_ex(lib, _lib.NSA_BF16, _lib.NSA_BF16, k=FAKE + 2) == -6
+
+
+def test_binding_rejects_mixed_dtypes():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 4, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 4, 1, 64, dtype=torch.float16)
+    idx = torch.zeros(1, 4, 1, 1, dtype=torch.int32)
+    with pytest.raises(TypeError):
+        _lib.sel_attn_fwd(q, k, k, idx, 32)
+    with pytest.raises(TypeError):
+        _lib.sel_attn_fwd(q.float(), k.float(), k.float(), idx, 32)
