@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-bwd", action="store_true")
+    ap.add_argument("--skip-topk", action="store_true",
+                    help="skip timing the top-k block selection kernel")
     ap.add_argument("--skip-variants", action="store_true",
                     help="skip timing the bf16-input and 16-bit-O forward variants")
     ap.add_argument("--cpu-rows", type=int, default=24576,
@@ -376,6 +378,11 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.skip_bwd:
         backward = run_backward(w, q, k, v, idx, out, lse, work, flush, args)
 
+    # top-k block selection producing an index tensor of this workload's shape
+    topk = None
+    if rank == 0 and world == 1 and not args.skip_topk:
+        topk = run_topk(w, flush, args, dev)
+
     # element-type variants of the forward on the same workload
     variants = None
     if rank == 0 and world == 1 and not args.skip_variants:
@@ -420,6 +427,7 @@ def run_ours(args):
         "dense_causal": dense,
         "backward": backward,
         "variants": variants,
+        "topk": topk,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -433,6 +441,50 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def topk_bytes(B, M, N, G, T, bs, n_init, n_local):
+    """Algorithmic bytes of nsa_topk_blocks: the scores of the free
+    candidates of rows with more than T candidates (read once) and the
+    index rows (written)."""
+    import numpy as np
+
+    m = np.arange(M, dtype=np.int64)
+    c = np.minimum(m, N - 1) // bs if N > 0 else np.full(M, -1)
+    free = np.where(c + 1 > T, c + 1 - n_init - n_local, 0)
+    return int(B * G * (4 * free.sum() + 4 * T * M))
+
+
+def run_topk(w, flush, args, dev):
+    """nsa_topk_blocks on i.i.d. scores [B, M, G, ceil(N/bs)] (drawn on the
+    device), T, block 0 and the two most recent blocks forced: the index
+    rule of the workload as a top-k."""
+    import torch
+
+    from nsa_block_selection_gb300 import inputs as gen
+    from nsa_block_selection_gb300 import topk_blocks
+
+    nblk = -(-w.N // w.block_size)
+    sc = gen.make_block_scores_torch(w.B, w.M, w.G, nblk, 99, dev)
+    out = torch.empty((w.B, w.M, w.G, w.T), dtype=torch.int32, device=dev)
+
+    def step():
+        topk_blocks(sc, w.N, w.block_size, w.T, 1, 2, out=out)
+
+    steps = max(5, args.steps // 4)
+    times, _ = time_steps(step, steps, 3, flush, lambda: None)
+    t = statistics.mean(times)
+    nbytes = topk_bytes(w.B, w.M, w.N, w.G, w.T, w.block_size, 1, 2)
+    peaks = load_peaks()
+    gbs = nbytes / (t * 1e-3) / 1e9
+    res = {"ms_per_step": t, "gbs": gbs, "bytes_per_step": nbytes,
+           "hbm_frac": gbs / peaks["hbm_gbs"], "rows": w.B * w.M * w.G, "steps": steps,
+           "scores_bytes": sc.numel() * 4, "n_init": 1, "n_local": 2,
+           "note": "bytes = scores of the free candidates of rows with more than T "
+                   "candidates + the index rows written; L2 flushed between steps"}
+    del sc, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_variants(w, q, k, v, idx, work, flush, args):

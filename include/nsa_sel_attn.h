@@ -247,6 +247,43 @@ int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
                              int block_size, float scale, void* stream);
 
 /*
+ * nsa_topk_blocks -- top-k block selection: block_indices from block scores.
+ *
+ * The selection-attention issue takes block_indices from a top-k selection
+ * kernel ("[wave] NSA: selection attention forward kernel", section
+ * "Depends on"); its section "Operation" fixes the output [B,M,G,T] and
+ * section "Requirements" one row per GQA group. The pages do not say how
+ * blocks are scored, so the scores are the input:
+ *
+ *   scores         device, fp32,  [B, M, G, ceil(N/block_size)]; the score
+ *                  of key block t for query (b, m) and KV group g. Only
+ *                  entries of free candidate blocks (below) are read.
+ *   block_indices  device, int32, [B, M, G, T] (output)
+ *   B, M, N, T     >= 0; G > 0; ceil(N/block_size) <= 4096
+ *   block_size     >= 1 (keys per block, as in nsa_sel_attn_fwd)
+ *   n_init,        >= 0 with n_init + n_local <= T: the first n_init and the
+ *   n_local        last n_local candidate blocks of a row are always chosen
+ *   stream         cudaStream_t to launch on
+ *
+ * Row (b, m, g): the candidates are the blocks t = 0..c holding a key
+ * visible to query m, c = floor(min(m, N-1) / block_size) (none if N = 0).
+ * With at most T candidates all are chosen. Otherwise the forced blocks are
+ * chosen and the remaining T - n_init - n_local slots go to the other
+ * candidates with the highest scores; equal scores choose the lower block
+ * (-0.0 equals +0.0) and NaN ranks below every number. The row is written
+ * in ascending block order and padded with -1, so it is a valid
+ * block_indices row for nsa_sel_attn_fwd (distinct, causal).
+ *
+ * Asynchronous: one kernel on `stream`, no allocation, no synchronisation.
+ * Returns NSA_ERR_SHAPE (bad sizes, n_init/n_local out of range, too many
+ * blocks), NSA_ERR_BLOCK_SIZE, NSA_ERR_NULL, NSA_ERR_ALIGN (a pointer not
+ * 4-byte aligned) before launch; an empty output returns NSA_OK at once.
+ */
+int nsa_topk_blocks(const float* scores, int32_t* block_indices, int64_t B, int64_t M,
+                    int64_t N, int64_t G, int64_t T, int block_size, int n_init,
+                    int n_local, void* stream);
+
+/*
  * nsa_sync_status -- wait for `stream`, then read and clear the device status
  * word of the current device.
  *

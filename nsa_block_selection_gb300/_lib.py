@@ -23,7 +23,7 @@ EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sel_attn
            "nsa_sync_status",
            "nsa_selftest_wait_timeout", "nsa_sel_attn_fwd_host_workspace_bytes",
            "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd",
-           "nsa_sel_attn_bwd_noalloc")
+           "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks")
 
 _lib = None
 
@@ -71,6 +71,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_bwd_noalloc.restype = c_int
     lib.nsa_sel_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64,
                                              i64, i64, i64, i64, i64, c_int, ctypes.c_float, vp]
+    lib.nsa_topk_blocks.restype = c_int
+    lib.nsa_topk_blocks.argtypes = [vp, vp, i64, i64, i64, i64, i64, c_int, c_int, c_int, vp]
     lib.nsa_sel_attn_fwd_host.restype = c_int
     lib.nsa_sel_attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                           i64, c_int, ctypes.c_float, vp, i64, i64, vp]
@@ -275,3 +277,33 @@ def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
     return load().nsa_selftest_wait_timeout(int(limit_ns), ctypes.c_void_p(stream.cuda_stream))
+
+
+def topk_blocks(scores, N: int, block_size: int, T: int, n_init: int = 0, n_local: int = 0,
+                out=None, stream=None):
+    """Top-k block selection on the GPU (nsa_topk_blocks).
+
+    scores: fp32 [B, M, G, ceil(N/block_size)], contiguous on a CUDA device.
+    Returns block_indices int32 [B, M, G, T] (ascending, -1 padded): per
+    (b, m, g) the first n_init and last n_local causal blocks and the
+    highest-scoring others.
+    """
+    import torch
+
+    lib = load()
+    if scores.dtype != torch.float32 or not scores.is_cuda or not scores.is_contiguous():
+        raise TypeError("scores must be a contiguous fp32 CUDA tensor")
+    B, M, G, S = scores.shape
+    if S != -(-int(N) // int(block_size)):
+        raise ValueError("scores must have ceil(N/block_size) entries per row")
+    if out is None:
+        out = torch.empty((B, M, G, T), dtype=torch.int32, device=scores.device)
+    if out.dtype != torch.int32 or tuple(out.shape) != (B, M, G, T) or not out.is_contiguous():
+        raise ValueError("out must be contiguous int32 [B, M, G, T]")
+    if stream is None:
+        stream = torch.cuda.current_stream(scores.device)
+    st = lib.nsa_topk_blocks(_ptr(scores), _ptr(out), B, M, int(N), G, int(T), int(block_size),
+                             int(n_init), int(n_local), ctypes.c_void_p(stream.cuda_stream))
+    if st != NSA_OK:
+        raise NsaError(st, "nsa_topk_blocks")
+    return out

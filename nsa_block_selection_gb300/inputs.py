@@ -270,3 +270,27 @@ def dense_causal_indices_torch(B: int, M: int, G: int, T: int, block_size: int, 
     tt = torch.arange(T, device=device, dtype=torch.int64)
     rows = torch.where(tt[None, :] <= c[:, None], tt[None, :], torch.full_like(tt[None, :], -1))
     return rows.to(torch.int32)[None, :, None, :].expand(B, M, G, T).contiguous()
+
+
+def make_block_scores(B: int, M: int, G: int, nblk: int, seed: int) -> np.ndarray:
+    """Block scores [B, M, G, nblk] for top-k selection: i.i.d. uniform [0, 1)
+    float32 (with the initial and local blocks forced, a top-k over them
+    picks the other blocks of a row uniformly, as the index rules do)."""
+    n = B * M * G * nblk
+    out = np.empty(n, dtype=np.float32)
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+    children = np.random.SeedSequence([seed, 7]).spawn(max(nchunks, 1))
+    for i in range(nchunks):
+        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)
+        out[lo:hi] = np.random.Generator(np.random.PCG64(children[i])).random(
+            hi - lo, dtype=np.float32)
+    return out.reshape(B, M, G, nblk)
+
+
+def make_block_scores_torch(B: int, M: int, G: int, nblk: int, seed: int, device):
+    """The same kind of scores drawn on the device by torch (for sizes too
+    large to draw on the host quickly); seeded, not equal to the host draw."""
+    import torch
+
+    g = torch.Generator(device=device).manual_seed(seed)
+    return torch.rand((B, M, G, nblk), generator=g, device=device, dtype=torch.float32)

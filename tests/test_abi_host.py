@@ -171,3 +171,25 @@ def test_binding_rejects_mixed_dtypes():
         _lib.sel_attn_fwd(q, k, k, idx, 32)
     with pytest.raises(TypeError):
         _lib.sel_attn_fwd(q.float(), k.float(), k.float(), idx, 32)
+
+
+def call_topk(lib, scores=FAKE, idx=FAKE, B=1, M=128, N=128, G=2, T=4, bs=64, n_init=1,
+              n_local=1):
+    vp = ctypes.c_void_p
+    return lib.nsa_topk_blocks(vp(scores), vp(idx), B, M, N, G, T, bs, n_init, n_local, None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(B=-1), -2), (dict(M=-1), -2), (dict(N=-1), -2), (dict(T=-1), -2), (dict(G=0), -2),
+    (dict(bs=0), -3), (dict(n_init=-1), -2), (dict(n_local=-1), -2),
+    (dict(n_init=3, n_local=2), -2), (dict(N=4097 * 64), -2), (dict(N=4097, bs=1), -2),
+    (dict(idx=None), -1), (dict(scores=None), -1), (dict(idx=FAKE + 2), -6),
+    (dict(scores=FAKE + 1), -6),
+])
+def test_topk_bad_arguments(lib, over, status):
+    assert call_topk(lib, **over) == status
+
+
+@pytest.mark.parametrize("over", [dict(B=0), dict(M=0), dict(T=0, n_init=0, n_local=0)])
+def test_topk_empty_output_is_a_no_op(lib, over):
+    assert call_topk(lib, scores=None, idx=None, **over) == 0
