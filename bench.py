@@ -61,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-bwd", action="store_true")
+    ap.add_argument("--skip-swa", action="store_true",
+                    help="skip timing the sliding-window attention kernel")
+    ap.add_argument("--swa-seq", type=int, default=65536)
     ap.add_argument("--skip-topk", action="store_true",
                     help="skip timing the top-k block selection kernel")
     ap.add_argument("--skip-variants", action="store_true",
@@ -383,6 +386,11 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.skip_topk:
         topk = run_topk(w, flush, args, dev)
 
+    # GQA sliding-window attention (the pages' second kernel), tcgen05
+    swa = None
+    if rank == 0 and world == 1 and not args.skip_swa:
+        swa = run_swa(flush, args, dev)
+
     # element-type variants of the forward on the same workload
     variants = None
     if rank == 0 and world == 1 and not args.skip_variants:
@@ -428,6 +436,7 @@ def run_ours(args):
         "backward": backward,
         "variants": variants,
         "topk": topk,
+        "swa": swa,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -441,6 +450,51 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def swa_pairs(M, N, left, right):
+    """(query, key) pairs inside the windows: sum over i of |[i-left, i+right] & [0, N)|."""
+    import numpy as np
+
+    i = np.arange(M, dtype=np.int64)
+    lo = np.zeros(M, np.int64) if left < 0 else np.maximum(0, i - left)
+    hi = np.full(M, N - 1, np.int64) if right < 0 else np.minimum(N - 1, i + right)
+    return int(np.maximum(hi - lo + 1, 0).sum())
+
+
+def run_swa(flush, args, dev):
+    """nsa_swa_fwd, bf16, B=1, H=64, H_kv=8, D=128 (the page's API example
+    shape) at seq = --swa-seq for the page's windows. FLOPs: 4*D per (query,
+    head, key in the window). Inputs drawn on the device; L2 flushed."""
+    import torch
+
+    from nsa_block_selection_gb300 import swa_fwd
+
+    B, S, H, Hkv, D = 1, args.swa_seq, 64, 8, 128
+    g = torch.Generator(device=dev).manual_seed(5)
+    q = torch.randn((B, S, H, D), generator=g, device=dev).bfloat16()
+    k = torch.randn((B, S, Hkv, D), generator=g, device=dev).bfloat16()
+    v = torch.randn((B, S, Hkv, D), generator=g, device=dev).bfloat16()
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    peaks = load_peaks()
+    res = {"shape": {"B": B, "seq": S, "H": H, "H_kv": Hkv, "D": D, "dtype": "bf16"},
+           "windows": []}
+    for left, right in ((512, 0), (1024, 0), (4096, 0), (8192, 0), (-1, 0)):
+        def step():
+            swa_fwd(q, k, v, window=(left, right), out=out, lse=lse)
+
+        steps = max(3, args.steps // 6)
+        times, _ = time_steps(step, steps, 3, flush, lambda: None)
+        t = statistics.mean(times)
+        flops = 4 * D * H * B * swa_pairs(S, S, left, right)
+        tf = flops / (t * 1e-3) / 1e12
+        res["windows"].append({"window": [left, right], "ms_per_step": t, "tflops": tf,
+                               "tensor_frac": tf / peaks["bf16_tflops"], "flops": flops,
+                               "steps": steps})
+    del q, k, v, out, lse
+    torch.cuda.empty_cache()
+    return res
 
 
 def topk_bytes(B, M, N, G, T, bs, n_init, n_local):

@@ -284,6 +284,39 @@ int nsa_topk_blocks(const float* scores, int32_t* block_indices, int64_t B, int6
                     int n_local, void* stream);
 
 /*
+ * nsa_swa_fwd -- GQA sliding-window (or dense) attention forward, the
+ * second workload on the pages ("[Kernel][MI350] Add 8 wave GQA
+ * sliding-window attention kernel", sections "Summary" and "What it does").
+ *
+ *   Q              device, [B, M, H, D],    fp16 or bf16 (dtype)
+ *   K, V           device, [B, N, H_kv, D], same type
+ *   O              device, [B, M, H, D],    same type (output)
+ *   LSE            device, fp32 [B, H, M] (output, natural log), or NULL
+ *   H % H_kv == 0  query head h reads KV head h / (H / H_kv)
+ *   D              64 or 128
+ *   window_left,   query i attends to keys j with i - window_left <= j <=
+ *   window_right   i + window_right and 0 <= j < N; a negative value leaves
+ *                  that side unbounded: (-1, -1) is dense attention, (-1, 0)
+ *                  causal, (L, 0) causal with L keys of history
+ *   scale          score multiplier; <= 0 selects 1/sqrt(D)
+ *   dtype          NSA_F16 or NSA_BF16
+ *
+ * Query i is aligned with key i. Both products run on the 5th-generation
+ * tensor cores (tcgen05, fp32 accumulation in tensor memory). P is rounded
+ * to the input type before the PV product, and O is the fp32 result rounded
+ * once. A row with no visible key gets O = 0 and LSE = -inf. The call is
+ * asynchronous and allocates nothing. Each CTA holds 512 tensor-memory
+ * columns of its SM for its lifetime. Errors returned before launch:
+ * NSA_ERR_SHAPE, NSA_ERR_GROUPS, NSA_ERR_HEAD_DIM, NSA_ERR_DTYPE,
+ * NSA_ERR_NULL, NSA_ERR_ALIGN (Q, K, V, O not 16-byte aligned, LSE not
+ * 4-byte aligned). A timed-out device wait is reported by nsa_sync_status.
+ */
+int nsa_swa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                int64_t B, int64_t M, int64_t N, int64_t H, int64_t H_kv, int64_t D,
+                int64_t window_left, int64_t window_right, float scale, int dtype,
+                void* stream);
+
+/*
  * nsa_sync_status -- wait for `stream`, then read and clear the device status
  * word of the current device.
  *

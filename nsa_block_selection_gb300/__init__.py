@@ -7,14 +7,16 @@ Public API (GPU only; the CUDA library must be built):
 * :func:`sel_attn_bwd` -- dQ, dK, dV from dO and the forward's O and LSE;
 * :func:`topk_blocks` -- block_indices from per-block scores (top-k with
   forced initial and local blocks);
-* :func:`sel_attn_fwd_host` -- the forward with host buffers in and out.
+* :func:`sel_attn_fwd_host` -- the forward with host buffers in and out;
+* :func:`swa_fwd` -- GQA sliding-window (or dense) attention forward on the
+  tcgen05 tensor cores.
 
 The C ABI is declared in ``include/nsa_sel_attn.h``; ``inputs`` draws the
 seeded synthetic workloads.
 """
 
 from ._lib import (NsaError, load, sel_attn_bwd, sel_attn_fwd, sel_attn_fwd_host,  # noqa: F401
-                   status_string, topk_blocks)
+                   status_string, swa_fwd, topk_blocks)
 
-__all__ = ["sel_attn_fwd", "sel_attn_bwd", "sel_attn_fwd_host", "topk_blocks", "load",
+__all__ = ["sel_attn_fwd", "sel_attn_bwd", "sel_attn_fwd_host", "topk_blocks", "swa_fwd", "load",
            "status_string", "NsaError"]

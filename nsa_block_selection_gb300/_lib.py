@@ -23,7 +23,7 @@ EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sel_attn
            "nsa_sync_status",
            "nsa_selftest_wait_timeout", "nsa_sel_attn_fwd_host_workspace_bytes",
            "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd",
-           "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks")
+           "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks", "nsa_swa_fwd")
 
 _lib = None
 
@@ -71,6 +71,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_bwd_noalloc.restype = c_int
     lib.nsa_sel_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64,
                                              i64, i64, i64, i64, i64, c_int, ctypes.c_float, vp]
+    lib.nsa_swa_fwd.restype = c_int
+    lib.nsa_swa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
+                                ctypes.c_float, c_int, vp]
     lib.nsa_topk_blocks.restype = c_int
     lib.nsa_topk_blocks.argtypes = [vp, vp, i64, i64, i64, i64, i64, c_int, c_int, c_int, vp]
     lib.nsa_sel_attn_fwd_host.restype = c_int
@@ -307,3 +310,48 @@ def topk_blocks(scores, N: int, block_size: int, T: int, n_init: int = 0, n_loca
     if st != NSA_OK:
         raise NsaError(st, "nsa_topk_blocks")
     return out
+
+
+def swa_fwd(q, k, v, window=(-1, -1), scale: Optional[float] = None, out=None, lse=None,
+            return_lse: bool = True, stream=None):
+    """GQA sliding-window attention forward on the GPU (nsa_swa_fwd).
+
+    q: bf16 or fp16 [B, M, H, D]; k, v: [B, N, H_kv, D] of q's dtype, all
+    contiguous on one CUDA device. ``window`` = (left, right): query i sees
+    keys [i - left, i + right]; a negative side is unbounded. Returns
+    (O [B, M, H, D] in q's dtype, LSE fp32 [B, H, M] or None).
+    """
+    import torch
+
+    lib = load()
+    if q.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError(f"q must be fp16 or bf16, got {q.dtype}")
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must be {q.dtype}, got {t.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    B, M, H, D = q.shape
+    Bk, N, Hkv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch: q [B,M,H,D], k/v [B,N,H_kv,D]")
+    if out is None:
+        out = torch.empty((B, M, H, D), dtype=q.dtype, device=q.device)
+    if out.dtype != q.dtype or tuple(out.shape) != (B, M, H, D) or not out.is_contiguous():
+        raise ValueError(f"out must be contiguous {q.dtype} [B, M, H, D]")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, M)
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be contiguous fp32 [B, H, M]")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    left, right = (int(window[0]), int(window[1])) if window is not None else (-1, -1)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.nsa_swa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, M, N, H, Hkv, D,
+                         left, right, sc, _dtype_code(q.dtype),
+                         ctypes.c_void_p(stream.cuda_stream))
+    if st != NSA_OK:
+        raise NsaError(st, "nsa_swa_fwd")
+    return out, lse

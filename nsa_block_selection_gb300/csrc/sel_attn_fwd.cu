@@ -501,10 +501,11 @@ int nsa_sel_attn_fwd_ex(const void* Q, const void* K, const void* V,
 int nsa_sync_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return NSA_ERR_LAUNCH;
-  unsigned int fwd = 0u, bwd = 0u;
+  unsigned int fwd = 0u, bwd = 0u, swa = 0u;
   if (nsa::read_and_clear_status(&fwd) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::bwd_read_and_clear_status(&bwd) != NSA_OK) return NSA_ERR_LAUNCH;
-  return (fwd | bwd) ? NSA_ERR_TIMEOUT : NSA_OK;
+  if (nsa::swa_read_and_clear_status(&swa) != NSA_OK) return NSA_ERR_LAUNCH;
+  return (fwd | bwd | swa) ? NSA_ERR_TIMEOUT : NSA_OK;
 }
 
 int nsa_selftest_wait_timeout(int64_t limit_ns, void* stream) {

@@ -25,4 +25,7 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
 // Reads and clears the status word of the backward kernels' translation unit.
 int bwd_read_and_clear_status(unsigned int* value);
 
+// Reads and clears the status word of the sliding-window kernel's translation unit.
+int swa_read_and_clear_status(unsigned int* value);
+
 }  // namespace nsa

@@ -193,3 +193,25 @@ def test_topk_bad_arguments(lib, over, status):
 @pytest.mark.parametrize("over", [dict(B=0), dict(M=0), dict(T=0, n_init=0, n_local=0)])
 def test_topk_empty_output_is_a_no_op(lib, over):
     assert call_topk(lib, scores=None, idx=None, **over) == 0
+
+
+def call_swa(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, M=128, N=128, H=8, Hkv=2, D=128,
+             left=-1, right=0, dtype=1):
+    vp = ctypes.c_void_p
+    return lib.nsa_swa_fwd(vp(q), vp(k), vp(v), vp(o), vp(lse), B, M, N, H, Hkv, D, left, right,
+                           0.0, dtype, None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(B=-1), -2), (dict(M=-1), -2), (dict(N=-1), -2), (dict(H=0), -2), (dict(Hkv=0), -2),
+    (dict(H=8, Hkv=3), -5), (dict(D=96), -4), (dict(dtype=2), -11), (dict(dtype=7), -11),
+    (dict(M=(1 << 30) + 1), -2), (dict(q=None), -1), (dict(o=None), -1), (dict(k=None), -1),
+    (dict(v=FAKE + 8), -6), (dict(o=FAKE + 2), -6), (dict(lse=FAKE + 1), -6),
+])
+def test_swa_bad_arguments(lib, over, status):
+    assert call_swa(lib, **over) == status
+
+
+@pytest.mark.parametrize("over", [dict(B=0), dict(M=0)])
+def test_swa_empty_is_a_no_op(lib, over):
+    assert call_swa(lib, q=None, k=None, v=None, o=None, lse=None, **over) == 0
