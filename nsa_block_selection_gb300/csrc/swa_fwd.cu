@@ -24,9 +24,11 @@
 //    it on edge tiles, keeps a reference max that moves only when a score
 //    exceeds it by more than 8 (log2 units; O in tensor memory is then
 //    rescaled in place, after the previous PV has completed), writes
-//    P = 2^(x - ref) rounded to the input type into shared memory in the
-//    swizzled K-major layout, and arrives on the P barrier. The epilogue
-//    reads O, divides by the row sum and stores the row and its LSE.
+//    P = 2^(x - ref) rounded to the input type into one of two shared-memory
+//    P buffers in the swizzled K-major layout, and arrives on its barrier:
+//    with two buffers the exponentials of tile i overlap both the PV of
+//    tile i - 1 and the QK^T of tile i + 1. The epilogue reads O, divides by
+//    the row sum and stores the row and its LSE.
 // Every mbarrier wait is bounded (1 s); a role that gives up sets the status
 // word and leaves its loop, so every role reaches the teardown, which frees
 // the tensor memory.
@@ -55,16 +57,18 @@ constexpr uint32_t kColS = 0;  // S buffers at columns 0 and 128
 constexpr uint32_t kColO = 256;
 constexpr float kSwaSlack = 8.0f;
 
+// One barrier per ring slot / buffer, so that no barrier can complete twice
+// before its waiter has seen the first completion.
 enum SwaBar : int {
   kQFull = 0,
   kKFull = 1,    // 2 stages
   kKEmpty = 3,   // 2
   kVFull = 5,    // 2
   kVEmpty = 7,   // 2
-  kSFull = 9,    // 2 S buffers
-  kPFull = 11,
-  kODone = 12,
-  kNumBars = 13
+  kSFull = 9,    // 2 S buffers (tensor memory)
+  kPFull = 11,   // 2 P buffers (shared memory)
+  kPvDone = 13,  // 2: PV of the tile that used P buffer b has completed
+  kNumBars = 15
 };
 
 template <int D>
@@ -78,7 +82,7 @@ struct SwaCfg {
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + 2 * kKVBytes;
   static constexpr int kOffP = kOffV + 2 * kKVBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   // at least 116 KB so that one CTA holds an SM (all 512 tensor-memory columns)
   static constexpr int kUsed = kOffTmem + 16 + 1024;
@@ -142,8 +146,10 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
       mbar_init(bar(kVEmpty + s), 1);
       mbar_init(bar(kSFull + s), 1);
     }
-    mbar_init(bar(kPFull), 4 * 32);
-    mbar_init(bar(kODone), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kPFull + s), 4 * 32);
+      mbar_init(bar(kPvDone + s), 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -211,20 +217,21 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
         return true;
       };
       auto issue_pv = [&](int i) -> bool {
-        const int s = i & 1;
-        if (!wait_phase(bar(kPFull), i & 1, kWaitLimitNs)) return false;
+        const int s = i & 1;  // V stage and P buffer
+        if (!wait_phase(bar(kPFull + s), (i >> 1) & 1, kWaitLimitNs)) return false;
         if (!wait_phase(bar(kVFull + s), (i >> 1) & 1, kWaitLimitNs)) return false;
         tc_fence_after();
         const uint32_t vb = base + C::kOffV + s * C::kKVBytes;
+        const uint32_t pb = base + C::kOffP + s * C::kPBytes;
 #pragma unroll
         for (int kk = 0; kk < kSwaKeys / 16; ++kk) {
           const uint32_t offp = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
-          tc_mma(tmem + kColO, umma_desc_sw128(base + C::kOffP + offp, 16),
+          tc_mma(tmem + kColO, umma_desc_sw128(pb + offp, 16),
                  umma_desc_sw128(vb + kk * 2048, C::kAtomBytes), idesc_o,
                  (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(kVEmpty + s));
-        tc_commit(bar(kODone));
+        tc_commit(bar(kPvDone + s));
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -242,13 +249,15 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int lo_i = max(0, iq - p.left);
     const int hi_i = min(p.N - 1, iq + p.right);
-    float ref = -INFINITY, neg = 0.f, l = 0.f;
+    float ref = -INFINITY, neg = 0.f, l = 0.f;  // ref, neg in the log2 domain
     const float sl2 = p.sl2;
-    uint8_t* const prow = gbase + C::kOffP + row * 128;
     // waits are decided warp-wide (tcgen05.ld/st are warp-collective)
+    auto wait_all = [&](int b, int parity) {
+      return __all_sync(kFull, wait_phase(bar(b), parity, kWaitLimitNs));
+    };
     for (int i = 0; i < nt; ++i) {
-      const int sb = i & 1;
-      if (!__all_sync(kFull, wait_phase(bar(kSFull + sb), (i >> 1) & 1, kWaitLimitNs))) {
+      const int sb = i & 1;  // S buffer and P buffer of this tile
+      if (!wait_all(kSFull + sb, (i >> 1) & 1)) {
         failed = true;
         break;
       }
@@ -260,29 +269,30 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
                 *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
       tc_wait_ld();
       const int j0 = (t0 + i) * kSwaKeys;
-      const bool edge = j0 < in_lo || j0 + kSwaKeys - 1 > in_hi;  // CTA-uniform
-      float mx = -INFINITY;
+      if (j0 < in_lo || j0 + kSwaKeys - 1 > in_hi) {  // edge tile (CTA-uniform)
 #pragma unroll
-      for (int j = 0; j < kSwaKeys; ++j) {
-        float v = __uint_as_float(sr[j]) * sl2;
-        if (edge && (j0 + j < lo_i || j0 + j > hi_i)) v = -INFINITY;
-        sr[j] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        for (int j = 0; j < kSwaKeys; ++j)
+          if (j0 + j < lo_i || j0 + j > hi_i) sr[j] = __float_as_uint(-INFINITY);
       }
-      // PV of the previous tile must be complete before P is overwritten
-      // and before O is rescaled
-      if (i > 0) {
-        if (!__all_sync(kFull, wait_phase(bar(kODone), (i - 1) & 1, kWaitLimitNs))) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-      }
+      // row max of the raw scores (scale > 0 commutes with max), 8 chains
+      float m8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m8[j] = __uint_as_float(sr[j]);
+#pragma unroll
+      for (int j = 8; j < kSwaKeys; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
       const bool move = mx > ref + kSwaSlack;
       if (__any_sync(kFull, move)) {
-        // alpha = 0 while a row has seen nothing (its O row is still 0)
+        // alpha = 0 while a row has seen nothing (its O row is still 0).
+        // O may be rescaled only once the previous tile's PV has completed.
         const float alpha = move ? ex2(ref - mx) : 1.f;
         if (i > 0) {
+          if (!wait_all(kPvDone + ((i - 1) & 1), ((i - 1) >> 1) & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -300,14 +310,25 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
           neg = -mx;
         }
       }
-      // P = 2^(x - ref) into the swizzled K-major P tile (row `row`)
+      // P buffer sb was last read by the PV of tile i - 2
+      if (i >= 2) {
+        if (!wait_all(kPvDone + sb, ((i - 2) >> 1) & 1)) {
+          failed = true;
+          break;
+        }
+      }
+      // P = 2^(s * scale * log2e - ref) into the swizzled K-major P tile
+      uint8_t* const prow = gbase + C::kOffP + sb * C::kPBytes + row * 128;
+      float l8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) l8[j] = 0.f;
 #pragma unroll
       for (int c = 0; c < kSwaKeys / 8; ++c) {
         float e[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          e[j] = ex2(__uint_as_float(sr[8 * c + j]) + neg);
-          l += e[j];
+          e[j] = ex2(fmaf(__uint_as_float(sr[8 * c + j]), sl2, neg));
+          l8[j] += e[j];
         }
         uint4 w;
         w.x = pack2<BF16>(e[0], e[1]);
@@ -317,13 +338,14 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
         *reinterpret_cast<uint4*>(prow + (c >> 3) * C::kAtomBytes +
                                   (((c & 7) ^ (row & 7)) << 4)) = w;
       }
+      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(kPFull));
+      mbar_arrive(bar(kPFull + sb));
     }
     // epilogue
     if (!failed && nt > 0) {
-      if (!__all_sync(kFull, wait_phase(bar(kODone), (nt - 1) & 1, kWaitLimitNs))) failed = true;
+      if (!wait_all(kPvDone + ((nt - 1) & 1), ((nt - 1) >> 1) & 1)) failed = true;
       tc_fence_after();
     }
     if (!failed) {  // warp-uniform: the tensor-memory loads are collective
