@@ -12,23 +12,25 @@
 // One CTA per (b, head, tile of 128 queries); 6 warps with fixed roles:
 //  * warp 0, one lane: TMA producer. Loads the Q tile once and streams the
 //    K and V tiles of 128 keys that the window of the query tile touches
-//    through a 2-stage ring (each tile two 128B-swizzled boxes of 64 dims);
+//    through a 3-stage ring (each tile two 128B-swizzled boxes of 64 dims);
 //  * warp 1: allocates 512 tensor-memory columns; one lane issues the MMAs:
 //    S_i = Q K_i^T (M = 128 queries, N = 128 keys, K = D; both operands
 //    K-major) into one of two S buffers, then O += P_i V_i (M = 128,
-//    N = D, K = 128 keys; P K-major from shared memory, V MN-major straight
-//    from its [keys][D] tile). The order is S_0, S_1, PV_0, S_2, PV_1, ... so
-//    the softmax of one tile overlaps the QK^T of the next;
+//    N = D, K = 128 keys; P from tensor memory, V MN-major straight from
+//    its [keys][D] tile). The order is S_0, S_1, PV_0, S_2, PV_1, ... so the
+//    softmax of one tile overlaps the QK^T of the next;
 //  * warps 2-5: softmax, one thread per query row (a warp reads the
 //    tensor-memory lanes of its quarter). Each reads its row of S_i, masks
 //    it on edge tiles, keeps a reference max that moves only when a score
 //    exceeds it by more than 8 (log2 units; O in tensor memory is then
 //    rescaled in place, after the previous PV has completed), writes
-//    P = 2^(x - ref) rounded to the input type into one of two shared-memory
-//    P buffers in the swizzled K-major layout, and arrives on its barrier:
+//    P = 2^(x - ref) rounded to the input type into one of two tensor-memory
+//    P buffers (two 16-bit values per column) and arrives on its barrier:
 //    with two buffers the exponentials of tile i overlap both the PV of
-//    tile i - 1 and the QK^T of tile i + 1. The epilogue reads O, divides by
-//    the row sum and stores the row and its LSE.
+//    tile i - 1 and the QK^T of tile i + 1. Keeping P out of shared memory
+//    leaves room for the third K/V stage, which the L2 latency needs at
+//    full MMA rate. The epilogue reads O, divides by the row sum and stores
+//    the row and its LSE.
 // Every mbarrier wait is bounded (1 s); a role that gives up sets the status
 // word and leaves its loop, so every role reaches the teardown, which frees
 // the tensor memory.
@@ -54,21 +56,23 @@ constexpr int kSwaKeys = 128;  // keys per tile
 constexpr int kSwaThreads = 192;
 constexpr uint32_t kSwaTmemCols = 512;
 constexpr uint32_t kColS = 0;  // S buffers at columns 0 and 128
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = 256;  // D columns
+constexpr uint32_t kColP = 384;  // two P buffers of 64 columns (128 keys, 16-bit pairs)
+constexpr int kSwaStages = 3;    // K/V ring
 constexpr float kSwaSlack = 8.0f;
 
 // One barrier per ring slot / buffer, so that no barrier can complete twice
 // before its waiter has seen the first completion.
 enum SwaBar : int {
   kQFull = 0,
-  kKFull = 1,    // 2 stages
-  kKEmpty = 3,   // 2
-  kVFull = 5,    // 2
-  kVEmpty = 7,   // 2
-  kSFull = 9,    // 2 S buffers (tensor memory)
-  kPFull = 11,   // 2 P buffers (shared memory)
-  kPvDone = 13,  // 2: PV of the tile that used P buffer b has completed
-  kNumBars = 15
+  kKFull = 1,    // 3 stages
+  kKEmpty = 4,   // 3
+  kVFull = 7,    // 3
+  kVEmpty = 10,  // 3
+  kSFull = 13,   // 2 S buffers (tensor memory)
+  kPFull = 15,   // 2 P buffers (tensor memory)
+  kPvDone = 17,  // 2: PV of the tile that used P buffer b has completed
+  kNumBars = 19
 };
 
 template <int D>
@@ -77,12 +81,10 @@ struct SwaCfg {
   static constexpr int kAtomBytes = kSwaQ * 128;         // 128 rows x 128 B
   static constexpr int kQBytes = kSwaQ * D * 2;
   static constexpr int kKVBytes = kSwaKeys * D * 2;      // one K (or V) stage
-  static constexpr int kPBytes = kSwaQ * kSwaKeys * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + 2 * kKVBytes;
-  static constexpr int kOffP = kOffV + 2 * kKVBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffV = kOffK + kSwaStages * kKVBytes;
+  static constexpr int kOffBar = kOffV + kSwaStages * kKVBytes;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   // at least 116 KB so that one CTA holds an SM (all 512 tensor-memory columns)
   static constexpr int kUsed = kOffTmem + 16 + 1024;
@@ -139,13 +141,13 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
   auto bar = [&](int i) { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
   if (threadIdx.x == 0) {
     mbar_init(bar(kQFull), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSwaStages; ++s) {
       mbar_init(bar(kKFull + s), 1);
       mbar_init(bar(kKEmpty + s), 1);
       mbar_init(bar(kVFull + s), 1);
       mbar_init(bar(kVEmpty + s), 1);
-      mbar_init(bar(kSFull + s), 1);
     }
+    for (int s = 0; s < 2; ++s) mbar_init(bar(kSFull + s), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kPFull + s), 4 * 32);
       mbar_init(bar(kPvDone + s), 1);
@@ -174,9 +176,10 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
         tma_load_4d(base + C::kOffQ + a * C::kAtomBytes, &tmQ, bar(kQFull), a * 64, h, q0, b,
                     l2_policy_evict_first());
       for (int i = 0; i < nt && !failed; ++i) {
-        const int s = i & 1;
+        const int s = i % kSwaStages;
         const int j0 = (t0 + i) * kSwaKeys;
-        if (i >= 2 && !wait_phase(bar(kKEmpty + s), ((i - 2) >> 1) & 1, kWaitLimitNs)) {
+        const uint32_t prev = ((i - kSwaStages) / kSwaStages) & 1;  // phase of tile i - 3
+        if (i >= kSwaStages && !wait_phase(bar(kKEmpty + s), prev, kWaitLimitNs)) {
           failed = true;
           break;
         }
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
         for (int a = 0; a < C::kAtoms; ++a)
           tma_load_4d(base + C::kOffK + s * C::kKVBytes + a * C::kAtomBytes, &tmK,
                       bar(kKFull + s), a * 64, g, j0, b, keep);
-        if (i >= 2 && !wait_phase(bar(kVEmpty + s), ((i - 2) >> 1) & 1, kWaitLimitNs)) {
+        if (i >= kSwaStages && !wait_phase(bar(kVEmpty + s), prev, kWaitLimitNs)) {
           failed = true;
           break;
         }
@@ -201,10 +204,10 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
       constexpr uint32_t idesc_o = umma_idesc_f16(kSwaQ, D, BF16, true);
       bool ok = wait_phase(bar(kQFull), 0, kWaitLimitNs);
       auto issue_s = [&](int i) -> bool {
-        const int s = i & 1;
-        if (!wait_phase(bar(kKFull + s), (i >> 1) & 1, kWaitLimitNs)) return false;
+        const int s = i % kSwaStages;
+        if (!wait_phase(bar(kKFull + s), (i / kSwaStages) & 1, kWaitLimitNs)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + kColS + static_cast<uint32_t>(s) * kSwaKeys;
+        const uint32_t d = tmem + kColS + static_cast<uint32_t>(i & 1) * kSwaKeys;
         const uint32_t kb = base + C::kOffK + s * C::kKVBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -213,25 +216,24 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
                  umma_desc_sw128(kb + off, 16), idesc_s, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(kKEmpty + s));
-        tc_commit(bar(kSFull + s));
+        tc_commit(bar(kSFull + (i & 1)));
         return true;
       };
       auto issue_pv = [&](int i) -> bool {
-        const int s = i & 1;  // V stage and P buffer
-        if (!wait_phase(bar(kPFull + s), (i >> 1) & 1, kWaitLimitNs)) return false;
-        if (!wait_phase(bar(kVFull + s), (i >> 1) & 1, kWaitLimitNs)) return false;
+        const int s = i % kSwaStages;  // V stage
+        const int pbuf = i & 1;        // P buffer
+        if (!wait_phase(bar(kPFull + pbuf), (i >> 1) & 1, kWaitLimitNs)) return false;
+        if (!wait_phase(bar(kVFull + s), (i / kSwaStages) & 1, kWaitLimitNs)) return false;
         tc_fence_after();
         const uint32_t vb = base + C::kOffV + s * C::kKVBytes;
-        const uint32_t pb = base + C::kOffP + s * C::kPBytes;
+        const uint32_t pcol = tmem + kColP + static_cast<uint32_t>(pbuf) * (kSwaKeys / 2);
 #pragma unroll
         for (int kk = 0; kk < kSwaKeys / 16; ++kk) {
-          const uint32_t offp = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
-          tc_mma(tmem + kColO, umma_desc_sw128(pb + offp, 16),
-                 umma_desc_sw128(vb + kk * 2048, C::kAtomBytes), idesc_o,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + kColO, pcol + 8 * kk, umma_desc_sw128(vb + kk * 2048, C::kAtomBytes),
+                    idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(kVEmpty + s));
-        tc_commit(bar(kPvDone + s));
+        tc_commit(bar(kPvDone + pbuf));
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -317,29 +319,27 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
           break;
         }
       }
-      // P = 2^(s * scale * log2e - ref) into the swizzled K-major P tile
-      uint8_t* const prow = gbase + C::kOffP + sb * C::kPBytes + row * 128;
+      // P = 2^(s * scale * log2e - ref) into tensor-memory P buffer sb:
+      // column c holds keys 2c (low half) and 2c + 1
       float l8[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) l8[j] = 0.f;
 #pragma unroll
-      for (int c = 0; c < kSwaKeys / 8; ++c) {
-        float e[8];
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t pw[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          e[j] = ex2(fmaf(__uint_as_float(sr[8 * c + j]), sl2, neg));
-          l8[j] += e[j];
+        for (int c = 0; c < 32; ++c) {
+          const int j = 64 * h2 + 2 * c;
+          const float e0 = ex2(fmaf(__uint_as_float(sr[j]), sl2, neg));
+          const float e1 = ex2(fmaf(__uint_as_float(sr[j + 1]), sl2, neg));
+          l8[(2 * c) & 7] += e0;
+          l8[(2 * c + 1) & 7] += e1;
+          pw[c] = pack2<BF16>(e0, e1);
         }
-        uint4 w;
-        w.x = pack2<BF16>(e[0], e[1]);
-        w.y = pack2<BF16>(e[2], e[3]);
-        w.z = pack2<BF16>(e[4], e[5]);
-        w.w = pack2<BF16>(e[6], e[7]);
-        *reinterpret_cast<uint4*>(prow + (c >> 3) * C::kAtomBytes +
-                                  (((c & 7) ^ (row & 7)) << 4)) = w;
+        tc_st32(lane_addr + kColP + sb * (kSwaKeys / 2) + 32 * h2, pw);
       }
       l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      fence_proxy_async_smem();
+      tc_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kPFull + sb));
     }
