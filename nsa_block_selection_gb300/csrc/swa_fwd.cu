@@ -51,40 +51,45 @@
 namespace nsa {
 namespace {
 
-constexpr int kSwaQ = 128;     // queries per CTA (MMA M)
+constexpr int kSwaQ = 128;     // queries per work item (MMA M)
 constexpr int kSwaKeys = 128;  // keys per tile
 constexpr int kSwaThreads = 192;
 constexpr uint32_t kSwaTmemCols = 512;
-constexpr uint32_t kColS = 0;  // S buffers at columns 0 and 128
+constexpr uint32_t kColS = 0;    // S buffers at columns 0 and 128
 constexpr uint32_t kColO = 256;  // D columns
 constexpr uint32_t kColP = 384;  // two P buffers of 64 columns (128 keys, 16-bit pairs)
-constexpr int kSwaStages = 3;    // K/V ring
 constexpr float kSwaSlack = 8.0f;
 
 // One barrier per ring slot / buffer, so that no barrier can complete twice
-// before its waiter has seen the first completion.
+// before its waiter has seen the first completion. Tiles are counted across
+// the CTA's work items (g); Q buffers and the O accumulator by work item (n).
 enum SwaBar : int {
-  kQFull = 0,
-  kKFull = 1,    // 3 stages
-  kKEmpty = 4,   // 3
-  kVFull = 7,    // 3
-  kVEmpty = 10,  // 3
-  kSFull = 13,   // 2 S buffers (tensor memory)
-  kPFull = 15,   // 2 P buffers (tensor memory)
-  kPvDone = 17,  // 2: PV of the tile that used P buffer b has completed
-  kNumBars = 19
+  kQFull = 0,    // 2 Q buffers
+  kQEmpty = 2,   // 2: every QK^T of the item that used Q buffer b has completed
+  kKFull = 4,    // 2 K stages
+  kKEmpty = 6,   // 2
+  kVFull = 8,    // 2 V stages
+  kVEmpty = 10,  // 2
+  kSFull = 12,   // 2 S buffers (tensor memory)
+  kPFull = 14,   // 2 P buffers (tensor memory)
+  kPvDone = 16,  // 2: PV of the tile that used P buffer b has completed
+  kOEmpty = 18,     // the softmax warps have read O of the previous item
+  kOStaged = 19,    // the softmax warps have written this item's O tile to shared memory
+  kOSmemFree = 20,  // the previous item's O tile store has read shared memory
+  kNumBars = 21
 };
 
 template <int D>
 struct SwaCfg {
   static constexpr int kAtoms = D / 64;                 // 64-element swizzle columns
   static constexpr int kAtomBytes = kSwaQ * 128;         // 128 rows x 128 B
-  static constexpr int kQBytes = kSwaQ * D * 2;
+  static constexpr int kQBytes = kSwaQ * D * 2;          // one Q buffer
   static constexpr int kKVBytes = kSwaKeys * D * 2;      // one K (or V) stage
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kSwaStages * kKVBytes;
-  static constexpr int kOffBar = kOffV + kSwaStages * kKVBytes;
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffV = kOffK + 2 * kKVBytes;
+  static constexpr int kOffO = kOffV + 2 * kKVBytes;  // O tile, staged for a TMA store
+  static constexpr int kOffBar = kOffO + kQBytes;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   // at least 116 KB so that one CTA holds an SM (all 512 tensor-memory columns)
   static constexpr int kUsed = kOffTmem + 16 + 1024;
@@ -92,12 +97,43 @@ struct SwaCfg {
 };
 
 struct SwaProblem {
-  void* O;
   float* LSE;
-  int M, N, H, Hkv, hpg, qtiles;
+  int B, M, N, H, Hkv, hpg, qtiles;
   int left, right;  // clamped to [0, M + N]: M + N is unbounded in effect
   float sl2;        // scale * log2(e)
+  int64_t items;    // B * H * qtiles
 };
+
+// One work item: a tile of 128 queries of one head, and the keys its
+// windows touch, in whole tiles of 128.
+struct SwaItem {
+  int b, g, h, q0, q_last, t0, nt, in_lo, in_hi;
+};
+
+// Items in the order (b, KV head, query tile, head within the group), the
+// head fastest: the CTAs working at the same time share K/V tiles in L2.
+// items < 2^31 (host check): 32-bit arithmetic.
+__device__ __forceinline__ SwaItem swa_item(const SwaProblem& p, int64_t item) {
+  SwaItem it;
+  uint32_t x = static_cast<uint32_t>(item);
+  const int hh = static_cast<int>(x % static_cast<uint32_t>(p.hpg));
+  x /= static_cast<uint32_t>(p.hpg);
+  const int qt = static_cast<int>(x % static_cast<uint32_t>(p.qtiles));
+  x /= static_cast<uint32_t>(p.qtiles);
+  it.g = static_cast<int>(x % static_cast<uint32_t>(p.Hkv));
+  it.b = static_cast<int>(x / static_cast<uint32_t>(p.Hkv));
+  it.h = it.g * p.hpg + hh;
+  it.q0 = qt * kSwaQ;
+  it.q_last = min(it.q0 + kSwaQ, p.M) - 1;
+  const int jlo = max(0, it.q0 - p.left);
+  const int jhi = min(p.N - 1, it.q_last + p.right);
+  it.t0 = jlo / kSwaKeys;
+  it.nt = jhi >= jlo ? jhi / kSwaKeys - it.t0 + 1 : 0;
+  // keys every row of the item sees (tiles inside need no mask)
+  it.in_lo = max(0, it.q_last - p.left);
+  it.in_hi = min(p.N - 1, it.q0 + p.right);
+  return it;
+}
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -108,7 +144,8 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kSwaThreads, 1)
     swa_fwd_kernel(const SwaProblem p, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV) {
+                   const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmO) {
   using C = SwaCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -117,41 +154,22 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // (b, KV head, query tile, head within the group), the head fastest: the
-  // CTAs in flight share their K/V tiles through L2
-  uint32_t x = blockIdx.x;
-  const int hh = static_cast<int>(x % p.hpg);
-  x /= p.hpg;
-  const int qt = static_cast<int>(x % p.qtiles);
-  x /= p.qtiles;
-  const int g = static_cast<int>(x % p.Hkv);
-  const int b = static_cast<int>(x / p.Hkv);
-  const int h = g * p.hpg + hh;
-  const int q0 = qt * kSwaQ;
-  const int q_last = min(q0 + kSwaQ, p.M) - 1;
-  // keys the tile's windows touch, in whole tiles of 128
-  const int jlo = max(0, q0 - p.left);
-  const int jhi = min(p.N - 1, q_last + p.right);
-  const int t0 = jlo / kSwaKeys;
-  const int nt = jhi >= jlo ? jhi / kSwaKeys - t0 + 1 : 0;
-  // keys every row of the tile sees (tiles inside need no mask)
-  const int in_lo = max(0, q_last - p.left);
-  const int in_hi = min(p.N - 1, q0 + p.right);
-
   auto bar = [&](int i) { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
   if (threadIdx.x == 0) {
-    mbar_init(bar(kQFull), 1);
-    for (int s = 0; s < kSwaStages; ++s) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kQFull + s), 1);
+      mbar_init(bar(kQEmpty + s), 1);
       mbar_init(bar(kKFull + s), 1);
       mbar_init(bar(kKEmpty + s), 1);
       mbar_init(bar(kVFull + s), 1);
       mbar_init(bar(kVEmpty + s), 1);
-    }
-    for (int s = 0; s < 2; ++s) mbar_init(bar(kSFull + s), 1);
-    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kSFull + s), 1);
       mbar_init(bar(kPFull + s), 4 * 32);
       mbar_init(bar(kPvDone + s), 1);
     }
+    mbar_init(bar(kOEmpty), 4 * 32);
+    mbar_init(bar(kOStaged), 4 * 32);
+    mbar_init(bar(kOSmemFree), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -163,227 +181,313 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kOffTmem);
   bool failed = false;
+  // Work items are dealt in rounds of gridDim.x, in snake order (the
+  // direction reverses every round) so that no CTA takes the same position
+  // -- the same query-tile offset, the same amount of work -- in every round.
+  const int64_t nrounds = (p.items + gridDim.x - 1) / gridDim.x;
+  auto item_of = [&](int64_t k) -> int64_t {
+    const int64_t pos = (k & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x;
+    return k * gridDim.x + pos;  // may be >= p.items in the last round
+  };
 
   if (warp == 0) {
-    if (lane == 0 && nt > 0) {
+    if (lane == 0) {
       // ---- TMA producer ----
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       const uint64_t keep = l2_policy_evict_last();
-      mbar_arrive_expect_tx(bar(kQFull), C::kQBytes);
-      for (int a = 0; a < C::kAtoms; ++a)
-        tma_load_4d(base + C::kOffQ + a * C::kAtomBytes, &tmQ, bar(kQFull), a * 64, h, q0, b,
-                    l2_policy_evict_first());
-      for (int i = 0; i < nt && !failed; ++i) {
-        const int s = i % kSwaStages;
-        const int j0 = (t0 + i) * kSwaKeys;
-        const uint32_t prev = ((i - kSwaStages) / kSwaStages) & 1;  // phase of tile i - 3
-        if (i >= kSwaStages && !wait_phase(bar(kKEmpty + s), prev, kWaitLimitNs)) {
+      const uint64_t once = l2_policy_evict_first();
+      int64_t gt = 0;  // tiles loaded so far
+      int n = 0;       // items with keys so far
+      for (int64_t k = 0; k < nrounds && !failed; ++k) {
+        const int64_t x = item_of(k);
+        if (x >= p.items) continue;
+        const SwaItem it = swa_item(p, x);
+        if (it.nt == 0) continue;
+        const int qb = n & 1;
+        if (n >= 2 && !wait_phase(bar(kQEmpty + qb), ((n - 2) >> 1) & 1, kWaitLimitNs)) {
           failed = true;
           break;
         }
-        mbar_arrive_expect_tx(bar(kKFull + s), C::kKVBytes);
+        mbar_arrive_expect_tx(bar(kQFull + qb), C::kQBytes);
         for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_4d(base + C::kOffK + s * C::kKVBytes + a * C::kAtomBytes, &tmK,
-                      bar(kKFull + s), a * 64, g, j0, b, keep);
-        if (i >= kSwaStages && !wait_phase(bar(kVEmpty + s), prev, kWaitLimitNs)) {
-          failed = true;
-          break;
+          tma_load_4d(base + C::kOffQ + qb * C::kQBytes + a * C::kAtomBytes, &tmQ,
+                      bar(kQFull + qb), a * 64, it.h, it.q0, it.b, once);
+        for (int i = 0; i < it.nt; ++i) {
+          const int64_t gi = gt + i;
+          const int s = static_cast<int>(gi & 1);
+          const uint32_t prev = static_cast<uint32_t>(((gi - 2) >> 1) & 1);
+          const int j0 = (it.t0 + i) * kSwaKeys;
+          if (gi >= 2 && !wait_phase(bar(kKEmpty + s), prev, kWaitLimitNs)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kKFull + s), C::kKVBytes);
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_4d(base + C::kOffK + s * C::kKVBytes + a * C::kAtomBytes, &tmK,
+                        bar(kKFull + s), a * 64, it.g, j0, it.b, keep);
+          if (gi >= 2 && !wait_phase(bar(kVEmpty + s), prev, kWaitLimitNs)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kVFull + s), C::kKVBytes);
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_4d(base + C::kOffV + s * C::kKVBytes + a * C::kAtomBytes, &tmV,
+                        bar(kVFull + s), a * 64, it.g, j0, it.b, keep);
         }
-        mbar_arrive_expect_tx(bar(kVFull + s), C::kKVBytes);
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_4d(base + C::kOffV + s * C::kKVBytes + a * C::kAtomBytes, &tmV,
-                      bar(kVFull + s), a * 64, g, j0, b, keep);
+        gt += it.nt;
+        ++n;
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && nt > 0) {
-      // ---- MMA issuer ----
+    if (lane == 0) {
+      // ---- MMA issuer: the tiles of all items as one stream ----
       constexpr uint32_t idesc_s = umma_idesc_f16(kSwaQ, kSwaKeys, BF16, false);
       constexpr uint32_t idesc_o = umma_idesc_f16(kSwaQ, D, BF16, true);
-      bool ok = wait_phase(bar(kQFull), 0, kWaitLimitNs);
-      auto issue_s = [&](int i) -> bool {
-        const int s = i % kSwaStages;
-        if (!wait_phase(bar(kKFull + s), (i / kSwaStages) & 1, kWaitLimitNs)) return false;
+      auto issue_s = [&](int64_t gi, int qb) -> bool {
+        const int s = static_cast<int>(gi & 1);
+        if (!wait_phase(bar(kKFull + s), static_cast<uint32_t>((gi >> 1) & 1), kWaitLimitNs))
+          return false;
         tc_fence_after();
-        const uint32_t d = tmem + kColS + static_cast<uint32_t>(i & 1) * kSwaKeys;
+        const uint32_t d = tmem + kColS + static_cast<uint32_t>(s) * kSwaKeys;
+        const uint32_t qbase = base + C::kOffQ + qb * C::kQBytes;
         const uint32_t kb = base + C::kOffK + s * C::kKVBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * C::kAtomBytes + (k & 3) * 32;
-          tc_mma(d, umma_desc_sw128(base + C::kOffQ + off, 16),
-                 umma_desc_sw128(kb + off, 16), idesc_s, k > 0 ? 1u : 0u);
+          tc_mma(d, umma_desc_sw128(qbase + off, 16), umma_desc_sw128(kb + off, 16), idesc_s,
+                 k > 0 ? 1u : 0u);
         }
         tc_commit(bar(kKEmpty + s));
-        tc_commit(bar(kSFull + (i & 1)));
+        tc_commit(bar(kSFull + s));
         return true;
       };
-      auto issue_pv = [&](int i) -> bool {
-        const int s = i % kSwaStages;  // V stage
-        const int pbuf = i & 1;        // P buffer
-        if (!wait_phase(bar(kPFull + pbuf), (i >> 1) & 1, kWaitLimitNs)) return false;
-        if (!wait_phase(bar(kVFull + s), (i / kSwaStages) & 1, kWaitLimitNs)) return false;
+      // PV of global tile gi; `first`: the item's first tile (O starts from
+      // zero, after the softmax warps have read the previous item's O)
+      auto issue_pv = [&](int64_t gi, bool first, int n) -> bool {
+        const int s = static_cast<int>(gi & 1);  // V stage and P buffer
+        const uint32_t ph = static_cast<uint32_t>((gi >> 1) & 1);
+        if (!wait_phase(bar(kPFull + s), ph, kWaitLimitNs)) return false;
+        if (!wait_phase(bar(kVFull + s), ph, kWaitLimitNs)) return false;
+        if (first && n >= 1 && !wait_phase(bar(kOEmpty), (n - 1) & 1, kWaitLimitNs))
+          return false;
         tc_fence_after();
         const uint32_t vb = base + C::kOffV + s * C::kKVBytes;
-        const uint32_t pcol = tmem + kColP + static_cast<uint32_t>(pbuf) * (kSwaKeys / 2);
+        const uint32_t pcol = tmem + kColP + static_cast<uint32_t>(s) * (kSwaKeys / 2);
 #pragma unroll
-        for (int kk = 0; kk < kSwaKeys / 16; ++kk) {
+        for (int kk = 0; kk < kSwaKeys / 16; ++kk)
           tc_mma_ts(tmem + kColO, pcol + 8 * kk, umma_desc_sw128(vb + kk * 2048, C::kAtomBytes),
-                    idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+                    idesc_o, (!first || kk > 0) ? 1u : 0u);
         tc_commit(bar(kVEmpty + s));
-        tc_commit(bar(kPvDone + pbuf));
+        tc_commit(bar(kPvDone + s));
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int i = 1; i <= nt && ok; ++i) {
-        if (i < nt) ok = issue_s(i);
-        if (ok) ok = issue_pv(i - 1);
+      bool ok = true;
+      int64_t gt = 0;
+      int n = 0;
+      int64_t pend = -1;  // global tile whose PV is still to be issued
+      bool pend_first = false;
+      int pend_n = 0;
+      for (int64_t k = 0; k < nrounds && ok; ++k) {
+        const int64_t x = item_of(k);
+        if (x >= p.items) continue;
+        const SwaItem it = swa_item(p, x);
+        if (it.nt == 0) continue;
+        const int qb = n & 1;
+        ok = wait_phase(bar(kQFull + qb), (n >> 1) & 1, kWaitLimitNs);
+        for (int i = 0; i < it.nt && ok; ++i) {
+          ok = issue_s(gt + i, qb);
+          if (ok && i == it.nt - 1) tc_commit(bar(kQEmpty + qb));
+          if (ok && pend >= 0) ok = issue_pv(pend, pend_first, pend_n);
+          pend = gt + i;
+          pend_first = i == 0;
+          pend_n = n;
+        }
+        gt += it.nt;
+        ++n;
       }
+      if (ok && pend >= 0) ok = issue_pv(pend, pend_first, pend_n);
       failed = !ok;
     }
   } else {
-    // ---- softmax (warps 2..5): thread <-> query row ----
+    // ---- softmax (warps 2..5): thread <-> query row of each item ----
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int iq = q0 + row;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int lo_i = max(0, iq - p.left);
-    const int hi_i = min(p.N - 1, iq + p.right);
-    float ref = -INFINITY, neg = 0.f, l = 0.f;  // ref, neg in the log2 domain
     const float sl2 = p.sl2;
     // waits are decided warp-wide (tcgen05.ld/st are warp-collective)
-    auto wait_all = [&](int b, int parity) {
+    auto wait_all = [&](int b, uint32_t parity) {
       return __all_sync(kFull, wait_phase(bar(b), parity, kWaitLimitNs));
     };
-    for (int i = 0; i < nt; ++i) {
-      const int sb = i & 1;  // S buffer and P buffer of this tile
-      if (!wait_all(kSFull + sb, (i >> 1) & 1)) {
-        failed = true;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[kSwaKeys];
+    int64_t gt = 0;
+    int n = 0;
+    int e = 0;  // epilogues (O tiles stored) so far
+    for (int64_t k = 0; k < nrounds && !failed; ++k) {
+      const int64_t x = item_of(k);
+      if (x >= p.items) continue;
+      const SwaItem it = swa_item(p, x);
+      const int iq = it.q0 + row;
+      const int lo_i = max(0, iq - p.left);
+      const int hi_i = min(p.N - 1, iq + p.right);
+      float ref = -INFINITY, neg = 0.f, l = 0.f;  // ref, neg in the log2 domain
+      for (int i = 0; i < it.nt; ++i) {
+        const int64_t gi = gt + i;
+        const int sb = static_cast<int>(gi & 1);  // S buffer and P buffer of this tile
+        if (!wait_all(kSFull + sb, static_cast<uint32_t>((gi >> 1) & 1))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[kSwaKeys];
 #pragma unroll
-      for (int c = 0; c < kSwaKeys / 32; ++c)
-        tc_ld32(lane_addr + kColS + sb * kSwaKeys + 32 * c,
-                *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      tc_wait_ld();
-      const int j0 = (t0 + i) * kSwaKeys;
-      if (j0 < in_lo || j0 + kSwaKeys - 1 > in_hi) {  // edge tile (CTA-uniform)
+        for (int c = 0; c < kSwaKeys / 32; ++c)
+          tc_ld32(lane_addr + kColS + sb * kSwaKeys + 32 * c,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        tc_wait_ld();
+        const int j0 = (it.t0 + i) * kSwaKeys;
+        if (j0 < it.in_lo || j0 + kSwaKeys - 1 > it.in_hi) {  // edge tile (CTA-uniform)
 #pragma unroll
-        for (int j = 0; j < kSwaKeys; ++j)
-          if (j0 + j < lo_i || j0 + j > hi_i) sr[j] = __float_as_uint(-INFINITY);
-      }
-      // row max of the raw scores (scale > 0 commutes with max), 8 chains
-      float m8[8];
+          for (int j = 0; j < kSwaKeys; ++j)
+            if (j0 + j < lo_i || j0 + j > hi_i) sr[j] = __float_as_uint(-INFINITY);
+        }
+        // row max of the raw scores (scale > 0 commutes with max), 8 chains
+        float m8[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) m8[j] = __uint_as_float(sr[j]);
+        for (int j = 0; j < 8; ++j) m8[j] = __uint_as_float(sr[j]);
 #pragma unroll
-      for (int j = 8; j < kSwaKeys; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
-      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
-      const bool move = mx > ref + kSwaSlack;
-      if (__any_sync(kFull, move)) {
-        // alpha = 0 while a row has seen nothing (its O row is still 0).
-        // O may be rescaled only once the previous tile's PV has completed.
-        const float alpha = move ? ex2(ref - mx) : 1.f;
-        if (i > 0) {
-          if (!wait_all(kPvDone + ((i - 1) & 1), ((i - 1) >> 1) & 1)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
+        for (int j = 8; j < kSwaKeys; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
+        const bool move = mx > ref + kSwaSlack;
+        if (__any_sync(kFull, move)) {
+          // alpha = 0 while a row has seen nothing (its O row is still 0).
+          // O may be rescaled only once the previous tile's PV has completed.
+          const float alpha = move ? ex2(ref - mx) : 1.f;
+          if (i > 0) {
+            if (!wait_all(kPvDone + static_cast<int>((gi - 1) & 1),
+                          static_cast<uint32_t>(((gi - 1) >> 1) & 1))) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tc_ld32(lane_addr + kColO + 32 * c, o);
-            tc_wait_ld();
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tc_ld32(lane_addr + kColO + 32 * c, o);
+              tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tc_st32(lane_addr + kColO + 32 * c, o);
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tc_st32(lane_addr + kColO + 32 * c, o);
+            }
+            tc_wait_st();
           }
-          tc_wait_st();
+          if (move) {
+            l *= alpha;
+            ref = mx;
+            neg = -mx;
+          }
         }
-        if (move) {
-          l *= alpha;
-          ref = mx;
-          neg = -mx;
+        // P buffer sb was last read by the PV of tile gi - 2
+        if (gi >= 2 && !wait_all(kPvDone + sb, static_cast<uint32_t>(((gi - 2) >> 1) & 1))) {
+          failed = true;
+          break;
         }
+        // P = 2^(s * scale * log2e - ref) into tensor-memory P buffer sb:
+        // column c holds keys 2c (low half) and 2c + 1
+        float l8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) l8[j] = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int j = 64 * h2 + 2 * c;
+            const float e0 = ex2(fmaf(__uint_as_float(sr[j]), sl2, neg));
+            const float e1 = ex2(fmaf(__uint_as_float(sr[j + 1]), sl2, neg));
+            l8[(2 * c) & 7] += e0;
+            l8[(2 * c + 1) & 7] += e1;
+            pw[c] = pack2<BF16>(e0, e1);
+          }
+          tc_st32(lane_addr + kColP + sb * (kSwaKeys / 2) + 32 * h2, pw);
+        }
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kPFull + sb));
       }
-      // P buffer sb was last read by the PV of tile i - 2
-      if (i >= 2) {
-        if (!wait_all(kPvDone + sb, ((i - 2) >> 1) & 1)) {
+      if (failed) break;
+      // epilogue: read O into registers and release it to the next item's
+      // PVs; normalise, stage the tile in shared memory (128B-swizzled rows)
+      // and let one thread store it with TMA; LSE is stored directly
+      uint32_t o[D];
+      if (it.nt > 0) {
+        const int64_t gl = gt + it.nt - 1;
+        if (!wait_all(kPvDone + static_cast<int>(gl & 1), static_cast<uint32_t>((gl >> 1) & 1))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          tc_ld32(lane_addr + kColO + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&o[32 * c]));
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(kOEmpty));
+      } else {
+#pragma unroll
+        for (int j = 0; j < D; ++j) o[j] = 0u;
+      }
+      const bool leader = warp == 2 && lane == 0;
+      if (e >= 1) {  // the previous tile's store must have read the staging buffer
+        if (leader) {
+          bulk_wait_group_read0();
+          mbar_arrive(bar(kOSmemFree));
+        }
+        if (!wait_all(kOSmemFree, static_cast<uint32_t>((e - 1) & 1))) {
           failed = true;
           break;
         }
       }
-      // P = 2^(s * scale * log2e - ref) into tensor-memory P buffer sb:
-      // column c holds keys 2c (low half) and 2c + 1
-      float l8[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) l8[j] = 0.f;
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t pw[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int j = 64 * h2 + 2 * c;
-          const float e0 = ex2(fmaf(__uint_as_float(sr[j]), sl2, neg));
-          const float e1 = ex2(fmaf(__uint_as_float(sr[j + 1]), sl2, neg));
-          l8[(2 * c) & 7] += e0;
-          l8[(2 * c + 1) & 7] += e1;
-          pw[c] = pack2<BF16>(e0, e1);
-        }
-        tc_st32(lane_addr + kColP + sb * (kSwaKeys / 2) + 32 * h2, pw);
-      }
-      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-      tc_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kPFull + sb));
-    }
-    // epilogue
-    if (!failed && nt > 0) {
-      if (!wait_all(kPvDone + ((nt - 1) & 1), ((nt - 1) >> 1) & 1)) failed = true;
-      tc_fence_after();
-    }
-    if (!failed) {  // warp-uniform: the tensor-memory loads are collective
-      const bool store = iq < p.M;
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = static_cast<uint16_t*>(p.O) +
-                       ((static_cast<int64_t>(b) * p.M + (store ? iq : 0)) * p.H + h) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        if (nt > 0) {
-          tc_ld32(lane_addr + kColO + 32 * c, o);
-          tc_wait_ld();
-        } else {
+      uint8_t* const orow = gbase + C::kOffO + row * 128;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = 0u;
-        }
-        if (!store) continue;
-        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack2<BF16>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-          w.y = pack2<BF16>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          w.z = pack2<BF16>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-          w.w = pack2<BF16>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-          dst[q] = w;
+      for (int q = 0; q < D / 8; ++q) {
+        uint4 w;
+        w.x = pack2<BF16>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+        w.y = pack2<BF16>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+        w.z = pack2<BF16>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+        w.w = pack2<BF16>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+        *reinterpret_cast<uint4*>(orow + (q >> 3) * C::kAtomBytes + (((q & 7) ^ (row & 7)) << 4)) =
+            w;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kOStaged));
+      bool staged = true;
+      if (leader) {
+        staged = wait_phase(bar(kOStaged), static_cast<uint32_t>(e & 1), kWaitLimitNs);
+        if (staged) {
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_store_4d(&tmO, base + C::kOffO + a * C::kAtomBytes, a * 64, it.h, it.q0, it.b);
+          bulk_commit_group();
         }
       }
-      if (store && p.LSE != nullptr) {
+      if (!__all_sync(kFull, staged)) failed = true;  // warp-wide, like every other decision
+      if (iq < p.M && p.LSE != nullptr) {
         constexpr float kLn2 = 0.69314718055994530942f;
-        p.LSE[(static_cast<int64_t>(b) * p.H + h) * p.M + iq] =
+        p.LSE[(static_cast<int64_t>(it.b) * p.H + it.h) * p.M + iq] =
             l > 0.f ? (ref + __log2f(l)) * kLn2 : -INFINITY;
       }
+      ++e;
+      gt += it.nt;
+      if (it.nt > 0) ++n;
     }
   }
 
-  // teardown: every role is here; the tensor memory is freed
+  // teardown: every role is here; the O stores have completed; the tensor
+  // memory is freed
+  if (warp == 2 && lane == 0) bulk_wait_group0();
   if (failed) report_timeout();
   tc_fence_before();
   __syncthreads();
@@ -395,16 +499,18 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
 }
 
 template <int D, bool BF16>
-int launch_swa(const SwaProblem& p, const void* Q, const void* K, const void* V, int64_t B,
+int launch_swa(const SwaProblem& p, const void* Q, const void* K, const void* V, void* O,
                cudaStream_t st) {
   using C = SwaCfg<D>;
   constexpr CUtensorMapDataType dt =
       BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap tq, tk, tv;
-  if (!encode_kv_map(&tq, Q, B, p.M, p.H, D, kSwaQ, dt)) return NSA_ERR_LAUNCH;
+  CUtensorMap tq, tk, tv, to;
+  if (!encode_kv_map(&tq, Q, p.B, p.M, p.H, D, kSwaQ, dt) ||
+      !encode_kv_map(&to, O, p.B, p.M, p.H, D, kSwaQ, dt))
+    return NSA_ERR_LAUNCH;
   if (p.N > 0) {
-    if (!encode_kv_map(&tk, K, B, p.N, p.Hkv, D, kSwaKeys, dt) ||
-        !encode_kv_map(&tv, V, B, p.N, p.Hkv, D, kSwaKeys, dt))
+    if (!encode_kv_map(&tk, K, p.B, p.N, p.Hkv, D, kSwaKeys, dt) ||
+        !encode_kv_map(&tv, V, p.B, p.N, p.Hkv, D, kSwaKeys, dt))
       return NSA_ERR_LAUNCH;
   } else {
     memset(&tk, 0, sizeof(tk));  // no key: no tile is ever loaded
@@ -414,8 +520,13 @@ int launch_swa(const SwaProblem& p, const void* Q, const void* K, const void* V,
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return NSA_ERR_LAUNCH;
-  const int64_t blocks = B * p.H * p.qtiles;
-  kern<<<static_cast<unsigned>(blocks), kSwaThreads, C::kSmemBytes, st>>>(p, tq, tk, tv);
+  // persistent: one CTA per SM, work items dealt round-robin
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return NSA_ERR_LAUNCH;
+  const int64_t blocks = p.items < sms ? p.items : sms;
+  kern<<<static_cast<unsigned>(blocks), kSwaThreads, C::kSmemBytes, st>>>(p, tq, tk, tv, to);
   return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
@@ -446,8 +557,9 @@ extern "C" int nsa_swa_fwd(const void* Q, const void* K, const void* V, void* O,
   };
   if (mis(Q, 16) || mis(K, 16) || mis(V, 16) || mis(O, 16) || mis(LSE, 4)) return NSA_ERR_ALIGN;
   SwaProblem p;
-  p.O = O;
   p.LSE = LSE;
+  p.B = static_cast<int>(B);
+  p.items = B * H * qtiles;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.H = static_cast<int>(H);
@@ -462,6 +574,7 @@ extern "C" int nsa_swa_fwd(const void* Q, const void* K, const void* V, void* O,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf = dtype == NSA_BF16;
   if (D == 64)
-    return bf ? launch_swa<64, true>(p, Q, K, V, B, st) : launch_swa<64, false>(p, Q, K, V, B, st);
-  return bf ? launch_swa<128, true>(p, Q, K, V, B, st) : launch_swa<128, false>(p, Q, K, V, B, st);
+    return bf ? launch_swa<64, true>(p, Q, K, V, O, st) : launch_swa<64, false>(p, Q, K, V, O, st);
+  return bf ? launch_swa<128, true>(p, Q, K, V, O, st)
+            : launch_swa<128, false>(p, Q, K, V, O, st);
 }
