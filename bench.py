@@ -99,7 +99,7 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-FWD_KERNEL_SOURCES = ("common.cuh", "ptx.cuh", "sel_attn_fwd.cu", "sel_attn_fwd.cuh")
+FWD_KERNEL_SOURCES = ("common.cuh", "ptx.cuh", "sel_attn_fwd.cu", "sel_attn_fwd.cuh", "status.cuh")
 
 
 def kernel_source_hash():

@@ -43,6 +43,7 @@
 #include "nsa_sel_attn.h"
 #include "ptx.cuh"
 #include "sel_attn_fwd.cuh"
+#include "status.cuh"
 
 #ifndef NSA_WARPS
 #define NSA_WARPS 4
@@ -456,32 +457,11 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
              : launch_fwd<128, false, false>(p, K, V, B, st);
 }
 
+int fwd_read_and_clear_status(unsigned int* value) { return read_and_clear_status(value); }
+
 }  // namespace nsa
 
 extern "C" {
-
-const char* nsa_status_string(int status) {
-  switch (status) {
-    case NSA_OK: return "ok";
-    case NSA_ERR_NULL: return "null pointer";
-    case NSA_ERR_SHAPE: return "invalid shape";
-    case NSA_ERR_BLOCK_SIZE: return "block_size must be 32 or 64";
-    case NSA_ERR_HEAD_DIM: return "head dim D must be 64 or 128";
-    case NSA_ERR_GROUPS:
-      return "H must be a multiple of G, with H/G <= 8 or a multiple of 8";
-    case NSA_ERR_ALIGN: return "misaligned pointer";
-    case NSA_ERR_LAUNCH: return "CUDA launch failed";
-    case NSA_ERR_TIMEOUT: return "device wait timed out";
-    case NSA_ERR_WORKSPACE: return "workspace too small";
-    case NSA_ERR_SCRATCH:
-      return "problem needs more scratch than the fixed buffer of the no-allocation entry point";
-    case NSA_ERR_DTYPE:
-      return "unsupported dtype: Q/K/V fp16 or bf16; O fp32 or the type of Q/K/V";
-    default: return "unknown status";
-  }
-}
-
-int nsa_version(void) { return 200; }
 
 int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* block_indices,
                      float* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
@@ -496,16 +476,6 @@ int nsa_sel_attn_fwd_ex(const void* Q, const void* K, const void* V,
                         float scale, int qkv_dtype, int o_dtype, void* stream) {
   return nsa::launch_forward(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T, 0, block_size,
                              scale, qkv_dtype, o_dtype, static_cast<cudaStream_t>(stream));
-}
-
-int nsa_sync_status(void* stream) {
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return NSA_ERR_LAUNCH;
-  unsigned int fwd = 0u, bwd = 0u, swa = 0u;
-  if (nsa::read_and_clear_status(&fwd) != NSA_OK) return NSA_ERR_LAUNCH;
-  if (nsa::bwd_read_and_clear_status(&bwd) != NSA_OK) return NSA_ERR_LAUNCH;
-  if (nsa::swa_read_and_clear_status(&swa) != NSA_OK) return NSA_ERR_LAUNCH;
-  return (fwd | bwd | swa) ? NSA_ERR_TIMEOUT : NSA_OK;
 }
 
 int nsa_selftest_wait_timeout(int64_t limit_ns, void* stream) {

@@ -22,10 +22,4 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
                    int64_t D, int64_t T, int64_t m_off, int block_size, float scale,
                    int qkv_dtype, int o_dtype, cudaStream_t st);
 
-// Reads and clears the status word of the backward kernels' translation unit.
-int bwd_read_and_clear_status(unsigned int* value);
-
-// Reads and clears the status word of the sliding-window kernel's translation unit.
-int swa_read_and_clear_status(unsigned int* value);
-
 }  // namespace nsa

@@ -46,6 +46,7 @@
 #include "nsa_sel_attn.h"
 #include "ptx.cuh"
 #include "sel_attn_fwd.cuh"
+#include "status.cuh"
 #include "tc.cuh"
 
 namespace nsa {
