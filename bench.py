@@ -492,9 +492,48 @@ def run_swa(flush, args, dev):
         res["windows"].append({"window": [left, right], "ms_per_step": t, "tflops": tf,
                                "tensor_frac": tf / peaks["bf16_tflops"], "flops": flops,
                                "steps": steps})
+    if not args.skip_cpu:
+        res["cpu_oracle"] = swa_cpu_oracle(q, k, v, (4096, 0))
     del q, k, v, out, lse
     torch.cuda.empty_cache()
     return res
+
+
+def swa_cpu_oracle(q, k, v, window, n_rows=96, seed=4):
+    """oracle/swa.py on a seeded sample of (i, KV head) rows of the same
+    inputs, one process; TFLOP/s counted like the kernel's (4*D per query,
+    head and key in the window)."""
+    import numpy as np
+
+    import oracle.swa as W
+
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    hpg = H // Hkv
+    rng = np.random.default_rng(seed)
+    ms = rng.integers(0, S, n_rows)
+    gs = rng.integers(0, Hkv, n_rows)
+    kh = k.float().cpu().numpy()
+    vh = v.float().cpu().numpy()
+    qrows = {int(m): q[0, int(m)].float().cpu().numpy() for m in ms}
+
+    class _Q:  # the sampled query rows, indexed like Q [B, S, H, D]
+        shape = (B, S, H, D)
+
+        def __getitem__(self, key):
+            b, i, hs = key
+            return qrows[int(i)][hs]
+
+    flops = 0
+    t0 = time.perf_counter()
+    for m, g in zip(ms, gs):
+        W.swa_row(_Q(), kh, vh, 0, int(m), int(g), window[0], window[1])
+        flops += 4 * D * hpg * len(W.window_keys(int(m), S, window[0], window[1]))
+    secs = time.perf_counter() - t0
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "window": list(window),
+            "sample": f"{n_rows} seeded random (query, KV head) rows, fp64 numpy, one process, "
+                      f"{secs:.2f} s"}
 
 
 def topk_bytes(B, M, N, G, T, bs, n_init, n_local):
@@ -507,6 +546,27 @@ def topk_bytes(B, M, N, G, T, bs, n_init, n_local):
     c = np.minimum(m, N - 1) // bs if N > 0 else np.full(M, -1)
     free = np.where(c + 1 > T, c + 1 - n_init - n_local, 0)
     return int(B * G * (4 * free.sum() + 4 * T * M))
+
+
+def topk_cpu_oracle(sc, w, nblk, n_rows=2048, seed=3):
+    """oracle/topk.py on a seeded sample of rows of the same score tensor, one
+    process; GB/s counted like the kernel's algorithmic bytes."""
+    import numpy as np
+
+    import oracle.topk as K
+
+    rng = np.random.default_rng(seed)
+    ms = rng.integers(0, w.M, n_rows)
+    gs = rng.integers(0, w.G, n_rows)
+    rows = sc[0, ms, gs].cpu().numpy()
+    t0 = time.perf_counter()
+    for r in range(n_rows):
+        K.topk_row(rows[r], int(ms[r]), w.N, w.block_size, w.T, 1, 2)
+    secs = time.perf_counter() - t0
+    c = np.minimum(ms, w.N - 1) // w.block_size
+    nbytes = int((4 * np.where(c + 1 > w.T, c + 1 - 3, 0) + 4 * w.T).sum())
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_rows} seeded random (m, g) rows, one process, {secs:.2f} s"}
 
 
 def run_topk(w, flush, args, dev):
@@ -536,6 +596,8 @@ def run_topk(w, flush, args, dev):
            "scores_bytes": sc.numel() * 4, "n_init": 1, "n_local": 2,
            "note": "bytes = scores of the free candidates of rows with more than T "
                    "candidates + the index rows written; L2 flushed between steps"}
+    if not args.skip_cpu:
+        res["cpu_oracle"] = topk_cpu_oracle(sc, w, nblk)
     del sc, out
     torch.cuda.empty_cache()
     return res
