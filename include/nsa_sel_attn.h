@@ -133,6 +133,30 @@ int nsa_sel_attn_fwd_ex(const void* Q, const void* K, const void* V,
                         int qkv_dtype, int o_dtype, void* stream);
 
 /*
+ * nsa_sel_attn_fwd_strided -- nsa_sel_attn_fwd_ex on strided tensors.
+ *
+ *   strides  host array of 12 element strides, or NULL for contiguous:
+ *            [0..2]  Q over (b, m, h)     [3..5]  K over (b, n, g)
+ *            [6..8]  V over (b, n, g)     [9..11] O over (b, m, h)
+ *            The last dimension (d) of Q, K, V and O is contiguous; LSE and
+ *            block_indices are contiguous as in nsa_sel_attn_fwd.
+ *
+ * Lets Q, K and V be views into one fused projection (for example
+ * [B, M, H + 2G, D] with Q the first H heads) and O a slice of a larger
+ * buffer, without copies. Every stride must be a multiple of 8 elements (so
+ * every row starts 16-byte aligned; else NSA_ERR_ALIGN) and in
+ * [0, 2^40] (else NSA_ERR_SHAPE); the strides must describe memory the
+ * caller owns, and O must not overlap Q, K or V. Everything else is
+ * nsa_sel_attn_fwd_ex.
+ */
+int nsa_sel_attn_fwd_strided(const void* Q, const void* K, const void* V,
+                             const int32_t* block_indices, void* O, float* LSE,
+                             int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
+                             int64_t D, int64_t T, int block_size, float scale,
+                             int qkv_dtype, int o_dtype, const int64_t* strides,
+                             void* stream);
+
+/*
  * nsa_sel_attn_fwd_host_workspace_bytes -- device workspace that
  * nsa_sel_attn_fwd_host needs for these sizes and query chunk length
  * (chunk_m <= 0 selects the default). Returns the byte count, or a negative

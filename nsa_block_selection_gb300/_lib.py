@@ -20,7 +20,7 @@ NSA_OK = 0
 NSA_F16, NSA_BF16, NSA_F32 = 0, 1, 2
 
 EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sel_attn_fwd_ex",
-           "nsa_sync_status",
+           "nsa_sel_attn_fwd_strided", "nsa_sync_status",
            "nsa_selftest_wait_timeout", "nsa_sel_attn_fwd_host_workspace_bytes",
            "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd",
            "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks", "nsa_swa_fwd")
@@ -56,6 +56,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_fwd_ex.restype = c_int
     lib.nsa_sel_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                         i64, c_int, ctypes.c_float, c_int, c_int, vp]
+    lib.nsa_sel_attn_fwd_strided.restype = c_int
+    lib.nsa_sel_attn_fwd_strided.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                             i64, i64, c_int, ctypes.c_float, c_int, c_int, vp,
+                                             vp]
     lib.nsa_sync_status.restype = c_int
     lib.nsa_sync_status.argtypes = [vp]
     lib.nsa_selftest_wait_timeout.restype = c_int
@@ -103,16 +107,20 @@ def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float]
     """NSA selection-attention forward on the GPU.
 
     q: fp16 or bf16 [B, M, H, D]; k, v: [B, N, G, D] of q's dtype;
-    block_indices: int32 [B, M, G, T] (-1 = padding); all contiguous on one
-    CUDA device. Returns (O [B, M, H, D], LSE fp32 [B, H, M]). O is fp32
-    unless ``out_dtype`` (or a preallocated ``out``) is q's dtype.
-    ``stream`` defaults to torch's current stream.
+    block_indices: int32 [B, M, G, T] (-1 = padding), contiguous; all on one
+    CUDA device. q, k, v (and a preallocated ``out``) may be strided views
+    (for example slices of one fused projection) whose last dimension is
+    contiguous and whose strides are multiples of 8 elements. Returns
+    (O [B, M, H, D], LSE fp32 [B, H, M]). O is fp32 unless ``out_dtype`` (or
+    a preallocated ``out``) is q's dtype. ``stream`` defaults to torch's
+    current stream.
     """
     import torch
 
     lib = load()
     B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=True,
-                                        qkv_dtypes=(torch.float16, torch.bfloat16))
+                                        qkv_dtypes=(torch.float16, torch.bfloat16),
+                                        strided=True)
     if out_dtype is None:
         out_dtype = out.dtype if out is not None else torch.float32
     if out_dtype not in (torch.float32, q.dtype):
@@ -121,8 +129,8 @@ def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float]
         out = torch.empty((B, M, H, D), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
-    if out.dtype != out_dtype or tuple(out.shape) != (B, M, H, D) or not out.is_contiguous():
-        raise ValueError(f"out must be contiguous {out_dtype} [B, M, H, D]")
+    if out.dtype != out_dtype or tuple(out.shape) != (B, M, H, D) or out.stride(-1) != 1:
+        raise ValueError(f"out must be {out_dtype} [B, M, H, D] with a contiguous last dim")
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, M) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous fp32 [B, H, M]")
     if stream is None:
@@ -130,7 +138,13 @@ def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float]
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out), _ptr(lse), B, M, N, H,
             G, D, T, int(block_size), sc)
-    if q.dtype == torch.float16 and out.dtype == torch.float32:
+    if not all(t.is_contiguous() or t.numel() == 0 for t in (q, k, v, out)):
+        strides = (ctypes.c_int64 * 12)(*(list(q.stride()[:3]) + list(k.stride()[:3]) +
+                                          list(v.stride()[:3]) + list(out.stride()[:3])))
+        st = lib.nsa_sel_attn_fwd_strided(*args, _dtype_code(q.dtype), _dtype_code(out.dtype),
+                                          strides, ctypes.c_void_p(stream.cuda_stream))
+        what = "nsa_sel_attn_fwd_strided"
+    elif q.dtype == torch.float16 and out.dtype == torch.float32:
         st = lib.nsa_sel_attn_fwd(*args, ctypes.c_void_p(stream.cuda_stream))
         what = "nsa_sel_attn_fwd"
     else:
@@ -142,7 +156,8 @@ def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float]
     return out, lse
 
 
-def _check_common(q, k, v, block_indices, device_expected: bool, qkv_dtypes=None):
+def _check_common(q, k, v, block_indices, device_expected: bool, qkv_dtypes=None,
+                  strided: bool = False):
     import torch
 
     qkv_dtypes = qkv_dtypes or (torch.float16,)
@@ -164,7 +179,10 @@ def _check_common(q, k, v, block_indices, device_expected: bool, qkv_dtypes=None
     for name, t, _ in named:
         if t.is_cuda != device_expected:
             raise ValueError(f"{name} must be a {'CUDA' if device_expected else 'CPU'} tensor")
-        if not t.is_contiguous():
+        if strided and name != "block_indices":
+            if t.numel() > 0 and t.stride(-1) != 1:
+                raise ValueError(f"{name} must have a contiguous last dimension")
+        elif not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     return B, M, N, H, G, D, T
 

@@ -133,7 +133,31 @@ static inline EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// K or V [B, N, G, D] fp16 as a 4-D map (d, g, n, b); box = 64 d x 1 x rows x 1.
+// A [B, N, G, D] 16-bit tensor with element strides (sb, sn, sg) for b, n, g
+// (d contiguous) as a 4-D map (d, g, n, b); box = 64 d x 1 x rows x 1. A
+// stride of an extent-1 dimension is never used and is replaced by the
+// contiguous value (the encoder wants every stride a positive multiple of
+// 16 bytes).
+static inline bool encode_kv_map_strided(CUtensorMap* tm, const void* ptr, int64_t B, int64_t N,
+                                         int64_t G, int64_t D, int rows, CUtensorMapDataType dt,
+                                         int64_t sb, int64_t sn, int64_t sg) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  if (G == 1) sg = D;
+  if (N == 1) sn = G * sg;
+  if (B == 1) sb = N * sn;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(G),
+                              static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(sg * 2), static_cast<cuuint64_t>(sn * 2),
+                                 static_cast<cuuint64_t>(sb * 2)};
+  const cuuint32_t box[4] = {kBoxCols, 1, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return enc(tm, dt, 4, const_cast<void*>(ptr), dims, strides, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K or V [B, N, G, D] contiguous as a 4-D map (d, g, n, b); box = 64 d x 1 x rows x 1.
 static inline bool encode_kv_map(CUtensorMap* tm, const void* ptr, int64_t B, int64_t N,
                                  int64_t G, int64_t D, int rows = kTileKeys,
                                  CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16) {

@@ -208,7 +208,7 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
     const int rc = launch_forward(dQ, N > 0 ? dK : nullptr, N > 0 ? dV : nullptr,
                                   T > 0 ? reinterpret_cast<const int32_t*>(dI) : nullptr, dO,
                                   dL, B, mc, N, H, G, D, T, m0, block_size, scale, NSA_F16,
-                                  NSA_F32, fs);
+                                  NSA_F32, nullptr, fs);
     if (rc != NSA_OK) return rc;
     ok = cudaEventRecord(r.fw_ev[s], fs) == cudaSuccess;
 

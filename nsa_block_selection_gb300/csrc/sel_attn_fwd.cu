@@ -60,6 +60,8 @@ struct Problem {
   void* O;            // fp32, or the inputs' 16-bit type
   float* LSE;
   int64_t M, N, H, G, T;
+  int64_t q_sb, q_sm, q_sh;  // element strides of Q over b, m, h (d contiguous)
+  int64_t o_sb, o_sm, o_sh;  // element strides of O over b, m, h (d contiguous)
   int64_t m_off;  // query position of row 0 (a chunk of a longer sequence)
   int64_t units;  // B * G * nsub * M
   int hpg;        // query heads per KV group
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   // zero for padding columns
   uint32_t qf[C::kSteps][2];
   {
-    const uint16_t* q = p.Q + ((b * p.M + m) * p.H + hbase + gid) * D + 2 * tig;
+    const uint16_t* q = p.Q + b * p.q_sb + m * p.q_sm + (hbase + gid) * p.q_sh + 2 * tig;
 #pragma unroll
     for (int k = 0; k < C::kSteps; ++k) {
       qf[k][0] = gid < hw ? __ldg(reinterpret_cast<const unsigned int*>(q + 16 * k)) : 0u;
@@ -307,8 +309,8 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   if constexpr (O16) {
     // round, then transpose each 8x8 (dim x head) quarter in registers so a
     // lane holds two adjacent dims of head gid: one 4-byte store per pair
-    uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.O) +
-                                              ((b * p.M + m) * p.H + hbase + gid) * D) +
+    uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.O) + b * p.o_sb +
+                                              m * p.o_sm + (hbase + gid) * p.o_sh) +
                   tig;
 #pragma unroll
     for (int i = 0; i < C::kSteps; ++i) {
@@ -321,7 +323,9 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     }
   } else {
     const bool ha = 2 * tig < hw, hb = 2 * tig + 1 < hw;  // real heads, not padding
-    float* o = static_cast<float*>(p.O) + ((b * p.M + m) * p.H + hbase + 2 * tig) * D + gid;
+    float* o = static_cast<float*>(p.O) + b * p.o_sb + m * p.o_sm + (hbase + 2 * tig) * p.o_sh +
+               gid;
+    float* o2 = o + p.o_sh;  // head 2 tig + 1
 #pragma unroll
     for (int i = 0; i < C::kSteps; ++i) {
       if (ha) {
@@ -329,8 +333,8 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
         o[16 * i + 8] = acc[i][2] * inva;
       }
       if (hb) {
-        o[D + 16 * i] = acc[i][1] * invb;
-        o[D + 16 * i + 8] = acc[i][3] * invb;
+        o2[16 * i] = acc[i][1] * invb;
+        o2[16 * i + 8] = acc[i][3] * invb;
       }
     }
   }
@@ -361,15 +365,15 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns) {
 
 template <int D, bool BF16, bool O16>
 static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
-                      cudaStream_t stream) {
+                      const int64_t (&ks)[3], const int64_t (&vs)[3], cudaStream_t stream) {
   constexpr int W = NSA_WARPS;
   using C = Cfg<D, W>;
   constexpr CUtensorMapDataType dt =
       BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tk, tv;
   if (p.N > 0) {
-    if (!encode_kv_map(&tk, K, B, p.N, p.G, D, kTileKeys, dt) ||
-        !encode_kv_map(&tv, V, B, p.N, p.G, D, kTileKeys, dt))
+    if (!encode_kv_map_strided(&tk, K, B, p.N, p.G, D, kTileKeys, dt, ks[0], ks[1], ks[2]) ||
+        !encode_kv_map_strided(&tv, V, B, p.N, p.G, D, kTileKeys, dt, vs[0], vs[1], vs[2]))
       return NSA_ERR_LAUNCH;
   } else {
     memset(&tk, 0, sizeof(tk));  // no key: no tile is ever loaded
@@ -408,7 +412,7 @@ int check_sizes(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D
 int launch_forward(const void* Q, const void* K, const void* V, const int32_t* block_indices,
                    void* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                    int64_t D, int64_t T, int64_t m_off, int block_size, float scale,
-                   int qkv_dtype, int o_dtype, cudaStream_t st) {
+                   int qkv_dtype, int o_dtype, const int64_t* strides, cudaStream_t st) {
   const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
   if (chk != NSA_OK) return chk;
   if ((qkv_dtype != NSA_F16 && qkv_dtype != NSA_BF16) ||
@@ -425,6 +429,22 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
   if (mis(Q, 16) || mis(K, 16) || mis(V, 16) || mis(O, 16) || mis(LSE, 4) ||
       mis(block_indices, 4))
     return NSA_ERR_ALIGN;
+  // element strides (b, m|n, h|g) of Q, K, V, O; d is contiguous
+  int64_t sq[3] = {M * H * D, H * D, D}, sk[3] = {N * G * D, G * D, D};
+  int64_t sv[3] = {sk[0], sk[1], sk[2]}, so[3] = {sq[0], sq[1], sq[2]};
+  if (strides != nullptr) {
+    for (int i = 0; i < 3; ++i) {
+      sq[i] = strides[i];
+      sk[i] = strides[3 + i];
+      sv[i] = strides[6 + i];
+      so[i] = strides[9 + i];
+    }
+    // every row start stays 16-byte aligned (TMA, vector loads and stores)
+    for (int i = 0; i < 12; ++i) {
+      if (strides[i] < 0 || strides[i] > (int64_t(1) << 40)) return NSA_ERR_SHAPE;
+      if (strides[i] % 8 != 0) return NSA_ERR_ALIGN;
+    }
+  }
 
   Problem p;
   p.Q = static_cast<const uint16_t*>(Q);
@@ -436,6 +456,12 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
   p.H = H;
   p.G = G;
   p.T = T;
+  p.q_sb = sq[0];
+  p.q_sm = sq[1];
+  p.q_sh = sq[2];
+  p.o_sb = so[0];
+  p.o_sm = so[1];
+  p.o_sh = so[2];
   p.m_off = m_off;
   p.hpg = static_cast<int>(H / G);
   p.nsub = head_subgroups(p.hpg);
@@ -446,15 +472,15 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
   p.sl2 = sc * 1.4426950408889634f;
   const bool bf = qkv_dtype == NSA_BF16, o16 = o_dtype != NSA_F32;
   if (D == 64) {
-    if (bf) return o16 ? launch_fwd<64, true, true>(p, K, V, B, st)
-                       : launch_fwd<64, true, false>(p, K, V, B, st);
-    return o16 ? launch_fwd<64, false, true>(p, K, V, B, st)
-               : launch_fwd<64, false, false>(p, K, V, B, st);
+    if (bf) return o16 ? launch_fwd<64, true, true>(p, K, V, B, sk, sv, st)
+                       : launch_fwd<64, true, false>(p, K, V, B, sk, sv, st);
+    return o16 ? launch_fwd<64, false, true>(p, K, V, B, sk, sv, st)
+               : launch_fwd<64, false, false>(p, K, V, B, sk, sv, st);
   }
-  if (bf) return o16 ? launch_fwd<128, true, true>(p, K, V, B, st)
-                     : launch_fwd<128, true, false>(p, K, V, B, st);
-  return o16 ? launch_fwd<128, false, true>(p, K, V, B, st)
-             : launch_fwd<128, false, false>(p, K, V, B, st);
+  if (bf) return o16 ? launch_fwd<128, true, true>(p, K, V, B, sk, sv, st)
+                     : launch_fwd<128, true, false>(p, K, V, B, sk, sv, st);
+  return o16 ? launch_fwd<128, false, true>(p, K, V, B, sk, sv, st)
+             : launch_fwd<128, false, false>(p, K, V, B, sk, sv, st);
 }
 
 int fwd_read_and_clear_status(unsigned int* value) { return read_and_clear_status(value); }
@@ -467,7 +493,7 @@ int nsa_sel_attn_fwd(const void* Q, const void* K, const void* V, const int32_t*
                      float* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                      int64_t D, int64_t T, int block_size, float scale, void* stream) {
   return nsa::launch_forward(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T, 0, block_size,
-                             scale, NSA_F16, NSA_F32, static_cast<cudaStream_t>(stream));
+                             scale, NSA_F16, NSA_F32, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int nsa_sel_attn_fwd_ex(const void* Q, const void* K, const void* V,
@@ -475,7 +501,17 @@ int nsa_sel_attn_fwd_ex(const void* Q, const void* K, const void* V,
                         int64_t N, int64_t H, int64_t G, int64_t D, int64_t T, int block_size,
                         float scale, int qkv_dtype, int o_dtype, void* stream) {
   return nsa::launch_forward(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T, 0, block_size,
-                             scale, qkv_dtype, o_dtype, static_cast<cudaStream_t>(stream));
+                             scale, qkv_dtype, o_dtype, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int nsa_sel_attn_fwd_strided(const void* Q, const void* K, const void* V,
+                             const int32_t* block_indices, void* O, float* LSE, int64_t B,
+                             int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                             int block_size, float scale, int qkv_dtype, int o_dtype,
+                             const int64_t* strides, void* stream) {
+  return nsa::launch_forward(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T, 0, block_size,
+                             scale, qkv_dtype, o_dtype, strides,
+                             static_cast<cudaStream_t>(stream));
 }
 
 int nsa_selftest_wait_timeout(int64_t limit_ns, void* stream) {

@@ -215,3 +215,33 @@ def test_swa_bad_arguments(lib, over, status):
 @pytest.mark.parametrize("over", [dict(B=0), dict(M=0)])
 def test_swa_empty_is_a_no_op(lib, over):
     assert call_swa(lib, q=None, k=None, v=None, o=None, lse=None, **over) == 0
+
+
+def call_strided(lib, strides, q=FAKE, k=FAKE, v=FAKE, idx=FAKE, o=FAKE, lse=FAKE, **over):
+    a = dict(GOOD)
+    a.update(over)
+    vp = ctypes.c_void_p
+    arr = (ctypes.c_int64 * 12)(*strides) if strides is not None else None
+    return lib.nsa_sel_attn_fwd_strided(vp(q), vp(k), vp(v), vp(idx), vp(o), vp(lse), a["B"],
+                                        a["M"], a["N"], a["H"], a["G"], a["D"], a["T"], a["bs"],
+                                        0.0, 0, 2, arr, None)
+
+
+def _contig_strides(B=1, M=128, N=128, H=16, G=2, D=128):
+    return [M * H * D, H * D, D, N * G * D, G * D, D, N * G * D, G * D, D, M * H * D, H * D, D]
+
+
+@pytest.mark.parametrize("i,value,status", [
+    (0, 4, -6), (1, 12, -6), (2, 1, -6), (4, 100, -6), (8, 3, -6), (11, 6, -6),
+    (3, -8, -2), (9, (1 << 41), -2),
+])
+def test_strided_checks(lib, i, value, status):
+    st = _contig_strides()
+    st[i] = value
+    assert call_strided(lib, st) == status
+
+
+def test_strided_empty_and_null_strides(lib):
+    assert call_strided(lib, None, q=None, k=None, v=None, idx=None, o=None, lse=None, B=0) == 0
+    assert call_strided(lib, _contig_strides(), q=None, k=None, v=None, idx=None, o=None,
+                        lse=None, M=0) == 0
