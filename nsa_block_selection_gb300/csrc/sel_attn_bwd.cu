@@ -39,6 +39,7 @@
 #include "ptx.cuh"
 #include "sel_attn_fwd.cuh"
 #include "status.cuh"
+#include "tc.cuh"
 
 namespace nsa {
 
@@ -693,6 +694,314 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Stage 3 on the 5th-generation tensor cores (D = 128): dK, dV (key-major)
+// ---------------------------------------------------------------------------
+//
+// One CTA per chunk of <= kQueriesPerChunk items of a list (as above). The
+// items (query, head sub-group) are taken 16 at a time: their 8 head rows
+// each are exactly one 1024-byte 128B-swizzled group, so 16 items gathered
+// by 2-D TMA form 128-row Q and dO operand tiles without any reshuffling.
+// Per batch of 128 rows, with the block's 64 keys (a block of 32 is read as
+// 64 keys, the second half masked):
+//   S  = Q_R K^T,  dP = dO_R V^T       (M = 128 rows, N = 64 keys, K = D)
+//   P  = 2^(S scale log2e - LSE log2e), dS = P (dP - delta)  (softmax warps,
+//        one row per thread; masked and padding rows give exact zeros)
+//   dV^T += dO_R^T P,  dK^T += Q_R^T dS  (M = D = 128, N = 64, K = 128 rows;
+//        the Q / dO tiles serve again as MN-major A operands, P and dS are
+//        written to shared memory as MN-major B operands)
+// with S / dP double-buffered in tensor memory and the Q / dO tiles in a
+// 2-stage ring, so the next batch's S and dP overlap this batch's softmax.
+// dV^T and dK^T accumulate in tensor memory over the chunk and are added
+// into dK / dV with fp32 atomics at the end (lane = d, coalesced per key).
+// Warps: 0 producer (one lane), 1 tensor-memory owner and MMA issuer (one
+// lane), 2-5 softmax and epilogue. Every wait is bounded.
+
+constexpr int kTcBatch = 16;  // items per batch: 128 rows
+enum DkvBar : int {
+  kBlkFull = 0,
+  kQdFull = 1,    // 2 stages
+  kQdEmpty = 3,   // 2
+  kSdFull = 5,    // 2 S / dP buffers
+  kPdsFull = 7,   // 2 P / dS buffers
+  kPdsFree = 9,   // 2
+  kAccDone = 11,
+  kDkvBars = 12
+};
+
+struct DkvTcCfg {
+  static constexpr int kAtom = 128 * 128;    // 128 rows x 128 B
+  static constexpr int kBlkAtom = 64 * 128;  // 64 keys x 128 B
+  static constexpr int kOffK = 0;            // 2 atoms (d 0-63, 64-127)
+  static constexpr int kOffV = kOffK + 2 * kBlkAtom;
+  static constexpr int kOffStage = kOffV + 2 * kBlkAtom;
+  static constexpr int kStageBytes = 4 * kAtom;  // Q tile (2 atoms), dO tile (2 atoms)
+  static constexpr int kOffPds = kOffStage + 2 * kStageBytes;
+  static constexpr int kPdsBytes = 2 * 128 * 128;  // P tile, dS tile (128 rows x 64 keys)
+  static constexpr int kOffBar = kOffPds + 2 * kPdsBytes;
+  static constexpr int kOffTmem = kOffBar + kDkvBars * 8;
+  static constexpr int kSmemBytes = kOffTmem + 16 + 1024;
+  static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 320;
+};
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(192, 1)
+    sel_attn_bwd_dkv_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
+                               const __grid_constant__ CUtensorMap tmV,
+                               const __grid_constant__ CUtensorMap tmQ,
+                               const __grid_constant__ CUtensorMap tmD) {
+  using C = DkvTcCfg;
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  const int c = blockIdx.x;
+  if (c >= p.choffs[p.L]) return;  // before any tensor memory is taken
+  int lo = 0, hi = p.L;            // list l with choffs[l] <= c < choffs[l + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.choffs[mid] <= c)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int l = lo;
+  const int q0 = p.offs[l] + (c - p.choffs[l]) * kQueriesPerChunk;
+  const int nq = min(q0 + kQueriesPerChunk, p.offs[l + 1]) - q0;
+  const int nsub = SPLIT ? p.nsub : 1;
+  const int nitems = nq * nsub;
+  const int nbat = (nitems + kTcBatch - 1) / kTcBatch;
+  const int t = l % p.nblk;
+  const int bg = l / p.nblk;
+  const int g = bg % static_cast<int>(p.G);
+  const int b = bg / static_cast<int>(p.G);
+  const int64_t hgroup = static_cast<int64_t>(g) * p.hpg;
+  const int hw0 = p.hpg < kHeadsPerGroup ? p.hpg : kHeadsPerGroup;  // head rows per item
+  const int n_blk = t * p.bs;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  auto bar = [&](int i) { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+  auto item_query = [&](int item, int& m, int& sub) {
+    m = __ldg(p.lists + q0 + (SPLIT ? item / nsub : item));
+    sub = SPLIT ? item % nsub : 0;
+  };
+
+  if (hw0 < kHeadsPerGroup) {
+    // head rows the copies never write (groups of fewer than 8 heads): zero,
+    // so the padding rows multiply zeros
+    const int per = 2 * 4 * kTcBatch * (kHeadsPerGroup - hw0) * 8;  // 16-byte pieces
+    for (int e = threadIdx.x; e < per; e += blockDim.x) {
+      const int piece = e % 8, rr = e / 8;
+      const int row = hw0 + rr % (kHeadsPerGroup - hw0);
+      const int item = (rr / (kHeadsPerGroup - hw0)) % kTcBatch;
+      const int atom = rr / ((kHeadsPerGroup - hw0) * kTcBatch);  // 8 atoms: 2 stages x 4
+      st_shared_zero16(base + C::kOffStage + atom * C::kAtom + (item * 8 + row) * 128 + piece * 16);
+    }
+    fence_proxy_async_smem();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBlkFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kQdFull + s), 1);
+      mbar_init(bar(kQdEmpty + s), 1);
+      mbar_init(bar(kSdFull + s), 1);
+      mbar_init(bar(kPdsFull + s), 4 * 32);
+      mbar_init(bar(kPdsFree + s), 1);
+    }
+    mbar_init(bar(kAccDone), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc_alloc(base + C::kOffTmem, 512);
+    tc_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kOffTmem);
+  bool failed = false;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer: the block's K / V (64 keys), then Q / dO rows per batch ----
+      const uint64_t keep = l2_policy_evict_last();
+      mbar_arrive_expect_tx(bar(kBlkFull), 4 * C::kBlkAtom);
+      for (int a = 0; a < 2; ++a) {
+        tma_load_4d(base + C::kOffK + a * C::kBlkAtom, &tmK, bar(kBlkFull), a * kBoxCols, g,
+                    n_blk, b, keep);
+        tma_load_4d(base + C::kOffV + a * C::kBlkAtom, &tmV, bar(kBlkFull), a * kBoxCols, g,
+                    n_blk, b, keep);
+      }
+      for (int i = 0; i < nbat && !failed; ++i) {
+        const int s = i & 1;
+        if (i >= 2 && !wait_phase(bar(kQdEmpty + s), ((i - 2) >> 1) & 1, kWaitLimitNs)) {
+          failed = true;
+          break;
+        }
+        const uint32_t st = base + C::kOffStage + s * C::kStageBytes;
+        mbar_arrive_expect_tx(bar(kQdFull + s), kTcBatch * 4 * hw0 * 128);
+        for (int j = 0; j < kTcBatch; ++j) {
+          // items past the chunk repeat its last item (their rows are masked)
+          const int item = min(i * kTcBatch + j, nitems - 1);
+          int m, sub;
+          item_query(item, m, sub);
+          const int qrow = static_cast<int>((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup);
+          for (int a = 0; a < 2; ++a) {
+            tma_load_2d(st + a * C::kAtom + j * 1024, &tmQ, bar(kQdFull + s), a * kBoxCols, qrow);
+            tma_load_2d(st + (2 + a) * C::kAtom + j * 1024, &tmD, bar(kQdFull + s), a * kBoxCols,
+                        qrow);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      constexpr uint32_t idesc_sd = umma_idesc_f16(128, 64, false, false);   // K-major A, B
+      constexpr uint32_t idesc_acc =
+          umma_idesc_f16(128, 64, false, true) | (1u << 15);  // MN-major A and B
+      bool ok = wait_phase(bar(kBlkFull), 0, kWaitLimitNs);
+      auto issue_sd = [&](int i) -> bool {
+        const int s = i & 1;
+        if (!wait_phase(bar(kQdFull + s), (i >> 1) & 1, kWaitLimitNs)) return false;
+        tc_fence_after();
+        const uint32_t st = base + C::kOffStage + s * C::kStageBytes;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t offa = (k >> 2) * C::kAtom + (k & 3) * 32;
+          const uint32_t offb = (k >> 2) * C::kBlkAtom + (k & 3) * 32;
+          tc_mma(tmem + C::kColS + 64 * s, umma_desc_sw128(st + offa, 16),
+                 umma_desc_sw128(base + C::kOffK + offb, 16), idesc_sd, k > 0 ? 1u : 0u);
+          tc_mma(tmem + C::kColDp + 64 * s, umma_desc_sw128(st + 2 * C::kAtom + offa, 16),
+                 umma_desc_sw128(base + C::kOffV + offb, 16), idesc_sd, k > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(kSdFull + s));
+        return true;
+      };
+      auto issue_acc = [&](int i) -> bool {
+        const int s = i & 1;
+        if (!wait_phase(bar(kPdsFull + s), (i >> 1) & 1, kWaitLimitNs)) return false;
+        tc_fence_after();
+        const uint32_t st = base + C::kOffStage + s * C::kStageBytes;
+        const uint32_t pds = base + C::kOffPds + s * C::kPdsBytes;
+#pragma unroll
+        for (int k = 0; k < 128 / 16; ++k) {  // 16 rows per step
+          const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
+          tc_mma(tmem + C::kColDv, umma_desc_sw128(st + 2 * C::kAtom + k * 2048, C::kAtom),
+                 umma_desc_sw128(pds + k * 2048, 16), idesc_acc, acc);
+          tc_mma(tmem + C::kColDk, umma_desc_sw128(st + k * 2048, C::kAtom),
+                 umma_desc_sw128(pds + 128 * 128 + k * 2048, 16), idesc_acc, acc);
+        }
+        tc_commit(bar(kQdEmpty + s));
+        tc_commit(bar(kPdsFree + s));
+        return true;
+      };
+      if (ok && nbat > 0) ok = issue_sd(0);
+      for (int i = 1; i <= nbat && ok; ++i) {
+        if (i < nbat) ok = issue_sd(i);
+        if (ok) ok = issue_acc(i - 1);
+      }
+      if (ok) tc_commit(bar(kAccDone));
+      failed = !ok;
+    }
+  } else {
+    // ---- softmax (warps 2..5): thread <-> row (item r / 8, head r % 8) ----
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = p.sl2;
+    auto wait_all = [&](int bb, uint32_t parity) {
+      return __all_sync(kFull, wait_phase(bar(bb), parity, kWaitLimitNs));
+    };
+    for (int i = 0; i < nbat; ++i) {
+      const int s = i & 1;
+      const int item = i * kTcBatch + r / 8;
+      const bool valid = item < nitems;
+      int m = 0, sub = 0;
+      if (valid) item_query(item, m, sub);
+      const float* rec = p.rec + (((b * p.M + m) * p.G + g) * nsub + sub) * 16;
+      const float lse2 = valid ? __ldg(rec + (r & 7)) : INFINITY;
+      const float delta = valid ? __ldg(rec + 8 + (r & 7)) : 0.f;
+      const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
+      // keys n_blk + j visible: j < block size and n_blk + j <= lastkey
+      const int nvis = valid ? min(p.bs, lastkey - n_blk + 1) : 0;
+      if (!wait_all(kSdFull + s, (i >> 1) & 1)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[64], dv[64];
+      tc_ld32(lane_addr + C::kColS + 64 * s, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tc_ld32(lane_addr + C::kColS + 64 * s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tc_ld32(lane_addr + C::kColDp + 64 * s, *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+      tc_ld32(lane_addr + C::kColDp + 64 * s + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+      tc_wait_ld();
+      if (i >= 2 && !wait_all(kPdsFree + s, ((i - 2) >> 1) & 1)) {
+        failed = true;
+        break;
+      }
+      uint8_t* const prow = gbase + C::kOffPds + s * C::kPdsBytes + r * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t pw[4], dw[4];
+#pragma unroll
+        for (int h2 = 0; h2 < 4; ++h2) {
+          const int j = 8 * cc + 2 * h2;
+          const bool v0 = j < nvis, v1 = j + 1 < nvis;
+          const float p0 = v0 ? ex2(fmaf(__uint_as_float(sv[j]), sl2, -lse2)) : 0.f;
+          const float p1 = v1 ? ex2(fmaf(__uint_as_float(sv[j + 1]), sl2, -lse2)) : 0.f;
+          const float d0 = v0 ? p0 * (__uint_as_float(dv[j]) - delta) : 0.f;
+          const float d1 = v1 ? p1 * (__uint_as_float(dv[j + 1]) - delta) : 0.f;
+          pw[h2] = pack_half2(p0, p1);
+          dw[h2] = pack_half2(d0, d1);
+        }
+        const uint32_t off = ((cc ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(prow + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        *reinterpret_cast<uint4*>(prow + 128 * 128 + off) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(kPdsFull + s));
+    }
+    // epilogue: lane = d; add the chunk's dV and dK (scaled) into global memory
+    if (!failed && nbat > 0) {
+      if (!wait_all(kAccDone, 0)) {
+        failed = true;
+      } else {
+        tc_fence_after();
+        const int d = r;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t vv[32], kv[32];
+          tc_ld32(lane_addr + C::kColDv + 32 * half, vv);
+          tc_ld32(lane_addr + C::kColDk + 32 * half, kv);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int kidx = 32 * half + j;
+            const int n = n_blk + kidx;
+            if (kidx < p.bs && n < p.N) {
+              const int64_t at = ((b * p.N + n) * p.G + g) * D + d;
+              atomicAdd(p.dV + at, __uint_as_float(vv[j]));
+              atomicAdd(p.dK + at, __uint_as_float(kv[j]) * p.scale);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  if (failed) report_timeout();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tc_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host
 // ---------------------------------------------------------------------------
 
@@ -806,6 +1115,18 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   using Yes = std::true_type;
   using No = std::false_type;
   const bool split = p.nsub > 1;
+  if constexpr (D == 128) {
+    // the tensor-core (tcgen05) kernel; block K / V read as 64-key boxes
+    CUtensorMap tk64, tv64;
+    if (!encode_kv_map(&tk64, K, B, p.N, p.G, D, 64) || !encode_kv_map(&tv64, V, B, p.N, p.G, D, 64))
+      return NSA_ERR_LAUNCH;
+    auto kk = split ? sel_attn_bwd_dkv_tc_kernel<true> : sel_attn_bwd_dkv_tc_kernel<false>;
+    if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkvTcCfg::kSmemBytes) != cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    kk<<<static_cast<unsigned>(chunks), 192, DkvTcCfg::kSmemBytes, st>>>(p, tk64, tv64, tq, tdo);
+    return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
+  }
   int rc;
   if (p.bs == 64)
     rc = split ? run(I4{}, Yes{}) : run(I4{}, No{});
