@@ -716,6 +716,23 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
 // Warps: 0 producer (one lane), 1 tensor-memory owner and MMA issuer (one
 // lane), 2-5 softmax and epilogue. Every wait is bounded.
 
+// A row-major fp16 matrix [rows, 128] as a 3-D map (64 columns, rows, 2
+// column halves); box = 64 x `rows_per_box` x 2: one copy brings both halves
+// of `rows_per_box` rows, landing as two consecutive 128B-swizzled groups
+// (half 0's rows, then half 1's).
+static inline bool encode_rows_halves_map(CUtensorMap* tm, const void* ptr, int64_t rows,
+                                          int rows_per_box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), 2};
+  const cuuint64_t strides[2] = {128 * 2, 64 * 2};  // next row, next half (bytes)
+  const cuuint32_t box[3] = {kBoxCols, static_cast<cuuint32_t>(rows_per_box), 2};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr int kTcBatch = 16;  // items per batch: 128 rows
 enum DkvBar : int {
   kBlkFull = 0,
@@ -728,8 +745,12 @@ enum DkvBar : int {
   kDkvBars = 12
 };
 
+// Q / dO tiles of a batch: item j's 8 head rows at j * 2048, dims 0-63 in
+// the first 1024 bytes and dims 64-127 in the next (one 3-D copy per item);
+// 8-row groups of one column half are 2048 bytes apart.
 struct DkvTcCfg {
   static constexpr int kAtom = 128 * 128;    // 128 rows x 128 B
+  static constexpr int kItemBytes = 2048;    // 8 rows x 2 halves x 128 B
   static constexpr int kBlkAtom = 64 * 128;  // 64 keys x 128 B
   static constexpr int kOffK = 0;            // 2 atoms (d 0-63, 64-127)
   static constexpr int kOffV = kOffK + 2 * kBlkAtom;
@@ -739,7 +760,8 @@ struct DkvTcCfg {
   static constexpr int kPdsBytes = 2 * 128 * 128;  // P tile, dS tile (128 rows x 64 keys)
   static constexpr int kOffBar = kOffPds + 2 * kPdsBytes;
   static constexpr int kOffTmem = kOffBar + kDkvBars * 8;
-  static constexpr int kSmemBytes = kOffTmem + 16 + 1024;
+  static constexpr int kOffList = kOffTmem + 16;  // the chunk's query ids
+  static constexpr int kSmemBytes = kOffList + kQueriesPerChunk * 4 + 1024;
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 320;
 };
 
@@ -782,21 +804,23 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
   auto bar = [&](int i) { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+  int* const qlist = reinterpret_cast<int*>(gbase + C::kOffList);
+  for (int j = threadIdx.x; j < nq; j += blockDim.x) qlist[j] = __ldg(p.lists + q0 + j);
   auto item_query = [&](int item, int& m, int& sub) {
-    m = __ldg(p.lists + q0 + (SPLIT ? item / nsub : item));
+    m = qlist[SPLIT ? item / nsub : item];
     sub = SPLIT ? item % nsub : 0;
   };
 
   if (hw0 < kHeadsPerGroup) {
     // head rows the copies never write (groups of fewer than 8 heads): zero,
     // so the padding rows multiply zeros
-    const int per = 2 * 4 * kTcBatch * (kHeadsPerGroup - hw0) * 8;  // 16-byte pieces
+    // (stage, tensor, item, half) groups x (8 - hw0) rows x 8 pieces of 16 bytes
+    const int per = 2 * 2 * kTcBatch * 2 * (kHeadsPerGroup - hw0) * 8;
     for (int e = threadIdx.x; e < per; e += blockDim.x) {
       const int piece = e % 8, rr = e / 8;
       const int row = hw0 + rr % (kHeadsPerGroup - hw0);
-      const int item = (rr / (kHeadsPerGroup - hw0)) % kTcBatch;
-      const int atom = rr / ((kHeadsPerGroup - hw0) * kTcBatch);  // 8 atoms: 2 stages x 4
-      st_shared_zero16(base + C::kOffStage + atom * C::kAtom + (item * 8 + row) * 128 + piece * 16);
+      const int grp = rr / (kHeadsPerGroup - hw0);  // 1024-byte group: item-half of a tile
+      st_shared_zero16(base + C::kOffStage + grp * 1024 + row * 128 + piece * 16);
     }
     fence_proxy_async_smem();
   }
@@ -823,9 +847,10 @@ __global__ void __launch_bounds__(192, 1)
   bool failed = false;
 
   if (warp == 0) {
+    // ---- producer: the block's K / V (64 keys), then Q / dO rows per batch;
+    // lane j < 16 issues the copies of item j of a batch ----
+    const uint64_t keep = l2_policy_evict_last();
     if (lane == 0) {
-      // ---- producer: the block's K / V (64 keys), then Q / dO rows per batch ----
-      const uint64_t keep = l2_policy_evict_last();
       mbar_arrive_expect_tx(bar(kBlkFull), 4 * C::kBlkAtom);
       for (int a = 0; a < 2; ++a) {
         tma_load_4d(base + C::kOffK + a * C::kBlkAtom, &tmK, bar(kBlkFull), a * kBoxCols, g,
@@ -833,24 +858,51 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_4d(base + C::kOffV + a * C::kBlkAtom, &tmV, bar(kBlkFull), a * kBoxCols, g,
                     n_blk, b, keep);
       }
-      for (int i = 0; i < nbat && !failed; ++i) {
-        const int s = i & 1;
-        if (i >= 2 && !wait_phase(bar(kQdEmpty + s), ((i - 2) >> 1) & 1, kWaitLimitNs)) {
-          failed = true;
-          break;
-        }
-        const uint32_t st = base + C::kOffStage + s * C::kStageBytes;
-        mbar_arrive_expect_tx(bar(kQdFull + s), kTcBatch * 4 * hw0 * 128);
-        for (int j = 0; j < kTcBatch; ++j) {
-          // items past the chunk repeat its last item (their rows are masked)
-          const int item = min(i * kTcBatch + j, nitems - 1);
-          int m, sub;
-          item_query(item, m, sub);
-          const int qrow = static_cast<int>((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup);
+    }
+    // the rows of batch i into L2 (lane j: item j), ahead of their copies
+    auto prefetch = [&](int i) {
+      if (i < nbat && lane < kTcBatch) {
+        int m, sub;
+        item_query(min(i * kTcBatch + lane, nitems - 1), m, sub);
+        const int qrow = static_cast<int>((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup);
+        if (hw0 == kHeadsPerGroup) {
+          tma_prefetch_l2_3d(&tmQ, 0, qrow, 0);
+          tma_prefetch_l2_3d(&tmD, 0, qrow, 0);
+        } else {
           for (int a = 0; a < 2; ++a) {
-            tma_load_2d(st + a * C::kAtom + j * 1024, &tmQ, bar(kQdFull + s), a * kBoxCols, qrow);
-            tma_load_2d(st + (2 + a) * C::kAtom + j * 1024, &tmD, bar(kQdFull + s), a * kBoxCols,
-                        qrow);
+            tma_prefetch_l2_2d(&tmQ, a * kBoxCols, qrow);
+            tma_prefetch_l2_2d(&tmD, a * kBoxCols, qrow);
+          }
+        }
+      }
+    };
+    prefetch(0);
+    prefetch(1);
+    for (int i = 0; i < nbat && !failed; ++i) {
+      const int s = i & 1;
+      prefetch(i + 2);
+      if (i >= 2 &&
+          !__all_sync(kFull, wait_phase(bar(kQdEmpty + s), ((i - 2) >> 1) & 1, kWaitLimitNs))) {
+        failed = true;
+        break;
+      }
+      const uint32_t st = base + C::kOffStage + s * C::kStageBytes;
+      if (lane == 0) mbar_arrive_expect_tx(bar(kQdFull + s), kTcBatch * 4 * hw0 * 128);
+      __syncwarp();
+      if (lane < kTcBatch) {
+        // items past the chunk repeat its last item (their rows are masked)
+        const int item = min(i * kTcBatch + lane, nitems - 1);
+        int m, sub;
+        item_query(item, m, sub);
+        const int qrow = static_cast<int>((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup);
+        const uint32_t dq = st + lane * C::kItemBytes, dd = dq + 2 * C::kAtom;
+        if (hw0 == kHeadsPerGroup) {  // both column halves in one 3-D copy
+          tma_load_3d(dq, &tmQ, bar(kQdFull + s), 0, qrow, 0);
+          tma_load_3d(dd, &tmD, bar(kQdFull + s), 0, qrow, 0);
+        } else {  // fewer head rows: one 2-D copy per column half
+          for (int a = 0; a < 2; ++a) {
+            tma_load_2d(dq + a * 1024, &tmQ, bar(kQdFull + s), a * kBoxCols, qrow);
+            tma_load_2d(dd + a * 1024, &tmD, bar(kQdFull + s), a * kBoxCols, qrow);
           }
         }
       }
@@ -862,45 +914,65 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idesc_acc =
           umma_idesc_f16(128, 64, false, true) | (1u << 15);  // MN-major A and B
       bool ok = wait_phase(bar(kBlkFull), 0, kWaitLimitNs);
-      auto issue_sd = [&](int i) -> bool {
+      // S / dP of batch i: its Q / dO rows have landed (caller checked)
+      auto issue_sd = [&](int i) {
         const int s = i & 1;
-        if (!wait_phase(bar(kQdFull + s), (i >> 1) & 1, kWaitLimitNs)) return false;
         tc_fence_after();
         const uint32_t st = base + C::kOffStage + s * C::kStageBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t offa = (k >> 2) * C::kAtom + (k & 3) * 32;
+          const uint32_t offa = (k >> 2) * 1024 + (k & 3) * 32;  // column half, then 16 dims
           const uint32_t offb = (k >> 2) * C::kBlkAtom + (k & 3) * 32;
-          tc_mma(tmem + C::kColS + 64 * s, umma_desc_sw128(st + offa, 16),
+          tc_mma(tmem + C::kColS + 64 * s, umma_desc_sw128(st + offa, 16, C::kItemBytes),
                  umma_desc_sw128(base + C::kOffK + offb, 16), idesc_sd, k > 0 ? 1u : 0u);
-          tc_mma(tmem + C::kColDp + 64 * s, umma_desc_sw128(st + 2 * C::kAtom + offa, 16),
+          tc_mma(tmem + C::kColDp + 64 * s,
+                 umma_desc_sw128(st + 2 * C::kAtom + offa, 16, C::kItemBytes),
                  umma_desc_sw128(base + C::kOffV + offb, 16), idesc_sd, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(kSdFull + s));
-        return true;
       };
-      auto issue_acc = [&](int i) -> bool {
+      // dV / dK of batch i: its P / dS are written (caller checked)
+      auto issue_acc = [&](int i) {
         const int s = i & 1;
-        if (!wait_phase(bar(kPdsFull + s), (i >> 1) & 1, kWaitLimitNs)) return false;
         tc_fence_after();
         const uint32_t st = base + C::kOffStage + s * C::kStageBytes;
         const uint32_t pds = base + C::kOffPds + s * C::kPdsBytes;
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k) {  // 16 rows per step
           const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
-          tc_mma(tmem + C::kColDv, umma_desc_sw128(st + 2 * C::kAtom + k * 2048, C::kAtom),
+          // A: 16 rows = 2 items per step; column halves 1024 bytes apart
+          tc_mma(tmem + C::kColDv,
+                 umma_desc_sw128(st + 2 * C::kAtom + k * 2 * C::kItemBytes, 1024, C::kItemBytes),
                  umma_desc_sw128(pds + k * 2048, 16), idesc_acc, acc);
-          tc_mma(tmem + C::kColDk, umma_desc_sw128(st + k * 2048, C::kAtom),
+          tc_mma(tmem + C::kColDk, umma_desc_sw128(st + k * 2 * C::kItemBytes, 1024, C::kItemBytes),
                  umma_desc_sw128(pds + 128 * 128 + k * 2048, 16), idesc_acc, acc);
         }
         tc_commit(bar(kQdEmpty + s));
         tc_commit(bar(kPdsFree + s));
-        return true;
       };
-      if (ok && nbat > 0) ok = issue_sd(0);
-      for (int i = 1; i <= nbat && ok; ++i) {
-        if (i < nbat) ok = issue_sd(i);
-        if (ok) ok = issue_acc(i - 1);
+      // Issue whichever is ready first: S / dP of the next batch once its rows
+      // have landed (and the S / dP buffer is free: dV / dK of two batches
+      // before issued), dV / dK of the oldest batch once its P / dS are
+      // written -- so the dV / dK of batch i never waits for the rows of
+      // batch i + 1. One bounded wait: 1 s without progress fails.
+      int nsd = 0, nacc = 0;
+      uint64_t t_last = globaltimer_ns();
+      while (ok && nacc < nbat) {
+        bool progressed = false;
+        if (nsd < nbat && nsd <= nacc + 1 &&
+            mbar_try_wait(bar(kQdFull + (nsd & 1)), (nsd >> 1) & 1)) {
+          issue_sd(nsd++);
+          progressed = true;
+        }
+        if (nacc < nsd && mbar_try_wait(bar(kPdsFull + (nacc & 1)), (nacc >> 1) & 1)) {
+          issue_acc(nacc++);
+          progressed = true;
+        }
+        if (progressed) {
+          t_last = globaltimer_ns();
+        } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
+          ok = false;
+        }
       }
       if (ok) tc_commit(bar(kAccDone));
       failed = !ok;
@@ -914,15 +986,30 @@ __global__ void __launch_bounds__(192, 1)
     auto wait_all = [&](int bb, uint32_t parity) {
       return __all_sync(kFull, wait_phase(bar(bb), parity, kWaitLimitNs));
     };
+    // this row's query position and record of batch i; the next batch's are
+    // requested before this batch is processed
+    auto row_of = [&](int i, int& m, float& lse2, float& delta) {
+      const int item = i * kTcBatch + r / 8;
+      m = -1;
+      lse2 = INFINITY;
+      delta = 0.f;
+      if (i < nbat && item < nitems) {
+        int sub;
+        item_query(item, m, sub);
+        const float* rec = p.rec + (((b * p.M + m) * p.G + g) * nsub + sub) * 16;
+        lse2 = __ldg(rec + (r & 7));
+        delta = __ldg(rec + 8 + (r & 7));
+      }
+    };
+    int m_next;
+    float lse_next, delta_next;
+    row_of(0, m_next, lse_next, delta_next);
     for (int i = 0; i < nbat; ++i) {
       const int s = i & 1;
-      const int item = i * kTcBatch + r / 8;
-      const bool valid = item < nitems;
-      int m = 0, sub = 0;
-      if (valid) item_query(item, m, sub);
-      const float* rec = p.rec + (((b * p.M + m) * p.G + g) * nsub + sub) * 16;
-      const float lse2 = valid ? __ldg(rec + (r & 7)) : INFINITY;
-      const float delta = valid ? __ldg(rec + 8 + (r & 7)) : 0.f;
+      const int m = m_next;
+      const float lse2 = lse_next, delta = delta_next;
+      const bool valid = m >= 0;
+      row_of(i + 1, m_next, lse_next, delta_next);
       const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
       // keys n_blk + j visible: j < block size and n_blk + j <= lastkey
       const int nvis = valid ? min(p.bs, lastkey - n_blk + 1) : 0;
@@ -1116,15 +1203,21 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   using No = std::false_type;
   const bool split = p.nsub > 1;
   if constexpr (D == 128) {
-    // the tensor-core (tcgen05) kernel; block K / V read as 64-key boxes
-    CUtensorMap tk64, tv64;
-    if (!encode_kv_map(&tk64, K, B, p.N, p.G, D, 64) || !encode_kv_map(&tv64, V, B, p.N, p.G, D, 64))
+    // the tensor-core (tcgen05) kernel; block K / V read as 64-key boxes, the
+    // Q / dO rows of an item as one 3-D box (both column halves)
+    CUtensorMap tk64, tv64, tq3 = tq, tdo3 = tdo;
+    if (!encode_kv_map(&tk64, K, B, p.N, p.G, D, 64) ||
+        !encode_kv_map(&tv64, V, B, p.N, p.G, D, 64))
+      return NSA_ERR_LAUNCH;
+    if (hw0 == kHeadsPerGroup && (!encode_rows_halves_map(&tq3, p.Q, B * p.M * p.H, hw0) ||
+                                  !encode_rows_halves_map(&tdo3, p.dO16, B * p.M * p.H, hw0)))
       return NSA_ERR_LAUNCH;
     auto kk = split ? sel_attn_bwd_dkv_tc_kernel<true> : sel_attn_bwd_dkv_tc_kernel<false>;
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkvTcCfg::kSmemBytes) != cudaSuccess)
       return NSA_ERR_LAUNCH;
-    kk<<<static_cast<unsigned>(chunks), 192, DkvTcCfg::kSmemBytes, st>>>(p, tk64, tv64, tq, tdo);
+    kk<<<static_cast<unsigned>(chunks), 192, DkvTcCfg::kSmemBytes, st>>>(p, tk64, tv64, tq3,
+                                                                          tdo3);
     return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
   }
   int rc;
