@@ -88,7 +88,7 @@ struct DqCfg {
 };
 
 template <int D, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32, 3)
+__global__ void __launch_bounds__(WARPS * 32, 4)
     sel_attn_bwd_dq_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV) {
   using C = DqCfg<D, WARPS>;
