@@ -659,8 +659,9 @@ def run_backward(w, q, k, v, idx, out, lse, work, flush, args):
     res = {"ms_per_step": t, "tflops": flops / (t * 1e-3) / 1e12, "flops_per_step": flops,
            "gathered_gbs_dq_stage": work["gathered_bytes"] / (t * 1e-3) / 1e9,
            "workspace_bytes": need, "steps": steps,
-           "kernels": "dQ (query-major), index transpose (count, scan, fill), dK/dV "
-                      "(key-major, float2 atomics)"}
+           "kernels": "dQ (query-major, mma.sync), index transpose (count, scan, fill), "
+                      "dK/dV (key-major; tcgen05 with tensor-memory accumulators for D = 128, "
+                      "mma.sync for D = 64; fp32 atomics)"}
     del ws, do, dq, dk, dv
     torch.cuda.empty_cache()
     return res

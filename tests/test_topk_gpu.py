@@ -1,9 +1,11 @@
 """nsa_topk_blocks against the top-k oracle: bit for bit (integer output).
 
 Covers every register layout of the kernel (up to 256, 1024, 2048 and 4096
-blocks per row), rows with at most T candidates, queries past the last key,
-no keys, ties, NaN, infinities, signed zeros and subnormal scores, forced
-block counts from 0 to T, and the 64k-query workload on sampled rows with
+blocks per row), rows whose length is and is not a multiple of 4 (16-byte
+and scalar loads), both selection paths (few survivors; many ties or more
+than 32 free picks), rows with at most T candidates, queries past the last
+key, no keys, ties, NaN, infinities, signed zeros and subnormal scores,
+forced block counts from 0 to T, and the 64k-query workload on sampled rows with
 the structure of every row checked on the device. Its output then drives
 the selection-attention forward.
 """
@@ -21,6 +23,16 @@ def _scores(rng, shape, kind):
         return rng.random(shape, dtype=np.float32)
     if kind == "ties":
         return rng.integers(0, 3, shape).astype(np.float32)
+    if kind == "quantized":
+        # a few equal scores at the threshold: ties decided by block among
+        # the fast path's survivors
+        return np.floor(rng.random(shape, dtype=np.float32) * 256) / np.float32(256)
+    if kind == "zeros_on_top":
+        # negative scores with a few +0.0 and -0.0 on top (equal scores)
+        x = -rng.random(shape, dtype=np.float32) - np.float32(0.5)
+        pick = rng.random(shape) < 0.01
+        x[pick] = np.where(rng.random(int(pick.sum())) < 0.5, np.float32(0.0), np.float32(-0.0))
+        return x
     if kind == "special":
         pool = np.float32([0.0, -0.0, 0.5, -0.5, np.inf, -np.inf, np.nan, 1e-45, -1e-45,
                            3e-39, -3e-39, 1.0])
@@ -38,7 +50,7 @@ def _run(sc, N, bs, T, n_init, n_local):
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("kind", ["uniform", "ties", "special"])
+@pytest.mark.parametrize("kind", ["uniform", "ties", "quantized", "zeros_on_top", "special"])
 @pytest.mark.parametrize("B,M,N,G,bs,T,n_init,n_local", [
     (2, 700, 700, 3, 32, 6, 1, 2),       # <= 256 blocks
     (1, 1000, 1000, 2, 4, 16, 0, 0),     # <= 256 blocks, no forced
