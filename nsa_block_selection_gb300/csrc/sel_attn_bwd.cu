@@ -9,22 +9,29 @@
 //   dK[n] += scale dS_n q;      dV[n] += p_n dO.
 //
 // Three stages, all on the caller's stream:
-//  1. query-major kernel (one warp per (b, m, g), same TMA tile gather as the
-//     forward): recomputes S^T = K Q^T, P, dP^T = V dO^T and dS on the tensor
-//     cores (mma.sync m16n8k16, fp16 operands, fp32 accumulate) and
-//     accumulates dQ^T += K^T dS^T in registers; it also writes delta.
+//  1. D = 64: query-major kernel (one warp per (b, m, g), same TMA tile
+//     gather as the forward): recomputes S^T = K Q^T, P, dP^T = V dO^T and dS
+//     on the tensor cores (mma.sync m16n8k16, fp16 operands, fp32
+//     accumulate) and accumulates dQ^T += K^T dS^T in registers; it also
+//     writes delta. D = 128: a small kernel writes only the per-row inputs of
+//     stage 3 (fp16 dO, LSE, delta) and dQ is zeroed.
 //  2. transposed index: for every (b, g, block) the list of queries whose row
 //     selects it (count with atomics, one-CTA scan, fill with atomics). The
 //     order inside a list follows atomic order.
 //  3. key-major kernel: one CTA per chunk of <= kQueriesPerChunk queries of a
-//     list. Its bs/16 warps each own 16 keys of the block (loaded once by TMA)
-//     and, for each query of the chunk, recompute S^T, P, dP^T, dS and
-//     accumulate dV += P^T dO and dK += dS^T Q with mma.sync m16n8k8 (the C
-//     layout of S^T is already the A layout of that MMA); the partial sums
-//     are added into dK / dV (fp32, zeroed first) with float2 atomics.
-// Masked keys get exact zero weights by select (never multiplied through),
-// and K/V rows past a query's last visible key are zeroed in shared memory
-// before they enter a product in stage 1.
+//     list; the block's K / V are loaded once and each query's S, P, dP, dS
+//     recomputed against them. D = 64: bs/16 warps each own 16 keys and use
+//     mma.sync m16n8k8 (the C layout of S^T is already the A layout of that
+//     MMA) for dV += P^T dO and dK += dS^T Q. D = 128: tcgen05 MMAs with
+//     tensor-memory accumulators on 128-row batches of (query, head) rows,
+//     which also give dQ = dS K per batch; dQ is added into global memory
+//     with fp32 reductions. dK / dV partial sums are added with fp32 atomics
+//     at the end of a chunk. Summation orders follow the atomics.
+// Masked keys get exact zero weights by select (never multiplied through).
+// In stage 1 (D = 64), K / V rows past a query's last visible key are zeroed
+// in shared memory before they enter a product; with D = 128 the whole
+// block's K rows enter dQ = dS K with dS = 0 for masked keys, so those rows
+// must hold finite values.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -66,6 +73,13 @@ struct BwdProblem {
   float sl2;           // scale * log2(e)
   float scale;
 };
+
+// 16-byte fp32 reduction into global memory (no return value).
+__device__ __forceinline__ void red_add_v4(float* p, float4 v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
 
 // fp32 pair -> fp16x2 (round to nearest even)
 __device__ __forceinline__ uint32_t ld_f32x2_as_half2(const float* p) {
@@ -312,6 +326,51 @@ __global__ void __launch_bounds__(WARPS * 32, 4)
       o[D + 16 * d] = acc[d][1] * p.scale;
       o[D + 16 * d + 8] = acc[d][3] * p.scale;
     }
+  }
+}
+
+// Per-row inputs of the key-major kernel when it also produces dQ (D = 128):
+// one warp per (b, m, g, head sub-group): dO as fp16 rows, and the 64-byte
+// record (LSE * log2(e) of its 8 heads, then delta = dO . O of each head;
+// padding heads get LSE = +inf and delta = 0, so their probabilities are 0).
+template <int D>
+__global__ void __launch_bounds__(256) sel_attn_bwd_prep_kernel(const BwdProblem p) {
+  static_assert(D == 128, "one float4 per lane and head row");
+  constexpr int kPer = D / 32;  // dims per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (unit >= p.units) return;
+  const int sub = static_cast<int>(unit % p.nsub);
+  const int64_t bmg = unit / p.nsub;  // (b * M + m) * G + g
+  const int g = static_cast<int>(bmg % p.G);
+  const int64_t bm = bmg / p.G;
+  const int64_t m = bm % p.M, b = bm / p.M;
+  const int hw = p.hpg - sub * kHeadsPerGroup < kHeadsPerGroup ? p.hpg - sub * kHeadsPerGroup
+                                                                : kHeadsPerGroup;
+  const int64_t hbase = static_cast<int64_t>(g) * p.hpg + sub * kHeadsPerGroup;
+  float dl = 0.f;  // lane h < 8: delta of head h
+  for (int h = 0; h < hw; ++h) {
+    const int64_t at = (bm * p.H + hbase + h) * D + kPer * lane;
+    float part = 0.f;
+    uint32_t w[kPer / 2];
+#pragma unroll
+    for (int v = 0; v < kPer / 4; ++v) {
+      const float4 d4 = __ldg(reinterpret_cast<const float4*>(p.dO + at) + v);
+      const float4 o4 = __ldg(reinterpret_cast<const float4*>(p.O + at) + v);
+      part = fmaf(d4.x, o4.x, fmaf(d4.y, o4.y, fmaf(d4.z, o4.z, fmaf(d4.w, o4.w, part))));
+      w[2 * v] = pack_half2(d4.x, d4.y);
+      w[2 * v + 1] = pack_half2(d4.z, d4.w);
+    }
+    *reinterpret_cast<uint2*>(p.dO16 + at) = make_uint2(w[0], w[1]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+    if (lane == h) dl = part;
+  }
+  if (lane < kHeadsPerGroup) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    float* rec = p.rec + unit * 16;
+    rec[lane] = lane < hw ? p.LSE[(b * p.H + hbase + lane) * p.M + m] * kLog2e : INFINITY;
+    rec[8 + lane] = lane < hw ? dl : 0.f;
   }
 }
 
@@ -700,19 +759,25 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
 // One CTA per chunk of <= kQueriesPerChunk items of a list (as above). The
 // items (query, head sub-group) are taken 16 at a time: their 8 head rows
 // each are exactly one 1024-byte 128B-swizzled group, so 16 items gathered
-// by 2-D TMA form 128-row Q and dO operand tiles without any reshuffling.
+// by TMA form 128-row Q and dO operand tiles without any reshuffling.
 // Per batch of 128 rows, with the block's 64 keys (a block of 32 is read as
-// 64 keys, the second half masked):
+// 32 rows of a 64-row tile whose other rows are zero):
 //   S  = Q_R K^T,  dP = dO_R V^T       (M = 128 rows, N = 64 keys, K = D)
 //   P  = 2^(S scale log2e - LSE log2e), dS = P (dP - delta)  (softmax warps,
 //        one row per thread; masked and padding rows give exact zeros)
 //   dV^T += dO_R^T P,  dK^T += Q_R^T dS  (M = D = 128, N = 64, K = 128 rows;
 //        the Q / dO tiles serve again as MN-major A operands, P and dS are
 //        written to shared memory as MN-major B operands)
+//   dQ_R = dS K  (M = 128 rows, N = D, K = 64 keys; dS read as a K-major A
+//        operand, the K tile as an MN-major B operand)
 // with S / dP double-buffered in tensor memory and the Q / dO tiles in a
 // 2-stage ring, so the next batch's S and dP overlap this batch's softmax.
-// dV^T and dK^T accumulate in tensor memory over the chunk and are added
-// into dK / dV with fp32 atomics at the end (lane = d, coalesced per key).
+// The softmax warps read each batch's dQ_R out of tensor memory after the
+// next batch's softmax, stage it through their rows of the batch's (then
+// free) P / dS buffer and add it into dQ with 16-byte fp32 reductions, 16
+// lanes per 256 contiguous bytes. dV^T and dK^T accumulate in tensor memory
+// over the chunk and are added into dK / dV with fp32 atomics at the end
+// (lane = d, coalesced per key).
 // Warps: 0 producer (one lane), 1 tensor-memory owner and MMA issuer (one
 // lane), 2-5 softmax and epilogue. Every wait is bounded.
 
@@ -742,7 +807,9 @@ enum DkvBar : int {
   kPdsFull = 7,   // 2 P / dS buffers
   kPdsFree = 9,   // 2
   kAccDone = 11,
-  kDkvBars = 12
+  kDqFull = 12,   // dQ of a batch is in tensor memory
+  kDqFree = 13,   // the softmax warps have read it
+  kDkvBars = 14
 };
 
 // Q / dO tiles of a batch: item j's 8 head rows at j * 2048, dims 0-63 in
@@ -762,7 +829,7 @@ struct DkvTcCfg {
   static constexpr int kOffTmem = kOffBar + kDkvBars * 8;
   static constexpr int kOffList = kOffTmem + 16;  // the chunk's query ids
   static constexpr int kSmemBytes = kOffList + kQueriesPerChunk * 4 + 1024;
-  static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 320;
+  static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 320, kColDq = 384;
 };
 
 template <bool SPLIT>
@@ -824,6 +891,17 @@ __global__ void __launch_bounds__(192, 1)
     }
     fence_proxy_async_smem();
   }
+  if (p.bs < 64) {
+    // a block of 32 keys arrives as 32 rows of each K / V column half; the
+    // other 32 rows stay zero (dQ multiplies every row of the tile)
+    const int per = 4 * (64 - p.bs) * 8;  // (tensor, half) x rows x 16-byte pieces
+    for (int e = threadIdx.x; e < per; e += blockDim.x) {
+      const int piece = e % 8, rr = e / 8;
+      const int row = p.bs + rr % (64 - p.bs), atom = rr / (64 - p.bs);  // K0, K1, V0, V1
+      st_shared_zero16(base + C::kOffK + atom * C::kBlkAtom + row * 128 + piece * 16);
+    }
+    fence_proxy_async_smem();
+  }
   if (threadIdx.x == 0) {
     mbar_init(bar(kBlkFull), 1);
     for (int s = 0; s < 2; ++s) {
@@ -834,6 +912,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(bar(kPdsFree + s), 1);
     }
     mbar_init(bar(kAccDone), 1);
+    mbar_init(bar(kDqFull), 1);
+    mbar_init(bar(kDqFree), 4 * 32);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -851,7 +931,7 @@ __global__ void __launch_bounds__(192, 1)
     // lane j < 16 issues the copies of item j of a batch ----
     const uint64_t keep = l2_policy_evict_last();
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(kBlkFull), 4 * C::kBlkAtom);
+      mbar_arrive_expect_tx(bar(kBlkFull), 4 * p.bs * 128);
       for (int a = 0; a < 2; ++a) {
         tma_load_4d(base + C::kOffK + a * C::kBlkAtom, &tmK, bar(kBlkFull), a * kBoxCols, g,
                     n_blk, b, keep);
@@ -931,7 +1011,10 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_commit(bar(kSdFull + s));
       };
-      // dV / dK of batch i: its P / dS are written (caller checked)
+      // dV / dK / dQ of batch i: its P / dS are written and dQ of batch i - 1
+      // has been read out of tensor memory (caller checked)
+      constexpr uint32_t idesc_dq =
+          umma_idesc_f16(128, 128, false, true);  // dS K-major A, K MN-major B
       auto issue_acc = [&](int i) {
         const int s = i & 1;
         tc_fence_after();
@@ -947,14 +1030,24 @@ __global__ void __launch_bounds__(192, 1)
           tc_mma(tmem + C::kColDk, umma_desc_sw128(st + k * 2 * C::kItemBytes, 1024, C::kItemBytes),
                  umma_desc_sw128(pds + 128 * 128 + k * 2048, 16), idesc_acc, acc);
         }
+        // dQ_R (128 rows x D) = dS (rows x 64 keys) K (keys x D): A = dS rows,
+        // 16 keys (32 bytes) per step; B = the K tile read N-major, the two
+        // 64-column halves 8 KB apart, 16 keys (2 row groups) per step
+#pragma unroll
+        for (int k = 0; k < 64 / 16; ++k)
+          tc_mma(tmem + C::kColDq, umma_desc_sw128(pds + 128 * 128 + k * 32, 16),
+                 umma_desc_sw128(base + C::kOffK + k * 2048, C::kBlkAtom), idesc_dq,
+                 k > 0 ? 1u : 0u);
         tc_commit(bar(kQdEmpty + s));
         tc_commit(bar(kPdsFree + s));
+        tc_commit(bar(kDqFull));
       };
       // Issue whichever is ready first: S / dP of the next batch once its rows
       // have landed (and the S / dP buffer is free: dV / dK of two batches
-      // before issued), dV / dK of the oldest batch once its P / dS are
-      // written -- so the dV / dK of batch i never waits for the rows of
-      // batch i + 1. One bounded wait: 1 s without progress fails.
+      // before issued), dV / dK / dQ of the oldest batch once its P / dS are
+      // written and the previous dQ has been read -- so the dV / dK of batch
+      // i never waits for the rows of batch i + 1. One bounded wait: 1 s
+      // without progress fails.
       int nsd = 0, nacc = 0;
       uint64_t t_last = globaltimer_ns();
       while (ok && nacc < nbat) {
@@ -964,7 +1057,8 @@ __global__ void __launch_bounds__(192, 1)
           issue_sd(nsd++);
           progressed = true;
         }
-        if (nacc < nsd && mbar_try_wait(bar(kPdsFull + (nacc & 1)), (nacc >> 1) & 1)) {
+        if (nacc < nsd && mbar_try_wait(bar(kPdsFull + (nacc & 1)), (nacc >> 1) & 1) &&
+            (nacc == 0 || mbar_try_wait(bar(kDqFree), (nacc - 1) & 1))) {
           issue_acc(nacc++);
           progressed = true;
         }
@@ -1000,6 +1094,60 @@ __global__ void __launch_bounds__(192, 1)
         lse2 = __ldg(rec + (r & 7));
         delta = __ldg(rec + 8 + (r & 7));
       }
+    };
+    // dQ of batch j out of tensor memory (this thread: row r), scaled, and
+    // into global memory with 16-byte fp32 reductions. Staged through this
+    // warp's 32 rows of batch j's P / dS buffer (free: batch j's MMAs are
+    // done) so that 16 lanes cover 256 contiguous bytes of one dQ row.
+    auto dq_out = [&](int j) -> bool {
+      if (!wait_all(kDqFull, j & 1)) return false;
+      tc_fence_after();
+      float* rowp = nullptr;  // this row's dQ, or none (padding head, past the chunk)
+      {
+        const int item = j * kTcBatch + r / 8;
+        if (item < nitems && (r & 7) < hw0) {
+          int m, sub;
+          item_query(item, m, sub);
+          rowp = p.dQ + ((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup + (r & 7)) * D;
+        }
+      }
+      // staging row rho (0..31) of this warp: 256 bytes, 16-byte piece c at
+      // c ^ (rho & 15); rows 0-15 in the P rows, 16-31 in the dS rows
+      uint8_t* const stg = gbase + C::kOffPds + (j & 1) * C::kPdsBytes + quarter * 32 * 128;
+      auto srow = [&](int rho) { return stg + (rho >> 4) * (128 * 128) + (rho & 15) * 256; };
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[64];
+        tc_ld32(lane_addr + C::kColDq + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tc_ld32(lane_addr + C::kColDq + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tc_wait_ld();
+        if (h == 1) {
+          tc_fence_before();
+          mbar_arrive(bar(kDqFree));
+        }
+        uint8_t* const mine = srow(lane);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float4 f = make_float4(__uint_as_float(v[4 * c]) * p.scale,
+                                       __uint_as_float(v[4 * c + 1]) * p.scale,
+                                       __uint_as_float(v[4 * c + 2]) * p.scale,
+                                       __uint_as_float(v[4 * c + 3]) * p.scale);
+          *reinterpret_cast<float4*>(mine + ((c ^ (lane & 15)) << 4)) = f;
+        }
+        __syncwarp();
+        const int pc = lane & 15;
+#pragma unroll 4
+        for (int t2 = 0; t2 < 16; ++t2) {
+          const int rho = 2 * t2 + (lane >> 4);
+          float* const dst = reinterpret_cast<float*>(
+              __shfl_sync(kFull, reinterpret_cast<unsigned long long>(rowp), rho));
+          if (dst) {
+            const float4 f = *reinterpret_cast<const float4*>(srow(rho) + ((pc ^ (rho & 15)) << 4));
+            red_add_v4(dst + 64 * h + 4 * pc, f);
+          }
+        }
+        __syncwarp();
+      }
+      return true;
     };
     int m_next;
     float lse_next, delta_next;
@@ -1050,7 +1198,12 @@ __global__ void __launch_bounds__(192, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kPdsFull + s));
+      if (i > 0 && !dq_out(i - 1)) {
+        failed = true;
+        break;
+      }
     }
+    if (!failed && nbat > 0 && !dq_out(nbat - 1)) failed = true;
     // epilogue: lane = d; add the chunk's dV and dK (scaled) into global memory
     if (!failed && nbat > 0) {
       if (!wait_all(kAccDone, 0)) {
@@ -1162,14 +1315,24 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     memset(&tvb, 0, sizeof(tvb));
   }
 
-  // stage 1: dQ and delta
-  auto kq = sel_attn_bwd_dq_kernel<D, W>;
-  if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, Cq::kSmemBytes) !=
-      cudaSuccess)
-    return NSA_ERR_LAUNCH;
-  kq<<<static_cast<unsigned>((p.units + W - 1) / W), W * 32, Cq::kSmemBytes, st>>>(p, tk, tv);
-  if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
-  if (!have_keys || p.T == 0) return NSA_OK;  // dK = dV = 0
+  if constexpr (D == 128) {
+    // stage 1: the key-major kernel accumulates dQ too; here only its
+    // per-row inputs (fp16 dO, LSE, delta) and a zeroed dQ
+    if (cudaMemsetAsync(p.dQ, 0, static_cast<size_t>(B * p.M * p.H * D) * 4, st) != cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    if (!have_keys || p.T == 0) return NSA_OK;  // dQ = dK = dV = 0
+    sel_attn_bwd_prep_kernel<D><<<static_cast<unsigned>((p.units + 7) / 8), 256, 0, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
+  } else {
+    // stage 1: dQ and delta
+    auto kq = sel_attn_bwd_dq_kernel<D, W>;
+    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, Cq::kSmemBytes) !=
+        cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    kq<<<static_cast<unsigned>((p.units + W - 1) / W), W * 32, Cq::kSmemBytes, st>>>(p, tk, tv);
+    if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
+    if (!have_keys || p.T == 0) return NSA_OK;  // dK = dV = 0
+  }
 
   // stage 2: transposed index
   const int64_t grid_e = (pl.entries + 255) / 256 < 152 * 64 ? (pl.entries + 255) / 256 : 152 * 64;
@@ -1203,11 +1366,12 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   using No = std::false_type;
   const bool split = p.nsub > 1;
   if constexpr (D == 128) {
-    // the tensor-core (tcgen05) kernel; block K / V read as 64-key boxes, the
-    // Q / dO rows of an item as one 3-D box (both column halves)
+    // the tensor-core (tcgen05) kernel, which also produces dQ; block K / V
+    // read as one box per column half, the Q / dO rows of an item as one 3-D
+    // box (both column halves)
     CUtensorMap tk64, tv64, tq3 = tq, tdo3 = tdo;
-    if (!encode_kv_map(&tk64, K, B, p.N, p.G, D, 64) ||
-        !encode_kv_map(&tv64, V, B, p.N, p.G, D, 64))
+    if (!encode_kv_map(&tk64, K, B, p.N, p.G, D, p.bs) ||
+        !encode_kv_map(&tv64, V, B, p.N, p.G, D, p.bs))
       return NSA_ERR_LAUNCH;
     if (hw0 == kHeadsPerGroup && (!encode_rows_halves_map(&tq3, p.Q, B * p.M * p.H, hw0) ||
                                   !encode_rows_halves_map(&tdo3, p.dO16, B * p.M * p.H, hw0)))
