@@ -74,11 +74,24 @@ struct BwdProblem {
   float scale;
 };
 
-// 16-byte fp32 reduction into global memory (no return value).
-__device__ __forceinline__ void red_add_v4(float* p, float4 v) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y),
-               "f"(v.z), "f"(v.w)
-               : "memory");
+// 8-byte fp32 reduction into global memory (no return value).
+__device__ __forceinline__ void red_add_v2(float* p, float x, float y) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(x), "f"(y) : "memory");
+}
+
+// Tensor memory -> registers, shape .16x256b, 8 repetitions (64 columns of a
+// 16-lane slice): thread t gets, for repetition q, columns 8q + 2(t % 4) and
+// + 1 of lanes t / 4 (registers 4q, 4q + 1) and t / 4 + 8 (4q + 2, 4q + 3).
+__device__ __forceinline__ void tc_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
 }
 
 // fp32 pair -> fp16x2 (round to nearest even)
@@ -832,8 +845,10 @@ struct DkvTcCfg {
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 320, kColDq = 384;
 };
 
+constexpr int kDkvTcThreads = 320;
+
 template <bool SPLIT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kDkvTcThreads, 1)
     sel_attn_bwd_dkv_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
                                const __grid_constant__ CUtensorMap tmV,
                                const __grid_constant__ CUtensorMap tmQ,
@@ -1071,6 +1086,56 @@ __global__ void __launch_bounds__(192, 1)
       if (ok) tc_commit(bar(kAccDone));
       failed = !ok;
     }
+  } else if (warp >= 6) {
+    // ---- dQ out (warps 6..9): each batch's dQ_R from tensor memory, scaled,
+    // added into dQ with 8-byte fp32 reductions. A .16x256b load gives
+    // thread (g8 = lane / 4, c4 = lane % 4) columns 2 c4, 2 c4 + 1 (+ 8 per
+    // repetition) of rows g8 and g8 + 8 of a 16-row slice, so the 4 threads
+    // of a row cover 32 contiguous bytes. This thread: head g8 of items
+    // 16 j + 4 quarter + a, a = 0..3 (rows 32 quarter + g8 + 8 a). ----
+    const int quarter = warp & 3;
+    const int g8 = lane >> 2, c4 = lane & 3;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    for (int j = 0; j < nbat; ++j) {
+      float* rowp[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int item = j * kTcBatch + quarter * 4 + a;
+        rowp[a] = nullptr;
+        if (item < nitems && g8 < hw0) {
+          int m, sub;
+          item_query(item, m, sub);
+          rowp[a] = p.dQ + ((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup + g8) * D + 2 * c4;
+        }
+      }
+      if (!__all_sync(kFull, wait_phase(bar(kDqFull), j & 1, kWaitLimitNs))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int piece = 0; piece < 4; ++piece) {  // (16-row slice, 64-column half)
+        const int slice = piece >> 1, half = piece & 1;
+        uint32_t v[32];
+        tc_ld_16x256b_x8(lane_addr + (static_cast<uint32_t>(16 * slice) << 16) + C::kColDq + 64 * half,
+                         v);
+        tc_wait_ld();
+        if (piece == 3) {
+          tc_fence_before();
+          mbar_arrive(bar(kDqFree));
+        }
+#pragma unroll
+        for (int up = 0; up < 2; ++up) {  // rows g8 and g8 + 8 of the slice: items a = 2 slice + up
+          float* const dst = rowp[2 * slice + up];
+          if (dst) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              red_add_v2(dst + 64 * half + 8 * q, __uint_as_float(v[4 * q + 2 * up]) * p.scale,
+                         __uint_as_float(v[4 * q + 2 * up + 1]) * p.scale);
+          }
+        }
+      }
+    }
   } else {
     // ---- softmax (warps 2..5): thread <-> row (item r / 8, head r % 8) ----
     const int quarter = warp & 3;
@@ -1094,60 +1159,6 @@ __global__ void __launch_bounds__(192, 1)
         lse2 = __ldg(rec + (r & 7));
         delta = __ldg(rec + 8 + (r & 7));
       }
-    };
-    // dQ of batch j out of tensor memory (this thread: row r), scaled, and
-    // into global memory with 16-byte fp32 reductions. Staged through this
-    // warp's 32 rows of batch j's P / dS buffer (free: batch j's MMAs are
-    // done) so that 16 lanes cover 256 contiguous bytes of one dQ row.
-    auto dq_out = [&](int j) -> bool {
-      if (!wait_all(kDqFull, j & 1)) return false;
-      tc_fence_after();
-      float* rowp = nullptr;  // this row's dQ, or none (padding head, past the chunk)
-      {
-        const int item = j * kTcBatch + r / 8;
-        if (item < nitems && (r & 7) < hw0) {
-          int m, sub;
-          item_query(item, m, sub);
-          rowp = p.dQ + ((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup + (r & 7)) * D;
-        }
-      }
-      // staging row rho (0..31) of this warp: 256 bytes, 16-byte piece c at
-      // c ^ (rho & 15); rows 0-15 in the P rows, 16-31 in the dS rows
-      uint8_t* const stg = gbase + C::kOffPds + (j & 1) * C::kPdsBytes + quarter * 32 * 128;
-      auto srow = [&](int rho) { return stg + (rho >> 4) * (128 * 128) + (rho & 15) * 256; };
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[64];
-        tc_ld32(lane_addr + C::kColDq + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tc_ld32(lane_addr + C::kColDq + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tc_wait_ld();
-        if (h == 1) {
-          tc_fence_before();
-          mbar_arrive(bar(kDqFree));
-        }
-        uint8_t* const mine = srow(lane);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 f = make_float4(__uint_as_float(v[4 * c]) * p.scale,
-                                       __uint_as_float(v[4 * c + 1]) * p.scale,
-                                       __uint_as_float(v[4 * c + 2]) * p.scale,
-                                       __uint_as_float(v[4 * c + 3]) * p.scale);
-          *reinterpret_cast<float4*>(mine + ((c ^ (lane & 15)) << 4)) = f;
-        }
-        __syncwarp();
-        const int pc = lane & 15;
-#pragma unroll 4
-        for (int t2 = 0; t2 < 16; ++t2) {
-          const int rho = 2 * t2 + (lane >> 4);
-          float* const dst = reinterpret_cast<float*>(
-              __shfl_sync(kFull, reinterpret_cast<unsigned long long>(rowp), rho));
-          if (dst) {
-            const float4 f = *reinterpret_cast<const float4*>(srow(rho) + ((pc ^ (rho & 15)) << 4));
-            red_add_v4(dst + 64 * h + 4 * pc, f);
-          }
-        }
-        __syncwarp();
-      }
-      return true;
     };
     int m_next;
     float lse_next, delta_next;
@@ -1198,12 +1209,7 @@ __global__ void __launch_bounds__(192, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kPdsFull + s));
-      if (i > 0 && !dq_out(i - 1)) {
-        failed = true;
-        break;
-      }
     }
-    if (!failed && nbat > 0 && !dq_out(nbat - 1)) failed = true;
     // epilogue: lane = d; add the chunk's dV and dK (scaled) into global memory
     if (!failed && nbat > 0) {
       if (!wait_all(kAccDone, 0)) {
@@ -1380,8 +1386,8 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkvTcCfg::kSmemBytes) != cudaSuccess)
       return NSA_ERR_LAUNCH;
-    kk<<<static_cast<unsigned>(chunks), 192, DkvTcCfg::kSmemBytes, st>>>(p, tk64, tv64, tq3,
-                                                                          tdo3);
+    kk<<<static_cast<unsigned>(chunks), kDkvTcThreads, DkvTcCfg::kSmemBytes, st>>>(
+        p, tk64, tv64, tq3, tdo3);
     return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
   }
   int rc;
