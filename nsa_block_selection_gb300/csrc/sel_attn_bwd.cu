@@ -74,9 +74,11 @@ struct BwdProblem {
   float scale;
 };
 
-// 8-byte fp32 reduction into global memory (no return value).
-__device__ __forceinline__ void red_add_v2(float* p, float x, float y) {
-  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(x), "f"(y) : "memory");
+// 16-byte fp32 reduction into global memory (no return value).
+__device__ __forceinline__ void red_add_v4(float* p, float x, float y, float z, float w) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(x), "f"(y), "f"(z),
+               "f"(w)
+               : "memory");
 }
 
 // Tensor memory -> registers, shape .16x256b, 8 repetitions (64 columns of a
@@ -1088,14 +1090,18 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
     }
   } else if (warp >= 6) {
     // ---- dQ out (warps 6..9): each batch's dQ_R from tensor memory, scaled,
-    // added into dQ with 8-byte fp32 reductions. A .16x256b load gives
+    // added into dQ with 16-byte fp32 reductions. A .16x256b load gives
     // thread (g8 = lane / 4, c4 = lane % 4) columns 2 c4, 2 c4 + 1 (+ 8 per
-    // repetition) of rows g8 and g8 + 8 of a 16-row slice, so the 4 threads
-    // of a row cover 32 contiguous bytes. This thread: head g8 of items
-    // 16 j + 4 quarter + a, a = 0..3 (rows 32 quarter + g8 + 8 a). ----
+    // repetition) of rows g8 and g8 + 8 of a 16-row slice; shuffles among
+    // the 4 threads of a row turn that into columns 16k + 4 c4 .. + 3, so
+    // one reduction instruction covers 64 contiguous bytes of each of 8
+    // rows. This thread: head g8 of items 16 j + 4 quarter + a, a = 0..3
+    // (rows 32 quarter + g8 + 8 a). ----
     const int quarter = warp & 3;
     const int g8 = lane >> 2, c4 = lane & 3;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int src_lo = (lane & ~3) | (2 * (c4 & 1));  // holds columns 4 c4 % 8, + 1
+    const bool upper = c4 >= 2;                        // wants the odd repetition
     for (int j = 0; j < nbat; ++j) {
       float* rowp[4];
 #pragma unroll
@@ -1105,7 +1111,7 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
         if (item < nitems && g8 < hw0) {
           int m, sub;
           item_query(item, m, sub);
-          rowp[a] = p.dQ + ((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup + g8) * D + 2 * c4;
+          rowp[a] = p.dQ + ((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup + g8) * D + 4 * c4;
         }
       }
       if (!__all_sync(kFull, wait_phase(bar(kDqFull), j & 1, kWaitLimitNs))) {
@@ -1127,11 +1133,18 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
 #pragma unroll
         for (int up = 0; up < 2; ++up) {  // rows g8 and g8 + 8 of the slice: items a = 2 slice + up
           float* const dst = rowp[2 * slice + up];
-          if (dst) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              red_add_v2(dst + 64 * half + 8 * q, __uint_as_float(v[4 * q + 2 * up]) * p.scale,
-                         __uint_as_float(v[4 * q + 2 * up + 1]) * p.scale);
+          for (int k = 0; k < 4; ++k) {  // columns 16k .. 16k + 15 of the half
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int src = src_lo + (e >> 1);
+              const float x = __shfl_sync(kFull, __uint_as_float(v[8 * k + 2 * up + (e & 1)]), src);
+              const float y =
+                  __shfl_sync(kFull, __uint_as_float(v[8 * k + 4 + 2 * up + (e & 1)]), src);
+              o[e] = (upper ? y : x) * p.scale;
+            }
+            if (dst) red_add_v4(dst + 64 * half + 16 * k, o[0], o[1], o[2], o[3]);
           }
         }
       }
