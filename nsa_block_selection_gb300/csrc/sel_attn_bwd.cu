@@ -1037,6 +1037,16 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
         tc_fence_after();
         const uint32_t st = base + C::kOffStage + s * C::kStageBytes;
         const uint32_t pds = base + C::kOffPds + s * C::kPdsBytes;
+        // dQ_R (128 rows x D) = dS (rows x 64 keys) K (keys x D) first, so the
+        // dQ warps can start: A = dS rows, 16 keys (32 bytes) per step; B = the
+        // K tile read N-major, the two 64-column halves 8 KB apart, 16 keys
+        // (2 row groups) per step
+#pragma unroll
+        for (int k = 0; k < 64 / 16; ++k)
+          tc_mma(tmem + C::kColDq, umma_desc_sw128(pds + 128 * 128 + k * 32, 16),
+                 umma_desc_sw128(base + C::kOffK + k * 2048, C::kBlkAtom), idesc_dq,
+                 k > 0 ? 1u : 0u);
+        tc_commit(bar(kDqFull));
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k) {  // 16 rows per step
           const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
@@ -1047,17 +1057,8 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
           tc_mma(tmem + C::kColDk, umma_desc_sw128(st + k * 2 * C::kItemBytes, 1024, C::kItemBytes),
                  umma_desc_sw128(pds + 128 * 128 + k * 2048, 16), idesc_acc, acc);
         }
-        // dQ_R (128 rows x D) = dS (rows x 64 keys) K (keys x D): A = dS rows,
-        // 16 keys (32 bytes) per step; B = the K tile read N-major, the two
-        // 64-column halves 8 KB apart, 16 keys (2 row groups) per step
-#pragma unroll
-        for (int k = 0; k < 64 / 16; ++k)
-          tc_mma(tmem + C::kColDq, umma_desc_sw128(pds + 128 * 128 + k * 32, 16),
-                 umma_desc_sw128(base + C::kOffK + k * 2048, C::kBlkAtom), idesc_dq,
-                 k > 0 ? 1u : 0u);
         tc_commit(bar(kQdEmpty + s));
         tc_commit(bar(kPdsFree + s));
-        tc_commit(bar(kDqFull));
       };
       // Issue whichever is ready first: S / dP of the next batch once its rows
       // have landed (and the S / dP buffer is free: dV / dK of two batches
@@ -1119,17 +1120,20 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
         break;
       }
       tc_fence_after();
+      // all four pieces (16-row slice, 64-column half) first: the tensor
+      // memory is released before the reductions
+      uint32_t v[4][32];
 #pragma unroll
-      for (int piece = 0; piece < 4; ++piece) {  // (16-row slice, 64-column half)
+      for (int piece = 0; piece < 4; ++piece)
+        tc_ld_16x256b_x8(lane_addr + (static_cast<uint32_t>(16 * (piece >> 1)) << 16) +
+                             C::kColDq + 64 * (piece & 1),
+                         v[piece]);
+      tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(kDqFree));
+#pragma unroll
+      for (int piece = 0; piece < 4; ++piece) {
         const int slice = piece >> 1, half = piece & 1;
-        uint32_t v[32];
-        tc_ld_16x256b_x8(lane_addr + (static_cast<uint32_t>(16 * slice) << 16) + C::kColDq + 64 * half,
-                         v);
-        tc_wait_ld();
-        if (piece == 3) {
-          tc_fence_before();
-          mbar_arrive(bar(kDqFree));
-        }
 #pragma unroll
         for (int up = 0; up < 2; ++up) {  // rows g8 and g8 + 8 of the slice: items a = 2 slice + up
           float* const dst = rowp[2 * slice + up];
@@ -1139,9 +1143,10 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int src = src_lo + (e >> 1);
-              const float x = __shfl_sync(kFull, __uint_as_float(v[8 * k + 2 * up + (e & 1)]), src);
+              const float x =
+                  __shfl_sync(kFull, __uint_as_float(v[piece][8 * k + 2 * up + (e & 1)]), src);
               const float y =
-                  __shfl_sync(kFull, __uint_as_float(v[8 * k + 4 + 2 * up + (e & 1)]), src);
+                  __shfl_sync(kFull, __uint_as_float(v[piece][8 * k + 4 + 2 * up + (e & 1)]), src);
               o[e] = (upper ? y : x) * p.scale;
             }
             if (dst) red_add_v4(dst + 64 * half + 16 * k, o[0], o[1], o[2], o[3]);
