@@ -204,8 +204,9 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
 
 /*
  * nsa_sel_attn_bwd_workspace_bytes -- device workspace nsa_sel_attn_bwd
- * needs: delta [B,H,M] fp32, the per-(b, g, block) query lists (at most
- * B*M*G*T entries) and their counts and offsets. Negative nsa_status for
+ * needs: an fp16 copy of dO, one 64-byte (LSE, delta) record per (b, m, g,
+ * 8-head sub-group), the per-(b, g, block) query lists (at most B*M*G*T
+ * entries) and their counts and offsets. Negative nsa_status for
  * invalid sizes (B*M*G*T must stay below 2^31). Pure host arithmetic.
  */
 int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_t H,
@@ -226,12 +227,17 @@ int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_
  *
  * With p = exp(scale q.k - LSE), dP = dO.v and delta = dO.O per row and head:
  * dS = p (dP - delta), dQ = scale sum dS k, dK += scale dS q, dV += p dO over
- * every visible (query, head, key). Three stages on `stream`: a query-major
- * kernel for dQ (and delta); a transposed index listing, per (b, g, block),
- * the queries that selected it; a key-major kernel that loads each block
- * once per chunk of its list and adds its dK / dV partial sums with fp32
- * atomics. dQ is deterministic; dK / dV sum in an order set by atomics
- * (equal within rounding from run to run). Asynchronous, allocates nothing;
+ * every visible (query, head, key). Three stages on `stream`: per-row
+ * inputs (delta, an fp16 copy of dO; with D = 64 also dQ, from a
+ * query-major kernel); a transposed index listing, per (b, g, block), the
+ * queries that selected it; a key-major kernel that loads each block once
+ * per chunk of its list and adds its dK / dV partial sums with fp32
+ * atomics -- with D = 128 it also forms dQ = dS K on the tensor cores and
+ * adds it with fp32 reductions. dK / dV (and dQ when D = 128) sum in an
+ * order set by atomics (equal within rounding from run to run). With
+ * D = 128 every key of a selected block enters dQ (with weight 0 where the
+ * query does not see it), so K must be finite in the selected blocks,
+ * including keys after a query's position. Asynchronous, allocates nothing;
  * errors as nsa_sel_attn_fwd plus NSA_ERR_WORKSPACE. Pointers must be
  * 16-byte aligned (LSE and block_indices 4-byte).
  */
