@@ -653,15 +653,22 @@ def run_backward(w, q, k, v, idx, out, lse, work, flush, args):
                           dv=dv, workspace=ws)
 
     steps = max(3, args.steps // 6)
-    times, _ = time_steps(step, steps, 2, flush, lambda: None)
+    times, _ = time_steps(step, steps, 3, flush, lambda: None)
     t = statistics.mean(times)
     flops = work["flops"] // 4 * 10
     res = {"ms_per_step": t, "tflops": flops / (t * 1e-3) / 1e12, "flops_per_step": flops,
-           "gathered_gbs_dq_stage": work["gathered_bytes"] / (t * 1e-3) / 1e9,
-           "workspace_bytes": need, "steps": steps,
-           "kernels": "dQ (query-major, mma.sync), index transpose (count, scan, fill), "
-                      "dK/dV (key-major; tcgen05 with tensor-memory accumulators for D = 128, "
-                      "mma.sync for D = 64; fp32 atomics)"}
+           "workspace_bytes": need, "steps": steps}
+    if w.D == 128:
+        # dQ = dS K per (query, selected block): every head of the group,
+        # D fp32 values each, added with reductions
+        red = work["gathered_bytes"] * (w.H // w.G) // w.block_size
+        res.update({"dq_reduction_bytes": red, "dq_reduction_gbs": red / (t * 1e-3) / 1e9,
+                    "kernels": "prep (fp16 dO, LSE, delta), index transpose (count, scan, "
+                               "fill), key-major tcgen05 kernel: dK, dV (fp32 atomics per "
+                               "chunk) and dQ = dS K (fp32 reductions per batch)"})
+    else:
+        res["kernels"] = ("dQ (query-major, mma.sync), index transpose (count, scan, fill), "
+                          "dK/dV (key-major, mma.sync, fp32 atomics)")
     del ws, do, dq, dk, dv
     torch.cuda.empty_cache()
     return res
