@@ -65,6 +65,7 @@ struct BwdProblem {
   float* rec;          // [B * M * G * nsub][16]: LSE * log2(e) of 8 heads, then delta
   const int* offs;     // [L + 1] list starts (L = B * G * nblk)
   const int* choffs;   // [L + 1] chunk starts
+  const int* chunk_list;  // [chunks] the list of each chunk
   const int* lists;    // query ids, list by list
   int64_t B, M, N, H, G, T;
   int64_t units;       // B * G * nsub * M
@@ -478,6 +479,12 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(const int* count, int* o
   }
 }
 
+// chunk -> the list it belongs to (chunks of list l: choffs[l] .. choffs[l + 1])
+__global__ void csr_chunk_list_kernel(const int* choffs, int L, int* chunk_list) {
+  for (int l = blockIdx.x * blockDim.x + threadIdx.x; l < L; l += gridDim.x * blockDim.x)
+    for (int c = choffs[l]; c < choffs[l + 1]; ++c) chunk_list[c] = l;
+}
+
 __global__ void csr_fill_kernel(const BwdProblem p, int* cursor, int* lists) {
   const int64_t total = p.B * p.M * p.G * p.T;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
@@ -524,16 +531,7 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
   extern __shared__ uint8_t smem_raw[];
   const int c = blockIdx.x;
   if (c >= p.choffs[p.L]) return;
-  // list l with choffs[l] <= c < choffs[l + 1]
-  int lo = 0, hi = p.L;  // invariant: choffs[lo] <= c < choffs[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (p.choffs[mid] <= c)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  const int l = lo;
+  const int l = __ldg(p.chunk_list + c);  // the list of this chunk
   const int q0 = p.offs[l] + (c - p.choffs[l]) * kQueriesPerChunk;
   const int nq = min(q0 + kQueriesPerChunk, p.offs[l + 1]) - q0;
   const int nsub = SPLIT ? p.nsub : 1;
@@ -860,15 +858,7 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const int c = blockIdx.x;
   if (c >= p.choffs[p.L]) return;  // before any tensor memory is taken
-  int lo = 0, hi = p.L;            // list l with choffs[l] <= c < choffs[l + 1]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (p.choffs[mid] <= c)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  const int l = lo;
+  const int l = __ldg(p.chunk_list + c);
   const int q0 = p.offs[l] + (c - p.choffs[l]) * kQueriesPerChunk;
   const int nq = min(q0 + kQueriesPerChunk, p.offs[l + 1]) - q0;
   const int nsub = SPLIT ? p.nsub : 1;
@@ -1270,8 +1260,9 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
 // ---------------------------------------------------------------------------
 
 struct BwdPlan {
-  size_t off_do16, off_rec, off_count, off_cursor, off_offs, off_choffs, off_lists, total;
-  int64_t L, entries;
+  size_t off_do16, off_rec, off_count, off_cursor, off_offs, off_choffs, off_lists,
+      off_chunk_list, total;
+  int64_t L, entries, max_chunks;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1298,6 +1289,10 @@ static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, i
   at += align256(static_cast<size_t>(pl.L + 1) * 4);
   pl.off_lists = at;
   at += align256(static_cast<size_t>(pl.entries) * 4);
+  // chunks: sum over lists of ceil(count / chunk) <= entries / chunk + L
+  pl.max_chunks = (pl.entries + kQueriesPerChunk - 1) / kQueriesPerChunk + pl.L;
+  pl.off_chunk_list = at;
+  at += align256(static_cast<size_t>(pl.max_chunks) * 4);
   pl.total = at;
   return pl;
 }
@@ -1317,6 +1312,8 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   p.offs = offs;
   p.choffs = choffs;
   p.lists = lists;
+  int* chunk_list = reinterpret_cast<int*>(ws + pl.off_chunk_list);
+  p.chunk_list = chunk_list;
   const int64_t B = p.units / (p.M * p.G * p.nsub);
   if (p.N > 0 &&
       (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
@@ -1364,6 +1361,8 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   csr_scan_kernel<<<1, 1024, 0, st>>>(count, offs, choffs, static_cast<int>(pl.L),
                                       kQueriesPerChunk);
   csr_fill_kernel<<<static_cast<unsigned>(grid_e), 256, 0, st>>>(p, cursor, lists);
+  csr_chunk_list_kernel<<<static_cast<unsigned>((pl.L + 255) / 256), 256, 0, st>>>(
+      choffs, static_cast<int>(pl.L), chunk_list);
   if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
 
   // stage 3: dK, dV; grid bound: sum over lists of ceil(count / chunk)
@@ -1372,7 +1371,7 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   if (!encode_rows_map(&tq, p.Q, B * p.M * p.H, D, hw0) ||
       !encode_rows_map(&tdo, p.dO16, B * p.M * p.H, D, hw0))
     return NSA_ERR_LAUNCH;
-  const int64_t chunks = (pl.entries + kQueriesPerChunk - 1) / kQueriesPerChunk + pl.L;
+  const int64_t chunks = pl.max_chunks;
   auto run = [&](auto kt, auto split) -> int {
     constexpr int KT = decltype(kt)::value;
     using Ck = DkvCfg<D, KT>;
