@@ -112,18 +112,23 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since it was taken."""
+def profiled(workload):
+    """The committed ncu figures of the workload's forward kernel, or {} when
+    the kernel sources changed since they were taken."""
     path = os.path.join(ROOT, "profiles", f"{workload}_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
-        return None
+        return {}
     if d.get("kernel_source_sha") != kernel_source_hash():
-        return None
-    return d.get("dram_bytes_per_launch")
+        return {}
+    return d
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, or None."""
+    return profiled(workload).get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -416,6 +421,10 @@ def run_ours(args):
         "note": "achieved = gathered K/V bytes (whole selected blocks) / kernel time; "
                 "blocks are re-read from L2, so it can exceed HBM bandwidth",
     }
+    prof = profiled(w.name)
+    if "l2_to_sm_busy_pct" in prof:
+        roofline["l2_to_sm_busy_pct"] = prof["l2_to_sm_busy_pct"]
+        roofline["l2_to_sm_source"] = prof.get("summary", "")
     if rank != 0:
         return 0
     line = {
