@@ -90,7 +90,7 @@ __device__ __forceinline__ uint32_t ld_f32x2_as_half2(const float* p) {
 }
 
 // ---------------------------------------------------------------------------
-// Stage 1: dQ (query-major)
+// Stage 1 for D = 64: dQ (query-major)
 // ---------------------------------------------------------------------------
 
 template <int D, int WARPS>
@@ -482,7 +482,7 @@ __global__ void csr_fill_kernel(const BwdProblem p, int* cursor, int* lists) {
 }
 
 // ---------------------------------------------------------------------------
-// Stage 3: dK, dV (key-major)
+// Stage 3 for D = 64: dK, dV (key-major)
 // ---------------------------------------------------------------------------
 
 template <int D, int KT>
@@ -752,7 +752,8 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Stage 3 on the 5th-generation tensor cores (D = 128): dK, dV (key-major)
+// Stage 3 on the 5th-generation tensor cores (D = 128): dK, dV and dQ
+// (key-major)
 // ---------------------------------------------------------------------------
 //
 // One CTA per chunk of <= kQueriesPerChunk items of a list (as above). The
