@@ -331,6 +331,10 @@ __global__ void __launch_bounds__(WARPS * 32, 4)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Stage 1 for D = 128: per-row inputs
+// ---------------------------------------------------------------------------
+
 // Per-row inputs of the key-major kernel when it also produces dQ (D = 128):
 // one warp per (b, m, g, head sub-group): dO as fp16 rows, and the 64-byte
 // record (LSE * log2(e) of its 8 heads, then delta = dO . O of each head;
