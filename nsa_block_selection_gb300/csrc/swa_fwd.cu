@@ -9,7 +9,11 @@
 // head dim 64 or 128. Q [B,M,H,D], K and V [B,N,H_kv,D], O [B,M,H,D],
 // optional LSE [B,H,M] (natural log, fp32).
 //
-// One CTA per (b, head, tile of 128 queries); 6 warps with fixed roles:
+// Two kernels. With an even number of query heads per KV head and windows
+// of at least kSwaPairMinKeys keys, swa_fwd_pair_kernel (below) takes two
+// heads per work item, one softmax warpgroup each, so that one head's
+// exponentials overlap the other head's MMAs. Otherwise swa_fwd_kernel:
+// one CTA per (b, head, tile of 128 queries); 6 warps with fixed roles:
 //  * warp 0, one lane: TMA producer. Loads the Q tile once and streams the
 //    K and V tiles of 128 keys that the window of the query tile touches
 //    through a 3-stage ring (each tile two 128B-swizzled boxes of 64 dims);
@@ -98,6 +102,7 @@ struct SwaCfg {
 };
 
 struct SwaProblem {
+  void* O;  // [B, M, H, D] in the inputs' type (read by the head-pair kernel)
   float* LSE;
   int B, M, N, H, Hkv, hpg, qtiles;
   int left, right;  // clamped to [0, M + N]: M + N is unbounded in effect
@@ -134,6 +139,16 @@ __device__ __forceinline__ SwaItem swa_item(const SwaProblem& p, int64_t item) {
   it.in_lo = max(0, it.q_last - p.left);
   it.in_hi = min(p.N - 1, it.q0 + p.right);
   return it;
+}
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
 }
 
 template <bool BF16>
@@ -499,6 +514,397 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Head-pair variant (hpg even, windows of at least kSwaPairMinKeys keys). A
+// work item is one tile of 128 queries of two heads of the same KV group:
+// both read the same K/V tiles under the same masks. Each head has its own softmax warpgroup, so one
+// head's exponentials run while the tensor cores work on the other's tiles:
+//   S_A(i), S_B(i), PV_A(i), S_A(i + 1), PV_B(i), S_B(i + 1), PV_A(i + 1) ...
+// Tensor memory: S_A at 0, S_B at 128 (P is written over the first 64
+// columns of its S once S has been read: the tensor pipe runs the MMAs in
+// issue order, so the next S of that head is issued after the PV that reads
+// P), O_A at 256, O_B at 256 + D. Shared memory holds one Q pair, so the
+// next item's Q waits for the last QK^T of the current one. The softmax
+// warps write O rows straight to global memory (items are long).
+// Warpgroups: 0 softmax and epilogue of head A (warps 0-3), 1 of head B
+// (warps 4-7), 2 producer (warp 8), MMA issuer (warp 9), two idle warps.
+// ---------------------------------------------------------------------------
+
+enum SwaPairBar : int {
+  kPQFull = 0,     // the Q pair of the item has landed
+  kPQEmpty = 1,    // every QK^T of the item has completed
+  kPKFull = 2,     // 2 K stages
+  kPKEmpty = 4,    // 2
+  kPVFull = 6,     // 2 V stages
+  kPVEmpty = 8,    // 2
+  kPSFull = 10,    // 2 (head A, head B): S of the head's current tile
+  kPPFull = 12,    // 2: P written over that S
+  kPOFull = 14,    // 2: the item's last PV of the head has completed
+  kPOEmpty = 16,   // 2: the head's softmax warps have read its O
+  kPNumBars = 18
+};
+
+constexpr int kSwaPairThreads = 384;
+// keys a query tile must touch for the head-pair kernel to be used (its
+// single Q pair buffer stalls between short items)
+constexpr int64_t kSwaPairMinKeys = 512;
+
+template <int D>
+struct SwaPairCfg {
+  static constexpr int kAtoms = D / 64;
+  static constexpr int kAtomBytes = kSwaQ * 128;
+  static constexpr int kQBytes = kSwaQ * D * 2;      // one head's Q tile
+  static constexpr int kKVBytes = kSwaKeys * D * 2;  // one K (or V) stage
+  static constexpr int kOffQ = 0;                    // Q_A, Q_B
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffV = kOffK + 2 * kKVBytes;
+  static constexpr int kOffBar = kOffV + 2 * kKVBytes;
+  static constexpr int kOffTmem = kOffBar + kPNumBars * 8;
+  static constexpr int kUsed = kOffTmem + 16 + 1024;
+  static constexpr int kSmemBytes = kUsed > 118784 ? kUsed : 118784;
+};
+
+// Item -> (b, KV group, query tile, head pair), the pair fastest.
+__device__ __forceinline__ SwaItem swa_item_pair(const SwaProblem& p, int64_t item) {
+  const int pairs = p.hpg / 2;
+  uint32_t x = static_cast<uint32_t>(item);
+  const int pp = static_cast<int>(x % static_cast<uint32_t>(pairs));
+  x /= static_cast<uint32_t>(pairs);
+  // the same decode as swa_item with the head index 2 pp
+  const uint32_t rest = x;  // (b * Hkv + g) * qtiles + qt
+  return swa_item(p, static_cast<int64_t>(rest) * p.hpg + 2 * pp);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kSwaPairThreads, 1)
+    swa_fwd_pair_kernel(const SwaProblem p, const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV) {
+  using C = SwaPairCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kPQFull), 1);
+    mbar_init(bar(kPQEmpty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kPKFull + s), 1);
+      mbar_init(bar(kPKEmpty + s), 1);
+      mbar_init(bar(kPVFull + s), 1);
+      mbar_init(bar(kPVEmpty + s), 1);
+      mbar_init(bar(kPSFull + s), 1);
+      mbar_init(bar(kPPFull + s), 4 * 32);
+      mbar_init(bar(kPOFull + s), 1);
+      mbar_init(bar(kPOEmpty + s), 4 * 32);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tc_alloc(base + C::kOffTmem, kSwaTmemCols);
+    tc_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kOffTmem);
+  bool failed = false;
+  const int64_t nrounds = (p.items + gridDim.x - 1) / gridDim.x;
+  auto item_of = [&](int64_t k) -> int64_t {
+    const int64_t pos = (k & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x;
+    return k * gridDim.x + pos;
+  };
+  constexpr uint32_t kColSA = 0, kColSB = 128, kColOA = 256, kColOB = 256 + D;
+
+  // Registers: the block starts at 168 a thread; warpgroup 2 gives part of
+  // its share to the softmax warpgroups: 128 x (200 + 200 + 104) = 64,512 =
+  // 384 x 168, and 200 + 200 + 104 <= 512 per sub-partition (one warp of
+  // each warpgroup).
+  if (warp >= 8) {
+    setmaxnreg_dec<104>();  // every warp of warpgroup 2, converged
+    if (warp == 8 && lane == 0) {
+      // ---- TMA producer ----
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t keep = l2_policy_evict_last();
+      const uint64_t once = l2_policy_evict_first();
+      int64_t gt = 0;
+      int n = 0;
+      for (int64_t k = 0; k < nrounds && !failed; ++k) {
+        const int64_t x = item_of(k);
+        if (x >= p.items) continue;
+        const SwaItem it = swa_item_pair(p, x);
+        if (it.nt == 0) continue;
+        if (n >= 1 && !wait_phase(bar(kPQEmpty), (n - 1) & 1, kWaitLimitNs)) {
+          failed = true;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kPQFull), 2 * C::kQBytes);
+        for (int hx = 0; hx < 2; ++hx)
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_4d(base + C::kOffQ + hx * C::kQBytes + a * C::kAtomBytes, &tmQ,
+                        bar(kPQFull), a * 64, it.h + hx, it.q0, it.b, once);
+        for (int i = 0; i < it.nt; ++i) {
+          const int64_t gi = gt + i;
+          const int s = static_cast<int>(gi & 1);
+          const uint32_t prev = static_cast<uint32_t>(((gi - 2) >> 1) & 1);
+          const int j0 = (it.t0 + i) * kSwaKeys;
+          if (gi >= 2 && !wait_phase(bar(kPKEmpty + s), prev, kWaitLimitNs)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kPKFull + s), C::kKVBytes);
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_4d(base + C::kOffK + s * C::kKVBytes + a * C::kAtomBytes, &tmK,
+                        bar(kPKFull + s), a * 64, it.g, j0, it.b, keep);
+          if (gi >= 2 && !wait_phase(bar(kPVEmpty + s), prev, kWaitLimitNs)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kPVFull + s), C::kKVBytes);
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_4d(base + C::kOffV + s * C::kKVBytes + a * C::kAtomBytes, &tmV,
+                        bar(kPVFull + s), a * 64, it.g, j0, it.b, keep);
+        }
+        gt += it.nt;
+        ++n;
+      }
+    } else if (warp == 9 && lane == 0) {
+      // ---- MMA issuer ----
+      constexpr uint32_t idesc_s = umma_idesc_f16(kSwaQ, kSwaKeys, BF16, false);
+      constexpr uint32_t idesc_o = umma_idesc_f16(kSwaQ, D, BF16, true);
+      // S_X of global tile gi (hx: head 0 = A, 1 = B)
+      auto issue_s = [&](int64_t gi, int hx) {
+        const int s = static_cast<int>(gi & 1);
+        const uint32_t d = tmem + (hx ? kColSB : kColSA);
+        const uint32_t qbase = base + C::kOffQ + hx * C::kQBytes;
+        const uint32_t kb = base + C::kOffK + s * C::kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
+          tc_mma(d, umma_desc_sw128(qbase + off, 16), umma_desc_sw128(kb + off, 16), idesc_s,
+                 kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(kPSFull + hx));
+      };
+      int n = 0;  // items with keys so far
+      // PV_X of global tile gi (`first`: the item's first tile, O from zero,
+      // once the head's softmax warps have read the previous item's O)
+      auto issue_pv = [&](int64_t gi, int hx, bool first) -> bool {
+        if (first && n >= 1 &&
+            !wait_phase(bar(kPOEmpty + hx), static_cast<uint32_t>((n - 1) & 1), kWaitLimitNs))
+          return false;
+        tc_fence_after();
+        const int s = static_cast<int>(gi & 1);
+        const uint32_t vb = base + C::kOffV + s * C::kKVBytes;
+        const uint32_t pcol = tmem + (hx ? kColSB : kColSA);
+        const uint32_t o = tmem + (hx ? kColOB : kColOA);
+#pragma unroll
+        for (int kk = 0; kk < kSwaKeys / 16; ++kk)
+          tc_mma_ts(o, pcol + 8 * kk, umma_desc_sw128(vb + kk * 2048, C::kAtomBytes), idesc_o,
+                    (!first || kk > 0) ? 1u : 0u);
+        return true;
+      };
+      auto wait_ok = [&](int b, uint32_t parity) { return wait_phase(bar(b), parity, kWaitLimitNs); };
+      bool ok = true;
+      int64_t gt = 0;
+      for (int64_t k = 0; k < nrounds && ok; ++k) {
+        const int64_t x = item_of(k);
+        if (x >= p.items) continue;
+        const SwaItem it = swa_item_pair(p, x);
+        if (it.nt == 0) continue;
+        ok = wait_ok(kPQFull, n & 1);
+        for (int i = 0; i < it.nt && ok; ++i) {
+          const int64_t gi = gt + i;
+          const int s = static_cast<int>(gi & 1);
+          const uint32_t ph = static_cast<uint32_t>((gi >> 1) & 1);
+          ok = wait_ok(kPKFull + s, ph);
+          if (!ok) break;
+          tc_fence_after();
+          // S_A(i) follows PV_A(i - 1) in issue order (it overwrites P_A)
+          if (i > 0) {
+            ok = wait_ok(kPPFull + 0, static_cast<uint32_t>((gi - 1) & 1)) &&
+                 wait_ok(kPVFull + ((gi - 1) & 1), static_cast<uint32_t>(((gi - 1) >> 1) & 1)) &&
+                 issue_pv(gi - 1, 0, i == 1);
+            if (!ok) break;
+          }
+          issue_s(gi, 0);
+          if (i > 0) {
+            ok = wait_ok(kPPFull + 1, static_cast<uint32_t>((gi - 1) & 1)) &&
+                 issue_pv(gi - 1, 1, i == 1);
+            if (!ok) break;
+            tc_commit(bar(kPVEmpty + ((gi - 1) & 1)));
+          }
+          issue_s(gi, 1);
+          tc_commit(bar(kPKEmpty + s));
+          if (i == it.nt - 1) tc_commit(bar(kPQEmpty));
+        }
+        if (!ok) break;
+        // the item's last PVs
+        const int64_t gl = gt + it.nt - 1;
+        for (int hx = 0; hx < 2 && ok; ++hx) {
+          ok = wait_ok(kPPFull + hx, static_cast<uint32_t>(gl & 1)) &&
+               (hx == 1 || wait_ok(kPVFull + (gl & 1), static_cast<uint32_t>((gl >> 1) & 1))) &&
+               issue_pv(gl, hx, it.nt == 1);
+          if (!ok) break;
+          tc_commit(bar(kPOFull + hx));
+        }
+        if (ok) tc_commit(bar(kPVEmpty + (gl & 1)));
+        gt += it.nt;
+        ++n;
+      }
+      failed = !ok;
+    }
+  } else {
+    setmaxnreg_inc<200>();  // every warp of warpgroups 0 and 1, converged
+    // ---- softmax and epilogue of head hx (warps 4 hx .. 4 hx + 3) ----
+    const int hx = warp >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t col_s = hx ? kColSB : kColSA, col_o = hx ? kColOB : kColOA;
+    const float sl2 = p.sl2;
+    auto wait_all = [&](int b, uint32_t parity) {
+      return __all_sync(kFull, wait_phase(bar(b), parity, kWaitLimitNs));
+    };
+    int64_t gt = 0;
+    int n = 0;
+    for (int64_t k = 0; k < nrounds && !failed; ++k) {
+      const int64_t x = item_of(k);
+      if (x >= p.items) continue;
+      const SwaItem it = swa_item_pair(p, x);
+      const int h = it.h + hx;
+      const int iq = it.q0 + row;
+      const int lo_i = max(0, iq - p.left);
+      const int hi_i = min(p.N - 1, iq + p.right);
+      float ref = -INFINITY, neg = 0.f, l = 0.f;
+      for (int i = 0; i < it.nt; ++i) {
+        const int64_t gi = gt + i;
+        if (!wait_all(kPSFull + hx, static_cast<uint32_t>(gi & 1))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[kSwaKeys];
+#pragma unroll
+        for (int c = 0; c < kSwaKeys / 32; ++c)
+          tc_ld32(lane_addr + col_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        tc_wait_ld();
+        const int j0 = (it.t0 + i) * kSwaKeys;
+        if (j0 < it.in_lo || j0 + kSwaKeys - 1 > it.in_hi) {
+#pragma unroll
+          for (int j = 0; j < kSwaKeys; ++j)
+            if (j0 + j < lo_i || j0 + j > hi_i) sr[j] = __float_as_uint(-INFINITY);
+        }
+        float m8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m8[j] = __uint_as_float(sr[j]);
+#pragma unroll
+        for (int j = 8; j < kSwaKeys; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
+        const bool move = mx > ref + kSwaSlack;
+        if (__any_sync(kFull, move)) {
+          const float alpha = move ? ex2(ref - mx) : 1.f;
+          if (i > 0) {
+            // PV of the previous tile has completed: this tile's S was
+            // committed after it
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tc_ld32(lane_addr + col_o + 32 * c, o);
+              tc_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tc_st32(lane_addr + col_o + 32 * c, o);
+            }
+            tc_wait_st();
+          }
+          if (move) {
+            l *= alpha;
+            ref = mx;
+            neg = -mx;
+          }
+        }
+        float l8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) l8[j] = 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int j = 64 * h2 + 2 * c;
+            const float e0 = ex2(fmaf(__uint_as_float(sr[j]), sl2, neg));
+            const float e1 = ex2(fmaf(__uint_as_float(sr[j + 1]), sl2, neg));
+            l8[(2 * c) & 7] += e0;
+            l8[(2 * c + 1) & 7] += e1;
+            pw[c] = pack2<BF16>(e0, e1);
+          }
+          tc_st32(lane_addr + col_s + 32 * h2, pw);  // P over the S just read
+        }
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kPPFull + hx));
+      }
+      if (failed) break;
+      // epilogue: O of this head once the item's last PV has completed
+      uint32_t o[D];
+      if (it.nt > 0) {
+        if (!wait_all(kPOFull + hx, static_cast<uint32_t>(n & 1))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          tc_ld32(lane_addr + col_o + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&o[32 * c]));
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(kPOEmpty + hx));
+      } else {
+#pragma unroll
+        for (int j = 0; j < D; ++j) o[j] = 0u;
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (iq < p.M) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.O) +
+                                              ((static_cast<int64_t>(it.b) * p.M + iq) * p.H + h) * D);
+#pragma unroll
+        for (int q = 0; q < D / 8; ++q) {
+          uint4 w;
+          w.x = pack2<BF16>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+          w.y = pack2<BF16>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+          w.z = pack2<BF16>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+          w.w = pack2<BF16>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+          dst[q] = w;
+        }
+        if (p.LSE != nullptr) {
+          constexpr float kLn2 = 0.69314718055994530942f;
+          p.LSE[(static_cast<int64_t>(it.b) * p.H + h) * p.M + iq] =
+              l > 0.f ? (ref + __log2f(l)) * kLn2 : -INFINITY;
+        }
+      }
+      gt += it.nt;
+      if (it.nt > 0) ++n;
+    }
+  }
+
+  if (failed) report_timeout();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tc_dealloc(tmem, kSwaTmemCols);
+  }
+}
+
 template <int D, bool BF16>
 int launch_swa(const SwaProblem& p, const void* Q, const void* K, const void* V, void* O,
                cudaStream_t st) {
@@ -528,6 +934,31 @@ int launch_swa(const SwaProblem& p, const void* Q, const void* K, const void* V,
     return NSA_ERR_LAUNCH;
   const int64_t blocks = p.items < sms ? p.items : sms;
   kern<<<static_cast<unsigned>(blocks), kSwaThreads, C::kSmemBytes, st>>>(p, tq, tk, tv, to);
+  return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
+}
+
+template <int D, bool BF16>
+int launch_swa_pair(SwaProblem p, const void* Q, const void* K, const void* V,
+                    cudaStream_t st) {
+  using C = SwaPairCfg<D>;
+  constexpr CUtensorMapDataType dt =
+      BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap tq, tk, tv;
+  if (!encode_kv_map(&tq, Q, p.B, p.M, p.H, D, kSwaQ, dt) ||
+      !encode_kv_map(&tk, K, p.B, p.N, p.Hkv, D, kSwaKeys, dt) ||
+      !encode_kv_map(&tv, V, p.B, p.N, p.Hkv, D, kSwaKeys, dt))
+    return NSA_ERR_LAUNCH;
+  auto kern = swa_fwd_pair_kernel<D, BF16>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+      cudaSuccess)
+    return NSA_ERR_LAUNCH;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return NSA_ERR_LAUNCH;
+  p.items /= 2;  // items of two heads (hpg is even)
+  const int64_t blocks = p.items < sms ? p.items : sms;
+  kern<<<static_cast<unsigned>(blocks), kSwaPairThreads, C::kSmemBytes, st>>>(p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
@@ -572,8 +1003,19 @@ extern "C" int nsa_swa_fwd(const void* Q, const void* K, const void* V, void* O,
   p.right = static_cast<int>(window_right < 0 || window_right > unb ? unb : window_right);
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   p.sl2 = sc * 1.4426950408889634f;
+  p.O = O;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf = dtype == NSA_BF16;
+  // long windows (many key tiles per query tile) with an even number of
+  // heads per KV group: the head-pair kernel
+  const int64_t span = static_cast<int64_t>(p.left) + p.right + kSwaQ;  // keys a query tile touches
+  if (p.hpg % 2 == 0 && N > 0 && (span > N ? N : span) >= kSwaPairMinKeys) {
+    if (D == 64)
+      return bf ? launch_swa_pair<64, true>(p, Q, K, V, st)
+                : launch_swa_pair<64, false>(p, Q, K, V, st);
+    return bf ? launch_swa_pair<128, true>(p, Q, K, V, st)
+              : launch_swa_pair<128, false>(p, Q, K, V, st);
+  }
   if (D == 64)
     return bf ? launch_swa<64, true>(p, Q, K, V, O, st) : launch_swa<64, false>(p, Q, K, V, O, st);
   return bf ? launch_swa<128, true>(p, Q, K, V, O, st)
