@@ -370,8 +370,9 @@ __device__ __forceinline__ void topk_prefetch(const TopkProblem& p, const TopkRo
 // row's copies once the buffer is read. Returns false, having written at
 // most the forced blocks, when the row needs the general path.
 //  * Forced blocks and blocks past c become NaN, which no comparison passes.
-//  * t0 = the lower end of a KeyBracket over the group-maximum keys, stopped
-//    once at most k + 8 groups are >= it: the scores >= t0 hold every pick.
+//  * t0 = the k-th largest lane maximum (k <= 16), else the lower end of a
+//    KeyBracket over the group-maximum keys, stopped once at most k + 8
+//    groups are >= it: the scores >= t0 hold every pick.
 //  * The scores >= t0 (S of them, k <= S <= kSurvivors) are compacted in
 //    block order; a KeyBracket over them (one ballot per step) finds the k-th
 //    largest key tau; the picks are the keys above tau and the first ties at
@@ -419,33 +420,57 @@ __device__ __forceinline__ bool topk_select_fast(const TopkProblem& p, const Top
   if (k == 0) return true;
   if (k > 32) return false;
 
-  uint32_t kg[4];
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  int nz = 0;
+  // t0: with k <= 16 and at least k lanes holding a number, the k-th
+  // largest lane maximum (a warp bitonic sort of 32 keys); otherwise a
+  // KeyBracket over the 128 group maxima, stopped once at most k + 8 groups
+  // are >= it. Either way at least k scores are >= t0.
+  uint32_t t0key = 0u;
+  bool have_t0 = false;
+  if (k <= 16) {
+    const float lmx = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
+    uint32_t v = lmx == lmx ? order_key(lmx) : 0u;  // 0: the lane holds no number
+    if (__popc(__ballot_sync(kFull, v != 0u)) >= k) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    kg[i] = gm[i] == gm[i] ? order_key(gm[i]) : 0u;  // 0: the group holds no number
-    nz += kg[i] != 0u;
-    kmax = max(kmax, kg[i]);
-    kmin = min(kmin, kg[i] ? kg[i] : 0xffffffffu);
+      for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          const uint32_t o = __shfl_xor_sync(kFull, v, stride);
+          const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
+          v = keep_max ? max(v, o) : min(v, o);  // descending overall
+        }
+      }
+      t0key = __shfl_sync(kFull, v, k - 1);
+      have_t0 = true;
+    }
   }
-  KeyBracket br;
-  br.clo = __reduce_add_sync(kFull, nz);
-  if (br.clo < k) return false;
-  br.lo = __reduce_min_sync(kFull, kmin);
-  br.hi = __reduce_max_sync(kFull, kmax) + 1u;
-  br.chi = 0;
-  br.bisect = false;
-  // stop once at most k + 8 groups are >= lo (fewer steps here, a few more
-  // survivors below)
-  for (int it = 0; it < 80 && br.clo > k + 8 && br.hi - br.lo > 1u; ++it) {
-    const uint32_t w = br.hi - br.lo;
-    const uint32_t piv = br.pivot(k);
-    const int cnt = (kg[0] >= piv) + (kg[1] >= piv) + (kg[2] >= piv) + (kg[3] >= piv);
-    br.update(piv, __reduce_add_sync(kFull, cnt), w, k);
+  if (!have_t0) {
+    uint32_t kg[4];
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    int nz = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      kg[i] = gm[i] == gm[i] ? order_key(gm[i]) : 0u;  // 0: the group holds no number
+      nz += kg[i] != 0u;
+      kmax = max(kmax, kg[i]);
+      kmin = min(kmin, kg[i] ? kg[i] : 0xffffffffu);
+    }
+    KeyBracket br;
+    br.clo = __reduce_add_sync(kFull, nz);
+    if (br.clo < k) return false;
+    br.lo = __reduce_min_sync(kFull, kmin);
+    br.hi = __reduce_max_sync(kFull, kmax) + 1u;
+    br.chi = 0;
+    br.bisect = false;
+    for (int it = 0; it < 80 && br.clo > k + 8 && br.hi - br.lo > 1u; ++it) {
+      const uint32_t w = br.hi - br.lo;
+      const uint32_t piv = br.pivot(k);
+      const int cnt = (kg[0] >= piv) + (kg[1] >= piv) + (kg[2] >= piv) + (kg[3] >= piv);
+      br.update(piv, __reduce_add_sync(kFull, cnt), w, k);
+    }
+    t0key = br.lo;
   }
-  // the float whose key is lo (lo >= key(-inf) > 1: a number)
-  const float t0 = __uint_as_float((br.lo & 0x80000000u) ? (br.lo & 0x7fffffffu) : ~br.lo);
+  // the float whose key is t0key (>= key(-inf) > 1: a number)
+  const float t0 = __uint_as_float((t0key & 0x80000000u) ? (t0key & 0x7fffffffu) : ~t0key);
 
   // survivors in block order: count per lane, scan across lanes, write
   int cnt = 0;
