@@ -157,6 +157,54 @@ int nsa_sel_attn_fwd_strided(const void* Q, const void* K, const void* V,
                              void* stream);
 
 /*
+ * nsa_sel_attn_fwd_shared_workspace_bytes -- device workspace of
+ * nsa_sel_attn_fwd_shared: one 32-byte record per (b, g, tile of 16
+ * queries), rounded up to 256 bytes. Negative nsa_status for invalid sizes
+ * (B * G * ceil(M/16) must stay below 2^31). Pure host arithmetic.
+ */
+int64_t nsa_sel_attn_fwd_shared_workspace_bytes(int64_t B, int64_t M, int64_t G);
+
+/*
+ * nsa_sel_attn_fwd_shared -- the forward of nsa_sel_attn_fwd_ex (O fp32) in
+ * two passes over the blocks that consecutive queries share.
+ *
+ *   qkv_dtype   NSA_F16 or NSA_BF16
+ *   workspace   device memory of at least
+ *               nsa_sel_attn_fwd_shared_workspace_bytes(B, M, G) bytes,
+ *               16-byte aligned, owned by the caller (else NSA_ERR_WORKSPACE
+ *               or NSA_ERR_ALIGN); on return it holds the per-tile records
+ *
+ * Index rows that keep the initial block and the most recent blocks of
+ * every query (as nsa_topk_blocks with n_init, n_local > 0 writes them) give
+ * the queries of a tile of 16 consecutive positions some blocks in common.
+ * Per (b, g, tile) a list pass records up to 7
+ * blocks that every query of the tile lists and whose keys every one of
+ * them sees (the block ends at or before the tile's first query, and
+ * below N), in the order the tile's first query lists them. A tile-shared
+ * pass gathers those blocks once and computes, on the tcgen05 tensor cores,
+ * the softmax of all 16 x 8 (query, head) rows over their keys; it writes
+ * the normalised partial O and its LSE into O and LSE. The gather kernel of
+ * nsa_sel_attn_fwd then skips the recorded blocks and continues the online
+ * softmax from that state, so its outputs cover every selected key once.
+ * The result is the same operation as nsa_sel_attn_fwd_ex with the same
+ * tolerance (the partial sums are added in another order; outputs are not
+ * bit-identical to the one-pass call). Three kernels are enqueued on
+ * `stream`; nothing is allocated or synchronised.
+ *
+ * The two-pass path serves D = 128, H/G = 8, M >= 16, N >= block_size and
+ * T >= 1; any other valid problem runs the one-pass kernel (the workspace
+ * is then unused). Every other argument, layout, check and property is that
+ * of nsa_sel_attn_fwd_ex. A key row the tile-shared pass reads is visible
+ * to every query of the tile, so NaN or Inf in rows a query may not see
+ * still never reaches that query's output.
+ */
+int nsa_sel_attn_fwd_shared(const void* Q, const void* K, const void* V,
+                            const int32_t* block_indices, float* O, float* LSE, int64_t B,
+                            int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                            int block_size, float scale, int qkv_dtype, void* workspace,
+                            int64_t workspace_bytes, void* stream);
+
+/*
  * nsa_sel_attn_fwd_host_workspace_bytes -- device workspace that
  * nsa_sel_attn_fwd_host needs for these sizes and query chunk length
  * (chunk_m <= 0 selects the default). Returns the byte count, or a negative

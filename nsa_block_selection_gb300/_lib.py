@@ -23,7 +23,8 @@ EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sel_attn
            "nsa_sel_attn_fwd_strided", "nsa_sync_status",
            "nsa_selftest_wait_timeout", "nsa_sel_attn_fwd_host_workspace_bytes",
            "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd",
-           "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks", "nsa_swa_fwd")
+           "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks", "nsa_swa_fwd",
+           "nsa_sel_attn_fwd_shared_workspace_bytes", "nsa_sel_attn_fwd_shared")
 
 _lib = None
 
@@ -60,6 +61,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_fwd_strided.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                              i64, i64, c_int, ctypes.c_float, c_int, c_int, vp,
                                              vp]
+    lib.nsa_sel_attn_fwd_shared_workspace_bytes.restype = i64
+    lib.nsa_sel_attn_fwd_shared_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.nsa_sel_attn_fwd_shared.restype = c_int
+    lib.nsa_sel_attn_fwd_shared.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                            i64, c_int, ctypes.c_float, c_int, vp, i64, vp]
     lib.nsa_sync_status.restype = c_int
     lib.nsa_sync_status.argtypes = [vp]
     lib.nsa_selftest_wait_timeout.restype = c_int
@@ -153,6 +159,49 @@ def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float]
         what = "nsa_sel_attn_fwd_ex"
     if st != NSA_OK:
         raise NsaError(st, what)
+    return out, lse
+
+
+def shared_workspace_bytes(B, M, G) -> int:
+    n = load().nsa_sel_attn_fwd_shared_workspace_bytes(B, M, G)
+    if n < 0:
+        raise NsaError(int(n), "nsa_sel_attn_fwd_shared_workspace_bytes")
+    return int(n)
+
+
+def sel_attn_fwd_shared(q, k, v, block_indices, block_size: int, scale: Optional[float] = None,
+                        out=None, lse=None, workspace=None, stream=None):
+    """The two-pass forward (nsa_sel_attn_fwd_shared): blocks common to a tile
+    of 16 consecutive queries are gathered once per tile. Contiguous fp16 or
+    bf16 q, k, v; O fp32. ``workspace``: a CUDA uint8 tensor of at least
+    shared_workspace_bytes(B, M, G) bytes (allocated when None). Returns
+    (O, LSE); the per-tile records stay in ``workspace``.
+    """
+    import torch
+
+    lib = load()
+    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=True,
+                                        qkv_dtypes=(torch.float16, torch.bfloat16))
+    if out is None:
+        out = torch.empty((B, M, H, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    if out.dtype != torch.float32 or tuple(out.shape) != (B, M, H, D) or not out.is_contiguous():
+        raise ValueError("out must be contiguous fp32 [B, M, H, D]")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, M) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, H, M]")
+    if workspace is None:
+        workspace = torch.empty(max(shared_workspace_bytes(B, M, G), 1), dtype=torch.uint8,
+                                device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.nsa_sel_attn_fwd_shared(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out),
+                                     _ptr(lse), B, M, N, H, G, D, T, int(block_size), sc,
+                                     _dtype_code(q.dtype), _ptr(workspace), workspace.numel(),
+                                     ctypes.c_void_p(stream.cuda_stream))
+    if st != NSA_OK:
+        raise NsaError(st, "nsa_sel_attn_fwd_shared")
     return out, lse
 
 

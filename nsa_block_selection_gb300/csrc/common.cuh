@@ -25,6 +25,12 @@ __host__ __device__ inline int head_subgroups(int64_t hpg) {
   return static_cast<int>((hpg + kHeadsPerGroup - 1) / kHeadsPerGroup);
 }
 constexpr int kTileKeys = 16;
+// Two-pass forward: queries per tile whose common blocks are gathered once
+// (16 queries x 8 heads = 128 rows, the M of one tcgen05 MMA), and the
+// per-tile record the passes share: {count, ids[kSharedMax]} as int32.
+constexpr int kSharedTileQ = 16;
+constexpr int kSharedMax = 7;
+constexpr int kSharedRec = 8;
 constexpr int kBoxCols = 64;                   // d columns per TMA box: 128-byte rows
 constexpr int kBoxBytes = kTileKeys * 128;     // one box: 16 keys x 64 d x fp16
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -66,7 +72,8 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64
 // Warp-uniform walk over the 16-key tiles one index row selects, in the
 // order the row lists its blocks. Padding (< 0 or >= nblk) and blocks that
 // start after the last visible key are skipped, as are tiles of a block that
-// start after it.
+// start after it, and the blocks of an optional skip list (lane j holds id j
+// of skip_n ids: blocks another pass has already attended to).
 struct TileWalk {
   const int32_t* row;
   int T, nblk, bs, lastkey;
@@ -74,6 +81,7 @@ struct TileWalk {
   unsigned mask;  // lanes of the current window still to visit
   int lane_val;   // this lane's entry of the current window
   int n0, nend;   // next tile start, end of the visible keys of the block
+  int skip_val, skip_n;
 
   __device__ __forceinline__ void init(const int32_t* r, int T_, int nblk_, int bs_,
                                        int lastkey_) {
@@ -87,6 +95,13 @@ struct TileWalk {
     lane_val = -1;
     n0 = 0;
     nend = 0;
+    skip_val = -1;
+    skip_n = 0;
+  }
+
+  __device__ __forceinline__ void set_skip(int lane_id, int n) {
+    skip_val = lane_id;
+    skip_n = n;
   }
 
   __device__ __forceinline__ bool next(int& out) {
@@ -95,7 +110,11 @@ struct TileWalk {
         if (win >= T) return false;
         const int j = win + (threadIdx.x & 31);
         const int t = (j < T) ? __ldg(row + j) : -1;
-        const bool ok = t >= 0 && t < nblk && t * bs <= lastkey;
+        bool ok = t >= 0 && t < nblk && t * bs <= lastkey;
+        for (int k = 0; k < skip_n; ++k) {
+          const int sk = __shfl_sync(kFull, skip_val, k);  // every lane shuffles
+          ok = ok && t != sk;
+        }
         mask = __ballot_sync(kFull, ok);
         lane_val = t;
         win += 32;

@@ -64,6 +64,8 @@ struct Problem {
   int64_t o_sb, o_sm, o_sh;  // element strides of O over b, m, h (d contiguous)
   int64_t m_off;  // query position of row 0 (a chunk of a longer sequence)
   int64_t units;  // B * G * nsub * M
+  const int32_t* shared;  // two-pass path: per-tile records of the blocks already attended to
+  int64_t ntiles;         // query tiles per (b, g) of those records
   int hpg;        // query heads per KV group
   int nsub;       // sub-groups of 8 heads per KV group
   int bs;
@@ -88,8 +90,12 @@ struct Cfg {
 constexpr float kMaxSlack = 8.0f;
 
 // BF16: Q/K/V are bf16 (else fp16); P is rounded to the same type for the PV
-// product. O16: O is written in that 16-bit type (else fp32).
-template <int D, int WARPS, bool BF16, bool O16>
+// product. O16: O is written in that 16-bit type (else fp32). SHARED (fp32 O,
+// 8 heads per group): the tile-shared pass has attended to the blocks its
+// record lists and left the normalised partial O and its LSE in the outputs;
+// the warp skips those blocks and starts from that state (O = the partial O,
+// row sum 1, reference = its LSE in log2 units).
+template <int D, int WARPS, bool BF16, bool O16, bool SHARED = false>
 __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     sel_attn_fwd_kernel(const Problem p, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
@@ -113,6 +119,13 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
                                                                 : kHeadsPerGroup;
   const int gid = lane >> 2;  // MMA group id (row within an 8-row slab)
   const int tig = lane & 3;   // thread in group
+  // two-pass path: the record of this query's tile ({count, ids}), loaded
+  // first so that its latency overlaps the setup below
+  int rec_v = 0;
+  if constexpr (SHARED) {
+    const int32_t* rec = p.shared + (bg * p.ntiles + m / kSharedTileQ) * kSharedRec;
+    if (lane < kSharedRec) rec_v = __ldg(rec + lane);
+  }
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t slots = base + warp * C::kWarpBytes;
@@ -165,6 +178,13 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
 
   TileWalk walk;
   walk.init(irow, static_cast<int>(p.T), p.nblk, p.bs, lastkey);
+  int shared_cnt = 0;
+  if constexpr (SHARED) {
+    // lane j takes id j of the record
+    shared_cnt = __shfl_sync(kFull, rec_v, 0);
+    const int id = __shfl_sync(kFull, rec_v, (lane + 1) & 31);
+    if (shared_cnt > 0) walk.set_skip(id, shared_cnt < kSharedMax ? shared_cnt : kSharedMax);
+  }
   int n_next = 0;
   bool have = walk.next(n_next);
   if (have) {
@@ -179,6 +199,33 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   float nega = 0.f, negb = 0.f;            // -reference (0 while a head has seen nothing)
   float la = 0.f, lb = 0.f;                // this lane's share of the row sums
   const float sl2 = p.sl2;
+  if constexpr (SHARED) {
+    if (shared_cnt > 0) {
+      constexpr float kLog2e = 1.4426950408889634f;
+      const float* L = p.LSE + (b * p.H + hbase + 2 * tig) * p.M + m;
+      const float lsa = L[0], lsb = L[p.M];
+      const float* o = static_cast<const float*>(p.O) + b * p.o_sb + m * p.o_sm +
+                       (hbase + 2 * tig) * p.o_sh + gid;
+      const float* o2 = o + p.o_sh;
+#pragma unroll
+      for (int i = 0; i < C::kSteps; ++i) {
+        acc[i][0] = o[16 * i];
+        acc[i][2] = o[16 * i + 8];
+        acc[i][1] = o2[16 * i];
+        acc[i][3] = o2[16 * i + 8];
+      }
+      if (lsa > -INFINITY) {
+        m2a = lsa * kLog2e;
+        nega = -m2a;
+        la = gid == 0 ? 1.f : 0.f;
+      }
+      if (lsb > -INFINITY) {
+        m2b = lsb * kLog2e;
+        negb = -m2b;
+        lb = gid == 0 ? 1.f : 0.f;
+      }
+    }
+  }
 
   // ldmatrix row addresses: K tiles (row-major A), V tiles (transposed A).
   const uint32_t ka = sk + (lane & 7) * 128 + ((lane & 8) ? 8 * 128 : 0);
@@ -363,7 +410,7 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns) {
 
 // ---- host side ---------------------------------------------------------------
 
-template <int D, bool BF16, bool O16>
+template <int D, bool BF16, bool O16, bool SHARED = false>
 static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
                       const int64_t (&ks)[3], const int64_t (&vs)[3], cudaStream_t stream) {
   constexpr int W = NSA_WARPS;
@@ -379,7 +426,7 @@ static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
     memset(&tk, 0, sizeof(tk));  // no key: no tile is ever loaded
     memset(&tv, 0, sizeof(tv));
   }
-  auto kern = sel_attn_fwd_kernel<D, W, BF16, O16>;
+  auto kern = sel_attn_fwd_kernel<D, W, BF16, O16, SHARED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return NSA_ERR_LAUNCH;
@@ -412,7 +459,8 @@ int check_sizes(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D
 int launch_forward(const void* Q, const void* K, const void* V, const int32_t* block_indices,
                    void* O, float* LSE, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                    int64_t D, int64_t T, int64_t m_off, int block_size, float scale,
-                   int qkv_dtype, int o_dtype, const int64_t* strides, cudaStream_t st) {
+                   int qkv_dtype, int o_dtype, const int64_t* strides, cudaStream_t st,
+                   const SharedPass* shared) {
   const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
   if (chk != NSA_OK) return chk;
   if ((qkv_dtype != NSA_F16 && qkv_dtype != NSA_BF16) ||
@@ -429,6 +477,12 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
   if (mis(Q, 16) || mis(K, 16) || mis(V, 16) || mis(O, 16) || mis(LSE, 4) ||
       mis(block_indices, 4))
     return NSA_ERR_ALIGN;
+  if (shared != nullptr) {
+    const int64_t need = shared_workspace_bytes(B, M, G);
+    if (need < 0) return static_cast<int>(need);
+    if (shared->workspace == nullptr || shared->workspace_bytes < need) return NSA_ERR_WORKSPACE;
+    if (mis(shared->workspace, 16)) return NSA_ERR_ALIGN;
+  }
   // element strides (b, m|n, h|g) of Q, K, V, O; d is contiguous
   int64_t sq[3] = {M * H * D, H * D, D}, sk[3] = {N * G * D, G * D, D};
   int64_t sv[3] = {sk[0], sk[1], sk[2]}, so[3] = {sq[0], sq[1], sq[2]};
@@ -470,7 +524,20 @@ int launch_forward(const void* Q, const void* K, const void* V, const int32_t* b
   p.nblk = static_cast<int>((N + block_size - 1) / block_size);
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   p.sl2 = sc * 1.4426950408889634f;
+  p.shared = nullptr;
+  p.ntiles = 0;
   const bool bf = qkv_dtype == NSA_BF16, o16 = o_dtype != NSA_F32;
+  if (shared != nullptr && shared_pass_sizes_ok(M, N, T, block_size) &&
+      shared_pass_eligible(H, G, D, o_dtype, strides, m_off)) {
+    int32_t* lists = static_cast<int32_t*>(shared->workspace);
+    const int rc = launch_shared_passes(Q, K, V, block_indices, static_cast<float*>(O), LSE, B,
+                                        M, N, H, G, T, block_size, p.sl2, bf, lists, st);
+    if (rc != NSA_OK) return rc;
+    p.shared = lists;
+    p.ntiles = (M + kSharedTileQ - 1) / kSharedTileQ;
+    return bf ? launch_fwd<128, true, false, true>(p, K, V, B, sk, sv, st)
+              : launch_fwd<128, false, false, true>(p, K, V, B, sk, sv, st);
+  }
   if (D == 64) {
     if (bf) return o16 ? launch_fwd<64, true, true>(p, K, V, B, sk, sv, st)
                        : launch_fwd<64, true, false>(p, K, V, B, sk, sv, st);
@@ -512,6 +579,21 @@ int nsa_sel_attn_fwd_strided(const void* Q, const void* K, const void* V,
   return nsa::launch_forward(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T, 0, block_size,
                              scale, qkv_dtype, o_dtype, strides,
                              static_cast<cudaStream_t>(stream));
+}
+
+int64_t nsa_sel_attn_fwd_shared_workspace_bytes(int64_t B, int64_t M, int64_t G) {
+  return nsa::shared_workspace_bytes(B, M, G);
+}
+
+int nsa_sel_attn_fwd_shared(const void* Q, const void* K, const void* V,
+                            const int32_t* block_indices, float* O, float* LSE, int64_t B,
+                            int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                            int block_size, float scale, int qkv_dtype, void* workspace,
+                            int64_t workspace_bytes, void* stream) {
+  const nsa::SharedPass sp{workspace, workspace_bytes};
+  return nsa::launch_forward(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T, 0, block_size,
+                             scale, qkv_dtype, NSA_F32, nullptr,
+                             static_cast<cudaStream_t>(stream), &sp);
 }
 
 int nsa_selftest_wait_timeout(int64_t limit_ns, void* stream) {

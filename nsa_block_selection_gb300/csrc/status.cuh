@@ -7,5 +7,6 @@ namespace nsa {
 int fwd_read_and_clear_status(unsigned int* value);  // selection forward (+ wait self-test)
 int bwd_read_and_clear_status(unsigned int* value);  // selection backward
 int swa_read_and_clear_status(unsigned int* value);  // sliding-window forward
+int shared_read_and_clear_status(unsigned int* value);  // tile-shared pass of the forward
 
 }  // namespace nsa

@@ -127,6 +127,37 @@ def test_host_workspace_checks(lib):
     assert call_host(lib, B=0, q=None, k=None, v=None, idx=None, o=None, lse=None, ws=None) == 0
 
 
+def call_shared(lib, q=FAKE, k=FAKE, v=FAKE, idx=FAKE, o=FAKE, lse=FAKE, ws=FAKE,
+                ws_bytes=1 << 40, dtype=0, **over):
+    a = dict(GOOD)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return lib.nsa_sel_attn_fwd_shared(vp(q), vp(k), vp(v), vp(idx), vp(o), vp(lse), a["B"],
+                                       a["M"], a["N"], a["H"], a["G"], a["D"], a["T"], a["bs"],
+                                       0.0, dtype, vp(ws), ws_bytes, None)
+
+
+def test_shared_workspace_bytes(lib):
+    f = lib.nsa_sel_attn_fwd_shared_workspace_bytes
+    assert f(1, 65536, 8) == 8 * 4096 * 32  # one 32-byte record per (b, g, 16 queries)
+    assert f(2, 1000, 2) == -(-(2 * 2 * 63 * 32) // 256) * 256
+    assert f(1, 0, 8) == 0
+    assert f(1, 16, 0) == -2 and f(-1, 16, 8) == -2
+    assert f(1 << 20, 1 << 30, 64) == -2  # records past 2^31
+
+
+def test_shared_argument_checks(lib):
+    need = lib.nsa_sel_attn_fwd_shared_workspace_bytes(1, 128, 2)
+    assert call_shared(lib, ws=None) == -9
+    assert call_shared(lib, ws_bytes=need - 1) == -9
+    assert call_shared(lib, ws=FAKE + 8, ws_bytes=need) == -6
+    assert call_shared(lib, o=None) == -1
+    assert call_shared(lib, bs=16) == -3
+    assert call_shared(lib, dtype=2) == -11
+    assert call_shared(lib, H=24) == -5
+    assert call_shared(lib, B=0, q=None, k=None, v=None, idx=None, o=None, lse=None, ws=None) == 0
+
+
 @pytest.mark.parametrize("H,G", [(16, 16), (16, 8), (12, 4), (16, 2), (64, 4), (96, 3)])
 def test_heads_per_group_accepted(lib, H, G):
     # 1..8 heads per group, or a multiple of 8: the size checks pass (the
