@@ -68,6 +68,8 @@ def parse_args(argv=None):
                     help="skip timing the top-k block selection kernel")
     ap.add_argument("--skip-variants", action="store_true",
                     help="skip timing the bf16-input and 16-bit-O forward variants")
+    ap.add_argument("--skip-two-pass", action="store_true",
+                    help="skip the two-pass forward (nsa_sel_attn_fwd_shared) leg")
     ap.add_argument("--cpu-rows", type=int, default=24576,
                     help="rows of the CPU-oracle sample")
     ap.add_argument("--seed", type=int, default=None)
@@ -396,6 +398,11 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.skip_swa:
         swa = run_swa(flush, args, dev)
 
+    # the same forward in two passes (blocks common to a 16-query tile once)
+    two_pass = None
+    if rank == 0 and world == 1 and not args.skip_two_pass:
+        two_pass = run_two_pass(w, q, k, v, idx, work, flush, args, t_ms)
+
     # element-type variants of the forward on the same workload
     variants = None
     if rank == 0 and world == 1 and not args.skip_variants:
@@ -444,6 +451,7 @@ def run_ours(args):
         "dense_causal": dense,
         "backward": backward,
         "variants": variants,
+        "two_pass": two_pass,
         "topk": topk,
         "swa": swa,
         "roofline": roofline,
@@ -638,6 +646,42 @@ def run_variants(w, q, k, v, idx, work, flush, args):
                                       "tflops": work["flops"] / (t * 1e-3) / 1e12,
                                       "steps": steps}
         del tq, tk, tv, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_two_pass(w, q, k, v, idx, work, flush, args, t_one_ms):
+    """nsa_sel_attn_fwd_shared on the headline inputs, timed like the headline
+    run (three kernels per step: per-tile lists of the blocks every query of
+    a 16-query tile lists and sees whole; their softmax on tcgen05; the gather
+    kernel over the remaining blocks). FLOPs and gathered bytes are those of
+    the operation, as for the headline, so the numbers compare directly."""
+    import torch
+
+    from nsa_block_selection_gb300 import _lib
+
+    ws = torch.empty(max(_lib.shared_workspace_bytes(w.B, w.M, w.G), 256), dtype=torch.uint8,
+                     device=q.device)
+    out = torch.empty((w.B, w.M, w.H, w.D), dtype=torch.float32, device=q.device)
+    lse = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=q.device)
+
+    def step():
+        _lib.sel_attn_fwd_shared(q, k, v, idx, w.block_size, w.scale, out=out, lse=lse,
+                                 workspace=ws)
+
+    steps = max(5, args.steps // 4)
+    times, _ = time_steps(step, steps, 3, flush, lambda: None)
+    t = statistics.mean(times)
+    ntiles = -(-w.M // 16)
+    rec = ws[:w.B * w.G * ntiles * 32].view(torch.int32).reshape(-1, 8)
+    cnt = rec[:, 0].float()
+    res = {"ms_per_step": t, "tflops": work["flops"] / (t * 1e-3) / 1e12,
+           "gathered_gbs": work["gathered_bytes"] / (t * 1e-3) / 1e9,
+           "speedup_vs_one_pass": t_one_ms / t, "steps": steps,
+           "kernels_per_step": 3,
+           "shared_blocks_per_tile_mean": float(cnt.mean()),
+           "tiles_with_shared_blocks": float((cnt > 0).float().mean())}
+    del ws, out, lse
     torch.cuda.empty_cache()
     return res
 
