@@ -25,13 +25,15 @@
 // {count, ids} per tile is the workspace both other passes read.
 //
 // Tile-shared pass (sel_attn_shared_kernel): persistent, one CTA per SM
-// taking the tiles round-robin (tiles with an empty record are skipped), 10
+// taking the tiles round-robin (tiles with an empty record are skipped), 11
 // warps with fixed roles; the next tile's loads overlap the current tile's
 // softmax and epilogue:
-//  * warp 0, one lane: TMA producer. The Q tile is 16 queries x 8 heads =
-//    128 rows (row = 8 * query + head, 128B-swizzled boxes of 64 dims) in one
-//    of two buffers; the K and V blocks (block_size keys each) go through a
-//    3-stage ring that runs across tiles;
+//  * warp 0, one lane: TMA producer of Q and K. The Q tile is 16 queries x 8
+//    heads = 128 rows (row = 8 * query + head, 128B-swizzled boxes of 64
+//    dims) in one of two buffers; the K blocks (block_size keys each) go
+//    through a 4-stage ring that runs across tiles, a slot freed as soon as
+//    its QK^T has completed, so the next QK^T rarely waits for a load;
+//  * warp 10, one lane: TMA producer of V, a 2-stage ring freed by the PVs;
 //  * warp 1: allocates the 512 tensor-memory columns; one lane issues
 //    S_j = Q K_j^T (M = 128, N = block_size, K = 128) into one of two S
 //    buffers and O += P_j V_j (M = 128, N = 128, K = block_size; P from tensor
@@ -69,8 +71,9 @@ namespace {
 constexpr int kShHeads = 8;                       // heads per KV group served
 constexpr int kShRows = kSharedTileQ * kShHeads;  // 128: the MMA's M
 constexpr int kShD = 128;
-constexpr int kShThreads = 320;  // producer, MMA, softmax warpgroup, epilogue warpgroup
-constexpr int kStages = 3;                         // K/V ring
+constexpr int kShThreads = 352;  // K producer, MMA, softmax and epilogue warpgroups, V producer
+constexpr int kKStages = 4;  // K ring: a slot is free once its QK^T has completed
+constexpr int kVStages = 2;  // V ring: a slot is free once its PV has completed
 constexpr uint32_t kShTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S buffers at columns 0 and 64 (P over their first half)
 constexpr uint32_t kColO = 128;  // two O buffers of 128 columns (tiles alternate)
@@ -80,23 +83,22 @@ constexpr float kShSlack = 8.0f;
 // One barrier per buffer or ring slot, so that none can complete twice
 // before its waiter has seen the first completion. Blocks are counted across
 // the CTA's tiles (gi), tiles by n.
-enum ShBar : int {
-  kQFull = 0,    // 2 Q buffers
-  kQEmpty = 2,   // 2: every QK^T of the tile that used the buffer has completed
-  kSFull = 4,    // 2 S buffers
-  kPFull = 6,    // 2: P written over that S
-  kODone = 8,    // 2 O buffers: the tile's last PV has completed
-  kOEmpty = 10,  // 2: the softmax warps have read the O buffer
-  kKFull = 12,   // kStages
-  kVFull = 15,   // kStages
-  kKVFree = 18,  // kStages: the PV that read the slot (after its QK^T) has completed
-  kPvDone = 21,  // one completion per PV
-  kEnd = 22,     // every MMA of the CTA has completed
-  kOStaged = 23,    // the epilogue warps have staged the tile's O in shared memory
-  kOSmemFree = 24,  // the previous tile's O store has read the staging buffer
-  kStats = 25,      // 2 O buffers: the softmax warps have written the tile's (ref, l)
-  kNumBars = 27
-};
+constexpr int kQFull = 0;                    // 2 Q buffers
+constexpr int kQEmpty = 2;                   // 2: every QK^T of the tile that used the buffer has completed
+constexpr int kSFull = 4;                    // 2 S buffers
+constexpr int kPFull = 6;                    // 2: P written over that S
+constexpr int kODone = 8;                    // 2 O buffers: the tile's last PV has completed
+constexpr int kOEmpty = 10;                  // 2: the epilogue warps have read the O buffer
+constexpr int kPvDone = 12;                  // one completion per PV
+constexpr int kEnd = 13;                     // every MMA of the CTA has completed
+constexpr int kOStaged = 14;                 // the epilogue warps have staged the tile's O
+constexpr int kOSmemFree = 15;               // the previous tile's O store has read the staging buffer
+constexpr int kStats = 16;                   // 2 O buffers: the softmax warps have written (ref, l)
+constexpr int kKFull = 18;                   // kKStages
+constexpr int kKFree = kKFull + kKStages;    // kKStages: the QK^T that read the slot has completed
+constexpr int kVFull = kKFree + kKStages;    // kVStages
+constexpr int kVFree = kVFull + kVStages;    // kVStages: the PV that read the slot has completed
+constexpr int kNumBars = kVFree + kVStages;
 
 template <int BS>
 struct ShCfg {
@@ -106,9 +108,9 @@ struct ShCfg {
   static constexpr int kKVBytes = 2 * kKVBox;  // one K (or V) block
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKVBytes;
+  static constexpr int kOffV = kOffK + kKStages * kKVBytes;
   static constexpr int kOBox = kShRows * 128;  // 128 rows x 32 fp32
-  static constexpr int kOffO = kOffV + kStages * kKVBytes;  // O tile staged for the TMA store
+  static constexpr int kOffO = kOffV + kVStages * kKVBytes;  // O tile staged for the TMA store
   static constexpr int kOffBar = kOffO + (kShD / 32) * kOBox;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   // at least 116 KB so that one CTA holds an SM (all 512 tensor-memory columns)
@@ -219,10 +221,13 @@ __global__ void __launch_bounds__(kShThreads, 1)
       mbar_init(bar(kODone + s), 1);
       mbar_init(bar(kOEmpty + s), 4 * 32);
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kKFull + s), 1);
+      mbar_init(bar(kKFree + s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(bar(kVFull + s), 1);
-      mbar_init(bar(kKVFree + s), 1);
+      mbar_init(bar(kVFree + s), 1);
     }
     mbar_init(bar(kPvDone), 1);
     mbar_init(bar(kEnd), 1);
@@ -245,10 +250,9 @@ __global__ void __launch_bounds__(kShThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---- TMA producer: Q of each tile (two buffers), its blocks (ring) ----
+      // ---- TMA producer: Q of each tile (two buffers), its K blocks (ring) ----
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       const uint64_t keep = l2_policy_evict_last();
       const uint64_t once = l2_policy_evict_first();
       int64_t gi = 0;  // blocks loaded so far
@@ -271,9 +275,9 @@ __global__ void __launch_bounds__(kShThreads, 1)
                       a * 64, g * kShHeads, m0, b, once);
         const int32_t* ids = p.lists + x * kSharedRec + 1;
         for (int i = 0; i < cnt; ++i, ++gi) {
-          const int st = static_cast<int>(gi % kStages);
-          if (gi >= kStages &&
-              !wait_phase(bar(kKVFree + st), static_cast<uint32_t>(((gi - kStages) / kStages) & 1),
+          const int st = static_cast<int>(gi % kKStages);
+          if (gi >= kKStages &&
+              !wait_phase(bar(kKFree + st), static_cast<uint32_t>(((gi - kKStages) / kKStages) & 1),
                           kWaitLimitNs)) {
             failed = true;
             break;
@@ -283,22 +287,46 @@ __global__ void __launch_bounds__(kShThreads, 1)
           for (int a = 0; a < 2; ++a)
             tma_load_4d(base + C::kOffK + st * C::kKVBytes + a * C::kKVBox, &tmK, bar(kKFull + st),
                         a * 64, g, key0, b, keep);
-          mbar_arrive_expect_tx(bar(kVFull + st), C::kKVBytes);
-          for (int a = 0; a < 2; ++a)
-            tma_load_4d(base + C::kOffV + st * C::kKVBytes + a * C::kKVBox, &tmV, bar(kVFull + st),
-                        a * 64, g, key0, b, keep);
         }
         ++n;
       }
       // the copies in flight land before the CTA may exit
       for (int j = n >= 2 ? n - 2 : 0; j < n; ++j)
         wait_phase(bar(kQFull + (j & 1)), static_cast<uint32_t>((j >> 1) & 1), kWaitLimitNs);
-      for (int64_t j = gi >= kStages ? gi - kStages : 0; j < gi; ++j) {
-        const int st = static_cast<int>(j % kStages);
-        const uint32_t ph = static_cast<uint32_t>((j / kStages) & 1);
-        wait_phase(bar(kKFull + st), ph, kWaitLimitNs);
-        wait_phase(bar(kVFull + st), ph, kWaitLimitNs);
+      for (int64_t j = gi >= kKStages ? gi - kKStages : 0; j < gi; ++j)
+        wait_phase(bar(kKFull + static_cast<int>(j % kKStages)),
+                   static_cast<uint32_t>((j / kKStages) & 1), kWaitLimitNs);
+    }
+  } else if (warp == 10) {
+    if (lane == 0) {
+      // ---- TMA producer of the V blocks (ring), ahead of the PVs ----
+      tma_prefetch_desc(&tmV);
+      const uint64_t keep = l2_policy_evict_last();
+      int64_t gi = 0;  // blocks loaded so far
+      for (int64_t x = blockIdx.x; x < p.units && !failed; x += step) {
+        const int cnt = tile_count(p, x);
+        if (cnt == 0) continue;
+        const int g = static_cast<int>((x / p.ntiles) % p.G);
+        const int b = static_cast<int>(x / p.ntiles / p.G);
+        const int32_t* ids = p.lists + x * kSharedRec + 1;
+        for (int i = 0; i < cnt; ++i, ++gi) {
+          const int st = static_cast<int>(gi % kVStages);
+          if (gi >= kVStages &&
+              !wait_phase(bar(kVFree + st), static_cast<uint32_t>(((gi - kVStages) / kVStages) & 1),
+                          kWaitLimitNs)) {
+            failed = true;
+            break;
+          }
+          const int key0 = __ldg(ids + i) * BS;
+          mbar_arrive_expect_tx(bar(kVFull + st), C::kKVBytes);
+          for (int a = 0; a < 2; ++a)
+            tma_load_4d(base + C::kOffV + st * C::kKVBytes + a * C::kKVBox, &tmV, bar(kVFull + st),
+                        a * 64, g, key0, b, keep);
+        }
       }
+      for (int64_t j = gi >= kVStages ? gi - kVStages : 0; j < gi; ++j)
+        wait_phase(bar(kVFull + static_cast<int>(j % kVStages)),
+                   static_cast<uint32_t>((j / kVStages) & 1), kWaitLimitNs);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -309,8 +337,8 @@ __global__ void __launch_bounds__(kShThreads, 1)
       constexpr uint32_t idesc_s = umma_idesc_f16(kShRows, BS, BF16, false);
       constexpr uint32_t idesc_o = umma_idesc_f16(kShRows, kShD, BF16, true);
       auto issue_s = [&](int64_t gi, int qb) -> bool {
-        const int st = static_cast<int>(gi % kStages);
-        if (!wait_phase(bar(kKFull + st), static_cast<uint32_t>((gi / kStages) & 1), kWaitLimitNs))
+        const int st = static_cast<int>(gi % kKStages);
+        if (!wait_phase(bar(kKFull + st), static_cast<uint32_t>((gi / kKStages) & 1), kWaitLimitNs))
           return false;
         tc_fence_after();
         const uint32_t d = tmem + kColS + static_cast<uint32_t>(gi & 1) * 64;
@@ -322,18 +350,19 @@ __global__ void __launch_bounds__(kShThreads, 1)
           const uint32_t ka = kb + (k >> 2) * C::kKVBox + (k & 3) * 32;
           tc_mma(d, umma_desc_sw128(qa, 16), umma_desc_sw128(ka, 16), idesc_s, k > 0 ? 1u : 0u);
         }
+        tc_commit(bar(kKFree + st));
         tc_commit(bar(kSFull + static_cast<int>(gi & 1)));
         return true;
       };
       // PV of block gi into the O buffer of tile n; `first` / `last`: the
       // tile's first / last block
       auto issue_pv = [&](int64_t gi, int n, bool first, bool last) -> bool {
-        const int st = static_cast<int>(gi % kStages);
+        const int st = static_cast<int>(gi % kVStages);
         const int sb = static_cast<int>(gi & 1);
         const int ob = n & 1;
         if (!wait_phase(bar(kPFull + sb), static_cast<uint32_t>((gi >> 1) & 1), kWaitLimitNs))
           return false;
-        if (!wait_phase(bar(kVFull + st), static_cast<uint32_t>((gi / kStages) & 1), kWaitLimitNs))
+        if (!wait_phase(bar(kVFull + st), static_cast<uint32_t>((gi / kVStages) & 1), kWaitLimitNs))
           return false;
         if (first && n >= 2 &&
             !wait_phase(bar(kOEmpty + ob), static_cast<uint32_t>(((n - 2) >> 1) & 1), kWaitLimitNs))
@@ -346,7 +375,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
         for (int kk = 0; kk < BS / 16; ++kk)
           tc_mma_ts(ocol, pcol + 8 * kk, umma_desc_sw128(vb + kk * 2048, C::kKVBox), idesc_o,
                     (!first || kk > 0) ? 1u : 0u);
-        tc_commit(bar(kKVFree + st));
+        tc_commit(bar(kVFree + st));
         tc_commit(bar(kPvDone));
         if (last) tc_commit(bar(kODone + ob));
         return true;
@@ -489,7 +518,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
       mbar_arrive(bar(kStats + ob));
       ++n;
     }
-  } else {
+  } else if (warp >= 6) {
     // ---- epilogue (warps 6..9): O of each tile out of tensor memory, O / l
     // staged in shared memory (128B-swizzled rows, four boxes of 32 columns)
     // and stored by one TMA tensor store per tile (rows past M are clipped);
