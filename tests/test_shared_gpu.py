@@ -14,44 +14,15 @@ import pytest
 
 import oracle.sel_attn as oracle
 from _parity import check_all_rows, check_rows, compare, gather_rows, sample_rows, to_dev
+from _records import MAXREC, TILE, records_ref
 
 pytestmark = pytest.mark.gpu
-
-TILE, MAXREC = 16, 7
-
 
 @pytest.fixture(scope="module", autouse=True)
 def _need_gpu(cuda_lib):
     import torch
 
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
-
-
-def records_ref(idx, N, bs):
-    """[B, G, tiles, 8] int32: count, then up to 7 ids -- the blocks listed by
-    every query of the tile, in the order the tile's first query lists them,
-    whose last key is <= the first query's position and < N."""
-    B, M, G, T = idx.shape
-    nblk = -(-N // bs)
-    ntiles = -(-M // TILE)
-    out = np.full((B, G, ntiles, 8), -1, np.int32)
-    for b in range(B):
-        for g in range(G):
-            for t in range(ntiles):
-                m0 = t * TILE
-                rows = idx[b, m0:min(M, m0 + TILE), g]
-                sets = [set(r.tolist()) for r in rows]
-                lim = min(m0 + 1, N)
-                ids = []
-                for e in rows[0].tolist():
-                    if len(ids) == MAXREC:
-                        break
-                    if 0 <= e < nblk and (e + 1) * bs <= lim and e not in ids and \
-                            all(e in s for s in sets):
-                        ids.append(e)
-                out[b, g, t, 0] = len(ids)
-                out[b, g, t, 1:1 + len(ids)] = ids
-    return out
 
 
 def run_shared(q, k, v, idx, bs, dtype=None, scale=None):
