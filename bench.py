@@ -320,6 +320,19 @@ def run_reference(args):
     return 0
 
 
+def run_leg(enabled, fn, *a):
+    """fn(*a) when enabled, else None; an exception becomes {"error": repr}
+    (also printed to stderr), so one failing auxiliary measurement does not
+    take the measured headline with it."""
+    if not enabled:
+        return None
+    try:
+        return fn(*a)
+    except Exception as e:  # noqa: BLE001 -- reported in the JSON line, not hidden
+        print(f"bench: {fn.__name__} failed: {e!r}", file=sys.stderr, flush=True)
+        return {"error": repr(e)}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -383,35 +396,26 @@ def run_ours(args):
     if not args.skip_e2e:
         e2e = run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist)
 
+    # The legs below run on rank 0 of a 1-GPU run only. A leg that raises is
+    # reported in its own key ({"error": ...}) so the measured headline above
+    # is still printed.
+    solo = rank == 0 and world == 1
+
+    def leg(skip, fn, *a):
+        return run_leg(solo and not skip, fn, *a)
+
     # backward (dQ, dK, dV) on the same inputs, after the timed forward
-    backward = None
-    if rank == 0 and world == 1 and not args.skip_bwd:
-        backward = run_backward(w, q, k, v, idx, out, lse, work, flush, args)
-
+    backward = leg(args.skip_bwd, run_backward, w, q, k, v, idx, out, lse, work, flush, args)
     # top-k block selection producing an index tensor of this workload's shape
-    topk = None
-    if rank == 0 and world == 1 and not args.skip_topk:
-        topk = run_topk(w, flush, args, dev)
-
+    topk = leg(args.skip_topk, run_topk, w, flush, args, dev)
     # GQA sliding-window attention (the pages' second kernel), tcgen05
-    swa = None
-    if rank == 0 and world == 1 and not args.skip_swa:
-        swa = run_swa(flush, args, dev)
-
+    swa = leg(args.skip_swa, run_swa, flush, args, dev)
     # the same forward in two passes (blocks common to a 16-query tile once)
-    two_pass = None
-    if rank == 0 and world == 1 and not args.skip_two_pass:
-        two_pass = run_two_pass(w, q, k, v, idx, work, flush, args, t_ms)
-
+    two_pass = leg(args.skip_two_pass, run_two_pass, w, q, k, v, idx, work, flush, args, t_ms)
     # element-type variants of the forward on the same workload
-    variants = None
-    if rank == 0 and world == 1 and not args.skip_variants:
-        variants = run_variants(w, q, k, v, idx, work, flush, args)
-
+    variants = leg(args.skip_variants, run_variants, w, q, k, v, idx, work, flush, args)
     # dense-causal-equivalent run: same Q/K/V, every causal block listed
-    dense = None
-    if rank == 0 and world == 1 and not args.skip_dense:
-        dense = run_dense(w, q, k, v, out, lse, flush, args, t_ms)
+    dense = leg(args.skip_dense, run_dense, w, q, k, v, out, lse, flush, args, t_ms)
 
     peaks = load_peaks()
     t_roof = max(work["flops"] / (peaks["bf16_tflops"] * 1e12),
@@ -447,7 +451,7 @@ def run_ours(args):
                    "accumulate": "fp32"},
         "gathered_gbs": gbs,
         "flops_per_step": work["flops"], "gathered_bytes_per_step": work["gathered_bytes"],
-        "speedup_vs_dense_causal": dense["speedup"] if dense else None,
+        "speedup_vs_dense_causal": dense.get("speedup") if dense else None,
         "dense_causal": dense,
         "backward": backward,
         "variants": variants,

@@ -51,3 +51,21 @@ def test_single_rank_passthrough():
     import bench
 
     assert bench.reduce_over_ranks(3.5, 10, 20) == (3.5, 10.0, 20.0)
+
+
+def test_failing_leg_is_reported_not_fatal(capsys):
+    """An auxiliary measurement that raises becomes {"error": ...} in its
+    key; a disabled one is None; a working one returns its result."""
+    import bench
+
+    def boom(x):
+        raise RuntimeError(f"no device {x}")
+
+    def ok(x, y):
+        return {"ms_per_step": x + y}
+
+    assert bench.run_leg(False, boom, 1) is None
+    assert bench.run_leg(True, ok, 1, 2) == {"ms_per_step": 3}
+    r = bench.run_leg(True, boom, 7)
+    assert r == {"error": "RuntimeError('no device 7')"}
+    assert "boom failed" in capsys.readouterr().err
