@@ -11,10 +11,15 @@ Prints ONE JSON line (rank 0):
                 visible gathered key), inputs resident in HBM, L2 flushed
                 between steps (a 512 MiB write outside the timed events);
   gathered_gbs  gathered K/V bytes per second (whole selected blocks);
+  speedup_vs_dense_fa  time of dense causal attention at the same sequence
+                length on the same Q/K/V (the library's tcgen05 flash kernel,
+                nsa_swa_fwd with window (-1, 0)) over the sparse time;
   speedup_vs_dense_causal  time of the same build with every causal block
                 listed (T=1024, same Q/K/V) over the sparse time;
-  roofline      the kernel against max(FLOPs / fp16 tensor peak, gathered
-                bytes / HBM bandwidth) -- the gathered bytes dominate;
+  roofline      gathered bytes per second against the gather ceiling
+                measured in the same run (the probe kernel issuing the
+                forward's TMA copies from L2-resident K/V and nothing else);
+                the fraction of HBM bandwidth is kept under "hbm";
   e2e           the same metric through the C ABI's host-buffer entry point
                 (pinned host inputs uploaded and O / LSE downloaded every step,
                 chunked so copies overlap the kernels);
@@ -70,6 +75,11 @@ def parse_args(argv=None):
                     help="skip timing the bf16-input and 16-bit-O forward variants")
     ap.add_argument("--skip-two-pass", action="store_true",
                     help="skip the two-pass forward (nsa_sel_attn_fwd_shared) leg")
+    ap.add_argument("--skip-l2-ceiling", action="store_true",
+                    help="skip measuring the gather ceiling (the roofline then falls back to "
+                         "HBM bandwidth)")
+    ap.add_argument("--skip-dense-fa", action="store_true",
+                    help="skip timing dense causal attention (nsa_swa_fwd) on the same inputs")
     ap.add_argument("--cpu-rows", type=int, default=24576,
                     help="rows of the CPU-oracle sample")
     ap.add_argument("--seed", type=int, default=None)
@@ -416,26 +426,18 @@ def run_ours(args):
     variants = leg(args.skip_variants, run_variants, w, q, k, v, idx, work, flush, args)
     # dense-causal-equivalent run: same Q/K/V, every causal block listed
     dense = leg(args.skip_dense, run_dense, w, q, k, v, out, lse, flush, args, t_ms)
+    # dense causal attention (tcgen05 flash kernel) on the same Q/K/V
+    dense_fa = leg(args.skip_dense_fa, run_dense_fa, w, q, k, v, work, flush, args, t_ms)
 
+    # the gather ceiling: the forward's own TMA copies from the L2-resident
+    # K/V of one group, nothing else (measured on this GPU, in this run)
+    ceiling = run_leg(not args.skip_l2_ceiling, run_l2_ceiling, w, k, v, idx, work, flush, dev)
     peaks = load_peaks()
-    t_roof = max(work["flops"] / (peaks["bf16_tflops"] * 1e12),
-                 work["gathered_bytes"] / (peaks["hbm_gbs"] * 1e9))
-    per_launch_bytes = work["gathered_bytes"]
-    achieved = per_launch_bytes / (statistics.mean(times) * 1e-3) / 1e9
-    roofline = {
-        "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-        "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(w.name),
-        "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-        "t_roofline_ms": t_roof * 1e3,
-        "flop_frac_of_tensor_peak": (work["flops"] / (statistics.mean(times) * 1e-3))
-                                     / (peaks["bf16_tflops"] * 1e12),
-        "note": "achieved = gathered K/V bytes (whole selected blocks) / kernel time; "
-                "blocks are re-read from L2, so it can exceed HBM bandwidth",
-    }
-    prof = profiled(w.name)
-    if "l2_to_sm_busy_pct" in prof:
-        roofline["l2_to_sm_busy_pct"] = prof["l2_to_sm_busy_pct"]
-        roofline["l2_to_sm_source"] = prof.get("summary", "")
+    roofline = make_roofline(w, work, statistics.mean(times), peaks, ceiling)
+    if dense_fa and "ms_per_step" in dense_fa and ceiling and "peak_gbs" in ceiling:
+        t_floor = work["gathered_bytes"] / (ceiling["peak_gbs"] * 1e9) * 1e3
+        dense_fa["gather_floor_ms"] = t_floor
+        dense_fa["speedup_bound_at_floor"] = dense_fa["ms_per_step"] / t_floor
     if rank != 0:
         return 0
     line = {
@@ -451,8 +453,11 @@ def run_ours(args):
                    "accumulate": "fp32"},
         "gathered_gbs": gbs,
         "flops_per_step": work["flops"], "gathered_bytes_per_step": work["gathered_bytes"],
+        "speedup_vs_dense_fa": dense_fa.get("speedup") if dense_fa else None,
+        "dense_fa": dense_fa,
         "speedup_vs_dense_causal": dense.get("speedup") if dense else None,
         "dense_causal": dense,
+        "l2_ceiling": ceiling,
         "backward": backward,
         "variants": variants,
         "two_pass": two_pass,
@@ -471,6 +476,82 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def make_roofline(w, work, t_kernel_ms, peaks, ceiling):
+    """Roofline of the headline kernel. Its K/V blocks are served from L2
+    (one group's K/V stays resident while its queries run), so the bound is
+    the gather ceiling measured by the probe in this run; the ratio to HBM
+    bandwidth is kept beside it."""
+    achieved = work["gathered_bytes"] / (t_kernel_ms * 1e-3) / 1e9
+    t_roof_hbm = max(work["flops"] / (peaks["bf16_tflops"] * 1e12),
+                     work["gathered_bytes"] / (peaks["hbm_gbs"] * 1e9))
+    hbm = {"achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": achieved / peaks["hbm_gbs"], "t_roofline_ms": t_roof_hbm * 1e3,
+           "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
+    common = {
+        "traffic": profiled_traffic(w.name),
+        "traffic_note": "ncu DRAM bytes per launch (read + write); gathered bytes come from L2",
+        "flop_frac_of_tensor_peak": (work["flops"] / (t_kernel_ms * 1e-3))
+                                     / (peaks["bf16_tflops"] * 1e12),
+        "units_per_launch": work["gathered_bytes"],
+        "unit_note": "achieved = gathered K/V bytes (whole selected blocks, exact from the "
+                     "index tensor) / mean CUDA-event time of the launch",
+    }
+    if ceiling and "peak_gbs" in ceiling:
+        peak = ceiling["peak_gbs"]
+        return dict({"bound": "l2", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "peak_source": "measured in this run: the best of the gather probes "
+                                    "(the forward's TMA copies alone on every SM, random "
+                                    "blocks and the workload's own rows; l2_ceiling key), "
+                                    f"from {ceiling['peak_from']}",
+                     "t_floor_ms": work["gathered_bytes"] / (peak * 1e9) * 1e3,
+                     "hbm": hbm}, **common)
+    return dict({"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                 "unit": "GB/s", "frac": hbm["frac"], "peak_source": hbm["peak_source"],
+                 "t_roofline_ms": hbm["t_roofline_ms"],
+                 "note": "gather ceiling not measured; blocks are re-read from L2, so the "
+                         "fraction of HBM bandwidth can exceed 1"}, **common)
+
+
+def run_l2_ceiling(w, k, v, idx, work, flush, dev):
+    """The gather ceiling for this workload: random blocks of its K/V (group
+    0), and its own index rows' copies alone (no computation)."""
+    from nsa_block_selection_gb300 import l2_ceiling
+
+    return l2_ceiling.measure(k, v, w.block_size, g=0, idx=idx,
+                              gathered_bytes=work["gathered_bytes"], flush=flush,
+                              clocks=ClockSampler(gpu_smi_id(dev)))
+
+
+def run_dense_fa(w, q, k, v, work, flush, args, t_sparse_ms):
+    """Dense causal attention at the same sequence length on the same Q/K/V:
+    nsa_swa_fwd with window (-1, 0) (tcgen05 flash kernel, every key <= the
+    query), the "dense FA at same seqlen" of the page's performance target.
+    FLOPs: 4*D per (query, head, key <= query)."""
+    import torch
+
+    from nsa_block_selection_gb300 import swa_fwd
+
+    if w.M != w.N:
+        return {"error": "dense causal attention is timed for M == N only"}
+    o16 = torch.empty((w.B, w.M, w.H, w.D), dtype=q.dtype, device=q.device)
+    lse = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=q.device)
+
+    def step():
+        swa_fwd(q, k, v, window=(-1, 0), scale=w.scale, out=o16, lse=lse)
+
+    steps = max(3, args.steps // 6)
+    times, _ = time_steps(step, steps, 3, flush, lambda: None)
+    t = statistics.mean(times)
+    flops = 4 * w.D * w.H * w.B * swa_pairs(w.M, w.N, -1, 0)
+    del o16, lse
+    torch.cuda.empty_cache()
+    return {"kernel": "nsa_swa_fwd, window (-1, 0), fp16 in / fp16 O, same Q/K/V",
+            "ms_per_step": t, "tflops": flops / (t * 1e-3) / 1e12, "flops": flops,
+            "speedup": t / t_sparse_ms, "steps": steps,
+            "work_ratio": flops / work["flops"]}
 
 
 def swa_pairs(M, N, left, right):

@@ -310,13 +310,18 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V,
  * Arguments, layouts and results are those of nsa_sel_attn_bwd without the
  * workspace. A problem whose scratch (nsa_sel_attn_bwd_workspace_bytes)
  * exceeds 64 MiB is rejected with NSA_ERR_SCRATCH before anything is
- * launched. The call allocates and frees nothing. The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.
- * Every call uses the same array and finds the previous call's contents in
- * it; the parts that must start at zero are cleared on the call's stream.
- * Calls whose work overlaps on the GPU (on different streams, or from
- * different threads on one device) race on the array: serialise them.
+ * launched; a problem without queries (B == 0 or M == 0) needs no scratch
+ * and only zeroes dK and dV. The call allocates and frees nothing. Every
+ * call looks up the array's device address in the current device's context
+ * (cudaGetSymbolAddress: a host-side query, no allocation, no
+ * synchronisation), so a context created anew after cudaDeviceReset gets
+ * its own array. The first lookup on a device may load the library's
+ * device code: make the first call on each device before any stream
+ * capture. Every call uses the same array and finds the previous call's
+ * contents in it; the parts that must start at zero are cleared on the
+ * call's stream. Calls whose work overlaps on the GPU (on different
+ * streams, or from different threads on one device) race on the array:
+ * serialise them.
  */
 int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
                              const int32_t* block_indices, const float* O, const float* LSE,
@@ -416,6 +421,79 @@ int nsa_sync_status(void* stream);
  * other memory. Returns NSA_ERR_SHAPE for a limit out of range.
  */
 int nsa_selftest_wait_timeout(int64_t limit_ns, void* stream);
+
+/*
+ * nsa_probe_l2_gather -- measurement kernel: the gather of
+ * nsa_sel_attn_fwd with nothing else, to measure the ceiling that gather
+ * meets ("[wave] NSA: selection attention forward kernel", section "MI350
+ * considerations": the irregular block gather is the most
+ * performance-critical part of the kernel).
+ *
+ *   K, V            device, IEEE fp16, [N, G, D] (one batch), 16-byte aligned
+ *   N               >= block_size; blocks 0 .. floor(N/block_size)-1 are drawn
+ *   G, g            KV groups; the group read (0 <= g < G), or -1 for a
+ *                   group drawn with every block (all groups interleaved)
+ *   D               64 or 128
+ *   block_size      32 or 64
+ *   ctas            grid size (1 .. 2^31); size it as SMs x CTAs per SM
+ *   warps_per_cta   1 .. 32
+ *   slots_per_warp  1 .. 16 tiles each warp keeps in flight
+ *   loads_per_warp  tiles each warp copies (>= 0)
+ *   rows_per_box    key rows per TMA box and per tile: 16 (the forward's), 32
+ *                   or 64, at most block_size
+ *   seed            block draw seed
+ *   cta_record      device int64 [ctas, 3] written with (SM id, start ns,
+ *                   end ns) of every CTA (%globaltimer), or NULL
+ *
+ * Each warp copies loads_per_warp tiles of rows_per_box key rows x D (TMA
+ * boxes of rows_per_box x 64, 128-byte swizzle, L2 evict_last: with 16 rows,
+ * the forward's copies) into
+ * shared memory, alternating K and V and walking the 16-key tiles of
+ * randomly drawn blocks, keeping slots_per_warp copies in flight and doing
+ * nothing with the data. The bytes moved, nsa_probe_l2_gather_bytes(), over
+ * the kernel's time is the gather bandwidth this GPU delivers for that
+ * access pattern and in-flight depth. Shared memory per CTA is
+ * warps x slots x D/64 x rows_per_box x 128 B (+ 1 KB + barriers), within
+ * 227 KB (else NSA_ERR_SHAPE). Asynchronous; allocates nothing. Errors:
+ * NSA_ERR_NULL, NSA_ERR_ALIGN, NSA_ERR_HEAD_DIM, NSA_ERR_BLOCK_SIZE,
+ * NSA_ERR_SHAPE, NSA_ERR_LAUNCH. A timed-out wait is reported by
+ * nsa_sync_status.
+ */
+int nsa_probe_l2_gather(const void* K, const void* V, int64_t N, int64_t G, int64_t D,
+                        int64_t g, int block_size, int64_t ctas, int warps_per_cta,
+                        int slots_per_warp, int64_t loads_per_warp, int rows_per_box,
+                        uint32_t seed, int64_t* cta_record, void* stream);
+
+/* Bytes nsa_probe_l2_gather moves for these arguments (negative nsa_status
+ * for invalid ones). Pure host arithmetic. */
+int64_t nsa_probe_l2_gather_bytes(int64_t D, int64_t ctas, int warps_per_cta,
+                                  int64_t loads_per_warp, int rows_per_box);
+
+/*
+ * nsa_probe_gather_rows -- measurement kernel: exactly the copies
+ * nsa_sel_attn_fwd makes for these index rows, and nothing else.
+ *
+ *   K, V, block_indices, B, M, N, G, D, T, block_size
+ *                   as for nsa_sel_attn_fwd (H plays no part: the copies are
+ *                   per (b, m, g) row); same checks and errors
+ *   ctas            grid size (1 .. 2^31 - 1)
+ *   warps_per_cta   1 .. 32
+ *   slots_per_warp  1 .. 16 copies each warp keeps in flight
+ *
+ * Every warp takes the (b, g, m) rows w, w + W, w + 2W, ... (W warps in the
+ * grid, m fastest) and walks each row as the forward does -- padding,
+ * out-of-range ids and blocks after the query skipped, the 16-key tiles of
+ * each selected block that start at or before the query -- copying the K
+ * tile and then the V tile of every 16-key tile into shared memory (TMA
+ * boxes of 16 x 64, 128-byte swizzle, L2 evict_last). It moves the bytes of
+ * every whole 16-key tile the forward gathers, back to back across rows,
+ * so the forward's gathered bytes over this kernel's time bound the
+ * forward's gather rate from above for these rows. Shared memory and
+ * asynchrony as nsa_probe_l2_gather; allocates nothing.
+ */
+int nsa_probe_gather_rows(const void* K, const void* V, const int32_t* block_indices, int64_t B,
+                          int64_t M, int64_t N, int64_t G, int64_t D, int64_t T, int block_size,
+                          int64_t ctas, int warps_per_cta, int slots_per_warp, void* stream);
 
 #ifdef __cplusplus
 }

@@ -9,7 +9,6 @@ is no fallback: if the library is missing, calls raise.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from typing import Optional
 
@@ -24,7 +23,8 @@ EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sel_attn
            "nsa_selftest_wait_timeout", "nsa_sel_attn_fwd_host_workspace_bytes",
            "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd",
            "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks", "nsa_swa_fwd",
-           "nsa_sel_attn_fwd_shared_workspace_bytes", "nsa_sel_attn_fwd_shared")
+           "nsa_sel_attn_fwd_shared_workspace_bytes", "nsa_sel_attn_fwd_shared",
+           "nsa_probe_l2_gather", "nsa_probe_l2_gather_bytes", "nsa_probe_gather_rows")
 
 _lib = None
 
@@ -89,6 +89,14 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_fwd_host.restype = c_int
     lib.nsa_sel_attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                           i64, c_int, ctypes.c_float, vp, i64, i64, vp]
+    lib.nsa_probe_l2_gather.restype = c_int
+    lib.nsa_probe_l2_gather.argtypes = [vp, vp, i64, i64, i64, i64, c_int, i64, c_int, c_int,
+                                        i64, c_int, ctypes.c_uint32, vp, vp]
+    lib.nsa_probe_l2_gather_bytes.restype = i64
+    lib.nsa_probe_l2_gather_bytes.argtypes = [i64, i64, c_int, i64, c_int]
+    lib.nsa_probe_gather_rows.restype = c_int
+    lib.nsa_probe_gather_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, i64,
+                                          c_int, c_int, vp]
     if path is None:
         _lib = lib
     return lib
@@ -141,7 +149,7 @@ def sel_attn_fwd(q, k, v, block_indices, block_size: int, scale: Optional[float]
         raise ValueError("lse must be contiguous fp32 [B, H, M]")
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    sc = float(scale) if scale is not None else 0.0  # the ABI: <= 0 selects 1/sqrt(D)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out), _ptr(lse), B, M, N, H,
             G, D, T, int(block_size), sc)
     if not all(t.is_contiguous() or t.numel() == 0 for t in (q, k, v, out)):
@@ -195,7 +203,7 @@ def sel_attn_fwd_shared(q, k, v, block_indices, block_size: int, scale: Optional
                                 device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    sc = float(scale) if scale is not None else 0.0  # the ABI: <= 0 selects 1/sqrt(D)
     st = lib.nsa_sel_attn_fwd_shared(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out),
                                      _ptr(lse), B, M, N, H, G, D, T, int(block_size), sc,
                                      _dtype_code(q.dtype), _ptr(workspace), workspace.numel(),
@@ -274,7 +282,7 @@ def sel_attn_fwd_host(q, k, v, block_indices, block_size: int, scale: Optional[f
         raise ValueError("out must be [B, M, H, D] and lse [B, H, M]")
     if stream is None:
         stream = torch.cuda.current_stream(device)
-    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    sc = float(scale) if scale is not None else 0.0  # the ABI: <= 0 selects 1/sqrt(D)
     st = lib.nsa_sel_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out),
                                    _ptr(lse), B, M, N, H, G, D, T, int(block_size), sc,
                                    workspace.data_ptr(), workspace.numel(), int(chunk_m),
@@ -320,7 +328,7 @@ def sel_attn_bwd(q, k, v, block_indices, o, lse, do, block_size: int,
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    sc = float(scale) if scale is not None else 0.0  # the ABI: <= 0 selects 1/sqrt(D)
     st = lib.nsa_sel_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(o), _ptr(lse),
                               _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, M, N, H, G, D, T,
                               int(block_size), sc, workspace.data_ptr(), workspace.numel(),
@@ -415,10 +423,71 @@ def swa_fwd(q, k, v, window=(-1, -1), scale: Optional[float] = None, out=None, l
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     left, right = (int(window[0]), int(window[1])) if window is not None else (-1, -1)
-    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    sc = float(scale) if scale is not None else 0.0  # the ABI: <= 0 selects 1/sqrt(D)
     st = lib.nsa_swa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, M, N, H, Hkv, D,
                          left, right, sc, _dtype_code(q.dtype),
                          ctypes.c_void_p(stream.cuda_stream))
     if st != NSA_OK:
         raise NsaError(st, "nsa_swa_fwd")
     return out, lse
+
+
+def probe_l2_gather(k, v, g: int, block_size: int, ctas: int, warps_per_cta: int,
+                    slots_per_warp: int, loads_per_warp: int, seed: int = 1, record=None,
+                    stream=None, rows_per_box: int = 16) -> int:
+    """Launch the gather-bandwidth probe (nsa_probe_l2_gather) on K, V
+    [N, G, D] fp16 (one batch) and return the bytes it moves. ``record``: an
+    int64 CUDA tensor [ctas, 3] for per-CTA (SM id, start ns, end ns), or
+    None."""
+    import torch
+
+    lib = load()
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype != torch.float16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError(f"{name} must be a contiguous fp16 CUDA tensor [N, G, D]")
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must have the same shape")
+    N, G, D = k.shape
+    if record is not None and (record.dtype != torch.int64 or not record.is_cuda
+                               or tuple(record.shape) != (ctas, 3)
+                               or not record.is_contiguous()):
+        raise ValueError("record must be a contiguous int64 CUDA tensor [ctas, 3]")
+    if stream is None:
+        stream = torch.cuda.current_stream(k.device)
+    st = lib.nsa_probe_l2_gather(_ptr(k), _ptr(v), N, G, D, int(g), int(block_size), int(ctas),
+                                 int(warps_per_cta), int(slots_per_warp), int(loads_per_warp),
+                                 int(rows_per_box), int(seed) & 0xFFFFFFFF, _ptr(record),
+                                 ctypes.c_void_p(stream.cuda_stream))
+    if st != NSA_OK:
+        raise NsaError(st, "nsa_probe_l2_gather")
+    n = lib.nsa_probe_l2_gather_bytes(D, int(ctas), int(warps_per_cta), int(loads_per_warp),
+                                      int(rows_per_box))
+    if n < 0:
+        raise NsaError(int(n), "nsa_probe_l2_gather_bytes")
+    return int(n)
+
+
+def probe_gather_rows(k, v, block_indices, block_size: int, ctas: int, warps_per_cta: int,
+                      slots_per_warp: int, stream=None) -> None:
+    """Launch the index-driven gather probe (nsa_probe_gather_rows): the
+    forward's copies for these rows alone. k, v: fp16 [B, N, G, D];
+    block_indices: int32 [B, M, G, T], all contiguous on one CUDA device."""
+    import torch
+
+    lib = load()
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype != torch.float16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous fp16 CUDA tensor [B, N, G, D]")
+    if block_indices.dtype != torch.int32 or not block_indices.is_contiguous():
+        raise ValueError("block_indices must be contiguous int32 [B, M, G, T]")
+    B, N, G, D = k.shape
+    Bi, M, Gi, T = block_indices.shape
+    if (Bi, Gi) != (B, G) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch: k/v [B, N, G, D], block_indices [B, M, G, T]")
+    if stream is None:
+        stream = torch.cuda.current_stream(k.device)
+    st = lib.nsa_probe_gather_rows(_ptr(k), _ptr(v), _ptr(block_indices), B, M, N, G, D, T,
+                                   int(block_size), int(ctas), int(warps_per_cta),
+                                   int(slots_per_warp), ctypes.c_void_p(stream.cuda_stream))
+    if st != NSA_OK:
+        raise NsaError(st, "nsa_probe_gather_rows")

@@ -34,12 +34,13 @@ int nsa_version(void) { return 200; }
 int nsa_sync_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return NSA_ERR_LAUNCH;
-  unsigned int fwd = 0u, bwd = 0u, swa = 0u, shr = 0u;
+  unsigned int fwd = 0u, bwd = 0u, swa = 0u, shr = 0u, prb = 0u;
   if (nsa::fwd_read_and_clear_status(&fwd) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::bwd_read_and_clear_status(&bwd) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::swa_read_and_clear_status(&swa) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::shared_read_and_clear_status(&shr) != NSA_OK) return NSA_ERR_LAUNCH;
-  return (fwd | bwd | swa | shr) ? NSA_ERR_TIMEOUT : NSA_OK;
+  if (nsa::probe_read_and_clear_status(&prb) != NSA_OK) return NSA_ERR_LAUNCH;
+  return (fwd | bwd | swa | shr | prb) ? NSA_ERR_TIMEOUT : NSA_OK;
 }
 
 }  // extern "C"

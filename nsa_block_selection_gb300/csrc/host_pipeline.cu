@@ -85,7 +85,7 @@ HostPlan make_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_
 struct CallResources {
   cudaStream_t up = nullptr, dn = nullptr, fw2 = nullptr;
   cudaEvent_t start = nullptr, up_ev[2] = {nullptr, nullptr}, fw_ev[2] = {nullptr, nullptr},
-              dn_ev[2] = {nullptr, nullptr};
+              dn_ev[2] = {nullptr, nullptr}, join[3] = {nullptr, nullptr, nullptr};
   bool ok = true;
 
   CallResources() {
@@ -93,6 +93,8 @@ struct CallResources {
          cudaStreamCreateWithFlags(&dn, cudaStreamNonBlocking) == cudaSuccess &&
          cudaStreamCreateWithFlags(&fw2, cudaStreamNonBlocking) == cudaSuccess &&
          cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 3 && ok; ++i)
+      ok = cudaEventCreateWithFlags(&join[i], cudaEventDisableTiming) == cudaSuccess;
     for (int s = 0; s < 2 && ok; ++s)
       ok = cudaEventCreateWithFlags(&up_ev[s], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&fw_ev[s], cudaEventDisableTiming) == cudaSuccess &&
@@ -104,6 +106,8 @@ struct CallResources {
       if (fw_ev[s]) cudaEventDestroy(fw_ev[s]);
       if (dn_ev[s]) cudaEventDestroy(dn_ev[s]);
     }
+    for (int i = 0; i < 3; ++i)
+      if (join[i]) cudaEventDestroy(join[i]);
     if (start) cudaEventDestroy(start);
     if (up) cudaStreamDestroy(up);
     if (dn) cudaStreamDestroy(dn);
@@ -168,6 +172,7 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
             cudaStreamWaitEvent(r.up, r.start, 0) == cudaSuccess &&
             cudaStreamWaitEvent(r.dn, r.start, 0) == cudaSuccess &&
             cudaStreamWaitEvent(r.fw2, r.start, 0) == cudaSuccess;
+  int status = NSA_OK;
   int64_t kv_done = 0;
   for (int64_t c = 0; c < pl.nchunks && ok; ++c) {
     const int s = static_cast<int>(c & 1);
@@ -209,7 +214,10 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
                                   T > 0 ? reinterpret_cast<const int32_t*>(dI) : nullptr, dO,
                                   dL, B, mc, N, H, G, D, T, m0, block_size, scale, NSA_F16,
                                   NSA_F32, nullptr, fs);
-    if (rc != NSA_OK) return rc;
+    if (rc != NSA_OK) {
+      status = rc;
+      break;
+    }
     ok = cudaEventRecord(r.fw_ev[s], fs) == cudaSuccess;
 
     // download: O rows [m0, m0+mc) of every batch, LSE columns of every (b, h)
@@ -220,10 +228,19 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
                       r.dn);
     ok = ok && cudaEventRecord(r.dn_ev[s], r.dn) == cudaSuccess;
   }
-  // the caller's stream completes only after every download
-  for (int s = 0; s < 2 && ok; ++s)
-    if (pl.nchunks > s) ok = cudaStreamWaitEvent(st, r.dn_ev[s], 0) == cudaSuccess;
-  return ok ? NSA_OK : NSA_ERR_LAUNCH;
+  // The caller's stream completes only after everything this call queued on
+  // its internal streams, on every path: copies that read or write the
+  // caller's host buffers are never left in flight behind an error return.
+  // If the join itself fails, the internal streams are waited for here.
+  const cudaStream_t internal[3] = {r.up, r.fw2, r.dn};
+  bool joined = true;
+  for (int i = 0; i < 3; ++i)
+    joined = joined && cudaEventRecord(r.join[i], internal[i]) == cudaSuccess &&
+             cudaStreamWaitEvent(st, r.join[i], 0) == cudaSuccess;
+  if (!joined)
+    for (int i = 0; i < 3; ++i) cudaStreamSynchronize(internal[i]);
+  if (status != NSA_OK) return status;
+  return ok && joined ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
 }  // extern "C"

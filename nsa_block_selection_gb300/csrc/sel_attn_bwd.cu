@@ -38,7 +38,6 @@
 
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -1422,21 +1421,78 @@ int bwd_read_and_clear_status(unsigned int* value) { return read_and_clear_statu
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB per device
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device. In host code
-// the array's name is only a host-side handle, never a device address; the
-// address is looked up once per device, with that device current.
+// Device address of g_noalloc_scratch in the current device's context. In
+// host code the array's name is only a host-side handle, never a device
+// address. The address is looked up on every call (a host-side query that
+// allocates nothing and does not synchronise), so a context created anew
+// after cudaDeviceReset is never served a stale address.
 static void* noalloc_scratch_address() {
-  static std::mutex mu;
-  static void* addr[128] = {};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = ptr;
-  }
-  return addr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  return ptr;
+}
+
+// Size checks of both backward entry points; fills the scratch plan.
+static int bwd_check_sizes(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
+                           int64_t T, int block_size, BwdPlan* pl) {
+  const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
+  if (chk != NSA_OK) return chk;
+  if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
+  *pl = bwd_plan(B, M, N, H, G, D, T, block_size);
+  if (pl->L > (int64_t(1) << 31) - 2) return NSA_ERR_SHAPE;
+  return NSA_OK;
+}
+
+// Pointer checks of both backward entry points for a problem with queries
+// (B, M > 0): NSA_ERR_NULL, NSA_ERR_ALIGN or NSA_OK. `workspace` is checked
+// for alignment when given.
+static int bwd_check_pointers(const void* Q, const void* K, const void* V, const int32_t* idx,
+                              const float* O, const float* LSE, const float* dO, const float* dQ,
+                              const float* dK, const float* dV, int64_t N, int64_t T,
+                              const void* workspace) {
+  if (!Q || !O || !LSE || !dO || !dQ) return NSA_ERR_NULL;
+  if (N > 0 && (!K || !V || !dK || !dV)) return NSA_ERR_NULL;
+  if (T > 0 && !idx) return NSA_ERR_NULL;
+  auto mis = [](const void* ptr, uintptr_t a) {
+    return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+  };
+  if (mis(Q, 16) || mis(K, 16) || mis(V, 16) || mis(O, 16) || mis(dO, 16) || mis(dQ, 16) ||
+      mis(dK, 16) || mis(dV, 16) || mis(LSE, 4) || mis(idx, 4) || mis(workspace, 256))
+    return NSA_ERR_ALIGN;
+  return NSA_OK;
+}
+
+// Validated arguments -> the kernels' problem description, then the launch
+// of the three stages with `ws` as scratch.
+static int run_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
+                   const float* O, const float* LSE, const float* dO, float* dQ, float* dK,
+                   float* dV, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
+                   int64_t T, int block_size, float scale, const BwdPlan& pl, uint8_t* ws,
+                   cudaStream_t st) {
+  BwdProblem p;
+  p.Q = static_cast<const __half*>(Q);
+  p.idx = idx;
+  p.O = O;
+  p.LSE = LSE;
+  p.dO = dO;
+  p.dQ = dQ;
+  p.dK = dK;
+  p.dV = dV;
+  p.M = M;
+  p.N = N;
+  p.H = H;
+  p.G = G;
+  p.T = T;
+  p.B = B;
+  p.hpg = static_cast<int>(H / G);
+  p.nsub = head_subgroups(p.hpg);
+  p.units = B * G * p.nsub * M;
+  p.bs = block_size;
+  p.nblk = static_cast<int>((N + block_size - 1) / block_size);
+  p.L = static_cast<int>(pl.L);
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  p.sl2 = p.scale * 1.4426950408889634f;
+  return D == 64 ? launch_bwd<64>(p, K, V, ws, pl, st) : launch_bwd<128>(p, K, V, ws, pl, st);
 }
 
 }  // namespace nsa
@@ -1445,10 +1501,10 @@ extern "C" {
 
 int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G,
                                          int64_t D, int64_t T, int block_size) {
-  const int chk = nsa::check_sizes(B, M, N, H, G, D, T, block_size);
+  nsa::BwdPlan pl;
+  const int chk = nsa::bwd_check_sizes(B, M, N, H, G, D, T, block_size, &pl);
   if (chk != NSA_OK) return chk;
-  if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
-  return static_cast<int64_t>(nsa::bwd_plan(B, M, N, H, G, D, T, block_size).total);
+  return static_cast<int64_t>(pl.total);
 }
 
 int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* block_indices,
@@ -1457,11 +1513,9 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t*
                      int64_t T, int block_size, float scale, void* workspace,
                      int64_t workspace_bytes, void* stream) {
   using namespace nsa;
-  const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
+  BwdPlan pl;
+  const int chk = bwd_check_sizes(B, M, N, H, G, D, T, block_size, &pl);
   if (chk != NSA_OK) return chk;
-  if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
-  const BwdPlan pl = bwd_plan(B, M, N, H, G, D, T, block_size);
-  if (pl.L > (int64_t(1) << 31) - 2) return NSA_ERR_SHAPE;
   if (B == 0 || (M == 0 && N == 0)) return NSA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (M == 0) {  // no query: every key gradient is zero
@@ -1471,42 +1525,13 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t*
       return NSA_ERR_LAUNCH;
     return NSA_OK;
   }
-  if (!Q || !O || !LSE || !dO || !dQ) return NSA_ERR_NULL;
-  if (N > 0 && (!K || !V || !dK || !dV)) return NSA_ERR_NULL;
-  if (T > 0 && !block_indices) return NSA_ERR_NULL;
+  int rc = bwd_check_pointers(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, N, T, nullptr);
+  if (rc != NSA_OK) return rc;
   if (!workspace || workspace_bytes < static_cast<int64_t>(pl.total)) return NSA_ERR_WORKSPACE;
-  auto mis = [](const void* ptr, uintptr_t a) {
-    return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
-  };
-  if (mis(Q, 16) || mis(K, 16) || mis(V, 16) || mis(O, 16) || mis(dO, 16) || mis(dQ, 16) ||
-      mis(dK, 16) || mis(dV, 16) || mis(LSE, 4) || mis(block_indices, 4) || mis(workspace, 256))
-    return NSA_ERR_ALIGN;
-
-  BwdProblem p;
-  p.Q = static_cast<const __half*>(Q);
-  p.idx = block_indices;
-  p.O = O;
-  p.LSE = LSE;
-  p.dO = dO;
-  p.dQ = dQ;
-  p.dK = dK;
-  p.dV = dV;
-  p.M = M;
-  p.N = N;
-  p.H = H;
-  p.G = G;
-  p.T = T;
-  p.B = B;
-  p.hpg = static_cast<int>(H / G);
-  p.nsub = head_subgroups(p.hpg);
-  p.units = B * G * p.nsub * M;
-  p.bs = block_size;
-  p.nblk = static_cast<int>((N + block_size - 1) / block_size);
-  p.L = static_cast<int>(pl.L);
-  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
-  p.sl2 = p.scale * 1.4426950408889634f;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  return D == 64 ? launch_bwd<64>(p, K, V, ws, pl, st) : launch_bwd<128>(p, K, V, ws, pl, st);
+  rc = bwd_check_pointers(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, N, T, workspace);
+  if (rc != NSA_OK) return rc;
+  return run_bwd(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, B, M, N, H, G, D, T,
+                 block_size, scale, pl, static_cast<uint8_t*>(workspace), st);
 }
 
 int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
@@ -1515,55 +1540,23 @@ int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
                              int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
                              int block_size, float scale, void* stream) {
   using namespace nsa;
-  const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
+  BwdPlan pl;
+  const int chk = bwd_check_sizes(B, M, N, H, G, D, T, block_size, &pl);
   if (chk != NSA_OK) return chk;
-  if (B * M * G * T > (int64_t(1) << 31) - 1) return NSA_ERR_SHAPE;
-  const BwdPlan pl = bwd_plan(B, M, N, H, G, D, T, block_size);
-  if (pl.L > (int64_t(1) << 31) - 2) return NSA_ERR_SHAPE;
-  if (pl.total > kNoAllocScratchBytes) return NSA_ERR_SCRATCH;
   if (B == 0 || M == 0) {
     // no query, so no scratch: the workspace entry point zeroes dK and dV
     return nsa_sel_attn_bwd(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, B, M, N, H, G, D, T,
                             block_size, scale, nullptr, 0, stream);
   }
-  if (!Q || !O || !LSE || !dO || !dQ) return NSA_ERR_NULL;
-  if (N > 0 && (!K || !V || !dK || !dV)) return NSA_ERR_NULL;
-  if (T > 0 && !block_indices) return NSA_ERR_NULL;
-  auto mis = [](const void* ptr, uintptr_t a) {
-    return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
-  };
-  if (mis(Q, 16) || mis(K, 16) || mis(V, 16) || mis(O, 16) || mis(dO, 16) || mis(dQ, 16) ||
-      mis(dK, 16) || mis(dV, 16) || mis(LSE, 4) || mis(block_indices, 4))
-    return NSA_ERR_ALIGN;
+  if (pl.total > kNoAllocScratchBytes) return NSA_ERR_SCRATCH;
+  const int rc =
+      bwd_check_pointers(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, N, T, nullptr);
+  if (rc != NSA_OK) return rc;
   void* scratch = noalloc_scratch_address();
   if (scratch == nullptr) return NSA_ERR_LAUNCH;
-
-  BwdProblem p;
-  p.Q = static_cast<const __half*>(Q);
-  p.idx = block_indices;
-  p.O = O;
-  p.LSE = LSE;
-  p.dO = dO;
-  p.dQ = dQ;
-  p.dK = dK;
-  p.dV = dV;
-  p.M = M;
-  p.N = N;
-  p.H = H;
-  p.G = G;
-  p.T = T;
-  p.B = B;
-  p.hpg = static_cast<int>(H / G);
-  p.nsub = head_subgroups(p.hpg);
-  p.units = B * G * p.nsub * M;
-  p.bs = block_size;
-  p.nblk = static_cast<int>((N + block_size - 1) / block_size);
-  p.L = static_cast<int>(pl.L);
-  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
-  p.sl2 = p.scale * 1.4426950408889634f;
-  uint8_t* ws = static_cast<uint8_t*>(scratch);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return D == 64 ? launch_bwd<64>(p, K, V, ws, pl, st) : launch_bwd<128>(p, K, V, ws, pl, st);
+  return run_bwd(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, B, M, N, H, G, D, T,
+                 block_size, scale, pl, static_cast<uint8_t*>(scratch),
+                 static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

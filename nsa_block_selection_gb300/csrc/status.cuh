@@ -8,5 +8,6 @@ int fwd_read_and_clear_status(unsigned int* value);  // selection forward (+ wai
 int bwd_read_and_clear_status(unsigned int* value);  // selection backward
 int swa_read_and_clear_status(unsigned int* value);  // sliding-window forward
 int shared_read_and_clear_status(unsigned int* value);  // tile-shared pass of the forward
+int probe_read_and_clear_status(unsigned int* value);   // gather-bandwidth probe
 
 }  // namespace nsa

@@ -70,6 +70,7 @@ __all__ = [
     "sel_attn_rows",
     "sel_attn_fwd",
     "softmax_grad_terms",
+    "softmax_grad_magnitudes",
     "sel_attn_bwd",
     "sel_attn_bwd_dq_rows",
     "sel_attn_bwd_block",
@@ -307,19 +308,38 @@ def softmax_grad_terms(s: np.ndarray, lse: np.ndarray, v: np.ndarray, do: np.nda
     return p, p * (dp - delta[:, None])
 
 
+def softmax_grad_magnitudes(s: np.ndarray, lse: np.ndarray, v: np.ndarray, do: np.ndarray):
+    """p and an upper bound of |dS| for one row, built from absolute values
+    only: |dP_n| <= sum_d |dO_d| |v_nd| and |delta| <= sum_d |dO_d|
+    sum_n p_n |v_nd| (since O = sum_n p_n v_n), so |dS_n| <= p_n (those two
+    sums added). Each term is the magnitude an operand's relative error is
+    taken of, so a rounding error of relative size r in dO, V, O or dS moves
+    dS_n by at most r times this bound."""
+    p = np.exp(s - lse[:, None])
+    av, ado = np.abs(v), np.abs(do)
+    dp_mag = ado @ av.T
+    delta_mag = (ado * (p @ av)).sum(axis=1)
+    return p, p * (dp_mag + delta_mag[:, None])
+
+
 def _fp16(x: np.ndarray) -> np.ndarray:
     return x.astype(np.float16).astype(np.float64)
 
 
 def sel_attn_bwd(Q, K, V, idx, dO, block_size: int, scale: Optional[float] = None,
-                 emulate_kernel_rounding: bool = False):
+                 emulate_kernel_rounding: bool = False, magnitudes: bool = False):
     """Gradients dQ [B,M,H,D], dK [B,N,G,D], dV [B,N,G,D] (float64) of the
     forward for the upstream gradient dO [B,M,H,D] (LSE is recomputed).
 
     ``emulate_kernel_rounding=True`` rounds to fp16 the operands that enter
     fp16 matrix products on the GPU (dO, P for dV, dS for dQ and dK), all
-    else in float64: it measures what fp16 operands alone cost, the yardstick
-    of the GPU parity tolerance."""
+    else in float64: it measures what fp16 operands alone cost.
+
+    ``magnitudes=True`` returns instead, per element, the sum of the absolute
+    values of the terms that make it up (dS replaced by the bound of
+    :func:`softmax_grad_magnitudes`, q, k, dO by their absolute values): the
+    scale against which the rounding of those terms is measured, per
+    element, in the GPU parity tolerance."""
     B, M, H, D = Q.shape
     N, G = K.shape[1], K.shape[2]
     if scale is None:
@@ -338,7 +358,10 @@ def sel_attn_bwd(Q, K, V, idx, dO, block_size: int, scale: Optional[float] = Non
                 v = np.asarray(Vg[n], dtype=np.float64)
                 do = np.asarray(dO[b, m, heads], dtype=np.float64)
                 s = scores(q, k, scale)
-                if emulate_kernel_rounding:
+                if magnitudes:
+                    p, ds = softmax_grad_magnitudes(s, logsumexp_rows(s), v, do)
+                    q, k, do = np.abs(q), np.abs(k), np.abs(do)
+                elif emulate_kernel_rounding:
                     lse = logsumexp_rows(s)
                     p = np.exp(s - lse[:, None])
                     dp = _fp16(do) @ v.T
@@ -354,9 +377,10 @@ def sel_attn_bwd(Q, K, V, idx, dO, block_size: int, scale: Optional[float] = Non
 
 
 def sel_attn_bwd_dq_rows(Q, K, V, idx, dO, rows, block_size: int,
-                         scale: Optional[float] = None) -> np.ndarray:
+                         scale: Optional[float] = None, magnitudes: bool = False) -> np.ndarray:
     """dQ [R, H/G, D] of the listed (b, m, g) rows (each row's dQ depends on
-    that row only)."""
+    that row only); with ``magnitudes=True`` the per-element magnitudes of
+    :func:`sel_attn_bwd` instead."""
     B, M, H, D = Q.shape
     N, G = K.shape[1], K.shape[2]
     if scale is None:
@@ -370,16 +394,21 @@ def sel_attn_bwd_dq_rows(Q, K, V, idx, dO, rows, block_size: int,
         k = np.asarray(Kg[n], dtype=np.float64)
         v = np.asarray(Vg[n], dtype=np.float64)
         s = scores(q, k, scale)
-        _, ds = softmax_grad_terms(s, logsumexp_rows(s), v,
-                                   np.asarray(dO[b, m, heads], dtype=np.float64))
+        do = np.asarray(dO[b, m, heads], dtype=np.float64)
+        if magnitudes:
+            _, ds = softmax_grad_magnitudes(s, logsumexp_rows(s), v, do)
+            k = np.abs(k)
+        else:
+            _, ds = softmax_grad_terms(s, logsumexp_rows(s), v, do)
         out[r] = scale * (ds @ k)
     return out
 
 
 def sel_attn_bwd_block(Q, K, V, idx, dO, b: int, g: int, t: int, block_size: int,
-                       scale: Optional[float] = None):
+                       scale: Optional[float] = None, magnitudes: bool = False):
     """dK, dV rows [keys of block t, D] of (b, g): contributions of every row
-    of group g that selects block t."""
+    of group g that selects block t; with ``magnitudes=True`` the
+    per-element magnitudes of :func:`sel_attn_bwd` instead."""
     B, M, H, D = Q.shape
     N, G = K.shape[1], K.shape[2]
     if scale is None:
@@ -394,9 +423,13 @@ def sel_attn_bwd_block(Q, K, V, idx, dO, b: int, g: int, t: int, block_size: int
         k = np.asarray(Kg[n], dtype=np.float64)
         v = np.asarray(Vg[n], dtype=np.float64)
         s = scores(q, k, scale)
-        p, ds = softmax_grad_terms(s, logsumexp_rows(s), v,
-                                   np.asarray(dO[b, m, heads], dtype=np.float64))
+        do = np.asarray(dO[b, m, heads], dtype=np.float64)
+        if magnitudes:
+            p, ds = softmax_grad_magnitudes(s, logsumexp_rows(s), v, do)
+            q, do = np.abs(q), np.abs(do)
+        else:
+            p, ds = softmax_grad_terms(s, logsumexp_rows(s), v, do)
         sel = (n >= keys[0]) & (n <= keys[-1])
         dK[n[sel] - keys[0]] += scale * (ds[:, sel].T @ q)
-        dV[n[sel] - keys[0]] += p[:, sel].T @ np.asarray(dO[b, m, heads], dtype=np.float64)
+        dV[n[sel] - keys[0]] += p[:, sel].T @ do
     return dK, dV

@@ -16,6 +16,17 @@ O_RTOL = 2e-3
 LSE_ATOL = 1e-3
 
 
+def poisoned(shape, dtype, device="cuda"):
+    """An output buffer the kernel must overwrite: NaN for floating types,
+    a value no index can take (2^31 - 1) for int32. A row the kernel never
+    writes then fails the comparison instead of passing on whatever an
+    earlier result left in recycled memory."""
+    import torch
+
+    fill = float("nan") if dtype.is_floating_point else 2 ** 31 - 1
+    return torch.full(tuple(shape), fill, dtype=dtype, device=device)
+
+
 def to_dev(*arrays):
     import torch
 
@@ -29,7 +40,10 @@ def run_cuda(q, k, v, idx, bs, scale=None, stream=None):
     from nsa_block_selection_gb300 import sel_attn_fwd
 
     t = [x if isinstance(x, torch.Tensor) else to_dev(x)[0] for x in (q, k, v, idx)]
-    out = sel_attn_fwd(*t, bs, scale, stream=stream)
+    B, M, H, D = t[0].shape
+    out = sel_attn_fwd(*t, bs, scale, stream=stream,
+                       out=poisoned((B, M, H, D), torch.float32, t[0].device),
+                       lse=poisoned((B, H, M), torch.float32, t[0].device))
     torch.cuda.synchronize()
     return out
 

@@ -9,7 +9,10 @@ forward), against facts other than the oracle itself:
   the upstream gradients that reach it;
 * an exact invariant: for every query row and head the dS terms sum to zero,
   so dK summed over all keys of a (b, g) vanishes and dQ does not change when
-  a constant vector is added to every key.
+  a constant vector is added to every key;
+* the per-element magnitudes that scale the GPU tolerance: above |gradient|
+  everywhere, equal to dV when every term is non-negative, zero when V is,
+  and a closed form for one visible key.
 """
 
 from __future__ import annotations
@@ -142,9 +145,54 @@ def bpin_dk_sums_to_zero(S):
         _close(a, 2.5 * b, 1e-12, "linearity in dO")
 
 
+def bpin_magnitudes(S):
+    """The per-element magnitudes (``magnitudes=True``) that scale the GPU
+    tolerance: they bound the autograd-pinned gradients from above
+    (triangle inequality); with dO >= 0 every dV term is >= 0, so dV's
+    magnitude equals dV; with V = 0 every dS bound is 0, so dQ's and dK's
+    magnitudes vanish; with one visible key per row p = 1 and dP = delta =
+    dO.v, so the dS bound is 2 |dO.v| for V, dO >= 0 and dQ's magnitude is
+    scale * 2 (dO.v) |k| (a value the exact dQ = 0 never shows)."""
+    w = gen.Workload("t", 2, 30, 30, 4, 2, 8, 4, 4, 1.0, "first_local")
+    idx = gen.make_block_indices(w, 41)
+    Q, K, V = _rand((2, 30, 4, 8), 42), _rand((2, 30, 2, 8), 43), _rand((2, 30, 2, 8), 44)
+    dO = _rand((2, 30, 4, 8), 45)
+    exact = _library_grads(Q, K, V, idx, dO, 4, 0.4)
+    mags = S.sel_attn_bwd(Q, K, V, idx, dO, 4, 0.4, magnitudes=True)
+    for name, e, mg in zip(("dQ", "dK", "dV"), exact, mags):
+        assert np.all(mg >= np.abs(e) - 1e-12), f"{name} magnitude below |gradient|"
+        assert np.all(mg >= 0)
+    dOp = np.abs(dO)
+    _, _, dVp = _library_grads(Q, K, V, idx, dOp, 4, 0.4)
+    _close(S.sel_attn_bwd(Q, K, V, idx, dOp, 4, 0.4, magnitudes=True)[2], dVp, 1e-12,
+           "dV magnitude with dO >= 0")
+    mq, mk, _ = S.sel_attn_bwd(Q, K, np.zeros_like(V), idx, dO, 4, 0.4, magnitudes=True)
+    assert np.all(mq == 0) and np.all(mk == 0)
+    # one visible key per row (as in the single-key pin): query 0 sees key 0
+    B, M, H, G, D, bs = 1, 8, 4, 2, 5, 4
+    Q1, K1 = _rand((B, M, H, D), 51), _rand((B, M, G, D), 52)
+    V1, dO1 = np.abs(_rand((B, M, G, D), 53)), np.abs(_rand((B, M, H, D), 54))
+    idx1 = np.full((B, M, G, 1), -1, np.int32)
+    idx1[0, 0] = 0
+    mq, _, _ = S.sel_attn_bwd(Q1, K1, V1, idx1, dO1, bs, 0.5, magnitudes=True)
+    for h in range(H):
+        g = h // 2
+        want = 0.5 * 2 * float(dO1[0, 0, h] @ V1[0, 0, g]) * np.abs(K1[0, 0, g])
+        _close(mq[0, 0, h], want, 1e-12, "dQ magnitude, one key")
+    # the restricted helpers give the same magnitudes
+    rows = [(1, 29, 0), (0, 3, 1)]
+    got = S.sel_attn_bwd_dq_rows(Q, K, V, idx, dO, rows, 4, 0.4, magnitudes=True)
+    for r, (b, m, g) in enumerate(rows):
+        _close(got[r], mags[0][b, m, 2 * g:2 * g + 2], 1e-12, "dQ rows magnitude")
+    bk, bv = S.sel_attn_bwd_block(Q, K, V, idx, dO, 1, 1, 2, 4, 0.4, magnitudes=True)
+    _close(bk, mags[1][1, 8:12, 1], 1e-12, "dK block magnitude")
+    _close(bv, mags[2][1, 8:12, 1], 1e-12, "dV block magnitude")
+
+
 BPINS = [
     bpin_matches_library_autograd,
     bpin_finite_differences,
     bpin_single_key_closed_form,
     bpin_dk_sums_to_zero,
+    bpin_magnitudes,
 ]

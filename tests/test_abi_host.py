@@ -276,3 +276,51 @@ def test_strided_empty_and_null_strides(lib):
     assert call_strided(lib, None, q=None, k=None, v=None, idx=None, o=None, lse=None, B=0) == 0
     assert call_strided(lib, _contig_strides(), q=None, k=None, v=None, idx=None, o=None,
                         lse=None, M=0) == 0
+
+
+def call_probe(lib, k=FAKE, v=FAKE, N=4096, G=8, D=128, g=0, bs=64, ctas=152, warps=4, slots=2,
+               loads=16, rows=16, rec=None):
+    vp = ctypes.c_void_p
+    return lib.nsa_probe_l2_gather(vp(k), vp(v), N, G, D, g, bs, ctas, warps, slots, loads, rows,
+                                   1, vp(rec), None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(k=None), -1), (dict(v=None), -1), (dict(k=FAKE + 8), -6), (dict(rec=FAKE + 4), -6),
+    (dict(D=96), -4), (dict(bs=16), -3), (dict(N=63), -2), (dict(G=0), -2), (dict(g=8), -2),
+    (dict(g=-2), -2), (dict(ctas=0), -2), (dict(warps=0), -2), (dict(warps=33), -2),
+    (dict(slots=0), -2), (dict(slots=17), -2), (dict(loads=-1), -2),
+    (dict(warps=32, slots=2), -2),  # 256 KB of shared memory per CTA
+    (dict(rows=8), -2), (dict(rows=64, bs=32), -2), (dict(rows=64, warps=8, slots=4), -2),
+])
+def test_probe_rejects_bad_arguments(lib, over, status):
+    assert call_probe(lib, **over) == status
+
+
+def test_probe_bytes(lib):
+    f = lib.nsa_probe_l2_gather_bytes
+    assert f(128, 152, 4, 1000, 16) == 152 * 4 * 1000 * 4096
+    assert f(64, 10, 2, 3, 16) == 10 * 2 * 3 * 2048
+    assert f(128, 1, 1, 1, 64) == 16384
+    assert f(96, 1, 1, 1, 16) == -2
+    assert f(128, 1, 1, 1, 48) == -2
+
+
+def call_rows_probe(lib, k=FAKE, v=FAKE, idx=FAKE, B=1, M=256, N=256, G=8, D=128, T=4, bs=64,
+                    ctas=152, warps=4, slots=2):
+    vp = ctypes.c_void_p
+    return lib.nsa_probe_gather_rows(vp(k), vp(v), vp(idx), B, M, N, G, D, T, bs, ctas, warps,
+                                     slots, None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(k=None), -1), (dict(idx=None), -1), (dict(v=FAKE + 4), -6), (dict(idx=FAKE + 2), -6),
+    (dict(D=96), -4), (dict(bs=16), -3), (dict(M=-1), -2), (dict(ctas=0), -2),
+    (dict(warps=33), -2), (dict(slots=0), -2), (dict(warps=32, slots=2), -2),
+])
+def test_rows_probe_rejects_bad_arguments(lib, over, status):
+    assert call_rows_probe(lib, **over) == status
+
+
+def test_rows_probe_empty_is_a_no_op(lib):
+    assert call_rows_probe(lib, k=None, v=None, idx=None, M=0) == 0

@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 
 import oracle.sel_attn as oracle
-from _parity import compare, gather_rows, sample_rows
+from _parity import compare, gather_rows, poisoned, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -40,8 +40,11 @@ def _run(w, seed, qkv, out, rows=None):
     dt = _torch_dtype(qkv)
     tq, tk, tv = (torch.from_numpy(x).cuda().to(dt) for x in (q, k, v))
     ti = torch.from_numpy(idx).cuda()
-    O, L = sel_attn_fwd(tq, tk, tv, ti, w.block_size, out_dtype=_torch_dtype(out))
-    O32, L32 = sel_attn_fwd(tq, tk, tv, ti, w.block_size)
+    shp, lshp = (w.B, w.M, w.H, w.D), (w.B, w.H, w.M)
+    O, L = sel_attn_fwd(tq, tk, tv, ti, w.block_size, out=poisoned(shp, _torch_dtype(out)),
+                        lse=poisoned(lshp, torch.float32))
+    O32, L32 = sel_attn_fwd(tq, tk, tv, ti, w.block_size, out=poisoned(shp, torch.float32),
+                            lse=poisoned(lshp, torch.float32))
     torch.cuda.synchronize()
     assert O.dtype == _torch_dtype(out) and O32.dtype == torch.float32
     assert torch.equal(L, L32), "LSE depends on the O type"

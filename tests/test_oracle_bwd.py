@@ -41,7 +41,20 @@ def _ds_missing_p(s, lse, v, do):
     return p, dp - (p * dp).sum(axis=1)[:, None]
 
 
+def _mag_without_delta(s, lse, v, do):
+    p = np.exp(s - lse[:, None])
+    return p, p * (np.abs(do) @ np.abs(v).T)
+
+
+def _mag_signed(s, lse, v, do):
+    p = np.exp(s - lse[:, None])
+    dp = do @ v.T
+    return p, p * (dp + (p * dp).sum(axis=1)[:, None])
+
+
 BMUTANTS = {
+    "magnitude_without_delta": ("softmax_grad_magnitudes", _mag_without_delta),
+    "magnitude_signed": ("softmax_grad_magnitudes", _mag_signed),
     "delta_dropped": ("softmax_grad_terms", _no_delta),
     "delta_sign": ("softmax_grad_terms", _delta_sign),
     "p_unnormalised": ("softmax_grad_terms", _p_unnormalised),
@@ -67,7 +80,9 @@ def test_bwd_mutant_is_caught(name, monkeypatch):
 
 
 def test_bwd_rounding_emulation_is_close():
-    """fp16 operands (dO, P, dS) move the exact gradients only slightly."""
+    """fp16 operands (dO, P, dS) move the exact gradients by at most about
+    one fp16 unit roundoff (2^-11) times each element's magnitude -- well
+    inside the GPU tolerance of four units per element."""
     from nsa_block_selection_gb300 import inputs as gen
 
     w = gen.Workload("t", 1, 96, 96, 8, 1, 32, 16, 4, 1.0, "first_two_local")
@@ -75,8 +90,11 @@ def test_bwd_rounding_emulation_is_close():
     dO = np.random.default_rng(4).standard_normal(q.shape)
     exact = S.sel_attn_bwd(q, k, v, idx, dO, 16)
     emul = S.sel_attn_bwd(q, k, v, idx, dO, 16, emulate_kernel_rounding=True)
-    for a, b in zip(exact, emul):
+    mags = S.sel_attn_bwd(q, k, v, idx, dO, 16, magnitudes=True)
+    u16 = 2.0 ** -11
+    for a, b, mg in zip(exact, emul, mags):
         assert np.abs(a - b).max() <= 5e-3 * np.abs(a).max()
+        assert np.all(np.abs(a - b) <= 2 * u16 * mg + 1e-15)
 
 
 def test_bwd_restricted_helpers_agree_with_full():

@@ -215,15 +215,24 @@ def test_host_entry_matches_device_entry(B, M, N, T, bs, chunk):
         idx = np.where(idx < nb, idx, -1).astype(np.int32)  # M > N: ids past N are padding
     O_d, L_d = run_cuda(q, k, v, idx, bs)
     pin = [torch.from_numpy(x).pin_memory() for x in (q, k, v, idx)]
-    O_h, L_h = _lib.sel_attn_fwd_host(*pin, bs, chunk_m=chunk)
+    O_h, L_h = _lib.sel_attn_fwd_host(*pin, bs, chunk_m=chunk,
+                                      out=_nan_pinned(O_d.shape), lse=_nan_pinned(L_d.shape))
     assert torch.equal(O_h, O_d.cpu()) and torch.equal(L_h, L_d.cpu())
     # pageable host memory is also accepted
     O_p, L_p = _lib.sel_attn_fwd_host(*[torch.from_numpy(x) for x in (q, k, v, idx)], bs,
-                                      out=torch.empty_like(O_h), lse=torch.empty_like(L_h),
+                                      out=torch.full_like(O_h, float("nan")),
+                                      lse=torch.full_like(L_h, float("nan")),
                                       chunk_m=chunk)
     assert torch.equal(O_p, O_d.cpu()) and torch.equal(L_p, L_d.cpu())
     if T:
         check_all_rows(q, k, v, idx, bs, O_d, L_d, what="host entry")
+
+
+def _nan_pinned(shape):
+    """Pinned host output the host entry point must overwrite (NaN-filled)."""
+    import torch
+
+    return torch.full(tuple(shape), float("nan"), dtype=torch.float32).pin_memory()
 
 
 @pytest.mark.parametrize("M,bs,T,perm", [(2047, 32, 64, False), (1531, 64, 24, True),
@@ -253,5 +262,6 @@ def test_heads_per_group(H, G):
     O, L = run_cuda(q, k, v, idx, 64)
     check_all_rows(q, k, v, idx, 64, O, L, what=f"H{H} G{G}")
     pin = [torch.from_numpy(x).pin_memory() for x in (q, k, v, idx)]
-    O_h, L_h = _lib.sel_attn_fwd_host(*pin, 64, chunk_m=128)
+    O_h, L_h = _lib.sel_attn_fwd_host(*pin, 64, chunk_m=128, out=_nan_pinned(O.shape),
+                                      lse=_nan_pinned(L.shape))
     assert torch.equal(O_h, O.cpu()) and torch.equal(L_h, L.cpu())

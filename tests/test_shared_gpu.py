@@ -13,7 +13,8 @@ import numpy as np
 import pytest
 
 import oracle.sel_attn as oracle
-from _parity import check_all_rows, check_rows, compare, gather_rows, sample_rows, to_dev
+from _parity import (check_all_rows, check_rows, compare, gather_rows, poisoned, run_cuda,
+                     sample_rows, to_dev)
 from _records import MAXREC, TILE, records_ref
 
 pytestmark = pytest.mark.gpu
@@ -37,7 +38,9 @@ def run_shared(q, k, v, idx, bs, dtype=None, scale=None):
     G = k.shape[2]
     ws = torch.zeros(_lib.shared_workspace_bytes(B, M, G) + 256, dtype=torch.uint8,
                      device="cuda")
-    O, L = _lib.sel_attn_fwd_shared(tq, tk, tv, ti, bs, scale, workspace=ws)
+    O, L = _lib.sel_attn_fwd_shared(tq, tk, tv, ti, bs, scale, workspace=ws,
+                                    out=poisoned((B, M, H, D), torch.float32),
+                                    lse=poisoned((B, H, M), torch.float32))
     torch.cuda.synchronize()
     assert _lib.sync_status() == 0
     ntiles = -(-M // TILE)
@@ -163,23 +166,21 @@ def test_other_shapes_take_the_one_pass_kernel(H, G, D, M):
     untouched."""
     import torch
 
-    from nsa_block_selection_gb300 import sel_attn_fwd
 
     bs = 64
     q, k, v, idx = _inputs(1, M, M, H, G, D, bs, 4, "first_two_local", seed=H + D + M)
     O, L, _, ws = run_shared(q, k, v, idx, bs)
     assert int(ws.count_nonzero()) == 0
-    O1, L1 = sel_attn_fwd(*to_dev(q, k, v, idx), bs)
+    O1, L1 = run_cuda(q, k, v, idx, bs)
     assert torch.equal(O, O1) and torch.equal(L, L1)
 
 
 def test_close_to_one_pass():
-    from nsa_block_selection_gb300 import sel_attn_fwd
 
     bs = 64
     q, k, v, idx = _inputs(1, 2048, 2048, 16, 2, 128, bs, 16, "first_two_local", seed=2)
     O, L, _, _ = run_shared(q, k, v, idx, bs)
-    O1, L1 = sel_attn_fwd(*to_dev(q, k, v, idx), bs)
+    O1, L1 = run_cuda(q, k, v, idx, bs)
     assert float((O - O1).abs().max()) < 1e-3
     assert float((L - L1).abs().max()) < 1e-4
 
@@ -194,7 +195,9 @@ def test_full_size_sampled(name):
     w = gen.workload(name)
     q, k, v, idx = gen.make_inputs(w)
     tq, tk, tv, ti = to_dev(q, k, v, idx)
-    O, L = _lib.sel_attn_fwd_shared(tq, tk, tv, ti, w.block_size)
+    O, L = _lib.sel_attn_fwd_shared(tq, tk, tv, ti, w.block_size,
+                                    out=poisoned((w.B, w.M, w.H, w.D), torch.float32),
+                                    lse=poisoned((w.B, w.H, w.M), torch.float32))
     torch.cuda.synchronize()
     assert _lib.sync_status() == 0
     assert bool(torch.isfinite(L).all()) and bool(torch.isfinite(O).all())

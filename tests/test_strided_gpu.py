@@ -5,7 +5,7 @@ bit (same kernel arithmetic, other addresses), and the oracle's."""
 import numpy as np
 import pytest
 
-from _parity import check_rows, sample_rows
+from _parity import check_rows, poisoned, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -42,9 +42,10 @@ def test_fused_qkv_views_and_sliced_out(dtype_name, out_name, D):
     ti = torch.from_numpy(idx).cuda()
     big = torch.full((B, M, H + 8, D), 7.0, dtype=ot, device="cuda")
     out = big[:, :, 3:3 + H]
-    O, L = sel_attn_fwd(tq, tk, tv, ti, 64, out=out)
+    out.fill_(float("nan"))  # the kernel must overwrite every element of the slice
+    O, L = sel_attn_fwd(tq, tk, tv, ti, 64, out=out, lse=poisoned((B, H, M), torch.float32))
     Oc, Lc = sel_attn_fwd(tq.contiguous(), tk.contiguous(), tv.contiguous(), ti, 64,
-                          out_dtype=ot)
+                          out=poisoned((B, M, H, D), ot), lse=poisoned((B, H, M), torch.float32))
     torch.cuda.synchronize()
     assert O.data_ptr() == out.data_ptr()
     assert torch.equal(O, Oc) and torch.equal(L, Lc)

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle.swa as W
-from _parity import compare
+from _parity import compare, poisoned
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +34,9 @@ def _run(q, k, v, window, dtype, scale=None, lse=True):
 
     dt = torch.bfloat16 if dtype == "bf16" else torch.float16
     t = [torch.from_numpy(x).cuda().to(dt) for x in (q, k, v)]
-    O, L = swa_fwd(*t, window=window, scale=scale, return_lse=lse)
+    B, M, H, D = t[0].shape
+    O, L = swa_fwd(*t, window=window, scale=scale, return_lse=lse, out=poisoned((B, M, H, D), dt),
+                   lse=poisoned((B, H, M), torch.float32) if lse else None)
     torch.cuda.synchronize()
     assert O.dtype == dt
     return O, L
@@ -92,7 +94,8 @@ def test_swa_no_keys_and_no_lse():
 
     q = torch.randn(1, 200, 4, 64, device="cuda").bfloat16()
     k = torch.zeros(1, 0, 2, 64, device="cuda").bfloat16()
-    O, L = swa_fwd(q, k, k, window=(-1, 0))
+    O, L = swa_fwd(q, k, k, window=(-1, 0), out=poisoned(q.shape, q.dtype),
+                   lse=poisoned((1, 4, 200), torch.float32))
     torch.cuda.synchronize()
     assert (O == 0).all() and torch.isneginf(L).all()
     # queries past the last key, window (5, 5): rows 306.. see nothing

@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 
 import oracle.topk as K
+from _parity import poisoned
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +46,9 @@ def _run(sc, N, bs, T, n_init, n_local):
 
     from nsa_block_selection_gb300 import topk_blocks
 
-    out = topk_blocks(torch.from_numpy(sc).cuda(), N, bs, T, n_init, n_local)
+    B, M, G = sc.shape[:3]
+    out = topk_blocks(torch.from_numpy(sc).cuda(), N, bs, T, n_init, n_local,
+                      out=poisoned((B, M, G, T), torch.int32))
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
@@ -90,7 +93,7 @@ def test_topk_full_size_sampled_and_structure():
 
     B, M, G, bs, T = 1, 65536, 8, 64, 16
     sc = gen.make_block_scores_torch(B, M, G, M // bs, 17, "cuda")
-    idx = topk_blocks(sc, M, bs, T, 1, 2)
+    idx = topk_blocks(sc, M, bs, T, 1, 2, out=poisoned((B, M, G, T), torch.int32))
     torch.cuda.synchronize()
     m = torch.arange(M, device="cuda").view(1, M, 1, 1)
     c = m // bs
@@ -122,11 +125,14 @@ def test_topk_drives_the_forward():
     w = gen.Workload("topk", 1, 3000, 3000, 16, 2, 128, 64, 8, 1.0, "first_two_local")
     q, k, v = gen.make_qkv(w, 5)
     sc = gen.make_block_scores(1, w.M, w.G, -(-w.N // w.block_size), 5)
-    idx = topk_blocks(torch.from_numpy(sc).cuda(), w.N, w.block_size, w.T, 1, 2)
+    idx = topk_blocks(torch.from_numpy(sc).cuda(), w.N, w.block_size, w.T, 1, 2,
+                      out=poisoned((w.B, w.M, w.G, w.T), torch.int32))
     idx_np = idx.cpu().numpy()
     np.testing.assert_array_equal(idx_np, K.topk_blocks(sc, w.N, w.block_size, w.T, 1, 2))
     tq, tk, tv = (torch.from_numpy(x).cuda() for x in (q, k, v))
-    O, L = sel_attn_fwd(tq, tk, tv, idx, w.block_size)
+    O, L = sel_attn_fwd(tq, tk, tv, idx, w.block_size,
+                        out=poisoned((w.B, w.M, w.H, w.D), torch.float32),
+                        lse=poisoned((w.B, w.H, w.M), torch.float32))
     torch.cuda.synchronize()
     rows = sample_rows(w.B, w.M, w.G, w.block_size, 1, n_random=512)
     check_rows(q, k, v, idx_np, w.block_size, O, L, rows, what="topk->fwd")
