@@ -191,9 +191,12 @@ int64_t nsa_sel_attn_fwd_shared_workspace_bytes(int64_t B, int64_t M, int64_t G)
  * bit-identical to the one-pass call). Three kernels are enqueued on
  * `stream`; nothing is allocated or synchronised.
  *
- * The two-pass path serves D = 128, H/G = 8, M >= 16, N >= block_size and
- * T >= 1; any other valid problem runs the one-pass kernel (the workspace
- * is then unused). Every other argument, layout, check and property is that
+ * The two-pass path serves block_size = 64, D = 128, H/G = 8, M >= 16,
+ * N >= block_size and T >= 1; any other valid problem runs the one-pass
+ * kernel (the workspace is then unused). With 32-key blocks the common
+ * blocks are too small a share of a row's bytes for the extra passes to pay
+ * (measured slower than one pass), so those problems take the one-pass
+ * kernel too. Every other argument, layout, check and property is that
  * of nsa_sel_attn_fwd_ex. A key row the tile-shared pass reads is visible
  * to every query of the tile, so NaN or Inf in rows a query may not see
  * still never reaches that query's output.
@@ -479,6 +482,9 @@ int64_t nsa_probe_l2_gather_bytes(int64_t D, int64_t ctas, int warps_per_cta,
  *   ctas            grid size (1 .. 2^31 - 1)
  *   warps_per_cta   1 .. 32
  *   slots_per_warp  1 .. 16 copies each warp keeps in flight
+ *   extra_smem_bytes  >= 0: unused shared memory added to each CTA, to
+ *                   measure how the gather rate depends on the shared
+ *                   memory a kernel reserves (total within 227 KB)
  *
  * Every warp takes the (b, g, m) rows w, w + W, w + 2W, ... (W warps in the
  * grid, m fastest) and walks each row as the forward does -- padding,
@@ -493,7 +499,8 @@ int64_t nsa_probe_l2_gather_bytes(int64_t D, int64_t ctas, int warps_per_cta,
  */
 int nsa_probe_gather_rows(const void* K, const void* V, const int32_t* block_indices, int64_t B,
                           int64_t M, int64_t N, int64_t G, int64_t D, int64_t T, int block_size,
-                          int64_t ctas, int warps_per_cta, int slots_per_warp, void* stream);
+                          int64_t ctas, int warps_per_cta, int slots_per_warp,
+                          int64_t extra_smem_bytes, void* stream);
 
 #ifdef __cplusplus
 }

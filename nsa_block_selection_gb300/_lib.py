@@ -96,7 +96,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_probe_l2_gather_bytes.argtypes = [i64, i64, c_int, i64, c_int]
     lib.nsa_probe_gather_rows.restype = c_int
     lib.nsa_probe_gather_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, i64,
-                                          c_int, c_int, vp]
+                                          c_int, c_int, i64, vp]
     if path is None:
         _lib = lib
     return lib
@@ -468,7 +468,7 @@ def probe_l2_gather(k, v, g: int, block_size: int, ctas: int, warps_per_cta: int
 
 
 def probe_gather_rows(k, v, block_indices, block_size: int, ctas: int, warps_per_cta: int,
-                      slots_per_warp: int, stream=None) -> None:
+                      slots_per_warp: int, stream=None, extra_smem_bytes: int = 0) -> None:
     """Launch the index-driven gather probe (nsa_probe_gather_rows): the
     forward's copies for these rows alone. k, v: fp16 [B, N, G, D];
     block_indices: int32 [B, M, G, T], all contiguous on one CUDA device."""
@@ -488,6 +488,7 @@ def probe_gather_rows(k, v, block_indices, block_size: int, ctas: int, warps_per
         stream = torch.cuda.current_stream(k.device)
     st = lib.nsa_probe_gather_rows(_ptr(k), _ptr(v), _ptr(block_indices), B, M, N, G, D, T,
                                    int(block_size), int(ctas), int(warps_per_cta),
-                                   int(slots_per_warp), ctypes.c_void_p(stream.cuda_stream))
+                                   int(slots_per_warp), int(extra_smem_bytes),
+                                   ctypes.c_void_p(stream.cuda_stream))
     if st != NSA_OK:
         raise NsaError(st, "nsa_probe_gather_rows")

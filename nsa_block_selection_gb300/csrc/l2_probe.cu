@@ -260,11 +260,11 @@ static int launch_probe(const ProbeArgs& a, const void* K, const void* V, int64_
 
 template <int D>
 static int launch_rows_probe(const RowsProbeArgs& a, const void* K, const void* V, int64_t B,
-                             int64_t ctas, int warps, cudaStream_t st) {
+                             int64_t ctas, int warps, int64_t pad, cudaStream_t st) {
   CUtensorMap tk, tv;
   if (!encode_kv_map(&tk, K, B, a.N, a.G, D) || !encode_kv_map(&tv, V, B, a.N, a.G, D))
     return NSA_ERR_LAUNCH;
-  const int smem = static_cast<int>(probe_smem_bytes(D, warps, a.slots));
+  const int smem = static_cast<int>(probe_smem_bytes(D, warps, a.slots) + pad);
   auto kern = gather_rows_probe_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
@@ -327,14 +327,17 @@ int nsa_probe_l2_gather(const void* K, const void* V, int64_t N, int64_t G, int6
 
 int nsa_probe_gather_rows(const void* K, const void* V, const int32_t* block_indices, int64_t B,
                           int64_t M, int64_t N, int64_t G, int64_t D, int64_t T, int block_size,
-                          int64_t ctas, int warps_per_cta, int slots_per_warp, void* stream) {
+                          int64_t ctas, int warps_per_cta, int slots_per_warp,
+                          int64_t extra_smem_bytes, void* stream) {
   using namespace nsa;
   const int chk = check_sizes(B, M, N, G, G, D, T, block_size);
   if (chk != NSA_OK) return chk;
   if (ctas < 1 || ctas > (int64_t(1) << 31) - 1 || warps_per_cta < 1 ||
       warps_per_cta > kProbeMaxWarps || slots_per_warp < 1 || slots_per_warp > kProbeMaxSlots)
     return NSA_ERR_SHAPE;
-  if (probe_smem_bytes(D, warps_per_cta, slots_per_warp) > 227 * 1024) return NSA_ERR_SHAPE;
+  if (extra_smem_bytes < 0 ||
+      probe_smem_bytes(D, warps_per_cta, slots_per_warp) + extra_smem_bytes > 227 * 1024)
+    return NSA_ERR_SHAPE;
   if (B == 0 || M == 0 || N == 0 || T == 0) return NSA_OK;
   if (!K || !V || !block_indices) return NSA_ERR_NULL;
   if (((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V)) & 15u) ||
@@ -351,8 +354,8 @@ int nsa_probe_gather_rows(const void* K, const void* V, const int32_t* block_ind
   a.bs = block_size;
   a.slots = slots_per_warp;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return D == 64 ? launch_rows_probe<64>(a, K, V, B, ctas, warps_per_cta, st)
-                 : launch_rows_probe<128>(a, K, V, B, ctas, warps_per_cta, st);
+  return D == 64 ? launch_rows_probe<64>(a, K, V, B, ctas, warps_per_cta, extra_smem_bytes, st)
+                 : launch_rows_probe<128>(a, K, V, B, ctas, warps_per_cta, extra_smem_bytes, st);
 }
 
 }  // extern "C"

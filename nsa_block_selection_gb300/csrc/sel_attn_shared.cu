@@ -690,8 +690,12 @@ bool shared_pass_eligible(int64_t H, int64_t G, int64_t D, int o_dtype, const in
 }
 
 bool shared_pass_sizes_ok(int64_t M, int64_t N, int64_t T, int block_size) {
-  // tensor-map boxes (16 queries, block_size keys) within the tensors
-  return M >= kSharedTileQ && N >= block_size && T > 0;
+  // 64-key blocks only: two common blocks of 64 keys are an eighth of a
+  // 16-block row's bytes and the gather kernel saves more than the two extra
+  // passes cost; at 32 keys they are a sixteenth and the passes cost more
+  // than they save (6.36 against 6.21 ms one-pass at B=2, M=32k, T=32).
+  // Tensor-map boxes (16 queries, block_size keys) stay within the tensors.
+  return block_size == 64 && M >= kSharedTileQ && N >= block_size && T > 0;
 }
 
 int launch_shared_passes(const void* Q, const void* K, const void* V, const int32_t* idx,
@@ -724,11 +728,9 @@ int launch_shared_passes(const void* Q, const void* K, const void* V, const int3
   sp.ntiles = ntiles;
   sp.units = units;
   sp.sl2 = sl2;
-  if (block_size == 64)
-    return bf16 ? launch_shared_kernel<64, true>(sp, units, Q, K, V, B, M, N, H, G, st)
-                : launch_shared_kernel<64, false>(sp, units, Q, K, V, B, M, N, H, G, st);
-  return bf16 ? launch_shared_kernel<32, true>(sp, units, Q, K, V, B, M, N, H, G, st)
-              : launch_shared_kernel<32, false>(sp, units, Q, K, V, B, M, N, H, G, st);
+  // block_size == 64 (shared_pass_sizes_ok)
+  return bf16 ? launch_shared_kernel<64, true>(sp, units, Q, K, V, B, M, N, H, G, st)
+              : launch_shared_kernel<64, false>(sp, units, Q, K, V, B, M, N, H, G, st);
 }
 
 int shared_read_and_clear_status(unsigned int* value) { return read_and_clear_status(value); }

@@ -10,8 +10,10 @@ K/V and does nothing else. The best rate over a few in-flight depths is the
 ceiling of the forward's gathered bytes per second.
 
 ``python -m nsa_block_selection_gb300.l2_ceiling`` runs the full sweep on
-cuda:0 (depths, layouts, active SMs, per-SM rates) and prints one JSON
-object.
+cuda:0 (depths, box sizes, layouts, active SMs, per-SM rates, the
+workloads' own rows) and prints one JSON object; ``... l2_ceiling
+ncu-case`` launches each measured kernel twice on the m16k_bs64 workload,
+for a counter capture.
 """
 
 from __future__ import annotations
@@ -76,10 +78,12 @@ def run_once(k, v, g, bs, ctas, warps, slots, loads, seed=1, record=None, rows=1
     return n, e0.elapsed_time(e1)
 
 
-def time_config(k, v, g, bs, sms, cfg, seconds=0.25, sm_count=None, record=False):
+def time_config(k, v, g, bs, sms, cfg, seconds=0.25, sm_count=None, record=False,
+                rate_hint=None):
     """Rate of one (warps, CTAs per SM, slots) configuration on ``sm_count``
     SMs' worth of CTAs (default: all): a short calibration launch (which
-    also brings the K/V into L2), then one launch sized to last ``seconds``."""
+    also brings the K/V into L2), then one launch sized to last ``seconds``
+    at the calibration's rate (or at ``rate_hint`` bytes/s, when given)."""
     import torch
 
     warps, cps, slots = cfg[:3]
@@ -87,7 +91,7 @@ def time_config(k, v, g, bs, sms, cfg, seconds=0.25, sm_count=None, record=False
     D = k.shape[2]
     ctas = (sm_count or sms) * cps
     n, ms = run_once(k, v, g, bs, ctas, warps, slots, 64 * slots, rows=rows)
-    rate = n / (ms * 1e-3)
+    rate = rate_hint or n / (ms * 1e-3)
     per_warp = max(16 * slots, int(rate * seconds / (ctas * warps * (D // 64) * rows * 128)))
     rec = torch.zeros((ctas, 3), dtype=torch.int64, device=k.device) if record else None
     n, ms = run_once(k, v, g, bs, ctas, warps, slots, per_warp, seed=7, record=rec, rows=rows)
@@ -100,9 +104,10 @@ def time_config(k, v, g, bs, sms, cfg, seconds=0.25, sm_count=None, record=False
     return out
 
 
-def time_rows(k, v, idx, bs, sms, cfg, flush=None, reps=3):
+def time_rows(k, v, idx, bs, sms, cfg, flush=None, reps=3, pad=0):
     """Mean ms of the index-driven probe over ``reps`` launches (after one
-    untimed launch), each preceded by ``flush()`` outside the events."""
+    untimed launch), each preceded by ``flush()`` outside the events;
+    ``pad`` bytes of unused shared memory per CTA."""
     import torch
 
     warps, cps, slots = cfg
@@ -113,7 +118,8 @@ def time_rows(k, v, idx, bs, sms, cfg, flush=None, reps=3):
             flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(st)
-        _lib.probe_gather_rows(k, v, idx, bs, sms * cps, warps, slots, stream=st)
+        _lib.probe_gather_rows(k, v, idx, bs, sms * cps, warps, slots, stream=st,
+                               extra_smem_bytes=pad)
         e1.record(st)
         e1.synchronize()
         if r:
@@ -150,7 +156,7 @@ def measure(k, v, bs, g=0, idx=None, gathered_bytes=None, flush=None, seconds=0.
     cfg = (best["warps_per_cta"], best["ctas_per_sm"], best["slots_per_warp"])
     if clocks is not None:
         clocks.start()
-    final = time_config(k0, v0, g, bs, sms, cfg, long_seconds)
+    final = time_config(k0, v0, g, bs, sms, cfg, long_seconds, rate_hint=best["gbs"] * 1e9)
     clk = clocks.stop() if clocks is not None else None
     fwd = next((r for r in rows if (r["warps_per_cta"], r["ctas_per_sm"],
                                    r["slots_per_warp"]) == FORWARD_DEPTH), None)
@@ -251,6 +257,11 @@ def sweep(seconds=0.25):
         out["active_sms"].append({"sms": n, "gbs": r["gbs"], "gbs_per_sm": r["gbs"] / n})
     best_cfg = max(out["depth"], key=lambda r: r["gbs"])
     bc = (best_cfg["warps_per_cta"], best_cfg["ctas_per_sm"], best_cfg["slots_per_warp"])
+    out["active_sms_best"] = []
+    for n in (sms // 4, sms // 2, 3 * sms // 4, sms):
+        r = time_config(k, v, 0, 64, sms, bc, seconds, sm_count=n)
+        out["active_sms_best"].append({"config": list(bc), "sms": n, "gbs": r["gbs"],
+                                       "gbs_per_sm": r["gbs"] / n})
     # 4. layouts with the same 33.5 MB: the strided group (2 KB key stride),
     # a contiguous [65536, 1, 128] pair, all 8 groups of [8192, 8, 128]
     lay = []
@@ -294,12 +305,57 @@ def sweep(seconds=0.25):
                 ms = time_rows(kk, vv, idx, w.block_size, sms, c, lambda: flush_buf.fill_(1.0))
                 rr.append([c[0], c[1], c[2], round(nbytes / (ms * 1e-3) / 1e9, 1), round(ms, 4)])
         out["workload_rows"][name] = {"gathered_bytes": nbytes, "configs": rr}
+        if name == "m64k_bs64":
+            # the forward's depth with unused shared memory added per CTA:
+            # where the rate falls off as a kernel reserves more
+            pads = []
+            for pad_kb in (0, 8, 12, 16, 20, 24, 28, 32, 40, 48):
+                ms = time_rows(kk, vv, idx, w.block_size, sms, FORWARD_DEPTH,
+                               lambda: flush_buf.fill_(1.0), pad=pad_kb * 1024)
+                pads.append([pad_kb, (smem_bytes(w.D, 4, 2) + pad_kb * 1024) * 4 // 1024,
+                             round(nbytes / (ms * 1e-3) / 1e9, 1)])
+            out["workload_rows"][name]["smem_pad"] = pads
         del idx, kk, vv
     return out
 
 
+def ncu_case(name="m16k_bs64"):
+    """One launch each, after one untimed launch each, of: the forward on the
+    workload, the index-driven probe on its rows (the forward's depth), and
+    the random-block probe (32 warps per SM, one copy each) on group 0 of
+    the workload's K/V and on a contiguous [N, 1, 128] pair of the same
+    size -- the case the committed L2 counter summary is captured on."""
+    import torch
+
+    from . import inputs as ginp
+    from ._lib import sel_attn_fwd
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    w = ginp.workload(name)
+    q, k, v, idx = (torch.from_numpy(x).to(dev) for x in ginp.make_inputs(w))
+    gen = torch.Generator(device=dev).manual_seed(3)
+    kc = torch.randn((w.N, 1, w.D), generator=gen, device=dev).half()
+    vc = torch.randn((w.N, 1, w.D), generator=gen, device=dev).half()
+    ks, vs = k[0], v[0]
+    loads = 4000
+    for _ in range(2):  # untimed launch of each, then the one ncu captures
+        sel_attn_fwd(q, k, v, idx, w.block_size)
+        _lib.probe_gather_rows(k, v, idx, w.block_size, sms * 4, 4, 2)
+        _lib.probe_l2_gather(ks, vs, 0, w.block_size, sms, 32, 1, loads)
+        _lib.probe_l2_gather(kc, vc, 0, w.block_size, sms, 32, 1, loads)
+        torch.cuda.synchronize()
+    assert _lib.sync_status() == 0
+    print(f"ncu case {name}: forward, rows probe (4, 4, 2), random probe (32, 1, 1) on "
+          f"group 0 and on a contiguous [{w.N}, 1, {w.D}] pair; each launched twice")
+
+
 def main(argv=None):
     argv = sys.argv[1:] if argv is None else argv
+    if argv and argv[0] == "ncu-case":
+        ncu_case(argv[1] if len(argv) > 1 else "m16k_bs64")
+        return 0
     seconds = float(argv[0]) if argv else 0.25
     t0 = time.time()
     res = sweep(seconds)

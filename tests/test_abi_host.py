@@ -307,16 +307,17 @@ def test_probe_bytes(lib):
 
 
 def call_rows_probe(lib, k=FAKE, v=FAKE, idx=FAKE, B=1, M=256, N=256, G=8, D=128, T=4, bs=64,
-                    ctas=152, warps=4, slots=2):
+                    ctas=152, warps=4, slots=2, pad=0):
     vp = ctypes.c_void_p
     return lib.nsa_probe_gather_rows(vp(k), vp(v), vp(idx), B, M, N, G, D, T, bs, ctas, warps,
-                                     slots, None)
+                                     slots, pad, None)
 
 
 @pytest.mark.parametrize("over,status", [
     (dict(k=None), -1), (dict(idx=None), -1), (dict(v=FAKE + 4), -6), (dict(idx=FAKE + 2), -6),
     (dict(D=96), -4), (dict(bs=16), -3), (dict(M=-1), -2), (dict(ctas=0), -2),
     (dict(warps=33), -2), (dict(slots=0), -2), (dict(warps=32, slots=2), -2),
+    (dict(pad=-1), -2), (dict(pad=200 * 1024), -2),
 ])
 def test_rows_probe_rejects_bad_arguments(lib, over, status):
     assert call_rows_probe(lib, **over) == status
