@@ -65,6 +65,7 @@ struct BwdProblem {
   const int* offs;     // [L + 1] list starts (L = B * G * nblk)
   const int* choffs;   // [L + 1] chunk starts
   const int* chunk_list;  // [chunks] the list of each chunk
+  const int* chunk_order;  // [chunks] launch order of the chunks (D = 128), or null
   const int* lists;    // query ids, list by list
   int64_t B, M, N, H, G, T;
   int64_t units;       // B * G * nsub * M
@@ -474,6 +475,52 @@ __global__ void csr_chunk_list_kernel(const int* choffs, int L, int* chunk_list)
     for (int c = choffs[l]; c < choffs[l + 1]; ++c) chunk_list[c] = l;
 }
 
+// Launch order of the key-major tensor-core kernel's chunks (D = 128).
+// Numbered list by list, the CTAs in flight at any moment would work on ~150
+// consecutive blocks, whose queries span the whole sequence: the dQ rows they
+// add into (one 4 KB row per query and head group) would be scattered over
+// all of dQ, and every fp32 reduction would be a read-modify-write in HBM.
+// Ordered by the mean query position of each chunk (in buckets of
+// kOrderQueries positions, per (b, g)), the CTAs in flight add into a band of
+// dQ rows that L2 can hold, so most of a row's reductions from its blocks
+// meet in L2. Lists fill in roughly increasing query order (the fill walks
+// the index tensor in order), so a chunk covers a contiguous stretch of its
+// list's queries.
+#ifndef NSA_BWD_ORDER_QUERIES
+#define NSA_BWD_ORDER_QUERIES 512
+#endif
+constexpr int kOrderQueries = NSA_BWD_ORDER_QUERIES;
+
+// One warp per chunk: its bucket (b, g, mean query / kOrderQueries), counted.
+__global__ void chunk_key_kernel(const BwdProblem p, int nbkt, int* key, int* bcount) {
+  const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (c >= p.choffs[p.L]) return;
+  const int l = __ldg(p.chunk_list + c);
+  const int q0 = p.offs[l] + (static_cast<int>(c) - p.choffs[l]) * kQueriesPerChunk;
+  const int nq = min(q0 + kQueriesPerChunk, p.offs[l + 1]) - q0;  // >= 1
+  long long sum = 0;
+  for (int i = lane; i < nq; i += 32) sum += __ldg(p.lists + q0 + i);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+  if (lane == 0) {
+    const int bg = l / p.nblk;
+    const int bk = static_cast<int>(sum / nq) / kOrderQueries;
+    const int k = bg * nbkt + min(bk, nbkt - 1);
+    key[c] = k;
+    atomicAdd(bcount + k, 1);
+  }
+}
+
+__global__ void chunk_order_fill_kernel(const BwdProblem p, const int* key, const int* boffs,
+                                        int* bcursor, int* order) {
+  const int nch = p.choffs[p.L];
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < nch; c += gridDim.x * blockDim.x) {
+    const int k = key[c];
+    order[boffs[k] + atomicAdd(bcursor + k, 1)] = c;
+  }
+}
+
 __global__ void csr_fill_kernel(const BwdProblem p, int* cursor, int* lists) {
   const int64_t total = p.B * p.M * p.G * p.T;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
@@ -846,8 +893,8 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
   using C = DkvTcCfg;
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
-  const int c = blockIdx.x;
-  if (c >= p.choffs[p.L]) return;  // before any tensor memory is taken
+  if (static_cast<int>(blockIdx.x) >= p.choffs[p.L]) return;  // before any tensor memory is taken
+  const int c = p.chunk_order ? __ldg(p.chunk_order + blockIdx.x) : static_cast<int>(blockIdx.x);
   const int l = __ldg(p.chunk_list + c);
   const int q0 = p.offs[l] + (c - p.choffs[l]) * kQueriesPerChunk;
   const int nq = min(q0 + kQueriesPerChunk, p.offs[l + 1]) - q0;
@@ -1251,8 +1298,8 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
 
 struct BwdPlan {
   size_t off_do16, off_rec, off_count, off_cursor, off_offs, off_choffs, off_lists,
-      off_chunk_list, total;
-  int64_t L, entries, max_chunks;
+      off_chunk_list, off_order, off_key, off_bcount, off_bcursor, off_boffs, off_bscratch, total;
+  int64_t L, entries, max_chunks, nkeys, nbkt;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1283,6 +1330,23 @@ static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, i
   pl.max_chunks = (pl.entries + kQueriesPerChunk - 1) / kQueriesPerChunk + pl.L;
   pl.off_chunk_list = at;
   at += align256(static_cast<size_t>(pl.max_chunks) * 4);
+  // chunk launch order (D = 128): per chunk its order slot and bucket key;
+  // per (b, g, bucket of kOrderQueries queries) a count, cursor and offset
+  pl.nbkt = (M + kOrderQueries - 1) / kOrderQueries;
+  if (pl.nbkt < 1) pl.nbkt = 1;
+  pl.nkeys = B * G * pl.nbkt;
+  pl.off_order = at;
+  at += align256(static_cast<size_t>(pl.max_chunks) * 4);
+  pl.off_key = at;
+  at += align256(static_cast<size_t>(pl.max_chunks) * 4);
+  pl.off_bcount = at;
+  at += align256(static_cast<size_t>(pl.nkeys) * 4);
+  pl.off_bcursor = at;
+  at += align256(static_cast<size_t>(pl.nkeys) * 4);
+  pl.off_boffs = at;
+  at += align256(static_cast<size_t>(pl.nkeys + 1) * 4);
+  pl.off_bscratch = at;
+  at += align256(static_cast<size_t>(pl.nkeys + 1) * 4);
   pl.total = at;
   return pl;
 }
@@ -1304,6 +1368,7 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   p.lists = lists;
   int* chunk_list = reinterpret_cast<int*>(ws + pl.off_chunk_list);
   p.chunk_list = chunk_list;
+  p.chunk_order = nullptr;
   const int64_t B = p.units / (p.M * p.G * p.nsub);
   if (p.N > 0 &&
       (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
@@ -1389,6 +1454,23 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     if (hw0 == kHeadsPerGroup && (!encode_rows_halves_map(&tq3, p.Q, B * p.M * p.H, hw0) ||
                                   !encode_rows_halves_map(&tdo3, p.dO16, B * p.M * p.H, hw0)))
       return NSA_ERR_LAUNCH;
+    // launch order of the chunks: by mean query position, bucketed per (b, g)
+    int* order = reinterpret_cast<int*>(ws + pl.off_order);
+    int* key = reinterpret_cast<int*>(ws + pl.off_key);
+    int* bcount = reinterpret_cast<int*>(ws + pl.off_bcount);
+    int* bcursor = reinterpret_cast<int*>(ws + pl.off_bcursor);
+    int* boffs = reinterpret_cast<int*>(ws + pl.off_boffs);
+    int* bscratch = reinterpret_cast<int*>(ws + pl.off_bscratch);
+    if (cudaMemsetAsync(bcount, 0, static_cast<size_t>(pl.nkeys) * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(bcursor, 0, static_cast<size_t>(pl.nkeys) * 4, st) != cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    chunk_key_kernel<<<static_cast<unsigned>((chunks + 7) / 8), 256, 0, st>>>(
+        p, static_cast<int>(pl.nbkt), key, bcount);
+    csr_scan_kernel<<<1, 1024, 0, st>>>(bcount, boffs, bscratch, static_cast<int>(pl.nkeys), 1);
+    chunk_order_fill_kernel<<<static_cast<unsigned>((chunks + 255) / 256), 256, 0, st>>>(
+        p, key, boffs, bcursor, order);
+    if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
+    p.chunk_order = order;
     auto kk = split ? sel_attn_bwd_dkv_tc_kernel<true> : sel_attn_bwd_dkv_tc_kernel<false>;
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkvTcCfg::kSmemBytes) != cudaSuccess)
