@@ -80,8 +80,8 @@ def parse_args(argv=None):
                          "HBM bandwidth)")
     ap.add_argument("--skip-dense-fa", action="store_true",
                     help="skip timing dense causal attention (nsa_swa_fwd) on the same inputs")
-    ap.add_argument("--cpu-rows", type=int, default=24576,
-                    help="rows of the CPU-oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=393216,
+                    help="rows of the CPU-oracle sample (about 10-15 s of work on 16 cores)")
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--chunk-m", type=int, default=0,
                     help="queries per chunk of the host-buffer pipeline (0: default)")
