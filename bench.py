@@ -800,7 +800,11 @@ def run_backward(w, q, k, v, idx, out, lse, work, flush, args):
         # dQ = dS K per (query, selected block): every head of the group,
         # D fp32 values each, added with reductions
         red = work["gathered_bytes"] * (w.H // w.G) // w.block_size
+        ceiling = run_leg(True, reduction_ceiling, dq, w)
         res.update({"dq_reduction_bytes": red, "dq_reduction_gbs": red / (t * 1e-3) / 1e9,
+                    "dq_reduction_ceiling": ceiling,
+                    "dq_reduction_frac": (red / (t * 1e-3) / 1e9 / ceiling["gbs"]
+                                          if ceiling and "gbs" in ceiling else None),
                     "kernels": "prep (fp16 dO, LSE, delta), index transpose (count, scan, "
                                "fill), key-major tcgen05 kernel: dK, dV (fp32 atomics per "
                                "chunk) and dQ = dS K (fp32 reductions per batch)"})
@@ -810,6 +814,38 @@ def run_backward(w, q, k, v, idx, out, lse, work, flush, args):
     del ws, do, dq, dk, dv
     torch.cuda.empty_cache()
     return res
+
+
+def reduction_ceiling(dq, w, seconds=0.3):
+    """The rate of the backward's dQ reductions alone on this GPU: 4 KB rows
+    (one query's 8 heads of one KV group) added with 16-byte fp32 reductions
+    into random rows of the dQ tensor's first group (nsa_probe_reduce_rows;
+    adds zeros). Timed with CUDA events on the current stream."""
+    import torch
+
+    from nsa_block_selection_gb300 import _lib
+
+    sms = torch.cuda.get_device_properties(dq.device).multi_processor_count
+    rows, stride = w.B * w.M, w.H * w.D
+    flat = dq.view(-1)
+    st = torch.cuda.current_stream(dq.device)
+    ctas, warps = sms * 4, 8
+
+    def once(iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        n = _lib.probe_reduce_rows(flat, rows, stride, ctas, warps, iters, stream=st)
+        e1.record(st)
+        e1.synchronize()
+        return n, e0.elapsed_time(e1)
+
+    n, ms = once(64)
+    iters = max(64, int(n / (ms * 1e-3) * seconds / (ctas * warps * 4096)))
+    n, ms = once(iters)
+    return {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "bytes": n,
+            "pattern": f"4 KB fp32 rows (red.global.add.v4.f32, 16 B per lane) into random rows "
+                       f"of group 0 of dQ [{w.B}, {w.M}, {w.H}, {w.D}] ({rows} rows, "
+                       f"{rows * 4096 / 1e6:.0f} MB spread over {dq.numel() * 4 / 1e9:.2f} GB)"}
 
 
 def run_dense(w, q, k, v, out, lse, flush, args, t_sparse_ms):

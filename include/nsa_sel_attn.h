@@ -502,6 +502,29 @@ int nsa_probe_gather_rows(const void* K, const void* V, const int32_t* block_ind
                           int64_t ctas, int warps_per_cta, int slots_per_warp,
                           int64_t extra_smem_bytes, void* stream);
 
+/*
+ * nsa_probe_reduce_rows -- measurement kernel: the backward's dQ reductions
+ * alone, to measure the rate they can reach on this GPU.
+ *
+ *   buf             device fp32, at least rows * stride floats, 16-byte
+ *                   aligned; its contents are left unchanged (zeros are added)
+ *   rows, stride    rows of 1024 floats (4 KB: 8 head rows of 128 dims, one
+ *                   query and KV group of dQ), `stride` floats apart
+ *                   (>= 1024, a multiple of 4); dQ of one KV group is
+ *                   rows = B*M, stride = H*128
+ *   ctas, warps_per_cta  grid (warps_per_cta 1 .. 32)
+ *   iters_per_warp  rows each warp adds into
+ *
+ * Each warp adds one 4 KB row at a time into a row drawn at random, with
+ * 16-byte fp32 reductions (red.global.add.v4.f32), as the key-major backward
+ * kernel adds its dQ partial sums. Bytes reduced = ctas x warps x iters x
+ * 4096. Asynchronous; allocates nothing. Errors: NSA_ERR_NULL,
+ * NSA_ERR_ALIGN, NSA_ERR_SHAPE, NSA_ERR_LAUNCH.
+ */
+int nsa_probe_reduce_rows(float* buf, int64_t rows, int64_t stride, int64_t ctas,
+                          int warps_per_cta, int64_t iters_per_warp, uint32_t seed,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,8 @@ EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sel_attn
            "nsa_sel_attn_fwd_host", "nsa_sel_attn_bwd_workspace_bytes", "nsa_sel_attn_bwd",
            "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks", "nsa_swa_fwd",
            "nsa_sel_attn_fwd_shared_workspace_bytes", "nsa_sel_attn_fwd_shared",
-           "nsa_probe_l2_gather", "nsa_probe_l2_gather_bytes", "nsa_probe_gather_rows")
+           "nsa_probe_l2_gather", "nsa_probe_l2_gather_bytes", "nsa_probe_gather_rows",
+           "nsa_probe_reduce_rows")
 
 _lib = None
 
@@ -94,6 +95,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                         i64, c_int, ctypes.c_uint32, vp, vp]
     lib.nsa_probe_l2_gather_bytes.restype = i64
     lib.nsa_probe_l2_gather_bytes.argtypes = [i64, i64, c_int, i64, c_int]
+    lib.nsa_probe_reduce_rows.restype = c_int
+    lib.nsa_probe_reduce_rows.argtypes = [vp, i64, i64, i64, c_int, i64, ctypes.c_uint32, vp]
     lib.nsa_probe_gather_rows.restype = c_int
     lib.nsa_probe_gather_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int, i64,
                                           c_int, c_int, i64, vp]
@@ -492,3 +495,23 @@ def probe_gather_rows(k, v, block_indices, block_size: int, ctas: int, warps_per
                                    ctypes.c_void_p(stream.cuda_stream))
     if st != NSA_OK:
         raise NsaError(st, "nsa_probe_gather_rows")
+
+
+def probe_reduce_rows(buf, rows: int, stride: int, ctas: int, warps_per_cta: int,
+                      iters_per_warp: int, seed: int = 1, stream=None) -> int:
+    """Launch the reduction-rate probe (nsa_probe_reduce_rows) on an fp32
+    CUDA tensor of at least rows * stride elements; returns the bytes it
+    reduces. Adds zeros: the tensor's values are unchanged."""
+    import torch
+
+    lib = load()
+    if buf.dtype != torch.float32 or not buf.is_cuda or buf.numel() < rows * stride:
+        raise ValueError("buf must be an fp32 CUDA tensor of at least rows * stride elements")
+    if stream is None:
+        stream = torch.cuda.current_stream(buf.device)
+    st = lib.nsa_probe_reduce_rows(_ptr(buf), int(rows), int(stride), int(ctas),
+                                   int(warps_per_cta), int(iters_per_warp), int(seed) & 0xFFFFFFFF,
+                                   ctypes.c_void_p(stream.cuda_stream))
+    if st != NSA_OK:
+        raise NsaError(st, "nsa_probe_reduce_rows")
+    return int(ctas) * int(warps_per_cta) * int(iters_per_warp) * 4096

@@ -239,6 +239,28 @@ __global__ void __launch_bounds__(kProbeMaxWarps * 32)
   }
 }
 
+// The backward's dQ reductions alone: each warp adds 4 KB rows (the 8 head
+// rows of one query and KV group: 8 x 128 fp32, contiguous) into rows drawn
+// at random from `rows` rows spaced `stride` floats apart, 16 bytes per lane
+// per instruction (red.global.add.v4.f32), as the backward's dQ warps do.
+__global__ void reduce_rows_probe_kernel(float* buf, int64_t rows, int64_t stride, int64_t iters,
+                                         uint32_t seed) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (int64_t i = 0; i < iters; ++i) {
+    const uint32_t r = mix32(seed ^ mix32(gw * 0x9e3779b9u + static_cast<uint32_t>(i))) %
+                       static_cast<uint32_t>(rows);
+    float* row = buf + static_cast<int64_t>(r) * stride;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float* q = row + (k * 32 + lane) * 4;
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(q), "f"(0.f), "f"(0.f),
+                   "f"(0.f), "f"(0.f)
+                   : "memory");
+    }
+  }
+}
+
 static int64_t probe_smem_bytes(int64_t D, int64_t warps, int64_t slots, int64_t rows = kTileKeys) {
   return warps * slots * (D / kBoxCols) * rows * 128 + warps * slots * 8 + 1024;
 }
@@ -356,6 +378,22 @@ int nsa_probe_gather_rows(const void* K, const void* V, const int32_t* block_ind
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   return D == 64 ? launch_rows_probe<64>(a, K, V, B, ctas, warps_per_cta, extra_smem_bytes, st)
                  : launch_rows_probe<128>(a, K, V, B, ctas, warps_per_cta, extra_smem_bytes, st);
+}
+
+int nsa_probe_reduce_rows(float* buf, int64_t rows, int64_t stride, int64_t ctas,
+                          int warps_per_cta, int64_t iters_per_warp, uint32_t seed,
+                          void* stream) {
+  using namespace nsa;
+  if (!buf) return NSA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(buf) & 15u) return NSA_ERR_ALIGN;
+  if (rows < 1 || rows > (int64_t(1) << 31) - 1 || stride < 1024 || stride % 4 != 0 ||
+      ctas < 1 || ctas > (int64_t(1) << 31) - 1 || warps_per_cta < 1 ||
+      warps_per_cta > kProbeMaxWarps || iters_per_warp < 0 || iters_per_warp > (int64_t(1) << 40))
+    return NSA_ERR_SHAPE;
+  reduce_rows_probe_kernel<<<static_cast<unsigned>(ctas), warps_per_cta * 32, 0,
+                             static_cast<cudaStream_t>(stream)>>>(buf, rows, stride,
+                                                                  iters_per_warp, seed);
+  return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
 }  // extern "C"

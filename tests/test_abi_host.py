@@ -325,3 +325,15 @@ def test_rows_probe_rejects_bad_arguments(lib, over, status):
 
 def test_rows_probe_empty_is_a_no_op(lib):
     assert call_rows_probe(lib, k=None, v=None, idx=None, M=0) == 0
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(buf=None), -1), (dict(buf=FAKE + 4), -6), (dict(rows=0), -2), (dict(stride=512), -2),
+    (dict(stride=1026), -2), (dict(ctas=0), -2), (dict(warps=33), -2), (dict(iters=-1), -2),
+])
+def test_reduce_probe_rejects_bad_arguments(lib, over, status):
+    a = dict(buf=FAKE, rows=1024, stride=8192, ctas=152, warps=4, iters=16)
+    a.update(over)
+    vp = ctypes.c_void_p
+    assert lib.nsa_probe_reduce_rows(vp(a["buf"]), a["rows"], a["stride"], a["ctas"], a["warps"],
+                                     a["iters"], 1, None) == status
