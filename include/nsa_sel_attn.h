@@ -288,8 +288,10 @@ int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_
  * order set by atomics (equal within rounding from run to run). With
  * D = 128 every key of a selected block enters dQ (with weight 0 where the
  * query does not see it), so K must be finite in the selected blocks,
- * including keys after a query's position. Asynchronous, allocates nothing;
- * errors as nsa_sel_attn_fwd plus NSA_ERR_WORKSPACE. Pointers must be
+ * including keys after a query's position. With D = 128 the index transpose
+ * runs on a second stream that the call creates and releases, beside the
+ * per-row stage; `stream` waits for it. Asynchronous, allocates no device
+ * memory; errors as nsa_sel_attn_fwd plus NSA_ERR_WORKSPACE. Pointers must be
  * 16-byte aligned (LSE and block_indices 4-byte).
  */
 int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V,

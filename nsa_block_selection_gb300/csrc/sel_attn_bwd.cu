@@ -1351,6 +1351,37 @@ static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, i
   return pl;
 }
 
+// A second stream and its fork / join events for one call, released when
+// the call returns (CUDA defers the release until the queued work is done).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ok = false;
+  SideStream() {
+    // the highest priority: its few CTAs are scheduled as soon as SM slots
+    // free up, beside the long grid already running on the caller's stream
+    int lo = 0, hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) hi = 0;
+    ok = cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, hi) == cudaSuccess &&
+         cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess;
+  }
+  // `st` waits for everything queued on the side stream; if that cannot be
+  // arranged, the side stream is waited for here, so no queued work outlives
+  // an error return. False in that case.
+  bool join_into(cudaStream_t st) {
+    if (cudaEventRecord(join, s) == cudaSuccess && cudaStreamWaitEvent(st, join, 0) == cudaSuccess)
+      return true;
+    cudaStreamSynchronize(s);
+    return false;
+  }
+  ~SideStream() {
+    if (join) cudaEventDestroy(join);
+    if (fork) cudaEventDestroy(fork);
+    if (s) cudaStreamDestroy(s);
+  }
+};
+
 template <int D>
 static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
                       const BwdPlan& pl, cudaStream_t st) {
@@ -1372,10 +1403,46 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   const int64_t B = p.units / (p.M * p.G * p.nsub);
   if (p.N > 0 &&
       (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
-       cudaMemsetAsync(p.dV, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
-       cudaMemsetAsync(count, 0, static_cast<size_t>(pl.L) * 4, st) != cudaSuccess ||
-       cudaMemsetAsync(cursor, 0, static_cast<size_t>(pl.L) * 4, st) != cudaSuccess))
+       cudaMemsetAsync(p.dV, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess))
     return NSA_ERR_LAUNCH;
+  const int64_t chunks = pl.max_chunks;
+  int* order = reinterpret_cast<int*>(ws + pl.off_order);
+
+  // stage 2 on stream s2: the transposed index (count, scan, fill, chunk ->
+  // list table) and, with D = 128, the chunks' launch order. It reads only
+  // the index tensor.
+  auto stage2 = [&](cudaStream_t s2) -> int {
+    if (cudaMemsetAsync(count, 0, static_cast<size_t>(pl.L) * 4, s2) != cudaSuccess ||
+        cudaMemsetAsync(cursor, 0, static_cast<size_t>(pl.L) * 4, s2) != cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    // grid-stride: a few CTAs per SM are enough for atomics on small tables
+    const int64_t grid_e =
+        (pl.entries + 255) / 256 < 152 * 4 ? (pl.entries + 255) / 256 : 152 * 4;
+    csr_count_kernel<<<static_cast<unsigned>(grid_e), 256, 0, s2>>>(p, count);
+    csr_scan_kernel<<<1, 1024, 0, s2>>>(count, offs, choffs, static_cast<int>(pl.L),
+                                        kQueriesPerChunk);
+    csr_fill_kernel<<<static_cast<unsigned>(grid_e), 256, 0, s2>>>(p, cursor, lists);
+    csr_chunk_list_kernel<<<static_cast<unsigned>((pl.L + 255) / 256), 256, 0, s2>>>(
+        choffs, static_cast<int>(pl.L), chunk_list);
+    if constexpr (D == 128) {
+      // launch order of the chunks: by mean query position, bucketed per (b, g)
+      int* key = reinterpret_cast<int*>(ws + pl.off_key);
+      int* bcount = reinterpret_cast<int*>(ws + pl.off_bcount);
+      int* bcursor = reinterpret_cast<int*>(ws + pl.off_bcursor);
+      int* boffs = reinterpret_cast<int*>(ws + pl.off_boffs);
+      int* bscratch = reinterpret_cast<int*>(ws + pl.off_bscratch);
+      if (cudaMemsetAsync(bcount, 0, static_cast<size_t>(pl.nkeys) * 4, s2) != cudaSuccess ||
+          cudaMemsetAsync(bcursor, 0, static_cast<size_t>(pl.nkeys) * 4, s2) != cudaSuccess)
+        return NSA_ERR_LAUNCH;
+      chunk_key_kernel<<<static_cast<unsigned>((chunks + 7) / 8), 256, 0, s2>>>(
+          p, static_cast<int>(pl.nbkt), key, bcount);
+      csr_scan_kernel<<<1, 1024, 0, s2>>>(bcount, boffs, bscratch, static_cast<int>(pl.nkeys),
+                                          1);
+      chunk_order_fill_kernel<<<static_cast<unsigned>((chunks + 255) / 256), 256, 0, s2>>>(
+          p, key, boffs, bcursor, order);
+    }
+    return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
+  };
 
   CUtensorMap tk, tv, tkb, tvb;
   const bool have_keys = p.N > 0;
@@ -1394,11 +1461,31 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   if constexpr (D == 128) {
     // stage 1: the key-major kernel accumulates dQ too; here only its
     // per-row inputs (fp16 dO, LSE, delta) and a zeroed dQ
-    if (cudaMemsetAsync(p.dQ, 0, static_cast<size_t>(B * p.M * p.H * D) * 4, st) != cudaSuccess)
-      return NSA_ERR_LAUNCH;
-    if (!have_keys || p.T == 0) return NSA_OK;  // dQ = dK = dV = 0
+    if (!have_keys || p.T == 0) {  // dQ = dK = dV = 0
+      return cudaMemsetAsync(p.dQ, 0, static_cast<size_t>(B * p.M * p.H * D) * 4, st) ==
+                     cudaSuccess
+                 ? NSA_OK
+                 : NSA_ERR_LAUNCH;
+    }
+    // Stage 2 runs beside stage 1 on a second stream: stage 1 streams dO and
+    // O through HBM (and zeroes dQ), stage 2 counts and files the index
+    // entries with atomics on small tables, and neither touches what the
+    // other writes. The caller's stream waits for both before the key-major
+    // kernel.
+    SideStream side;
+    int rc2 = NSA_ERR_LAUNCH;
+    if (side.ok && cudaEventRecord(side.fork, st) == cudaSuccess &&
+        cudaStreamWaitEvent(side.s, side.fork, 0) == cudaSuccess)
+      rc2 = stage2(side.s);
+    else
+      rc2 = stage2(st);  // no second stream: in order on the caller's stream
+    bool rc1 =
+        cudaMemsetAsync(p.dQ, 0, static_cast<size_t>(B * p.M * p.H * D) * 4, st) == cudaSuccess;
     sel_attn_bwd_prep_kernel<D><<<static_cast<unsigned>((p.units + 7) / 8), 256, 0, st>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
+    rc1 = rc1 && cudaGetLastError() == cudaSuccess;
+    if (side.ok && !side.join_into(st)) return NSA_ERR_LAUNCH;
+    if (rc2 != NSA_OK) return rc2;
+    if (!rc1) return NSA_ERR_LAUNCH;
   } else {
     // stage 1: dQ and delta
     auto kq = sel_attn_bwd_dq_kernel<D, W>;
@@ -1410,15 +1497,10 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     if (!have_keys || p.T == 0) return NSA_OK;  // dK = dV = 0
   }
 
-  // stage 2: transposed index
-  const int64_t grid_e = (pl.entries + 255) / 256 < 152 * 64 ? (pl.entries + 255) / 256 : 152 * 64;
-  csr_count_kernel<<<static_cast<unsigned>(grid_e), 256, 0, st>>>(p, count);
-  csr_scan_kernel<<<1, 1024, 0, st>>>(count, offs, choffs, static_cast<int>(pl.L),
-                                      kQueriesPerChunk);
-  csr_fill_kernel<<<static_cast<unsigned>(grid_e), 256, 0, st>>>(p, cursor, lists);
-  csr_chunk_list_kernel<<<static_cast<unsigned>((pl.L + 255) / 256), 256, 0, st>>>(
-      choffs, static_cast<int>(pl.L), chunk_list);
-  if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
+  if constexpr (D != 128) {
+    const int rc2 = stage2(st);  // after stage 1, on the caller's stream
+    if (rc2 != NSA_OK) return rc2;
+  }
 
   // stage 3: dK, dV; grid bound: sum over lists of ceil(count / chunk)
   CUtensorMap tq, tdo;
@@ -1426,7 +1508,6 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   if (!encode_rows_map(&tq, p.Q, B * p.M * p.H, D, hw0) ||
       !encode_rows_map(&tdo, p.dO16, B * p.M * p.H, D, hw0))
     return NSA_ERR_LAUNCH;
-  const int64_t chunks = pl.max_chunks;
   auto run = [&](auto kt, auto split) -> int {
     constexpr int KT = decltype(kt)::value;
     using Ck = DkvCfg<D, KT>;
@@ -1454,23 +1535,7 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     if (hw0 == kHeadsPerGroup && (!encode_rows_halves_map(&tq3, p.Q, B * p.M * p.H, hw0) ||
                                   !encode_rows_halves_map(&tdo3, p.dO16, B * p.M * p.H, hw0)))
       return NSA_ERR_LAUNCH;
-    // launch order of the chunks: by mean query position, bucketed per (b, g)
-    int* order = reinterpret_cast<int*>(ws + pl.off_order);
-    int* key = reinterpret_cast<int*>(ws + pl.off_key);
-    int* bcount = reinterpret_cast<int*>(ws + pl.off_bcount);
-    int* bcursor = reinterpret_cast<int*>(ws + pl.off_bcursor);
-    int* boffs = reinterpret_cast<int*>(ws + pl.off_boffs);
-    int* bscratch = reinterpret_cast<int*>(ws + pl.off_bscratch);
-    if (cudaMemsetAsync(bcount, 0, static_cast<size_t>(pl.nkeys) * 4, st) != cudaSuccess ||
-        cudaMemsetAsync(bcursor, 0, static_cast<size_t>(pl.nkeys) * 4, st) != cudaSuccess)
-      return NSA_ERR_LAUNCH;
-    chunk_key_kernel<<<static_cast<unsigned>((chunks + 7) / 8), 256, 0, st>>>(
-        p, static_cast<int>(pl.nbkt), key, bcount);
-    csr_scan_kernel<<<1, 1024, 0, st>>>(bcount, boffs, bscratch, static_cast<int>(pl.nkeys), 1);
-    chunk_order_fill_kernel<<<static_cast<unsigned>((chunks + 255) / 256), 256, 0, st>>>(
-        p, key, boffs, bcursor, order);
-    if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
-    p.chunk_order = order;
+    p.chunk_order = order;  // written by stage 2
     auto kk = split ? sel_attn_bwd_dkv_tc_kernel<true> : sel_attn_bwd_dkv_tc_kernel<false>;
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkvTcCfg::kSmemBytes) != cudaSuccess)
