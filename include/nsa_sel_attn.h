@@ -316,7 +316,8 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V,
  * workspace. A problem whose scratch (nsa_sel_attn_bwd_workspace_bytes)
  * exceeds 64 MiB is rejected with NSA_ERR_SCRATCH before anything is
  * launched; a problem without queries (B == 0 or M == 0) needs no scratch
- * and only zeroes dK and dV. The call allocates and frees nothing. Every
+ * and only zeroes dK and dV. The call allocates and frees nothing and creates
+ * no stream: all of its stages run in order on `stream`. Every
  * call looks up the array's device address in the current device's context
  * (cudaGetSymbolAddress: a host-side query, no allocation, no
  * synchronisation), so a context created anew after cudaDeviceReset gets

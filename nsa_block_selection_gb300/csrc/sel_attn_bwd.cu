@@ -1357,7 +1357,8 @@ struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   bool ok = false;
-  SideStream() {
+  explicit SideStream(bool wanted) {
+    if (!wanted) return;  // ok stays false: everything runs on the caller's stream
     // the highest priority: its few CTAs are scheduled as soon as SM slots
     // free up, beside the long grid already running on the caller's stream
     int lo = 0, hi = 0;
@@ -1384,7 +1385,7 @@ struct SideStream {
 
 template <int D>
 static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
-                      const BwdPlan& pl, cudaStream_t st) {
+                      const BwdPlan& pl, cudaStream_t st, bool second_stream) {
   constexpr int W = 4;
   using Cq = DqCfg<D, W>;
   int* count = reinterpret_cast<int*>(ws + pl.off_count);
@@ -1472,7 +1473,7 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     // entries with atomics on small tables, and neither touches what the
     // other writes. The caller's stream waits for both before the key-major
     // kernel.
-    SideStream side;
+    SideStream side(second_stream);
     int rc2 = NSA_ERR_LAUNCH;
     if (side.ok && cudaEventRecord(side.fork, st) == cudaSuccess &&
         cudaStreamWaitEvent(side.s, side.fork, 0) == cudaSuccess)
@@ -1615,7 +1616,7 @@ static int run_bwd(const void* Q, const void* K, const void* V, const int32_t* i
                    const float* O, const float* LSE, const float* dO, float* dQ, float* dK,
                    float* dV, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
                    int64_t T, int block_size, float scale, const BwdPlan& pl, uint8_t* ws,
-                   cudaStream_t st) {
+                   cudaStream_t st, bool second_stream) {
   BwdProblem p;
   p.Q = static_cast<const __half*>(Q);
   p.idx = idx;
@@ -1639,7 +1640,8 @@ static int run_bwd(const void* Q, const void* K, const void* V, const int32_t* i
   p.L = static_cast<int>(pl.L);
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   p.sl2 = p.scale * 1.4426950408889634f;
-  return D == 64 ? launch_bwd<64>(p, K, V, ws, pl, st) : launch_bwd<128>(p, K, V, ws, pl, st);
+  return D == 64 ? launch_bwd<64>(p, K, V, ws, pl, st, second_stream)
+                 : launch_bwd<128>(p, K, V, ws, pl, st, second_stream);
 }
 
 }  // namespace nsa
@@ -1678,7 +1680,7 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t*
   rc = bwd_check_pointers(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, N, T, workspace);
   if (rc != NSA_OK) return rc;
   return run_bwd(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, B, M, N, H, G, D, T,
-                 block_size, scale, pl, static_cast<uint8_t*>(workspace), st);
+                 block_size, scale, pl, static_cast<uint8_t*>(workspace), st, true);
 }
 
 int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
@@ -1703,7 +1705,7 @@ int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
   if (scratch == nullptr) return NSA_ERR_LAUNCH;
   return run_bwd(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, B, M, N, H, G, D, T,
                  block_size, scale, pl, static_cast<uint8_t*>(scratch),
-                 static_cast<cudaStream_t>(stream));
+                 static_cast<cudaStream_t>(stream), false);
 }
 
 }  // extern "C"
