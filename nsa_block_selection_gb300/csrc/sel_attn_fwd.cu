@@ -73,13 +73,18 @@ struct Problem {
   float sl2;      // scale * log2(e)
 };
 
-template <int D, int WARPS>
+template <int D, int WARPS, bool SHARED = false>
 struct Cfg {
   static constexpr int kBoxes = D / kBoxCols;            // TMA boxes per tile
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one K (or V) tile = one slot
   static constexpr int kWarpBytes = 2 * kTileBytes;      // slot 0: K, slot 1: V
   static constexpr int kBarOffset = WARPS * kWarpBytes;
-  static constexpr int kSmemBytes = kBarOffset + WARPS * 2 * 8 + 1024;  // + align slack
+  // two-pass gather kernel: per warp, the tile-shared pass's partial O of its
+  // 8 heads (fp32, contiguous) and the barrier its bulk copy completes on
+  static constexpr int kPartBytes = SHARED ? kHeadsPerGroup * D * 4 : 0;
+  static constexpr int kPartBarOffset = kBarOffset + WARPS * 2 * 8;
+  static constexpr int kPartOffset = kPartBarOffset + (SHARED ? WARPS * 8 : 0);
+  static constexpr int kSmemBytes = kPartOffset + WARPS * kPartBytes + 1024;  // + align slack
   static constexpr int kSteps = D / 16;
 };
 
@@ -99,7 +104,7 @@ template <int D, int WARPS, bool BF16, bool O16, bool SHARED = false>
 __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
     sel_attn_fwd_kernel(const Problem p, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
-  using C = Cfg<D, WARPS>;
+  using C = Cfg<D, WARPS, SHARED>;
   extern __shared__ uint8_t smem_raw[];
 
   const int warp = threadIdx.x >> 5;
@@ -130,12 +135,15 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t slots = base + warp * C::kWarpBytes;
   const uint32_t bars = base + C::kBarOffset + warp * 2 * 8;
+  const uint32_t part_bar = base + C::kPartBarOffset + warp * 8;  // two-pass only
+  const uint32_t part = base + C::kPartOffset + warp * C::kPartBytes;
 
   if (lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     mbar_init(bars, 1);
     mbar_init(bars + 8, 1);
+    if constexpr (SHARED) mbar_init(part_bar, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -199,31 +207,21 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   float nega = 0.f, negb = 0.f;            // -reference (0 while a head has seen nothing)
   float la = 0.f, lb = 0.f;                // this lane's share of the row sums
   const float sl2 = p.sl2;
+  // two-pass: the tile-shared pass's normalised partial O (8 head rows, 4 KB
+  // contiguous) is copied into this warp's shared buffer now and its LSE
+  // read into registers; both are merged into the result in the epilogue,
+  // so their latency hides behind the whole gather
+  float lsa = -INFINITY, lsb = -INFINITY;
   if constexpr (SHARED) {
     if (shared_cnt > 0) {
-      constexpr float kLog2e = 1.4426950408889634f;
+      if (lane == 0) {
+        const float* o = static_cast<const float*>(p.O) + b * p.o_sb + m * p.o_sm + hbase * p.o_sh;
+        mbar_arrive_expect_tx(part_bar, C::kPartBytes);
+        bulk_load(part, o, C::kPartBytes, part_bar);
+      }
       const float* L = p.LSE + (b * p.H + hbase + 2 * tig) * p.M + m;
-      const float lsa = L[0], lsb = L[p.M];
-      const float* o = static_cast<const float*>(p.O) + b * p.o_sb + m * p.o_sm +
-                       (hbase + 2 * tig) * p.o_sh + gid;
-      const float* o2 = o + p.o_sh;
-#pragma unroll
-      for (int i = 0; i < C::kSteps; ++i) {
-        acc[i][0] = o[16 * i];
-        acc[i][2] = o[16 * i + 8];
-        acc[i][1] = o2[16 * i];
-        acc[i][3] = o2[16 * i + 8];
-      }
-      if (lsa > -INFINITY) {
-        m2a = lsa * kLog2e;
-        nega = -m2a;
-        la = gid == 0 ? 1.f : 0.f;
-      }
-      if (lsb > -INFINITY) {
-        m2b = lsb * kLog2e;
-        negb = -m2b;
-        lb = gid == 0 ? 1.f : 0.f;
-      }
+      lsa = L[0];
+      lsb = L[p.M];
     }
   }
 
@@ -335,6 +333,9 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   if (timed_out) {
     // copies still in flight target this warp's slots: let them land first
     if (lane == 0) report_timeout();
+    if constexpr (SHARED) {
+      if (shared_cnt > 0) wait_phase(part_bar, 0, kWaitLimitNs);
+    }
     if (timed_out == 1) {
       wait_phase(bar_k, phase, kWaitLimitNs);
       wait_phase(bar_v, phase, kWaitLimitNs);
@@ -350,6 +351,44 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   for (int off = 4; off < 32; off <<= 1) {
     la += __shfl_xor_sync(kFull, la, off);
     lb += __shfl_xor_sync(kFull, lb, off);
+  }
+  if constexpr (SHARED) {
+    if (shared_cnt > 0) {
+      // merge the partial state: O_s (normalised, weight 2^Ls in log2 units)
+      // with this warp's (acc, l) relative to 2^ref
+      if (!__all_sync(kFull, wait_phase(part_bar, 0, kWaitLimitNs))) {
+        if (lane == 0) report_timeout();
+        return;
+      }
+      constexpr float kLog2e = 1.4426950408889634f;
+      float ga = 1.f, sa = 0.f, gb = 1.f, sb = 0.f;  // gather and partial weights
+      if (lsa > -INFINITY) {
+        const float ls = lsa * kLog2e;
+        const float r = fmaxf(m2a, ls);
+        ga = m2a == -INFINITY ? 0.f : ex2(m2a - r);
+        sa = ex2(ls - r);
+        m2a = r;
+        la = la * ga + sa;
+      }
+      if (lsb > -INFINITY) {
+        const float ls = lsb * kLog2e;
+        const float r = fmaxf(m2b, ls);
+        gb = m2b == -INFINITY ? 0.f : ex2(m2b - r);
+        sb = ex2(ls - r);
+        m2b = r;
+        lb = lb * gb + sb;
+      }
+      // acc[i][0 / 2]: head 2 tig, dims 16 i + gid (+ 8); [1 / 3]: head 2 tig + 1
+      const uint32_t pa = part + (2 * tig) * (D * 4) + gid * 4;
+      const uint32_t pbh = pa + D * 4;
+#pragma unroll
+      for (int i = 0; i < C::kSteps; ++i) {
+        acc[i][0] = fmaf(acc[i][0], ga, sa * ld_shared_f32(pa + 64 * i));
+        acc[i][2] = fmaf(acc[i][2], ga, sa * ld_shared_f32(pa + 64 * i + 32));
+        acc[i][1] = fmaf(acc[i][1], gb, sb * ld_shared_f32(pbh + 64 * i));
+        acc[i][3] = fmaf(acc[i][3], gb, sb * ld_shared_f32(pbh + 64 * i + 32));
+      }
+    }
   }
   const float inva = la > 0.f ? 1.f / la : 0.f;
   const float invb = lb > 0.f ? 1.f / lb : 0.f;
@@ -414,7 +453,7 @@ template <int D, bool BF16, bool O16, bool SHARED = false>
 static int launch_fwd(const Problem& p, const void* K, const void* V, int64_t B,
                       const int64_t (&ks)[3], const int64_t (&vs)[3], cudaStream_t stream) {
   constexpr int W = NSA_WARPS;
-  using C = Cfg<D, W>;
+  using C = Cfg<D, W, SHARED>;
   constexpr CUtensorMapDataType dt =
       BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tk, tv;
