@@ -330,14 +330,41 @@ def run_reference(args):
     return 0
 
 
+class nvtx_range:
+    """An NVTX range around a bench leg (visible in a profiler's timeline;
+    a no-op without one)."""
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        try:
+            import torch
+
+            torch.cuda.nvtx.range_push(self.name)
+            self.pushed = True
+        except Exception:  # noqa: BLE001 -- no NVTX: nothing to mark
+            self.pushed = False
+        return self
+
+    def __exit__(self, *exc):
+        if self.pushed:
+            import torch
+
+            torch.cuda.nvtx.range_pop()
+        return False
+
+
 def run_leg(enabled, fn, *a):
     """fn(*a) when enabled, else None; an exception becomes {"error": repr}
     (also printed to stderr), so one failing auxiliary measurement does not
-    take the measured headline with it."""
+    take the measured headline with it. Each leg runs in an NVTX range of its
+    name."""
     if not enabled:
         return None
     try:
-        return fn(*a)
+        with nvtx_range(fn.__name__):
+            return fn(*a)
     except Exception as e:  # noqa: BLE001 -- reported in the JSON line, not hidden
         print(f"bench: {fn.__name__} failed: {e!r}", file=sys.stderr, flush=True)
         return {"error": repr(e)}
@@ -394,7 +421,8 @@ def run_ours(args):
 
     clocks = ClockSampler(gpu_smi_id(dev))
     clocks.start()
-    times, wall = time_steps(step, args.steps, args.warmup, flush, barrier)
+    with nvtx_range("headline forward"):
+        times, wall = time_steps(step, args.steps, args.warmup, flush, barrier)
     clk = clocks.stop()
     t_ms, flops_all, bytes_all = reduce_over_ranks(statistics.mean(times), work["flops"],
                                                    work["gathered_bytes"], dist)
@@ -404,7 +432,8 @@ def run_ours(args):
     # e2e: host buffers through the C ABI each step
     e2e = None
     if not args.skip_e2e:
-        e2e = run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist)
+        with nvtx_range("e2e host buffers"):
+            e2e = run_e2e(w, q_np, k_np, v_np, idx_np, work, args, barrier, dev, dist)
 
     # The legs below run on rank 0 of a 1-GPU run only. A leg that raises is
     # reported in its own key ({"error": ...}) so the measured headline above

@@ -61,8 +61,12 @@ typedef enum nsa_status {
   NSA_ERR_WORKSPACE = -9,   /* workspace NULL or smaller than required        */
   NSA_ERR_SCRATCH = -10,    /* problem needs more scratch than the fixed
                                buffer of nsa_sel_attn_bwd_noalloc (64 MiB)    */
-  NSA_ERR_DTYPE = -11       /* element type combination not supported by
+  NSA_ERR_DTYPE = -11,      /* element type combination not supported by
                                nsa_sel_attn_fwd_ex                            */
+  NSA_ERR_BOUNDS = -12      /* (library built with NSA_DEBUG_BOUNDS only) a
+                               kernel's own bounds check found a tile outside
+                               the keys its row may read; reported by
+                               nsa_sync_status                                */
 } nsa_status;
 
 /* Element types of nsa_sel_attn_fwd_ex. */
@@ -414,7 +418,11 @@ int nsa_swa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE
  * copies in flight land, and returns without writing its outputs. This call
  * returns NSA_ERR_TIMEOUT if that happened in any launch since the last call,
  * NSA_ERR_LAUNCH if synchronising the stream reports a CUDA error, NSA_OK
- * otherwise. It synchronises; it allocates nothing.
+ * otherwise. A library built with NSA_DEBUG_BOUNDS also checks, before every
+ * K/V tile copy of the selection forward, that the tile starts on a 16-key
+ * boundary, at or before the query's last visible key, inside a block of the
+ * index range; a failed check is returned here as NSA_ERR_BOUNDS (ahead of a
+ * timeout). It synchronises; it allocates nothing.
  */
 int nsa_sync_status(void* stream);
 

@@ -25,6 +25,8 @@ const char* nsa_status_string(int status) {
       return "problem needs more scratch than the fixed buffer of the no-allocation entry point";
     case NSA_ERR_DTYPE:
       return "unsupported dtype: Q/K/V fp16 or bf16; O fp32 or the type of Q/K/V";
+    case NSA_ERR_BOUNDS:
+      return "a debug-build bounds check failed (library built with NSA_DEBUG_BOUNDS)";
     default: return "unknown status";
   }
 }
@@ -40,7 +42,9 @@ int nsa_sync_status(void* stream) {
   if (nsa::swa_read_and_clear_status(&swa) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::shared_read_and_clear_status(&shr) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::probe_read_and_clear_status(&prb) != NSA_OK) return NSA_ERR_LAUNCH;
-  return (fwd | bwd | swa | shr | prb) ? NSA_ERR_TIMEOUT : NSA_OK;
+  const unsigned int all = fwd | bwd | swa | shr | prb;
+  if (all & 2u) return NSA_ERR_BOUNDS;
+  return all ? NSA_ERR_TIMEOUT : NSA_OK;
 }
 
 }  // extern "C"

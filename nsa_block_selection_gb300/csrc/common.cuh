@@ -41,6 +41,11 @@ static __device__ unsigned int g_status_word = 0u;
 
 __device__ __forceinline__ void report_timeout() { atomicOr(&g_status_word, 1u); }
 
+// Bit 1: a check of the NSA_DEBUG_BOUNDS build found an address outside
+// what the operation may touch (the access itself is still bounded: TMA
+// reads outside a tensor map return zeros).
+__device__ __forceinline__ void report_bounds() { atomicOr(&g_status_word, 2u); }
+
 // Reads and clears this translation unit's status word (current device).
 static inline int read_and_clear_status(unsigned int* value) {
   if (cudaMemcpyFromSymbol(value, g_status_word, sizeof(*value)) != cudaSuccess)

@@ -175,6 +175,12 @@ __global__ void __launch_bounds__(WARPS * 32, NSA_MIN_BLOCKS)
   const uint32_t sv = slots + C::kTileBytes;
   const uint32_t bar_k = bars, bar_v = bars + 8;
   auto issue = [&](uint32_t dst, uint32_t bar, const CUtensorMap* tm, int n0) {
+#ifdef NSA_DEBUG_BOUNDS
+    // a tile the row may read: on a 16-key boundary, at or before the last
+    // visible key, inside a block of the index range
+    if (lane == 0 && (n0 < 0 || n0 % kTileKeys != 0 || n0 > lastkey || n0 / p.bs >= p.nblk))
+      report_bounds();
+#endif
     if (lane == 0) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, C::kTileBytes);

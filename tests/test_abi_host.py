@@ -54,7 +54,7 @@ def test_exports_match_header(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, -12, -1):
+    for code in range(0, -13, -1):
         s = lib.nsa_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.nsa_status_string(-99).decode() == "unknown status"
