@@ -258,6 +258,23 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
                           int64_t workspace_bytes, int64_t chunk_m, void* stream);
 
 /*
+ * nsa_sel_attn_fwd_host_ex -- nsa_sel_attn_fwd_host with the element types of
+ * nsa_sel_attn_fwd_ex: Q, K, V in host memory as qkv_dtype (NSA_F16 or
+ * NSA_BF16), O written as o_dtype (NSA_F32 or qkv_dtype); LSE fp32. Any
+ * other combination returns NSA_ERR_DTYPE before anything is enqueued. The
+ * workspace of nsa_sel_attn_fwd_host_workspace_bytes (sized for fp32 O)
+ * suffices for every combination. Results are bit-identical to
+ * nsa_sel_attn_fwd_ex on the same inputs; everything else is
+ * nsa_sel_attn_fwd_host.
+ */
+int nsa_sel_attn_fwd_host_ex(const void* Q, const void* K, const void* V,
+                             const int32_t* block_indices, void* O, float* LSE, int64_t B,
+                             int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                             int block_size, float scale, int qkv_dtype, int o_dtype,
+                             void* workspace, int64_t workspace_bytes, int64_t chunk_m,
+                             void* stream);
+
+/*
  * nsa_sel_attn_bwd_workspace_bytes -- device workspace nsa_sel_attn_bwd
  * needs: an fp16 copy of dO, one 64-byte (LSE, delta) record per (b, m, g,
  * 8-head sub-group), the per-(b, g, block) query lists (at most B*M*G*T

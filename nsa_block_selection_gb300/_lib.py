@@ -25,7 +25,7 @@ EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sel_attn
            "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks", "nsa_swa_fwd",
            "nsa_sel_attn_fwd_shared_workspace_bytes", "nsa_sel_attn_fwd_shared",
            "nsa_probe_l2_gather", "nsa_probe_l2_gather_bytes", "nsa_probe_gather_rows",
-           "nsa_probe_reduce_rows")
+           "nsa_probe_reduce_rows", "nsa_sel_attn_fwd_host_ex")
 
 _lib = None
 
@@ -87,6 +87,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                 ctypes.c_float, c_int, vp]
     lib.nsa_topk_blocks.restype = c_int
     lib.nsa_topk_blocks.argtypes = [vp, vp, i64, i64, i64, i64, i64, c_int, c_int, c_int, vp]
+    lib.nsa_sel_attn_fwd_host_ex.restype = c_int
+    lib.nsa_sel_attn_fwd_host_ex.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                             i64, i64, c_int, ctypes.c_float, c_int, c_int, vp,
+                                             i64, i64, vp]
     lib.nsa_sel_attn_fwd_host.restype = c_int
     lib.nsa_sel_attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                           i64, c_int, ctypes.c_float, vp, i64, i64, vp]
@@ -257,41 +261,54 @@ def host_workspace_bytes(B, M, N, H, G, D, T, block_size, chunk_m=0) -> int:
 
 def sel_attn_fwd_host(q, k, v, block_indices, block_size: int, scale: Optional[float] = None,
                       out=None, lse=None, chunk_m: int = 0, workspace=None, device=None,
-                      stream=None, sync: bool = True):
+                      stream=None, sync: bool = True, out_dtype=None):
     """Forward with host (CPU) tensors in and out, through the library's
     pipelined host entry point (pin the tensors for overlapped copies).
 
-    Returns (O, LSE) as CPU fp32 tensors. ``workspace`` is a CUDA uint8
-    tensor of at least :func:`host_workspace_bytes`; one is allocated when
-    omitted. With ``sync=False`` the call returns once everything is
-    enqueued on ``stream``.
+    q, k, v fp16 or bf16. Returns (O, LSE) as CPU tensors: O fp32 unless
+    ``out_dtype`` (or a preallocated ``out``) is q's dtype, LSE fp32.
+    ``workspace`` is a CUDA uint8 tensor of at least
+    :func:`host_workspace_bytes`; one is allocated when omitted. With
+    ``sync=False`` the call returns once everything is enqueued on ``stream``.
     """
     import torch
 
     lib = load()
-    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=False)
+    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=False,
+                                        qkv_dtypes=(torch.float16, torch.bfloat16))
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.float32
+    if out_dtype not in (torch.float32, q.dtype):
+        raise TypeError(f"O must be fp32 or {q.dtype}, got {out_dtype}")
     device = torch.device(device) if device is not None else torch.device("cuda",
                                                                         torch.cuda.current_device())
     need = host_workspace_bytes(B, M, N, H, G, D, T, block_size, chunk_m)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
     if out is None:
-        out = torch.empty((B, M, H, D), dtype=torch.float32, pin_memory=True)
+        out = torch.empty((B, M, H, D), dtype=out_dtype, pin_memory=True)
     if lse is None:
         lse = torch.empty((B, H, M), dtype=torch.float32, pin_memory=True)
-    if out.is_cuda or lse.is_cuda or out.dtype != torch.float32 or lse.dtype != torch.float32:
-        raise ValueError("out and lse must be fp32 CPU tensors")
+    if out.is_cuda or lse.is_cuda or out.dtype != out_dtype or lse.dtype != torch.float32:
+        raise ValueError(f"out must be a {out_dtype} CPU tensor and lse an fp32 one")
     if tuple(out.shape) != (B, M, H, D) or tuple(lse.shape) != (B, H, M):
         raise ValueError("out must be [B, M, H, D] and lse [B, H, M]")
     if stream is None:
         stream = torch.cuda.current_stream(device)
     sc = float(scale) if scale is not None else 0.0  # the ABI: <= 0 selects 1/sqrt(D)
-    st = lib.nsa_sel_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out),
-                                   _ptr(lse), B, M, N, H, G, D, T, int(block_size), sc,
-                                   workspace.data_ptr(), workspace.numel(), int(chunk_m),
-                                   ctypes.c_void_p(stream.cuda_stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(out), _ptr(lse), B, M, N, H,
+            G, D, T, int(block_size), sc)
+    tail = (workspace.data_ptr(), workspace.numel(), int(chunk_m),
+            ctypes.c_void_p(stream.cuda_stream))
+    if q.dtype == torch.float16 and out.dtype == torch.float32:
+        st = lib.nsa_sel_attn_fwd_host(*args, *tail)
+        what = "nsa_sel_attn_fwd_host"
+    else:
+        st = lib.nsa_sel_attn_fwd_host_ex(*args, _dtype_code(q.dtype), _dtype_code(out.dtype),
+                                          *tail)
+        what = "nsa_sel_attn_fwd_host_ex"
     if st != NSA_OK:
-        raise NsaError(st, "nsa_sel_attn_fwd_host")
+        raise NsaError(st, what)
     if sync:
         stream.synchronize()
     return out, lse

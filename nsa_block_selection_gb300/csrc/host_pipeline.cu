@@ -135,14 +135,18 @@ int64_t nsa_sel_attn_fwd_host_workspace_bytes(int64_t B, int64_t M, int64_t N, i
   return static_cast<int64_t>(nsa::make_plan(B, M, N, H, G, D, T, chunk_m).total);
 }
 
-int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
-                          const int32_t* block_indices, float* O, float* LSE, int64_t B,
-                          int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
-                          int block_size, float scale, void* workspace, int64_t workspace_bytes,
-                          int64_t chunk_m, void* stream) {
+int nsa_sel_attn_fwd_host_ex(const void* Q, const void* K, const void* V,
+                             const int32_t* block_indices, void* O, float* LSE, int64_t B,
+                             int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                             int block_size, float scale, int qkv_dtype, int o_dtype,
+                             void* workspace, int64_t workspace_bytes, int64_t chunk_m,
+                             void* stream) {
   using namespace nsa;
   const int chk = check_sizes(B, M, N, H, G, D, T, block_size);
   if (chk != NSA_OK) return chk;
+  if ((qkv_dtype != NSA_F16 && qkv_dtype != NSA_BF16) ||
+      (o_dtype != NSA_F32 && o_dtype != qkv_dtype))
+    return NSA_ERR_DTYPE;
   if (B == 0 || M == 0) return NSA_OK;
   if (!Q || !O || !LSE) return NSA_ERR_NULL;
   if (N > 0 && (!K || !V)) return NSA_ERR_NULL;
@@ -160,7 +164,7 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
   const size_t kv_row = static_cast<size_t>(G * D) * 2;       // one key, all groups
   const size_t q_row = static_cast<size_t>(H * D) * 2;        // one query, all heads
   const size_t i_row = static_cast<size_t>(G * T) * 4;        // one query's index rows
-  const size_t o_row = static_cast<size_t>(H * D) * 4;        // one query's O rows
+  const size_t o_row = static_cast<size_t>(H * D) * (o_dtype == NSA_F32 ? 4 : 2);  // one query's O rows
   const uint8_t* hK = static_cast<const uint8_t*>(K);
   const uint8_t* hV = static_cast<const uint8_t*>(V);
   const uint8_t* hQ = static_cast<const uint8_t*>(Q);
@@ -180,7 +184,7 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
     const int64_t mc = (M - m0) < pl.chunk ? (M - m0) : pl.chunk;
     uint8_t* dQ = ws + pl.off_q[s];
     uint8_t* dI = ws + pl.off_idx[s];
-    float* dO = reinterpret_cast<float*>(ws + pl.off_o[s]);
+    void* dO = ws + pl.off_o[s];  // sized for fp32: a 16-bit O uses half
     float* dL = reinterpret_cast<float*>(ws + pl.off_lse[s]);
 
     // upload: visible K/V rows not yet on the device, then this chunk's rows
@@ -212,8 +216,8 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
     if (!ok) break;
     const int rc = launch_forward(dQ, N > 0 ? dK : nullptr, N > 0 ? dV : nullptr,
                                   T > 0 ? reinterpret_cast<const int32_t*>(dI) : nullptr, dO,
-                                  dL, B, mc, N, H, G, D, T, m0, block_size, scale, NSA_F16,
-                                  NSA_F32, nullptr, fs);
+                                  dL, B, mc, N, H, G, D, T, m0, block_size, scale, qkv_dtype,
+                                  o_dtype, nullptr, fs);
     if (rc != NSA_OK) {
       status = rc;
       break;
@@ -241,6 +245,16 @@ int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
     for (int i = 0; i < 3; ++i) cudaStreamSynchronize(internal[i]);
   if (status != NSA_OK) return status;
   return ok && joined ? NSA_OK : NSA_ERR_LAUNCH;
+}
+
+int nsa_sel_attn_fwd_host(const void* Q, const void* K, const void* V,
+                          const int32_t* block_indices, float* O, float* LSE, int64_t B,
+                          int64_t M, int64_t N, int64_t H, int64_t G, int64_t D, int64_t T,
+                          int block_size, float scale, void* workspace, int64_t workspace_bytes,
+                          int64_t chunk_m, void* stream) {
+  return nsa_sel_attn_fwd_host_ex(Q, K, V, block_indices, O, LSE, B, M, N, H, G, D, T,
+                                  block_size, scale, NSA_F16, NSA_F32, workspace, workspace_bytes,
+                                  chunk_m, stream);
 }
 
 }  // extern "C"

@@ -337,3 +337,13 @@ def test_reduce_probe_rejects_bad_arguments(lib, over, status):
     vp = ctypes.c_void_p
     assert lib.nsa_probe_reduce_rows(vp(a["buf"]), a["rows"], a["stride"], a["ctas"], a["warps"],
                                      a["iters"], 1, None) == status
+
+
+def test_host_ex_rejects_bad_dtypes(lib):
+    a = dict(GOOD)
+    vp = ctypes.c_void_p
+    for qkv, o in ((2, 2), (0, 1), (1, 0), (3, 2)):
+        st = lib.nsa_sel_attn_fwd_host_ex(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                          vp(FAKE), a["B"], a["M"], a["N"], a["H"], a["G"], a["D"],
+                                          a["T"], a["bs"], 0.0, qkv, o, vp(FAKE), 1 << 40, 0, None)
+        assert st == -11, (qkv, o)

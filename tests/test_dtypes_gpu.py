@@ -86,3 +86,30 @@ def test_dtype_variants_full_size_sampled(qkv, out):
     w = gen.workload("m8k_bs64")
     rows = sample_rows(w.B, w.M, w.G, w.block_size, 5, n_random=1024)
     _run(w, gen.default_seed(w.name), qkv, out, rows)
+
+
+@pytest.mark.parametrize("qkv,out", [("bf16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
+def test_host_entry_dtypes_match_device_entry(qkv, out):
+    """The host-buffer entry point with bf16 inputs and / or a 16-bit O:
+    bit-identical to the device entry point on the same inputs."""
+    import torch
+
+    from nsa_block_selection_gb300 import _lib
+    from nsa_block_selection_gb300 import inputs as gen
+    from nsa_block_selection_gb300 import sel_attn_fwd
+
+    w = gen.Workload("host_dt", 2, 700, 700, 16, 2, 128, 64, 6, 1.0, "first_two_local")
+    q, k, v = gen.make_qkv(w, 21, qkv)
+    idx = gen.make_block_indices(w, 21)
+    dt, ot = _torch_dtype(qkv), _torch_dtype(out)
+    hq, hk, hv = (torch.from_numpy(x).to(dt).pin_memory() for x in (q, k, v))
+    hi = torch.from_numpy(idx).pin_memory()
+    ho = torch.full((w.B, w.M, w.H, w.D), float("nan"), dtype=ot).pin_memory()
+    hl = torch.full((w.B, w.H, w.M), float("nan"), dtype=torch.float32).pin_memory()
+    O_h, L_h = _lib.sel_attn_fwd_host(hq, hk, hv, hi, w.block_size, out=ho, lse=hl, chunk_m=128)
+    O_d, L_d = sel_attn_fwd(*(t.cuda() for t in (hq, hk, hv, hi)), w.block_size,
+                            out=poisoned((w.B, w.M, w.H, w.D), ot),
+                            lse=poisoned((w.B, w.H, w.M), torch.float32))
+    torch.cuda.synchronize()
+    assert O_h.dtype == ot
+    assert torch.equal(O_h, O_d.cpu()) and torch.equal(L_h, L_d.cpu())
