@@ -825,6 +825,8 @@ def run_backward(w, q, k, v, idx, out, lse, work, flush, args):
     flops = work["flops"] // 4 * 10
     res = {"ms_per_step": t, "tflops": flops / (t * 1e-3) / 1e12, "flops_per_step": flops,
            "workspace_bytes": need, "steps": steps}
+    res["bf16"] = run_leg(True, backward_bf16, w, q, k, v, idx, out, lse, do, dq, dk, dv, ws,
+                          flush, steps, flops)
     if w.D == 128:
         # dQ = dS K per (query, selected block): every head of the group,
         # D fp32 values each, added with reductions
@@ -843,6 +845,29 @@ def run_backward(w, q, k, v, idx, out, lse, work, flush, args):
     del ws, do, dq, dk, dv
     torch.cuda.empty_cache()
     return res
+
+
+def backward_bf16(w, q, k, v, idx, out, lse, do, dq, dk, dv, ws, flush, steps, flops):
+    """The same backward with bf16 Q/K/V (nsa_sel_attn_bwd_ex): the inputs
+    converted once, O and LSE from the bf16 forward (untimed)."""
+    import torch
+
+    from nsa_block_selection_gb300 import _lib, sel_attn_fwd
+
+    qb, kb, vb = (x.to(torch.bfloat16) for x in (q, k, v))
+    ob, lb = torch.empty_like(out), torch.empty_like(lse)
+    sel_attn_fwd(qb, kb, vb, idx, w.block_size, w.scale, out=ob, lse=lb)
+
+    def step():
+        _lib.sel_attn_bwd(qb, kb, vb, idx, ob, lb, do, w.block_size, w.scale, dq=dq, dk=dk,
+                          dv=dv, workspace=ws)
+
+    times, _ = time_steps(step, steps, 3, flush, lambda: None)
+    t = statistics.mean(times)
+    del qb, kb, vb, ob, lb
+    torch.cuda.empty_cache()
+    return {"ms_per_step": t, "tflops": flops / (t * 1e-3) / 1e12, "steps": steps,
+            "inputs": "Q, K, V bf16; O, LSE, dO and the gradients fp32"}
 
 
 def reduction_ceiling(dq, w, seconds=0.3):

@@ -322,6 +322,26 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V,
                      float scale, void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
+ * nsa_sel_attn_bwd_ex -- nsa_sel_attn_bwd with a choice of input type.
+ *
+ *   qkv_dtype  NSA_F16 or NSA_BF16: the type of Q, K and V (else
+ *              NSA_ERR_DTYPE before anything is enqueued)
+ *
+ * With bf16 inputs every tensor-core product takes bf16 operands (the 16-bit
+ * copy of dO, P and dS are rounded to bf16) with fp32 accumulation -- the
+ * bf16 reading of "FP16 matmuls, FP32 accumulation" that nsa_sel_attn_fwd_ex
+ * takes for the forward. O, LSE, dO and the gradients stay fp32. Everything
+ * else, the workspace included, is nsa_sel_attn_bwd; nsa_sel_attn_bwd is
+ * this call with NSA_F16.
+ */
+int nsa_sel_attn_bwd_ex(const void* Q, const void* K, const void* V,
+                        const int32_t* block_indices, const float* O, const float* LSE,
+                        const float* dO, float* dQ, float* dK, float* dV, int64_t B, int64_t M,
+                        int64_t N, int64_t H, int64_t G, int64_t D, int64_t T, int block_size,
+                        float scale, int qkv_dtype, void* workspace, int64_t workspace_bytes,
+                        void* stream);
+
+/*
  * nsa_sel_attn_bwd_noalloc -- nsa_sel_attn_bwd for callers that cannot
  * allocate device memory. The pages have no counterpart to this entry point.
  *

@@ -25,7 +25,7 @@ EXPORTS = ("nsa_status_string", "nsa_version", "nsa_sel_attn_fwd", "nsa_sel_attn
            "nsa_sel_attn_bwd_noalloc", "nsa_topk_blocks", "nsa_swa_fwd",
            "nsa_sel_attn_fwd_shared_workspace_bytes", "nsa_sel_attn_fwd_shared",
            "nsa_probe_l2_gather", "nsa_probe_l2_gather_bytes", "nsa_probe_gather_rows",
-           "nsa_probe_reduce_rows", "nsa_sel_attn_fwd_host_ex")
+           "nsa_probe_reduce_rows", "nsa_sel_attn_fwd_host_ex", "nsa_sel_attn_bwd_ex")
 
 _lib = None
 
@@ -79,6 +79,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.nsa_sel_attn_bwd.restype = c_int
     lib.nsa_sel_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                      i64, i64, i64, c_int, ctypes.c_float, vp, i64, vp]
+    lib.nsa_sel_attn_bwd_ex.restype = c_int
+    lib.nsa_sel_attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                        i64, i64, i64, i64, c_int, ctypes.c_float, c_int, vp, i64,
+                                        vp]
     lib.nsa_sel_attn_bwd_noalloc.restype = c_int
     lib.nsa_sel_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64,
                                              i64, i64, i64, i64, i64, c_int, ctypes.c_float, vp]
@@ -326,14 +330,15 @@ def sel_attn_bwd(q, k, v, block_indices, o, lse, do, block_size: int,
                  stream=None):
     """Gradients of :func:`sel_attn_fwd`: returns (dQ, dK, dV) fp32 CUDA tensors.
 
-    ``o`` and ``lse`` are the forward's outputs, ``do`` the fp32 upstream
-    gradient [B, M, H, D]. ``workspace`` (CUDA uint8) is allocated when
-    omitted.
+    q, k, v fp16 or bf16 (as passed to the forward). ``o`` and ``lse`` are
+    the forward's fp32 outputs, ``do`` the fp32 upstream gradient
+    [B, M, H, D]. ``workspace`` (CUDA uint8) is allocated when omitted.
     """
     import torch
 
     lib = load()
-    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=True)
+    B, M, N, H, G, D, T = _check_common(q, k, v, block_indices, device_expected=True,
+                                        qkv_dtypes=(torch.float16, torch.bfloat16))
     for name, t, shape in (("o", o, (B, M, H, D)), ("lse", lse, (B, H, M)),
                            ("do", do, (B, M, H, D))):
         if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous() \
@@ -349,12 +354,17 @@ def sel_attn_bwd(q, k, v, block_indices, o, lse, do, block_size: int,
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     sc = float(scale) if scale is not None else 0.0  # the ABI: <= 0 selects 1/sqrt(D)
-    st = lib.nsa_sel_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(o), _ptr(lse),
-                              _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, M, N, H, G, D, T,
-                              int(block_size), sc, workspace.data_ptr(), workspace.numel(),
-                              ctypes.c_void_p(stream.cuda_stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(o), _ptr(lse), _ptr(do),
+            _ptr(dq), _ptr(dk), _ptr(dv), B, M, N, H, G, D, T, int(block_size), sc)
+    tail = (workspace.data_ptr(), workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if q.dtype == torch.float16:
+        st = lib.nsa_sel_attn_bwd(*args, *tail)
+        what = "nsa_sel_attn_bwd"
+    else:
+        st = lib.nsa_sel_attn_bwd_ex(*args, _dtype_code(q.dtype), *tail)
+        what = "nsa_sel_attn_bwd_ex"
     if st != NSA_OK:
-        raise NsaError(st, "nsa_sel_attn_bwd")
+        raise NsaError(st, what)
     return dq, dk, dv
 
 

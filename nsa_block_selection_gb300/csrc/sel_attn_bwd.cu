@@ -51,8 +51,27 @@ namespace nsa {
 
 constexpr int kQueriesPerChunk = 256;
 
+// D = A(16x8, row) * B(8x8, col) + D, bf16 inputs, fp32 accumulate: the
+// bf16 twin of mma_1688, used only by the key-major dK / dV products.
+__device__ __forceinline__ void mma_1688_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma_1688_t(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  if constexpr (BF16)
+    mma_1688_bf16(d, a0, a1, b0);
+  else
+    mma_1688(d, a0, a1, b0);
+}
+
 struct BwdProblem {
-  const __half* Q;
+  const uint16_t* Q;   // fp16 or bf16
   const int32_t* idx;
   const float* O;
   const float* LSE;
@@ -60,7 +79,7 @@ struct BwdProblem {
   float* dQ;
   float* dK;
   float* dV;
-  __half* dO16;        // [B, M, H, D] fp16 copy of dO (stage 1 -> stage 3)
+  uint16_t* dO16;      // [B, M, H, D] 16-bit copy of dO, in the inputs' type (stage 1 -> 3)
   float* rec;          // [B * M * G * nsub][16]: LSE * log2(e) of 8 heads, then delta
   const int* offs;     // [L + 1] list starts (L = B * G * nblk)
   const int* choffs;   // [L + 1] chunk starts
@@ -83,10 +102,24 @@ __device__ __forceinline__ void red_add_v4(float* p, float x, float y, float z, 
 }
 
 
-// fp32 pair -> fp16x2 (round to nearest even)
-__device__ __forceinline__ uint32_t ld_f32x2_as_half2(const float* p) {
-  const float2 v = __ldg(reinterpret_cast<const float2*>(p));
-  return pack_half2(v.x, v.y);
+// Tensor-map element type of the inputs (fp16 or bf16).
+static inline CUtensorMapDataType map_dtype(bool bf16) {
+  return bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// A row-major 16-bit matrix [rows, D] of element type `dt` as a 2-D map;
+// box = 64 columns x `rows_per_box` rows, 128-byte swizzle.
+static inline bool encode_rows_map_t(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t D,
+                                     int rows_per_box, CUtensorMapDataType dt) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D * 2)};
+  const cuuint32_t box[2] = {kBoxCols, static_cast<cuuint32_t>(rows_per_box)};
+  const cuuint32_t estride[2] = {1, 1};
+  return enc(tm, dt, 2, const_cast<void*>(ptr), dims, strides, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ---------------------------------------------------------------------------
@@ -103,7 +136,7 @@ struct DqCfg {
   static constexpr int kSteps = D / 16;
 };
 
-template <int D, int WARPS>
+template <int D, int WARPS, bool BF16>
 __global__ void __launch_bounds__(WARPS * 32, 4)
     sel_attn_bwd_dq_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV) {
@@ -148,7 +181,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4)
   float dpart = 0.f;
   {
     const bool real = gid < hw;
-    const __half* q = p.Q + (row + gid) * D + 2 * tig;
+    const uint16_t* q = p.Q + (row + gid) * D + 2 * tig;
     const float* dob = p.dO + (row + gid) * D + 2 * tig;
     const float* ob = p.O + (row + gid) * D + 2 * tig;
 #pragma unroll
@@ -161,7 +194,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4)
             real ? __ldg(reinterpret_cast<const float2*>(dob + 16 * k + 8 * h)) : float2{0.f, 0.f};
         const float2 o2 =
             real ? __ldg(reinterpret_cast<const float2*>(ob + 16 * k + 8 * h)) : float2{0.f, 0.f};
-        df[k][h] = pack_half2(d2.x, d2.y);
+        df[k][h] = pack2_t<BF16>(d2.x, d2.y);
         dpart = fmaf(d2.x, o2.x, fmaf(d2.y, o2.y, dpart));
       }
     }
@@ -241,8 +274,8 @@ __global__ void __launch_bounds__(WARPS * 32, 4)
       ldsm_x4(slot + ka + ((k + 1) >> 2) * kBoxBytes +
                   (((((k + 1) & 3) * 2 + ka_hi) ^ sw) << 4),
               b0, b1, b2, b3);
-      mma_16816(s, a0, a1, a2, a3, bf[k][0], bf[k][1]);
-      mma_16816(t, b0, b1, b2, b3, bf[k + 1][0], bf[k + 1][1]);
+      mma_16816_t<BF16>(s, a0, a1, a2, a3, bf[k][0], bf[k][1]);
+      mma_16816_t<BF16>(t, b0, b1, b2, b3, bf[k + 1][0], bf[k + 1][1]);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) x[j] = s[j] + t[j];
@@ -289,15 +322,15 @@ __global__ void __launch_bounds__(WARPS * 32, 4)
     ds[1] = x[1] == -INFINITY ? 0.f : ex2(fmaf(x[1], sl2, -lsb)) * (dp[1] - dlb);
     ds[2] = x[2] == -INFINITY ? 0.f : ex2(fmaf(x[2], sl2, -lsa)) * (dp[2] - dla);
     ds[3] = x[3] == -INFINITY ? 0.f : ex2(fmaf(x[3], sl2, -lsb)) * (dp[3] - dlb);
-    const uint32_t db0 = movmatrix_t(pack_half2(ds[0], ds[1]));
-    const uint32_t db1 = movmatrix_t(pack_half2(ds[2], ds[3]));
+    const uint32_t db0 = movmatrix_t(pack2_t<BF16>(ds[0], ds[1]));
+    const uint32_t db1 = movmatrix_t(pack2_t<BF16>(ds[2], ds[3]));
     // dQ^T (D x 8 heads) += K_tile^T dS^T
 #pragma unroll
     for (int d = 0; d < C::kSteps; ++d) {
       uint32_t a0, a1, a2, a3;
       ldsm_x4_t(sk + ta + (d >> 2) * kBoxBytes + ((((d & 3) * 2 + ta_hi) ^ sw) << 4), a0, a1, a2,
                 a3);
-      mma_16816(acc[d], a0, a1, a2, a3, db0, db1);
+      mma_16816_t<BF16>(acc[d], a0, a1, a2, a3, db0, db1);
     }
     __syncwarp();
     int nC = 0;
@@ -339,7 +372,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4)
 // one warp per (b, m, g, head sub-group): dO as fp16 rows, and the 64-byte
 // record (LSE * log2(e) of its 8 heads, then delta = dO . O of each head;
 // padding heads get LSE = +inf and delta = 0, so their probabilities are 0).
-template <int D>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256) sel_attn_bwd_prep_kernel(const BwdProblem p) {
   static_assert(D == 128, "one float4 per lane and head row");
   constexpr int kPer = D / 32;  // dims per lane
@@ -364,8 +397,8 @@ __global__ void __launch_bounds__(256) sel_attn_bwd_prep_kernel(const BwdProblem
       const float4 d4 = __ldg(reinterpret_cast<const float4*>(p.dO + at) + v);
       const float4 o4 = __ldg(reinterpret_cast<const float4*>(p.O + at) + v);
       part = fmaf(d4.x, o4.x, fmaf(d4.y, o4.y, fmaf(d4.z, o4.z, fmaf(d4.w, o4.w, part))));
-      w[2 * v] = pack_half2(d4.x, d4.y);
-      w[2 * v + 1] = pack_half2(d4.z, d4.w);
+      w[2 * v] = pack2_t<BF16>(d4.x, d4.y);
+      w[2 * v + 1] = pack2_t<BF16>(d4.z, d4.w);
     }
     *reinterpret_cast<uint2*>(p.dO16 + at) = make_uint2(w[0], w[1]);
 #pragma unroll
@@ -557,7 +590,7 @@ struct DkvCfg {
 
 // SPLIT: the group has more than 8 heads (items are (query, sub-group) pairs);
 // otherwise one item per query.
-template <int D, int KT, bool SPLIT>
+template <int D, int KT, bool SPLIT, bool BF16>
 __global__ void __launch_bounds__(2 * KT * 32, 1)
     sel_attn_bwd_dkv_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
@@ -712,11 +745,11 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < C::kSteps; k += 2) {
-      mma_16816(s0, kf[k][0], kf[k][1], kf[k][2], kf[k][3], qf[k][0], qf[k][1]);
-      mma_16816(d0, vf[k][0], vf[k][1], vf[k][2], vf[k][3], df[k][0], df[k][1]);
-      mma_16816(s1, kf[k + 1][0], kf[k + 1][1], kf[k + 1][2], kf[k + 1][3], qf[k + 1][0],
+      mma_16816_t<BF16>(s0, kf[k][0], kf[k][1], kf[k][2], kf[k][3], qf[k][0], qf[k][1]);
+      mma_16816_t<BF16>(d0, vf[k][0], vf[k][1], vf[k][2], vf[k][3], df[k][0], df[k][1]);
+      mma_16816_t<BF16>(s1, kf[k + 1][0], kf[k + 1][1], kf[k + 1][2], kf[k + 1][3], qf[k + 1][0],
                 qf[k + 1][1]);
-      mma_16816(d1, vf[k + 1][0], vf[k + 1][1], vf[k + 1][2], vf[k + 1][3], df[k + 1][0],
+      mma_16816_t<BF16>(d1, vf[k + 1][0], vf[k + 1][1], vf[k + 1][2], vf[k + 1][3], df[k + 1][0],
                 df[k + 1][1]);
     }
     const bool va = nw0 + gid <= lastkey, vb = nw0 + gid + 8 <= lastkey;
@@ -731,8 +764,8 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
     ds[3] = vb ? pr[3] * (d0[3] + d1[3] - rc[3]) : 0.f;
     // A operands (16 keys x 8 heads): the C layout of S^T is the A layout of
     // m16n8k8; B operands (8 heads x 8 dims) are transposed Q / dO fragments
-    const uint32_t pa0 = pack_half2(pr[0], pr[1]), pa1 = pack_half2(pr[2], pr[3]);
-    const uint32_t sa0 = pack_half2(ds[0], ds[1]), sa1 = pack_half2(ds[2], ds[3]);
+    const uint32_t pa0 = pack2_t<BF16>(pr[0], pr[1]), pa1 = pack2_t<BF16>(pr[2], pr[3]);
+    const uint32_t sa0 = pack2_t<BF16>(ds[0], ds[1]), sa1 = pack2_t<BF16>(ds[2], ds[3]);
     // this warp's half of D (branch on the warp-uniform half so that every
     // fragment index is a compile-time constant)
     auto accumulate = [&](auto half) {
@@ -740,8 +773,8 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
 #pragma unroll
       for (int jj = 0; jj < C::kHalfTiles; ++jj) {
         const int j = h0 + jj;  // 8-dim tile of D
-        mma_1688(dv[jj], pa0, pa1, movmatrix_t(df[j >> 1][j & 1]));
-        mma_1688(dk[jj], sa0, sa1, movmatrix_t(qf[j >> 1][j & 1]));
+        mma_1688_t<BF16>(dv[jj], pa0, pa1, movmatrix_t(df[j >> 1][j & 1]));
+        mma_1688_t<BF16>(dk[jj], sa0, sa1, movmatrix_t(qf[j >> 1][j & 1]));
       }
     };
     if (dh == 0)
@@ -836,15 +869,15 @@ __global__ void __launch_bounds__(2 * KT * 32, 1)
 // of `rows_per_box` rows, landing as two consecutive 128B-swizzled groups
 // (half 0's rows, then half 1's).
 static inline bool encode_rows_halves_map(CUtensorMap* tm, const void* ptr, int64_t rows,
-                                          int rows_per_box) {
+                                          int rows_per_box, CUtensorMapDataType dt) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), 2};
   const cuuint64_t strides[2] = {128 * 2, 64 * 2};  // next row, next half (bytes)
   const cuuint32_t box[3] = {kBoxCols, static_cast<cuuint32_t>(rows_per_box), 2};
   const cuuint32_t estride[3] = {1, 1, 1};
-  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return enc(tm, dt, 3, const_cast<void*>(ptr), dims, strides, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -884,7 +917,7 @@ struct DkvTcCfg {
 
 constexpr int kDkvTcThreads = 320;
 
-template <bool SPLIT>
+template <bool SPLIT, bool BF16>
 __global__ void __launch_bounds__(kDkvTcThreads, 1)
     sel_attn_bwd_dkv_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
                                const __grid_constant__ CUtensorMap tmV,
@@ -1034,9 +1067,9 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---- MMA issuer ----
-      constexpr uint32_t idesc_sd = umma_idesc_f16(128, 64, false, false);   // K-major A, B
+      constexpr uint32_t idesc_sd = umma_idesc_f16(128, 64, BF16, false);   // K-major A, B
       constexpr uint32_t idesc_acc =
-          umma_idesc_f16(128, 64, false, true) | (1u << 15);  // MN-major A and B
+          umma_idesc_f16(128, 64, BF16, true) | (1u << 15);  // MN-major A and B
       bool ok = wait_phase(bar(kBlkFull), 0, kWaitLimitNs);
       // S / dP of batch i: its Q / dO rows have landed (caller checked)
       auto issue_sd = [&](int i) {
@@ -1058,7 +1091,7 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
       // dV / dK / dQ of batch i: its P / dS are written and dQ of batch i - 1
       // has been read out of tensor memory (caller checked)
       constexpr uint32_t idesc_dq =
-          umma_idesc_f16(128, 128, false, true);  // dS K-major A, K MN-major B
+          umma_idesc_f16(128, 128, BF16, true);  // dS K-major A, K MN-major B
       auto issue_acc = [&](int i) {
         const int s = i & 1;
         tc_fence_after();
@@ -1244,8 +1277,8 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
           const float p1 = v1 ? ex2(fmaf(__uint_as_float(sv[j + 1]), sl2, -lse2)) : 0.f;
           const float d0 = v0 ? p0 * (__uint_as_float(dv[j]) - delta) : 0.f;
           const float d1 = v1 ? p1 * (__uint_as_float(dv[j + 1]) - delta) : 0.f;
-          pw[h2] = pack_half2(p0, p1);
-          dw[h2] = pack_half2(d0, d1);
+          pw[h2] = pack2_t<BF16>(p0, p1);
+          dw[h2] = pack2_t<BF16>(d0, d1);
         }
         const uint32_t off = ((cc ^ (r & 7)) << 4);
         *reinterpret_cast<uint4*>(prow + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
@@ -1383,7 +1416,7 @@ struct SideStream {
   }
 };
 
-template <int D>
+template <int D, bool BF16>
 static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
                       const BwdPlan& pl, cudaStream_t st, bool second_stream) {
   constexpr int W = 4;
@@ -1393,7 +1426,7 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   int* offs = reinterpret_cast<int*>(ws + pl.off_offs);
   int* choffs = reinterpret_cast<int*>(ws + pl.off_choffs);
   int* lists = reinterpret_cast<int*>(ws + pl.off_lists);
-  p.dO16 = reinterpret_cast<__half*>(ws + pl.off_do16);
+  p.dO16 = reinterpret_cast<uint16_t*>(ws + pl.off_do16);
   p.rec = reinterpret_cast<float*>(ws + pl.off_rec);
   p.offs = offs;
   p.choffs = choffs;
@@ -1448,9 +1481,10 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   CUtensorMap tk, tv, tkb, tvb;
   const bool have_keys = p.N > 0;
   if (have_keys) {
-    if (!encode_kv_map(&tk, K, B, p.N, p.G, D) || !encode_kv_map(&tv, V, B, p.N, p.G, D) ||
-        !encode_kv_map(&tkb, K, B, p.N, p.G, D, p.bs) ||
-        !encode_kv_map(&tvb, V, B, p.N, p.G, D, p.bs))
+    if (!encode_kv_map(&tk, K, B, p.N, p.G, D, kTileKeys, map_dtype(BF16)) ||
+        !encode_kv_map(&tv, V, B, p.N, p.G, D, kTileKeys, map_dtype(BF16)) ||
+        !encode_kv_map(&tkb, K, B, p.N, p.G, D, p.bs, map_dtype(BF16)) ||
+        !encode_kv_map(&tvb, V, B, p.N, p.G, D, p.bs, map_dtype(BF16)))
       return NSA_ERR_LAUNCH;
   } else {
     memset(&tk, 0, sizeof(tk));
@@ -1482,14 +1516,14 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
       rc2 = stage2(st);  // no second stream: in order on the caller's stream
     bool rc1 =
         cudaMemsetAsync(p.dQ, 0, static_cast<size_t>(B * p.M * p.H * D) * 4, st) == cudaSuccess;
-    sel_attn_bwd_prep_kernel<D><<<static_cast<unsigned>((p.units + 7) / 8), 256, 0, st>>>(p);
+    sel_attn_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((p.units + 7) / 8), 256, 0, st>>>(p);
     rc1 = rc1 && cudaGetLastError() == cudaSuccess;
     if (side.ok && !side.join_into(st)) return NSA_ERR_LAUNCH;
     if (rc2 != NSA_OK) return rc2;
     if (!rc1) return NSA_ERR_LAUNCH;
   } else {
     // stage 1: dQ and delta
-    auto kq = sel_attn_bwd_dq_kernel<D, W>;
+    auto kq = sel_attn_bwd_dq_kernel<D, W, BF16>;
     if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, Cq::kSmemBytes) !=
         cudaSuccess)
       return NSA_ERR_LAUNCH;
@@ -1506,13 +1540,13 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   // stage 3: dK, dV; grid bound: sum over lists of ceil(count / chunk)
   CUtensorMap tq, tdo;
   const int hw0 = p.hpg < kHeadsPerGroup ? p.hpg : kHeadsPerGroup;
-  if (!encode_rows_map(&tq, p.Q, B * p.M * p.H, D, hw0) ||
-      !encode_rows_map(&tdo, p.dO16, B * p.M * p.H, D, hw0))
+  if (!encode_rows_map_t(&tq, p.Q, B * p.M * p.H, D, hw0, map_dtype(BF16)) ||
+      !encode_rows_map_t(&tdo, p.dO16, B * p.M * p.H, D, hw0, map_dtype(BF16)))
     return NSA_ERR_LAUNCH;
   auto run = [&](auto kt, auto split) -> int {
     constexpr int KT = decltype(kt)::value;
     using Ck = DkvCfg<D, KT>;
-    auto kk = sel_attn_bwd_dkv_kernel<D, KT, decltype(split)::value>;
+    auto kk = sel_attn_bwd_dkv_kernel<D, KT, decltype(split)::value, BF16>;
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, Ck::kSmemBytes) !=
         cudaSuccess)
       return NSA_ERR_LAUNCH;
@@ -1530,14 +1564,15 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     // read as one box per column half, the Q / dO rows of an item as one 3-D
     // box (both column halves)
     CUtensorMap tk64, tv64, tq3 = tq, tdo3 = tdo;
-    if (!encode_kv_map(&tk64, K, B, p.N, p.G, D, p.bs) ||
-        !encode_kv_map(&tv64, V, B, p.N, p.G, D, p.bs))
+    if (!encode_kv_map(&tk64, K, B, p.N, p.G, D, p.bs, map_dtype(BF16)) ||
+        !encode_kv_map(&tv64, V, B, p.N, p.G, D, p.bs, map_dtype(BF16)))
       return NSA_ERR_LAUNCH;
-    if (hw0 == kHeadsPerGroup && (!encode_rows_halves_map(&tq3, p.Q, B * p.M * p.H, hw0) ||
-                                  !encode_rows_halves_map(&tdo3, p.dO16, B * p.M * p.H, hw0)))
+    if (hw0 == kHeadsPerGroup && (!encode_rows_halves_map(&tq3, p.Q, B * p.M * p.H, hw0, map_dtype(BF16)) ||
+                                  !encode_rows_halves_map(&tdo3, p.dO16, B * p.M * p.H, hw0,
+                                                          map_dtype(BF16))))
       return NSA_ERR_LAUNCH;
     p.chunk_order = order;  // written by stage 2
-    auto kk = split ? sel_attn_bwd_dkv_tc_kernel<true> : sel_attn_bwd_dkv_tc_kernel<false>;
+    auto kk = split ? sel_attn_bwd_dkv_tc_kernel<true, BF16> : sel_attn_bwd_dkv_tc_kernel<false, BF16>;
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkvTcCfg::kSmemBytes) != cudaSuccess)
       return NSA_ERR_LAUNCH;
@@ -1615,10 +1650,10 @@ static int bwd_check_pointers(const void* Q, const void* K, const void* V, const
 static int run_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                    const float* O, const float* LSE, const float* dO, float* dQ, float* dK,
                    float* dV, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
-                   int64_t T, int block_size, float scale, const BwdPlan& pl, uint8_t* ws,
-                   cudaStream_t st, bool second_stream) {
+                   int64_t T, int block_size, float scale, bool bf16, const BwdPlan& pl,
+                   uint8_t* ws, cudaStream_t st, bool second_stream) {
   BwdProblem p;
-  p.Q = static_cast<const __half*>(Q);
+  p.Q = static_cast<const uint16_t*>(Q);
   p.idx = idx;
   p.O = O;
   p.LSE = LSE;
@@ -1640,8 +1675,11 @@ static int run_bwd(const void* Q, const void* K, const void* V, const int32_t* i
   p.L = static_cast<int>(pl.L);
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   p.sl2 = p.scale * 1.4426950408889634f;
-  return D == 64 ? launch_bwd<64>(p, K, V, ws, pl, st, second_stream)
-                 : launch_bwd<128>(p, K, V, ws, pl, st, second_stream);
+  if (D == 64)
+    return bf16 ? launch_bwd<64, true>(p, K, V, ws, pl, st, second_stream)
+                : launch_bwd<64, false>(p, K, V, ws, pl, st, second_stream);
+  return bf16 ? launch_bwd<128, true>(p, K, V, ws, pl, st, second_stream)
+              : launch_bwd<128, false>(p, K, V, ws, pl, st, second_stream);
 }
 
 }  // namespace nsa
@@ -1656,12 +1694,14 @@ int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_
   return static_cast<int64_t>(pl.total);
 }
 
-int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* block_indices,
-                     const float* O, const float* LSE, const float* dO, float* dQ, float* dK,
-                     float* dV, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
-                     int64_t T, int block_size, float scale, void* workspace,
-                     int64_t workspace_bytes, void* stream) {
+int nsa_sel_attn_bwd_ex(const void* Q, const void* K, const void* V,
+                        const int32_t* block_indices, const float* O, const float* LSE,
+                        const float* dO, float* dQ, float* dK, float* dV, int64_t B, int64_t M,
+                        int64_t N, int64_t H, int64_t G, int64_t D, int64_t T, int block_size,
+                        float scale, int qkv_dtype, void* workspace, int64_t workspace_bytes,
+                        void* stream) {
   using namespace nsa;
+  if (qkv_dtype != NSA_F16 && qkv_dtype != NSA_BF16) return NSA_ERR_DTYPE;
   BwdPlan pl;
   const int chk = bwd_check_sizes(B, M, N, H, G, D, T, block_size, &pl);
   if (chk != NSA_OK) return chk;
@@ -1680,7 +1720,17 @@ int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t*
   rc = bwd_check_pointers(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, N, T, workspace);
   if (rc != NSA_OK) return rc;
   return run_bwd(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, B, M, N, H, G, D, T,
-                 block_size, scale, pl, static_cast<uint8_t*>(workspace), st, true);
+                 block_size, scale, qkv_dtype == NSA_BF16, pl, static_cast<uint8_t*>(workspace),
+                 st, true);
+}
+
+int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* block_indices,
+                     const float* O, const float* LSE, const float* dO, float* dQ, float* dK,
+                     float* dV, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
+                     int64_t T, int block_size, float scale, void* workspace,
+                     int64_t workspace_bytes, void* stream) {
+  return nsa_sel_attn_bwd_ex(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, B, M, N, H, G, D, T,
+                             block_size, scale, NSA_F16, workspace, workspace_bytes, stream);
 }
 
 int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
@@ -1704,7 +1754,7 @@ int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
   void* scratch = noalloc_scratch_address();
   if (scratch == nullptr) return NSA_ERR_LAUNCH;
   return run_bwd(Q, K, V, block_indices, O, LSE, dO, dQ, dK, dV, B, M, N, H, G, D, T,
-                 block_size, scale, pl, static_cast<uint8_t*>(scratch),
+                 block_size, scale, false, pl, static_cast<uint8_t*>(scratch),
                  static_cast<cudaStream_t>(stream), false);
 }
 

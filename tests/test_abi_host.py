@@ -347,3 +347,11 @@ def test_host_ex_rejects_bad_dtypes(lib):
                                           vp(FAKE), a["B"], a["M"], a["N"], a["H"], a["G"], a["D"],
                                           a["T"], a["bs"], 0.0, qkv, o, vp(FAKE), 1 << 40, 0, None)
         assert st == -11, (qkv, o)
+
+
+def test_bwd_ex_rejects_bad_dtypes(lib):
+    vp = ctypes.c_void_p
+    for dt in (2, 3, -1):
+        st = lib.nsa_sel_attn_bwd_ex(*([vp(FAKE)] * 10), 1, 128, 128, 16, 2, 128, 4, 64, 0.0, dt,
+                                     vp(FAKE), 1 << 40, None)
+        assert st == -11, dt

@@ -154,3 +154,46 @@ def test_bwd_heads_per_group(H, G, bs):
     dO = np.random.default_rng(H).standard_normal(q.shape).astype(np.float32)
     got = _run(q, k, v, idx, dO, bs)
     _check(got, q, k, v, idx, dO, bs, what=f"H{H} G{G}")
+
+
+U_BF16 = 2.0 ** -8  # bf16 unit roundoff
+
+
+@pytest.mark.parametrize("B,M,N,D,bs,T,rule", [
+    (2, 700, 700, 128, 64, 5, "first_two_local"),
+    (1, 900, 900, 64, 32, 4, "local"),
+    (1, 500, 500, 128, 32, 6, "first_local"),
+    (1, 300, 520, 128, 64, 3, "local"),
+])
+def test_bwd_bf16_matches_oracle(B, M, N, D, bs, T, rule):
+    """bf16 inputs (nsa_sel_attn_bwd_ex): the same per-element bound with the
+    bf16 unit roundoff, 4 u |terms| (dO, P and dS rounded to bf16 once each;
+    the forward's bf16 P enters delta through O)."""
+    import torch
+
+    from nsa_block_selection_gb300 import inputs as gen
+    from nsa_block_selection_gb300 import sel_attn_fwd
+    from nsa_block_selection_gb300._lib import sel_attn_bwd
+
+    w = gen.Workload("bwd_bf16", B, M, N, 16, 2, D, bs, T, 1.0, rule)
+    q, k, v = gen.make_qkv(w, M + T, "bf16")
+    idx = gen.make_block_indices(w.replace(N=min(M, N)) if M <= N else w, M + T)
+    dO = np.random.default_rng(M + 1).standard_normal(q.shape).astype(np.float32)
+    tq, tk, tv = (torch.from_numpy(np.asarray(x)).cuda().to(torch.bfloat16) for x in (q, k, v))
+    ti, tdo = to_dev(idx, dO)
+    f32 = torch.float32
+    O, L = sel_attn_fwd(tq, tk, tv, ti, bs, out=poisoned((B, M, 16, D), f32),
+                        lse=poisoned((B, 16, M), f32))
+    grads = sel_attn_bwd(tq, tk, tv, ti, O, L, tdo, bs, dq=poisoned(tq.shape, f32),
+                         dk=poisoned(tk.shape, f32), dv=poisoned(tv.shape, f32))
+    torch.cuda.synchronize()
+    got = [g.cpu().numpy().astype(np.float64) for g in grads]
+    qd, kd, vd = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    exact = oracle.sel_attn_bwd(qd, kd, vd, idx, dO, bs)
+    mags = oracle.sel_attn_bwd(qd, kd, vd, idx, dO, bs, magnitudes=True)
+    for name, g, ex, mg in zip(("dQ", "dK", "dV"), got, exact, mags):
+        assert np.isfinite(g).all(), f"bf16 {name}: non-finite"
+        err = np.abs(g - ex)
+        bound = KAPPA * U_BF16 * mg
+        assert np.all(err <= bound), \
+            f"bf16 {name}: {int((err > bound).sum())} elements beyond 4u|terms|"
