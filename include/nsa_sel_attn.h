@@ -408,6 +408,8 @@ int nsa_sel_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
  * Returns NSA_ERR_SHAPE (bad sizes, n_init/n_local out of range, too many
  * blocks), NSA_ERR_BLOCK_SIZE, NSA_ERR_NULL, NSA_ERR_ALIGN (a pointer not
  * 4-byte aligned) before launch; an empty output returns NSA_OK at once.
+ * A row copy that does not arrive within 1 s makes nsa_sync_status report
+ * NSA_ERR_TIMEOUT; the outputs of that launch are then undefined.
  */
 int nsa_topk_blocks(const float* scores, int32_t* block_indices, int64_t B, int64_t M,
                     int64_t N, int64_t G, int64_t T, int block_size, int n_init,

@@ -6,6 +6,10 @@
 #include "nsa_sel_attn.h"
 #include "status.cuh"
 
+namespace nsa {
+int topk_read_and_clear_status(unsigned int* value);  // top-k block selection (topk_blocks.cu)
+}  // namespace nsa
+
 extern "C" {
 
 const char* nsa_status_string(int status) {
@@ -36,13 +40,14 @@ int nsa_version(void) { return 200; }
 int nsa_sync_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return NSA_ERR_LAUNCH;
-  unsigned int fwd = 0u, bwd = 0u, swa = 0u, shr = 0u, prb = 0u;
+  unsigned int fwd = 0u, bwd = 0u, swa = 0u, shr = 0u, prb = 0u, tpk = 0u;
   if (nsa::fwd_read_and_clear_status(&fwd) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::bwd_read_and_clear_status(&bwd) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::swa_read_and_clear_status(&swa) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::shared_read_and_clear_status(&shr) != NSA_OK) return NSA_ERR_LAUNCH;
   if (nsa::probe_read_and_clear_status(&prb) != NSA_OK) return NSA_ERR_LAUNCH;
-  const unsigned int all = fwd | bwd | swa | shr | prb;
+  if (nsa::topk_read_and_clear_status(&tpk) != NSA_OK) return NSA_ERR_LAUNCH;
+  const unsigned int all = fwd | bwd | swa | shr | prb | tpk;
   if (all & 2u) return NSA_ERR_BOUNDS;
   return all ? NSA_ERR_TIMEOUT : NSA_OK;
 }

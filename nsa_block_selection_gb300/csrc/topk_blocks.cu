@@ -15,22 +15,24 @@
 //  * the row is written in ascending block order, -1 padded.
 //
 // Kernel shape (HBM-bound: each score is read at most once):
-//  * one warp per row, rows grid-stride. While a row is selected, the next
-//    row's scores are already being copied (cp.async) into the warp's
-//    shared-memory row buffer;
-//  * fast path: lane l holds the 4 nq consecutive blocks from 4 nq l
-//    (nq = ceil((c + 1) / 128)), so lane order is block order. g_j = the
-//    maximum of group j (lane, slot mod 4). The k-th largest g_j is at most
-//    the k-th largest score, so every pick is among the scores at or above
-//    it. Those few survivors are compacted in block order (per-lane counts,
-//    a warp scan) and the exact k-th largest of them is found by a ballot
-//    search;
+//  * one warp per row, rows grid-stride. A row's candidate scores arrive in
+//    the warp's shared-memory row buffer by one bulk copy (TMA, mbarrier
+//    with a bounded wait); the next row's copy starts once this row's
+//    survivors are out of the buffer;
+//  * fast path: lane l holds the 4 nqo consecutive blocks from 4 nqo l
+//    (nqo = ceil((c + 1) / 128) rounded up to odd, for conflict-free
+//    16-byte shared loads), so lane order is block order. A threshold t0
+//    from the lane (or group) maxima has at least k scores at or above it;
+//    those few survivors are marked with one bit each, placed in block
+//    order (per-lane counts, a warp scan) and the S - k smallest of them
+//    are dropped one at a time with a warp minimum;
 //  * general path (more than 32 free picks, fewer than k groups holding a
 //    number, or more than 64 survivors -- ties, clustered scores): lane l
-//    holds blocks 128q + 32i + l as order-preserving 32-bit keys; a search over the key range
-//    brackets the k-th largest key with one counting pass per step, and the
-//    chosen blocks (forced, keys above the threshold, and the first ties at
-//    it in block order) are written with ballot compaction.
+//    holds blocks 128q + 32i + l as order-preserving 32-bit keys; a search
+//    over the key range brackets the k-th largest key with one counting
+//    pass per step, and the chosen blocks (forced, keys above the
+//    threshold, and the first ties at it in block order) are written with
+//    ballot compaction.
 
 #include <cuda_runtime.h>
 
@@ -111,6 +113,7 @@ struct TopkRow {
   int c;         // last candidate block (-1: none)
   int lo_local;  // forced: t < n_init or lo_local <= t <= c
   int nq;        // quads of key slots in use (warp-uniform)
+  int nqo;       // nq rounded up to odd: quads per lane in the row buffer
   bool trivial;  // at most T candidates: all of them, no scores read
 };
 
@@ -125,6 +128,7 @@ __device__ __forceinline__ TopkRow topk_row_info(const TopkProblem& p, int64_t r
   r.trivial = r.c + 1 <= p.T;
   r.lo_local = r.c - p.n_local + 1;
   r.nq = (r.c + 1 + 127) >> 7;
+  r.nqo = r.nq | 1;
   return r;
 }
 
@@ -337,109 +341,156 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
 }
 
-// Starts copying the scores of blocks 0..c of a row into the warp's row
-// buffer. Lane l's segment is the 4 nq blocks from 4 nq l; its quad q
-// (blocks 4 nq l + 4q .. + 3) lands at 16-byte slot 32q + l, so each lane
-// reads a quad with one conflict-free 16-byte load. Slots past c are not
-// written.
+// Starts copying the scores of blocks 0..c of a row into a row buffer, in
+// block order. Lane l of the fast path reads blocks 4 nqo l .. 4 nqo l +
+// 4 nqo - 1 as nqo 16-byte quads from byte 16 nqo l; nqo is odd, so the 8
+// lanes of a quarter-warp load from distinct bank groups. 16-byte aligned
+// rows of a multiple of 4 blocks (p.vec): one bulk copy issued by lane 0,
+// completion counted on the buffer's mbarrier `bar`; other rows: coalesced
+// 4-byte cp.async copies, one commit group. Bytes past block c are not
+// written (the fast path masks them).
 template <int J>
 __device__ __forceinline__ void topk_prefetch(const TopkProblem& p, const TopkRow& r, int lane,
-                                              uint32_t sbuf) {
-  const int seg = 4 * r.nq * lane;
-  if (!r.trivial && seg <= r.c) {
-    const float* src = p.scores + r.row * p.nblk + seg;
-#pragma unroll
-    for (int q = 0; q < J / 4; ++q) {
-      if (q >= r.nq) break;
-      const int b0 = seg + 4 * q;
-      const uint32_t dst = sbuf + (32 * q + lane) * 16;
-      if (p.vec) {
-        // b0 % 4 == 0 and nblk % 4 == 0: the 16 bytes lie inside the row
-        if (b0 <= r.c) cp_async_16(dst, src + 4 * q, 16);
+                                              uint32_t sbuf, uint32_t bar) {
+  const float* src = p.scores + r.row * p.nblk;
+  if (p.vec) {
+    if (lane == 0) {
+      if (r.trivial) {
+        mbar_arrive(bar);
       } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (b0 + i <= r.c) cp_async_4(dst + 4 * i, src + 4 * q + i);
+        // 4 ceil((c + 1) / 4) <= nblk blocks: inside the row
+        const uint32_t bytes = 16u * static_cast<uint32_t>((r.c + 4) >> 2);
+        fence_proxy_async_smem();  // the buffer's earlier reads come first
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(sbuf, src, bytes, bar);
       }
     }
+  } else {
+    if (!r.trivial)
+      for (int t = lane; t <= r.c; t += 32) cp_async_4(sbuf + 4 * t, src + t);
+    cp_async_commit();
   }
-  cp_async_commit();
 }
 
-// Fast path for one row whose scores are in the row buffer; issues the next
-// row's copies once the buffer is read. Returns false, having written at
-// most the forced blocks, when the row needs the general path.
-//  * Forced blocks and blocks past c become NaN, which no comparison passes.
-//  * t0 = the k-th largest lane maximum (k <= 16), else the lower end of a
-//    KeyBracket over the group-maximum keys, stopped once at most k + 8
-//    groups are >= it: the scores >= t0 hold every pick.
-//  * The scores >= t0 (S of them, k <= S <= kSurvivors) are compacted in
-//    block order; a KeyBracket over them (one ballot per step) finds the k-th
-//    largest key tau; the picks are the keys above tau and the first ties at
-//    tau in block order.
-template <int J>
-__device__ __forceinline__ bool topk_select_fast(const TopkProblem& p, const TopkRow& r,
-                                                 const TopkRow& next, bool more, int lane,
-                                                 uint32_t (&raw)[J], uint32_t sbuf,
-                                                 TopkSmem& sm) {
-  int32_t* out = p.idx + r.row * p.T;
-  const uint32_t below = lanemask_lt();
-  const int seg = 4 * r.nq * lane;
-  float gm[4] = {__uint_as_float(kNanBits), __uint_as_float(kNanBits), __uint_as_float(kNanBits),
-                 __uint_as_float(kNanBits)};
-  if (!r.trivial) {
-    cp_async_wait<0>();
-    __syncwarp();
-    const bool edge = seg < p.n_init || seg + 4 * r.nq > r.lo_local;
+// Waits for the copies of the row in the buffer: its mbarrier phase
+// `parity` (bulk copy, bounded wait) or the cp.async group.
+__device__ __forceinline__ bool topk_wait(const TopkProblem& p, uint32_t bar, uint32_t parity) {
+  if (p.vec) return wait_phase(bar, parity, kWaitLimitNs);
+  cp_async_wait<0>();
+  return true;
+}
+
+__device__ __forceinline__ void ld_shared_v4f(uint32_t addr, float (&v)[4]) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+               : "r"(addr));
+}
+
+// Descending sort of one 32-bit key per lane across the warp (bitonic
+// network, 15 compare-exchange steps); lane i ends with the (i+1)-th largest.
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t v, int lane) {
 #pragma unroll
-    for (int q = 0; q < J / 4; ++q) {
-      if (q >= r.nq) break;
-      uint32_t v[4];
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
-                   : "r"(sbuf + (32 * q + lane) * 16));
+  for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int t = seg + 4 * q + i;
-        if (edge && (t < p.n_init || t >= r.lo_local)) v[i] = kNanBits;
-        raw[4 * q + i] = v[i];
-        gm[i] = fmaxf(gm[i], __uint_as_float(v[i]));
-      }
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t o = __shfl_xor_sync(kFull, v, stride);
+      const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
+      v = keep_max ? max(v, o) : min(v, o);
     }
   }
-  __syncwarp();  // every lane has read the buffer
-  if (more) topk_prefetch<J>(p, next, lane, sbuf);
+  return v;
+}
 
+// Bits [lo, hi) of word w of a per-lane element mask (element e is bit
+// e mod 32 of word e / 32); lo and hi may lie outside the word.
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int w) {
+  const int a = max(lo - 32 * w, 0);
+  const int b = min(hi - 32 * w, 32);
+  if (b <= a) return 0u;
+  const uint32_t upto_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+  return upto_b & ~((1u << a) - 1u);  // a <= 31 here
+}
+
+// Fast path for one row whose scores are in the row buffer `sbuf` (copies
+// complete). Returns false, having written at most the forced blocks, when
+// the row needs the general path. `pending`: the next row's copies are to
+// be issued into the buffer once this row no longer reads it; cleared when
+// issued.
+//  * Element e of lane l is block 4 nqo l + e (at byte 4 (4 nqo l + e) of
+//    the buffer). Forced blocks and blocks past c are masked to NaN (a
+//    per-lane bit mask of the free ones), which no comparison passes.
+//  * t0 = the k-th largest lane maximum (k <= 16), else the lower end of a
+//    KeyBracket over the 128 group maxima (group = lane and e mod 4),
+//    stopped once at most k + 8 groups are >= it: the scores >= t0 hold
+//    every pick.
+//  * Survivors (scores >= t0): one bit per element, a warp scan of the
+//    per-lane counts, then each lane copies its own survivors from the row
+//    buffer, in block order, to one slot each (S of them, k <= S <=
+//    kSurvivors).
+//  * S <= 32: the S - k smallest survivors (by score, then the later block
+//    first) are dropped one at a time with a warp minimum; the rest are the
+//    picks. S > 32: tau = the k-th largest survivor key by a KeyBracket over
+//    two keys per lane, and the picks are the keys above tau and the first
+//    ties at tau in block order.
+template <int J>
+__device__ __forceinline__ bool topk_select_fast(const TopkProblem& p, const TopkRow& r,
+                                                 const TopkRow& next, bool& pending, int lane,
+                                                 uint32_t sbuf, uint32_t bar, TopkSmem& sm) {
+  constexpr int Q = J / 4 + 1;         // quads per lane at most (nqo <= Q)
+  constexpr int W = (4 * Q + 31) / 32;  // survivor bit words per lane
+  int32_t* out = p.idx + r.row * p.T;
+  const uint32_t below = lanemask_lt();
+  auto release = [&]() {
+    if (pending) {  // warp-uniform
+      __syncwarp();
+      topk_prefetch<J>(p, next, lane, sbuf, bar);
+      pending = false;
+    }
+  };
   if (r.trivial) {
+    release();
     for (int t = lane; t < p.T; t += 32) out[t] = t <= r.c ? t : -1;
     return true;
   }
   const int k = p.T - p.n_init - p.n_local;
-  for (int t = lane; t < p.n_init; t += 32) out[t] = t;
-  for (int t = lane; t < p.n_local; t += 32) out[p.T - p.n_local + t] = r.lo_local + t;
-  if (k == 0) return true;
-  if (k > 32) return false;
+  if (p.n_init <= 32 && p.n_local <= 32) {
+    if (lane < p.n_init) out[lane] = lane;
+    if (lane < p.n_local) out[p.T - p.n_local + lane] = r.lo_local + lane;
+  } else {
+    for (int t = lane; t < p.n_init; t += 32) out[t] = t;
+    for (int t = lane; t < p.n_local; t += 32) out[p.T - p.n_local + t] = r.lo_local + t;
+  }
+  if (k == 0 || k > 32) {
+    release();
+    return k == 0;
+  }
 
-  // t0: with k <= 16 and at least k lanes holding a number, the k-th
-  // largest lane maximum (a warp bitonic sort of 32 keys); otherwise a
-  // KeyBracket over the 128 group maxima, stopped once at most k + 8 groups
-  // are >= it. Either way at least k scores are >= t0.
+  const int seg = 4 * r.nqo * lane;
+  const uint32_t base = sbuf + 16 * r.nqo * lane;  // element e at base + 4 e
+  uint32_t vm[W];  // free candidates: blocks n_init <= t < lo_local
+#pragma unroll
+  for (int w = 0; w < W; ++w) vm[w] = range_bits(p.n_init - seg, r.lo_local - seg, w);
+  float gm[4] = {__uint_as_float(kNanBits), __uint_as_float(kNanBits), __uint_as_float(kNanBits),
+                 __uint_as_float(kNanBits)};
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    if (q >= r.nqo) break;
+    float v[4];
+    ld_shared_v4f(base + 16 * q, v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = 4 * q + i;
+      gm[i] = fmaxf(gm[i], (vm[e >> 5] >> (e & 31)) & 1u ? v[i] : __uint_as_float(kNanBits));
+    }
+  }
+
   uint32_t t0key = 0u;
   bool have_t0 = false;
   if (k <= 16) {
     const float lmx = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
-    uint32_t v = lmx == lmx ? order_key(lmx) : 0u;  // 0: the lane holds no number
+    const uint32_t v = lmx == lmx ? order_key(lmx) : 0u;  // 0: the lane holds no number
     if (__popc(__ballot_sync(kFull, v != 0u)) >= k) {
-#pragma unroll
-      for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          const uint32_t o = __shfl_xor_sync(kFull, v, stride);
-          const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
-          v = keep_max ? max(v, o) : min(v, o);  // descending overall
-        }
-      }
-      t0key = __shfl_sync(kFull, v, k - 1);
+      t0key = __shfl_sync(kFull, warp_sort_desc(v, lane), k - 1);
       have_t0 = true;
     }
   }
@@ -456,7 +507,10 @@ __device__ __forceinline__ bool topk_select_fast(const TopkProblem& p, const Top
     }
     KeyBracket br;
     br.clo = __reduce_add_sync(kFull, nz);
-    if (br.clo < k) return false;
+    if (br.clo < k) {
+      release();
+      return false;
+    }
     br.lo = __reduce_min_sync(kFull, kmin);
     br.hi = __reduce_max_sync(kFull, kmax) + 1u;
     br.chi = 0;
@@ -472,13 +526,27 @@ __device__ __forceinline__ bool topk_select_fast(const TopkProblem& p, const Top
   // the float whose key is t0key (>= key(-inf) > 1: a number)
   const float t0 = __uint_as_float((t0key & 0x80000000u) ? (t0key & 0x7fffffffu) : ~t0key);
 
-  // survivors in block order: count per lane, scan across lanes, write
+  // survivors: a bit per element (the row read again from the buffer; the
+  // mask drops forced blocks and blocks past c), counts scanned across lanes
+  uint32_t bits[W];
+#pragma unroll
+  for (int w = 0; w < W; ++w) bits[w] = 0u;
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    if (q >= r.nqo) break;
+    float v[4];
+    ld_shared_v4f(base + 16 * q, v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = 4 * q + i;
+      if (v[i] >= t0) bits[e >> 5] |= 1u << (e & 31);
+    }
+  }
   int cnt = 0;
 #pragma unroll
-  for (int q = 0; q < J / 4; ++q) {
-    if (q >= r.nq) break;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) cnt += __uint_as_float(raw[4 * q + i]) >= t0;
+  for (int w = 0; w < W; ++w) {
+    bits[w] &= vm[w];
+    cnt += __popc(bits[w]);
   }
   int incl = cnt;
 #pragma unroll
@@ -487,30 +555,50 @@ __device__ __forceinline__ bool topk_select_fast(const TopkProblem& p, const Top
     if (lane >= d) incl += v;
   }
   const int S = __shfl_sync(kFull, incl, 31);
-  if (S > kSurvivors) return false;
-  if (cnt) {
-    int pos = incl - cnt;
+  if (S > kSurvivors) {
+    release();
+    return false;
+  }
+  // each lane copies its survivors (raw score bits) in block order
+  int pos = incl - cnt;
 #pragma unroll
-    for (int q = 0; q < J / 4; ++q) {
-      if (q >= r.nq) break;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (__uint_as_float(raw[4 * q + i]) >= t0) {
-          sm.key[pos] = raw[4 * q + i];  // raw bits; keys are formed below
-          sm.blk[pos] = seg + 4 * q + i;
-          ++pos;
-        }
-      }
+  for (int w = 0; w < W; ++w) {
+    uint32_t b = bits[w];
+    while (b) {
+      const int e = 32 * w + __ffs(b) - 1;
+      b &= b - 1u;
+      sm.key[pos] = __float_as_uint(ld_shared_f32(base + 4 * e));
+      sm.blk[pos] = seg + e;
+      ++pos;
     }
   }
   __syncwarp();
-  const uint32_t k0 = lane < S ? order_key(__uint_as_float(sm.key[lane])) : 0u;
-  const int b0 = lane < S ? sm.blk[lane] : 0;
+  release();
+  if (S <= 32) {
+    uint32_t key = lane < S ? order_key(__uint_as_float(sm.key[lane])) : 0xffffffffu;
+    const int blk = lane < S ? sm.blk[lane] : 0;
+    bool keep = lane < S;
+    __syncwarp();  // the next row may overwrite the arrays
+    // survivor keys are at most key(+inf) < 0xffffffff, the mark of a free slot
+    for (int d = S - k; d > 0; --d) {
+      const uint32_t m = __reduce_min_sync(kFull, key);
+      const uint32_t eq = __ballot_sync(kFull, key == m);
+      if (lane == 31 - __clz(eq)) {  // the latest block among the smallest
+        key = 0xffffffffu;
+        keep = false;
+      }
+    }
+    const uint32_t s0 = __ballot_sync(kFull, keep);
+    if (keep) out[p.n_init + __popc(s0 & below)] = blk;
+    return true;
+  }
+  const uint32_t k0 = order_key(__uint_as_float(sm.key[lane]));  // S > 32: every lane holds one
+  const int b0 = sm.blk[lane];
   const uint32_t k1 = lane + 32 < S ? order_key(__uint_as_float(sm.key[lane + 32])) : 0u;
   const int b1 = lane + 32 < S ? sm.blk[lane + 32] : 0;
   __syncwarp();  // the next row may overwrite the arrays
   KeyBracket bs;
-  bs.lo = __reduce_min_sync(kFull, min(k0 ? k0 : 0xffffffffu, k1 ? k1 : 0xffffffffu));
+  bs.lo = __reduce_min_sync(kFull, min(k0, k1 ? k1 : 0xffffffffu));
   bs.hi = __reduce_max_sync(kFull, max(k0, k1)) + 1u;
   bs.clo = S;
   bs.chi = 0;
@@ -524,7 +612,7 @@ __device__ __forceinline__ bool topk_select_fast(const TopkProblem& p, const Top
   const uint32_t tau = bs.lo;
   const int need =
       k - __popc(__ballot_sync(kFull, k0 > tau)) - __popc(__ballot_sync(kFull, k1 > tau));
-  const uint32_t e0 = __ballot_sync(kFull, k0 == tau && k0 != 0u);
+  const uint32_t e0 = __ballot_sync(kFull, k0 == tau);
   const uint32_t e1 = __ballot_sync(kFull, k1 == tau && k1 != 0u);
   const bool take0 = k0 > tau || (((e0 >> lane) & 1u) && __popc(e0 & below) < need);
   const bool take1 =
@@ -547,37 +635,68 @@ __device__ __noinline__ void topk_general(const TopkProblem* p, const TopkRow r,
 }
 
 // J: keys per lane (a multiple of 4), covering nblk <= 32 * J.
+
 template <int J>
-constexpr int topk_ctas_per_sm() {
+__host__ __device__ constexpr int topk_ctas_per_sm() {
   return J <= 8 ? 4 : (J <= 32 ? 3 : (J <= 64 ? 2 : 1));
 }
 
+// Row buffer: 32 lanes x nqo quads (nqo <= J/4 + 1), then its mbarrier.
+// A copy fills at most the first 4 nblk <= 128 J bytes; the lanes' reads
+// past block c land in the rest and are masked.
 template <int J>
-constexpr int topk_smem_bytes() {
-  return kTopkWarps * (J * 32 * 4 + static_cast<int>(sizeof(TopkSmem)));
+__host__ __device__ constexpr int topk_buffer_bytes() {
+  return J * 32 * 4 + 512 + 16;
 }
 
 template <int J>
+__host__ __device__ constexpr int topk_smem_bytes() {
+  return kTopkWarps * (topk_buffer_bytes<J>() + static_cast<int>(sizeof(TopkSmem)));
+}
+
+// One warp per row, rows grid-stride, one row buffer per warp: the next
+// row's copy starts as soon as this row's survivors are out of the buffer
+// (topk_select_fast), so it is in flight during the exact selection and the
+// output. (Two buffers per warp, the next row copied while this one is
+// read, measured slower with cp.async and with bulk copies alike.)
+template <int J>
 __global__ void __launch_bounds__(kTopkWarps * 32, topk_ctas_per_sm<J>())
     topk_blocks_kernel(const __grid_constant__ TopkProblem p) {
+  constexpr int kBar = J * 32 * 4 + 512;  // mbarrier offset inside the buffer
   extern __shared__ __align__(16) uint8_t topk_smem_raw[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t sbuf = smem_u32(topk_smem_raw) + warp * (J * 32 * 4);
-  TopkSmem& sm = reinterpret_cast<TopkSmem*>(topk_smem_raw + kTopkWarps * (J * 32 * 4))[warp];
+  const uint32_t sbuf = smem_u32(topk_smem_raw) + warp * topk_buffer_bytes<J>();
+  const uint32_t bar = sbuf + kBar;
+  TopkSmem& sm =
+      reinterpret_cast<TopkSmem*>(topk_smem_raw + kTopkWarps * topk_buffer_bytes<J>())[warp];
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kTopkWarps;
   int64_t row = static_cast<int64_t>(blockIdx.x) * kTopkWarps + warp;
   if (row >= p.rows) return;
-  uint32_t raw[J];
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
   TopkRow r = topk_row_info(p, row);
-  topk_prefetch<J>(p, r, lane, sbuf);
-  for (;;) {
+  topk_prefetch<J>(p, r, lane, sbuf, bar);
+  for (uint32_t parity = 0;; parity ^= 1u) {  // the buffer's mbarrier phase of this row
     const int64_t r1 = row + stride;
     const bool more = r1 < p.rows;
     const TopkRow next = more ? topk_row_info(p, r1) : r;
-    if (!topk_select_fast<J>(p, r, next, more, lane, raw, sbuf, sm))
+    if (!topk_wait(p, bar, parity)) {
+      report_timeout();  // the row's scores never arrived: stop (outputs undefined)
+      return;
+    }
+    __syncwarp();
+    bool pending = more;
+    if (!topk_select_fast<J>(p, r, next, pending, lane, sbuf, bar, sm))
       topk_general<J>(&p, r, lane, &sm);
-    __syncwarp();  // the shared arrays are free for the next row
+    if (pending) {  // not issued by the fast path
+      __syncwarp();
+      topk_prefetch<J>(p, next, lane, sbuf, bar);
+    }
+    __syncwarp();  // the buffer and the shared arrays are free for the next row
     if (!more) break;
     r = next;
     row = r1;
@@ -603,6 +722,9 @@ int launch_topk(const TopkProblem& p, cudaStream_t st) {
 }
 
 }  // namespace
+
+int topk_read_and_clear_status(unsigned int* value) { return read_and_clear_status(value); }
+
 }  // namespace nsa
 
 extern "C" int nsa_topk_blocks(const float* scores, int32_t* block_indices, int64_t B, int64_t M,

@@ -57,6 +57,7 @@ def _run(sc, N, bs, T, n_init, n_local):
 @pytest.mark.parametrize("B,M,N,G,bs,T,n_init,n_local", [
     (2, 700, 700, 3, 32, 6, 1, 2),       # <= 256 blocks
     (1, 1000, 1000, 2, 4, 16, 0, 0),     # <= 256 blocks, no forced
+    (1, 1024, 1024, 2, 4, 12, 1, 2),     # 256 blocks: a multiple of 4 (bulk copies)
     (1, 2000, 2000, 2, 2, 9, 4, 5),      # <= 1024 blocks, all forced
     (1, 1200, 900, 1, 1, 33, 3, 1),      # <= 1024, queries past the keys, T > 32
     (1, 1800, 1800, 1, 1, 20, 1, 2),     # <= 2048 blocks
