@@ -45,6 +45,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "nsa_sel_attn.h"
@@ -108,6 +109,7 @@ struct SwaProblem {
   int left, right;  // clamped to [0, M + N]: M + N is unbounded in effect
   float sl2;        // scale * log2(e)
   int64_t items;    // B * H * qtiles
+  bool o32;         // O 32-byte aligned: 32-byte stores of O rows (head-pair kernel)
 };
 
 // One work item: a tile of 128 queries of one head, and the keys its
@@ -795,62 +797,99 @@ __global__ void __launch_bounds__(kSwaPairThreads, 1)
           tc_ld32(lane_addr + col_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
         tc_wait_ld();
         const int j0 = (it.t0 + i) * kSwaKeys;
-        if (j0 < it.in_lo || j0 + kSwaKeys - 1 > it.in_hi) {
+        // The tile's softmax, compiled twice: interior tiles (every key
+        // visible to every row) without any mask code, edge tiles with it.
+        auto tile = [&](auto edge_c) {
+          // 32-key chunks of an edge tile, decided for the warp's 32 rows at
+          // once (the window bounds grow with the row): every key visible to
+          // every row, to none, or per element. Keys of empty chunks are
+          // neither maximised nor exponentiated (P = 0).
+          uint32_t empty = 0u;
+          if constexpr (decltype(edge_c)::value) {
+            const int qa = it.q0 + quarter * 32, qb = qa + 31;
+            const int lo_a = max(0, qa - p.left), lo_b = max(0, qb - p.left);
+            const int hi_a = min(p.N - 1, qa + p.right), hi_b = min(p.N - 1, qb + p.right);
 #pragma unroll
-          for (int j = 0; j < kSwaKeys; ++j)
-            if (j0 + j < lo_i || j0 + j > hi_i) sr[j] = __float_as_uint(-INFINITY);
-        }
-        float m8[8];
+            for (int c = 0; c < kSwaKeys / 32; ++c) {
+              const int cs = j0 + 32 * c, ce = cs + 31;
+              if (hi_b < cs || lo_a > ce) {
+                empty |= 1u << c;
+              } else if (lo_b > cs || hi_a < ce) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) m8[j] = __uint_as_float(sr[j]);
-#pragma unroll
-        for (int j = 8; j < kSwaKeys; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
-        const bool move = mx > ref + kSwaSlack;
-        if (__any_sync(kFull, move)) {
-          const float alpha = move ? ex2(ref - mx) : 1.f;
-          if (i > 0) {
-            // PV of the previous tile has completed: this tile's S was
-            // committed after it
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tc_ld32(lane_addr + col_o + 32 * c, o);
-              tc_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-              tc_st32(lane_addr + col_o + 32 * c, o);
+                for (int j = 32 * c; j < 32 * c + 32; ++j)
+                  if (j0 + j < lo_i || j0 + j > hi_i) sr[j] = __float_as_uint(-INFINITY);
+              }
             }
-            tc_wait_st();
           }
-          if (move) {
-            l *= alpha;
-            ref = mx;
-            neg = -mx;
+          float m8[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m8[j] = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kSwaKeys / 32; ++c) {
+            if ((empty >> c) & 1u) continue;
+#pragma unroll
+            for (int j = 32 * c; j < 32 * c + 32; ++j)
+              m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
           }
-        }
-        float l8[8];
+          const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
+          const bool move = mx > ref + kSwaSlack;
+          if (__any_sync(kFull, move)) {
+            const float alpha = move ? ex2(ref - mx) : 1.f;
+            if (i > 0) {
+              // PV of the previous tile has completed: this tile's S was
+              // committed after it
+#pragma unroll 1
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tc_ld32(lane_addr + col_o + 32 * c, o);
+                tc_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) l8[j] = 0.f;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t pw[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int j = 64 * h2 + 2 * c;
-            const float e0 = ex2(fmaf(__uint_as_float(sr[j]), sl2, neg));
-            const float e1 = ex2(fmaf(__uint_as_float(sr[j + 1]), sl2, neg));
-            l8[(2 * c) & 7] += e0;
-            l8[(2 * c + 1) & 7] += e1;
-            pw[c] = pack2<BF16>(e0, e1);
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                tc_st32(lane_addr + col_o + 32 * c, o);
+              }
+              tc_wait_st();
+            }
+            if (move) {
+              l *= alpha;
+              ref = mx;
+              neg = -mx;
+            }
           }
-          tc_st32(lane_addr + col_s + 32 * h2, pw);  // P over the S just read
-        }
-        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-        tc_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(kPPFull + hx));
+          float l8[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) l8[j] = 0.f;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t pw[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              if ((empty >> (2 * h2 + half)) & 1u) {
+#pragma unroll
+                for (int c = 16 * half; c < 16 * half + 16; ++c) pw[c] = 0u;
+                continue;
+              }
+#pragma unroll
+              for (int c = 16 * half; c < 16 * half + 16; ++c) {
+                const int j = 64 * h2 + 2 * c;
+                const float e0 = ex2(fmaf(__uint_as_float(sr[j]), sl2, neg));
+                const float e1 = ex2(fmaf(__uint_as_float(sr[j + 1]), sl2, neg));
+                l8[(2 * c) & 7] += e0;
+                l8[(2 * c + 1) & 7] += e1;
+                pw[c] = pack2<BF16>(e0, e1);
+              }
+            }
+            tc_st32(lane_addr + col_s + 32 * h2, pw);  // P over the S just read
+          }
+          l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+          tc_wait_st();
+          tc_fence_before();
+  mbar_arrive(bar(kPPFull + hx));
+        };
+        if (j0 < it.in_lo || j0 + kSwaKeys - 1 > it.in_hi)
+          tile(std::true_type{});
+        else
+          tile(std::false_type{});
       }
       if (failed) break;
       // epilogue: O of this head once the item's last PV has completed
@@ -873,16 +912,34 @@ __global__ void __launch_bounds__(kSwaPairThreads, 1)
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (iq < p.M) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.O) +
-                                              ((static_cast<int64_t>(it.b) * p.M + iq) * p.H + h) * D);
+        uint16_t* const orow =
+            static_cast<uint16_t*>(p.O) + ((static_cast<int64_t>(it.b) * p.M + iq) * p.H + h) * D;
+        if (p.o32) {
+          // 32-byte stores: whole sectors, half the store instructions
 #pragma unroll
-        for (int q = 0; q < D / 8; ++q) {
-          uint4 w;
-          w.x = pack2<BF16>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-          w.y = pack2<BF16>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          w.z = pack2<BF16>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-          w.w = pack2<BF16>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-          dst[q] = w;
+          for (int q = 0; q < D / 16; ++q) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[e] = pack2<BF16>(__uint_as_float(o[16 * q + 2 * e]) * inv,
+                                 __uint_as_float(o[16 * q + 2 * e + 1]) * inv);
+            asm volatile(
+                "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(orow + 16 * q),
+                "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                "r"(w[7])
+                : "memory");
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int q = 0; q < D / 8; ++q) {
+            uint4 w;
+            w.x = pack2<BF16>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+            w.y = pack2<BF16>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+            w.z = pack2<BF16>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+            w.w = pack2<BF16>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+            dst[q] = w;
+          }
         }
         if (p.LSE != nullptr) {
           constexpr float kLn2 = 0.69314718055994530942f;
@@ -1004,6 +1061,7 @@ extern "C" int nsa_swa_fwd(const void* Q, const void* K, const void* V, void* O,
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   p.sl2 = sc * 1.4426950408889634f;
   p.O = O;
+  p.o32 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf = dtype == NSA_BF16;
   // long windows (many key tiles per query tile) with an even number of

@@ -131,3 +131,26 @@ def test_swa_large_sampled(window):
     ms = np.concatenate([rng.integers(0, M, 200), [0, 1, 127, 128, 1023, 1024, M - 1]])
     rows = sorted({(0, int(m), int(rng.integers(8))) for m in ms})
     _check(q, k, v, window, "bf16", O, L, rows, what=f"8k {window}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_swa_output_alignment(D):
+    """The head-pair kernel stores O rows with 32-byte stores when O is
+    32-byte aligned and 16-byte stores otherwise: an O that starts 16 bytes
+    into an allocation gives the same bits."""
+    import torch
+
+    from nsa_block_selection_gb300 import swa_fwd
+
+    q, k, v = _inputs(1, 700, 700, 8, 2, D, "bf16", 12)
+    t = [torch.from_numpy(x).cuda().to(torch.bfloat16) for x in (q, k, v)]
+    shape = tuple(t[0].shape)
+    n = t[0].numel()
+    flat = torch.full((n + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o16 = flat[8:].view(shape)  # 16-byte aligned, not 32
+    assert o16.data_ptr() % 32 == 16
+    O16, L16 = swa_fwd(*t, window=(600, 0), out=o16)
+    O32, L32 = swa_fwd(*t, window=(600, 0), out=poisoned(shape, torch.bfloat16))
+    torch.cuda.synchronize()
+    assert torch.equal(O16, O32) and torch.equal(L16, L32)
+    _check(q, k, v, (600, 0), "bf16", O32, L32, _all_rows(1, 700, 2))
