@@ -182,12 +182,13 @@ int64_t nsa_sel_attn_fwd_shared_workspace_bytes(int64_t B, int64_t M, int64_t G)
  * every query (as nsa_topk_blocks with n_init, n_local > 0 writes them) give
  * the queries of a tile of 16 consecutive positions some blocks in common.
  * Per (b, g, tile) a list pass records up to 7
- * blocks that every query of the tile lists and whose keys every one of
- * them sees (the block ends at or before the tile's first query, and
- * below N), in the order the tile's first query lists them. A tile-shared
- * pass gathers those blocks once and computes, on the tcgen05 tensor cores,
- * the softmax of all 16 x 8 (query, head) rows over their keys; it writes
- * the normalised partial O and its LSE into O and LSE. The gather kernel of
+ * blocks that every query of the tile lists, whose first key the tile's
+ * first query sees and whose keys all lie below M and N, in the order the
+ * tile's first query lists them. A tile-shared pass gathers those blocks
+ * once and computes, on the tcgen05 tensor cores, the softmax of all
+ * 16 x 8 (query, head) rows over their keys (each row masked to the keys
+ * at or before its query); it writes the normalised partial O and its LSE
+ * into O and LSE. The gather kernel of
  * nsa_sel_attn_fwd then skips the recorded blocks and continues the online
  * softmax from that state, so its outputs cover every selected key once.
  * The result is the same operation as nsa_sel_attn_fwd_ex with the same
@@ -201,9 +202,13 @@ int64_t nsa_sel_attn_fwd_shared_workspace_bytes(int64_t B, int64_t M, int64_t G)
  * blocks are too small a share of a row's bytes for the extra passes to pay
  * (measured slower than one pass), so those problems take the one-pass
  * kernel too. Every other argument, layout, check and property is that
- * of nsa_sel_attn_fwd_ex. A key row the tile-shared pass reads is visible
- * to every query of the tile, so NaN or Inf in rows a query may not see
- * still never reaches that query's output.
+ * of nsa_sel_attn_fwd_ex, with one difference in what non-finite inputs
+ * may do: NaN or Inf in K/V rows past every query (>= M), in blocks no
+ * query lists, and in the keys of a tile's own block past the tile's last
+ * query never reach an output (as for the one-pass call), but a non-finite
+ * V row between two queries of the same 16-query tile reaches the earlier
+ * query's output too (the tile's rows share one P.V product over those
+ * keys).
  */
 int nsa_sel_attn_fwd_shared(const void* Q, const void* K, const void* V,
                             const int32_t* block_indices, float* O, float* LSE, int64_t B,

@@ -18,10 +18,12 @@
 //
 // List pass (shared_blocks_kernel, one warp per (b, g, tile)): the blocks
 // listed by every query of the tile, taken in the order the tile's first
-// query lists them, up to kSharedMax, and only blocks whose keys are all
-// visible to every query of the tile (last key <= the first query's
-// position, and < N): the tile-shared pass needs no causal mask, and a key
-// row it reads reaches no query that may not see it. The record
+// query lists them, up to kSharedMax, and only blocks whose first key is
+// visible to the tile's first query and whose keys all lie below both M and
+// N. Every query of the tile then sees at least one key of each such block;
+// the tile-shared pass masks the keys after a row's query (in the block the
+// tile's queries sit in), and a key it reads past a row's query is a key
+// row of the sequence (< M), never a row past its end. The record
 // {count, ids} per tile is the workspace both other passes read.
 //
 // Tile-shared pass (sel_attn_shared_kernel): persistent, one CTA per SM
@@ -137,16 +139,17 @@ __global__ void __launch_bounds__(128) shared_blocks_kernel(const ListProblem p)
   const int64_t b = bg / p.G;
   const int64_t m0 = tile * kSharedTileQ;
   const int R = static_cast<int>(p.M - m0 < kSharedTileQ ? p.M - m0 : kSharedTileQ);
-  // block e qualifies when (e + 1) * bs <= lim: its last key is visible to
-  // the tile's first query and lies below N
-  const int64_t lim = m0 + 1 < p.N ? m0 + 1 : p.N;
+  // block e qualifies when e * bs <= m0 (the tile's first query sees its
+  // first key) and (e + 1) * bs <= min(M, N) (all its keys exist, below M)
+  const int64_t lim = p.M < p.N ? p.M : p.N;
   const int64_t qstride = p.G * p.T;  // between the index rows of consecutive queries
   const int32_t* row0 = p.idx + ((b * p.M + m0) * p.G + g) * p.T;
   int cnt = 0, mine = -1;  // lane j < cnt holds recorded id j
   for (int64_t w = 0; w < p.T && cnt < kSharedMax; w += 32) {
     const int64_t j = w + lane;
     const int e = j < p.T ? __ldg(row0 + j) : -1;
-    bool cand = e >= 0 && e < p.nblk && static_cast<int64_t>(e + 1) * p.bs <= lim;
+    bool cand = e >= 0 && e < p.nblk && static_cast<int64_t>(e) * p.bs <= m0 &&
+                static_cast<int64_t>(e + 1) * p.bs <= lim;
     // an id repeated in the window counts at its first lane; recorded ids once
     const unsigned same = __match_any_sync(kFull, e);
     cand = cand && (same & ((1u << lane) - 1u)) == 0u;
@@ -355,8 +358,10 @@ __global__ void __launch_bounds__(kShThreads, 1)
         return true;
       };
       // PV of block gi into the O buffer of tile n; `first` / `last`: the
-      // tile's first / last block
-      auto issue_pv = [&](int64_t gi, int n, bool first, bool last) -> bool {
+      // tile's first / last block; `nk`: its 16-key steps that reach a key
+      // some row of the tile sees (the keys past the tile's last query are
+      // left out: their P is 0, and their V rows are never multiplied)
+      auto issue_pv = [&](int64_t gi, int n, bool first, bool last, int nk) -> bool {
         const int st = static_cast<int>(gi % kVStages);
         const int sb = static_cast<int>(gi & 1);
         const int ob = n & 1;
@@ -371,8 +376,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
         const uint32_t vb = base + C::kOffV + st * C::kKVBytes;
         const uint32_t pcol = tmem + kColS + static_cast<uint32_t>(sb) * 64;
         const uint32_t ocol = tmem + kColO + static_cast<uint32_t>(ob) * kShD;
-#pragma unroll
-        for (int kk = 0; kk < BS / 16; ++kk)
+        for (int kk = 0; kk < nk; ++kk)
           tc_mma_ts(ocol, pcol + 8 * kk, umma_desc_sw128(vb + kk * 2048, C::kKVBox), idesc_o,
                     (!first || kk > 0) ? 1u : 0u);
         tc_commit(bar(kVFree + st));
@@ -384,26 +388,31 @@ __global__ void __launch_bounds__(kShThreads, 1)
       int64_t gi = 0;
       int n = 0;
       int64_t pend = -1;  // block whose PV is still to be issued
-      int pend_n = 0;
+      int pend_n = 0, pend_nk = BS / 16;
       bool pend_first = false, pend_last = false;
       for (int64_t x = blockIdx.x; x < p.units && ok; x += step) {
         const int cnt = tile_count(p, x);
         if (cnt == 0) continue;
         const int qb = n & 1;
+        const int64_t m0 = (x % p.ntiles) * kSharedTileQ;
+        const int64_t last_q = m0 + kSharedTileQ - 1 < p.M - 1 ? m0 + kSharedTileQ - 1 : p.M - 1;
         ok = wait_phase(bar(kQFull + qb), static_cast<uint32_t>((n >> 1) & 1), kWaitLimitNs);
         for (int i = 0; i < cnt && ok; ++i) {
           ok = issue_s(gi + i, qb);
           if (ok && i == cnt - 1) tc_commit(bar(kQEmpty + qb));
-          if (ok && pend >= 0) ok = issue_pv(pend, pend_n, pend_first, pend_last);
+          if (ok && pend >= 0) ok = issue_pv(pend, pend_n, pend_first, pend_last, pend_nk);
+          // keys e * BS .. last_q of block e (e * BS <= m0 <= last_q)
+          const int64_t span = last_q + 1 - static_cast<int64_t>(__ldg(p.lists + x * kSharedRec + 1 + i)) * BS;
           pend = gi + i;
           pend_n = n;
+          pend_nk = span >= BS ? BS / 16 : static_cast<int>((span + 15) / 16);
           pend_first = i == 0;
           pend_last = i == cnt - 1;
         }
         gi += cnt;
         ++n;
       }
-      if (ok && pend >= 0) ok = issue_pv(pend, pend_n, pend_first, pend_last);
+      if (ok && pend >= 0) ok = issue_pv(pend, pend_n, pend_first, pend_last, pend_nk);
       // every MMA issued has completed once kEnd completes
       tc_commit(bar(kEnd));
       if (!wait_phase(bar(kEnd), 0, kWaitLimitNs)) ok = false;
@@ -441,7 +450,18 @@ __global__ void __launch_bounds__(kShThreads, 1)
         for (int c = 0; c < BS / 32; ++c)
           tc_ld32(scol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
         tc_wait_ld();
-        // every key of the block is visible to every row: no mask
+        // keys after the row's query (only in a block that reaches past the
+        // tile's first query) are masked; every row sees the block's first key
+        {
+          const int e = __ldg(p.lists + x * kSharedRec + 1 + i);
+          const int m0 = static_cast<int>((x % p.ntiles) * kSharedTileQ);
+          if ((e + 1) * BS - 1 > m0) {  // CTA-uniform
+            const int thr = m0 + (quarter * 32 + lane) / kShHeads - e * BS;  // last visible j
+#pragma unroll
+            for (int j = 0; j < BS; ++j)
+              if (j > thr) sr[j] = __float_as_uint(-INFINITY);
+          }
+        }
         float m8[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) m8[j] = __uint_as_float(sr[j]);

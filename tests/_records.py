@@ -9,7 +9,8 @@ TILE, MAXREC = 16, 7
 def records_ref(idx, N, bs):
     """[B, G, tiles, 8] int32: count, then up to 7 ids -- the blocks listed by
     every query of the tile, in the order the tile's first query lists them,
-    whose last key is <= the first query's position and < N."""
+    whose first key is <= the first query's position and whose keys all lie
+    below min(M, N)."""
     B, M, G, T = idx.shape
     nblk = -(-N // bs)
     ntiles = -(-M // TILE)
@@ -20,12 +21,13 @@ def records_ref(idx, N, bs):
                 m0 = t * TILE
                 rows = idx[b, m0:min(M, m0 + TILE), g]
                 sets = [set(r.tolist()) for r in rows]
-                lim = min(m0 + 1, N)
+                lim = min(M, N)
                 ids = []
                 for e in rows[0].tolist():
                     if len(ids) == MAXREC:
                         break
-                    if 0 <= e < nblk and (e + 1) * bs <= lim and e not in ids and \
+                    if 0 <= e < nblk and e * bs <= m0 and (e + 1) * bs <= lim and \
+                            e not in ids and \
                             all(e in s for s in sets):
                         ids.append(e)
                 out[b, g, t, 0] = len(ids)

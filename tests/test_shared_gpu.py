@@ -1,8 +1,10 @@
 """The two-pass forward (nsa_sel_attn_fwd_shared) against the CPU oracle.
 
 Per tile of 16 queries the list pass records the blocks every query of the
-tile lists and sees whole; the tile-shared pass attends to them on the
-tcgen05 tensor cores, and the gather kernel continues from that state. The
+tile lists whose first key the tile's first query sees and whose keys all
+lie below M and N; the tile-shared pass attends to them on the tcgen05
+tensor cores (masking the keys after each row's query in the block the
+tile sits in), and the gather kernel continues from that state. The
 records are integer work and are compared exactly with a restatement of
 their definition here; O and LSE are compared with the oracle under the
 forward's tolerance (bf16 inputs add the bf16 rounding term of P, as in the
@@ -157,6 +159,25 @@ def test_unselected_and_future_rows_may_hold_nan(M):
     O2, L2, _, _ = run_shared(q, k2, v2, idx, bs)
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
     assert torch.isfinite(O2).all()
+
+
+def test_keys_past_a_tiles_last_query_never_reach_it():
+    """The tile-shared pass takes the block its queries sit in, masked per
+    row; the keys of that block past the tile's last query enter no product
+    of the tile. K/V rows 80..127 poisoned: the rows of queries 0..79 are
+    bit-identical to the clean run (queries 80.. see those keys and are not
+    compared)."""
+    import torch
+
+    bs, M = 64, 512
+    q, k, v, idx = _inputs(1, M, M, 16, 2, 128, bs, 6, "first_two_local", seed=12)
+    O1, L1, rec, _ = run_shared(q, k, v, idx, bs)
+    assert (rec[0, :, 64 // TILE, 1:4] == 1).any(-1).all()  # tile of queries 64..79 shares block 1
+    k2, v2 = k.copy(), v.copy()
+    k2[:, 80:128] = np.float16(np.nan)
+    v2[:, 80:128] = np.float16(np.nan)
+    O2, L2, _, _ = run_shared(q, k2, v2, idx, bs)
+    assert torch.equal(O1[:, :80], O2[:, :80]) and torch.equal(L1[:, :, :80], L2[:, :, :80])
 
 
 @pytest.mark.parametrize("H,G,D,M,bs", [(8, 2, 128, 300, 64), (16, 2, 64, 300, 64),
