@@ -710,10 +710,11 @@ bool shared_pass_eligible(int64_t H, int64_t G, int64_t D, int o_dtype, const in
 }
 
 bool shared_pass_sizes_ok(int64_t M, int64_t N, int64_t T, int block_size) {
-  // 64-key blocks only: two common blocks of 64 keys are an eighth of a
-  // 16-block row's bytes and the gather kernel saves more than the two extra
-  // passes cost; at 32 keys they are a sixteenth and the passes cost more
-  // than they save (6.36 against 6.21 ms one-pass at B=2, M=32k, T=32).
+  // 64-key blocks only: three common blocks of 64 keys are about a fifth of
+  // a 16-block row's bytes and the gather kernel saves more than the two
+  // extra passes cost; at 32 keys they are about a tenth of a 32-block row
+  // and the passes cost more than they save (6.27 against 6.19 ms one-pass
+  // at B=2, M=32k, T=32).
   // Tensor-map boxes (16 queries, block_size keys) stay within the tensors.
   return block_size == 64 && M >= kSharedTileQ && N >= block_size && T > 0;
 }
