@@ -526,10 +526,13 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
 // columns of its S once S has been read: the tensor pipe runs the MMAs in
 // issue order, so the next S of that head is issued after the PV that reads
 // P), O_A at 256, O_B at 256 + D. Shared memory holds one Q pair, so the
-// next item's Q waits for the last QK^T of the current one. The softmax
-// warps write O rows straight to global memory (items are long).
+// next item's Q waits for the last QK^T of the current one. For long
+// windows the softmax warps write O rows straight to global memory; for
+// short ones (TMA_O) they stage them in a shared buffer that warp 10 stores
+// with TMA tensor stores.
 // Warpgroups: 0 softmax and epilogue of head A (warps 0-3), 1 of head B
-// (warps 4-7), 2 producer (warp 8), MMA issuer (warp 9), two idle warps.
+// (warps 4-7), 2 producer (warp 8), MMA issuer (warp 9), O store warp
+// (warp 10, TMA_O) and an idle warp.
 // ---------------------------------------------------------------------------
 
 enum SwaPairBar : int {
@@ -543,7 +546,9 @@ enum SwaPairBar : int {
   kPPFull = 12,    // 2: P written over that S
   kPOFull = 14,    // 2: the item's last PV of the head has completed
   kPOEmpty = 16,   // 2: the head's softmax warps have read its O
-  kPNumBars = 18
+  kPOStaged = 18,  // 2 (TMA_O): the head's softmax warps have staged its O tile
+  kPOSmemFree = 20,  // (TMA_O) the last O tile store has read the staging buffer
+  kPNumBars = 21
 };
 
 constexpr int kSwaPairThreads = 384;
@@ -551,7 +556,12 @@ constexpr int kSwaPairThreads = 384;
 // single Q pair buffer stalls between short items)
 constexpr int64_t kSwaPairMinKeys = 512;
 
-template <int D>
+// TMA_O: the O tiles go through one shared staging buffer (heads A, B in
+// turn) and are written by TMA tensor stores from an otherwise idle warp;
+// otherwise each softmax thread stores its own O row. The first pays at
+// short windows (many items per key), the second at long ones (it keeps the
+// softmax path free of the staging protocol's registers).
+template <int D, bool TMA_O>
 struct SwaPairCfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kAtomBytes = kSwaQ * 128;
@@ -560,11 +570,16 @@ struct SwaPairCfg {
   static constexpr int kOffQ = 0;                    // Q_A, Q_B
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + 2 * kKVBytes;
-  static constexpr int kOffBar = kOffV + 2 * kKVBytes;
+  static constexpr int kOffO = kOffV + 2 * kKVBytes;  // (TMA_O) one head's O tile, staged
+  static constexpr int kOffBar = kOffO + (TMA_O ? kQBytes : 0);
   static constexpr int kOffTmem = kOffBar + kPNumBars * 8;
   static constexpr int kUsed = kOffTmem + 16 + 1024;
   static constexpr int kSmemBytes = kUsed > 118784 ? kUsed : 118784;
+  static_assert(kSmemBytes <= 232448, "fits one SM");
 };
+
+// Windows up to this many keys per query tile use the TMA_O variant.
+constexpr int64_t kSwaPairTmaOMaxKeys = 1152;
 
 // Item -> (b, KV group, query tile, head pair), the pair fastest.
 __device__ __forceinline__ SwaItem swa_item_pair(const SwaProblem& p, int64_t item) {
@@ -577,12 +592,13 @@ __device__ __forceinline__ SwaItem swa_item_pair(const SwaProblem& p, int64_t it
   return swa_item(p, static_cast<int64_t>(rest) * p.hpg + 2 * pp);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool TMA_O>
 __global__ void __launch_bounds__(kSwaPairThreads, 1)
     swa_fwd_pair_kernel(const SwaProblem p, const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV) {
-  using C = SwaPairCfg<D>;
+                        const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmO) {
+  using C = SwaPairCfg<D, TMA_O>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -602,7 +618,9 @@ __global__ void __launch_bounds__(kSwaPairThreads, 1)
       mbar_init(bar(kPPFull + s), 4 * 32);
       mbar_init(bar(kPOFull + s), 1);
       mbar_init(bar(kPOEmpty + s), 4 * 32);
+      mbar_init(bar(kPOStaged + s), 4 * 32);
     }
+    mbar_init(bar(kPOSmemFree), 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -760,6 +778,30 @@ __global__ void __launch_bounds__(kSwaPairThreads, 1)
         ++n;
       }
       failed = !ok;
+    } else if (TMA_O && warp == 10 && lane == 0) {
+      // ---- O tile stores: the heads' staged tiles in the order A, B of
+      // every item, one TMA tensor store each; the staging buffer is handed
+      // back once the store has read it ----
+      tma_prefetch_desc(&tmO);
+      int ne = 0;  // items so far
+      for (int64_t k = 0; k < nrounds && !failed; ++k) {
+        const int64_t x = item_of(k);
+        if (x >= p.items) continue;
+        const SwaItem it = swa_item_pair(p, x);
+        for (int hx = 0; hx < 2; ++hx) {
+          if (!wait_phase(bar(kPOStaged + hx), static_cast<uint32_t>(ne & 1), kWaitLimitNs)) {
+            failed = true;
+            break;
+          }
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_store_4d(&tmO, base + C::kOffO + a * C::kAtomBytes, a * 64, it.h + hx, it.q0, it.b);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(bar(kPOSmemFree));
+        }
+        ++ne;
+      }
+      bulk_wait_group0();  // the stores have completed
     }
   } else {
     setmaxnreg_inc<200>();  // every warp of warpgroups 0 and 1, converged
@@ -774,7 +816,8 @@ __global__ void __launch_bounds__(kSwaPairThreads, 1)
       return __all_sync(kFull, wait_phase(bar(b), parity, kWaitLimitNs));
     };
     int64_t gt = 0;
-    int n = 0;
+    int n = 0;   // items with keys so far
+    int ne = 0;  // (TMA_O) items so far: O tiles staged by this head
     for (int64_t k = 0; k < nrounds && !failed; ++k) {
       const int64_t x = item_of(k);
       if (x >= p.items) continue;
@@ -911,10 +954,36 @@ __global__ void __launch_bounds__(kSwaPairThreads, 1)
         for (int j = 0; j < D; ++j) o[j] = 0u;
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      if constexpr (TMA_O) {
+        // stage the O row (128B-swizzled, one 64-column atom after the
+        // other) once the previous tile store, of either head, has read the
+        // buffer: the tiles go A, B of every item
+        const int e = 2 * ne + hx;
+        if (e >= 1 && !wait_all(kPOSmemFree, static_cast<uint32_t>((e - 1) & 1))) {
+          failed = true;
+          break;
+        }
+        uint8_t* const srow = gbase + C::kOffO + row * 128;
+#pragma unroll
+        for (int q = 0; q < D / 8; ++q) {
+          uint4 w;
+          w.x = pack2<BF16>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+          w.y = pack2<BF16>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+          w.z = pack2<BF16>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+          w.w = pack2<BF16>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+          *reinterpret_cast<uint4*>(srow + (q >> 3) * C::kAtomBytes +
+                                    (((q & 7) ^ (row & 7)) << 4)) = w;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kPOStaged + hx));
+        ++ne;
+      }
       if (iq < p.M) {
         uint16_t* const orow =
             static_cast<uint16_t*>(p.O) + ((static_cast<int64_t>(it.b) * p.M + iq) * p.H + h) * D;
-        if (p.o32) {
+        if constexpr (TMA_O) {
+          // O went through the staging buffer
+        } else if (p.o32) {
           // 32-byte stores: whole sectors, half the store instructions
 #pragma unroll
           for (int q = 0; q < D / 16; ++q) {
@@ -994,18 +1063,23 @@ int launch_swa(const SwaProblem& p, const void* Q, const void* K, const void* V,
   return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool TMA_O>
 int launch_swa_pair(SwaProblem p, const void* Q, const void* K, const void* V,
                     cudaStream_t st) {
-  using C = SwaPairCfg<D>;
+  using C = SwaPairCfg<D, TMA_O>;
   constexpr CUtensorMapDataType dt =
       BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!encode_kv_map(&tq, Q, p.B, p.M, p.H, D, kSwaQ, dt) ||
       !encode_kv_map(&tk, K, p.B, p.N, p.Hkv, D, kSwaKeys, dt) ||
       !encode_kv_map(&tv, V, p.B, p.N, p.Hkv, D, kSwaKeys, dt))
     return NSA_ERR_LAUNCH;
-  auto kern = swa_fwd_pair_kernel<D, BF16>;
+  if (TMA_O) {
+    if (!encode_kv_map(&to, p.O, p.B, p.M, p.H, D, kSwaQ, dt)) return NSA_ERR_LAUNCH;
+  } else {
+    memset(&to, 0, sizeof(to));  // never read
+  }
+  auto kern = swa_fwd_pair_kernel<D, BF16, TMA_O>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return NSA_ERR_LAUNCH;
@@ -1015,7 +1089,7 @@ int launch_swa_pair(SwaProblem p, const void* Q, const void* K, const void* V,
     return NSA_ERR_LAUNCH;
   p.items /= 2;  // items of two heads (hpg is even)
   const int64_t blocks = p.items < sms ? p.items : sms;
-  kern<<<static_cast<unsigned>(blocks), kSwaPairThreads, C::kSmemBytes, st>>>(p, tq, tk, tv);
+  kern<<<static_cast<unsigned>(blocks), kSwaPairThreads, C::kSmemBytes, st>>>(p, tq, tk, tv, to);
   return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
@@ -1068,11 +1142,18 @@ extern "C" int nsa_swa_fwd(const void* Q, const void* K, const void* V, void* O,
   // heads per KV group: the head-pair kernel
   const int64_t span = static_cast<int64_t>(p.left) + p.right + kSwaQ;  // keys a query tile touches
   if (p.hpg % 2 == 0 && N > 0 && (span > N ? N : span) >= kSwaPairMinKeys) {
+    if (span <= kSwaPairTmaOMaxKeys) {  // short windows: O by TMA stores
+      if (D == 64)
+        return bf ? launch_swa_pair<64, true, true>(p, Q, K, V, st)
+                  : launch_swa_pair<64, false, true>(p, Q, K, V, st);
+      return bf ? launch_swa_pair<128, true, true>(p, Q, K, V, st)
+                : launch_swa_pair<128, false, true>(p, Q, K, V, st);
+    }
     if (D == 64)
-      return bf ? launch_swa_pair<64, true>(p, Q, K, V, st)
-                : launch_swa_pair<64, false>(p, Q, K, V, st);
-    return bf ? launch_swa_pair<128, true>(p, Q, K, V, st)
-              : launch_swa_pair<128, false>(p, Q, K, V, st);
+      return bf ? launch_swa_pair<64, true, false>(p, Q, K, V, st)
+                : launch_swa_pair<64, false, false>(p, Q, K, V, st);
+    return bf ? launch_swa_pair<128, true, false>(p, Q, K, V, st)
+              : launch_swa_pair<128, false, false>(p, Q, K, V, st);
   }
   if (D == 64)
     return bf ? launch_swa<64, true>(p, Q, K, V, O, st) : launch_swa<64, false>(p, Q, K, V, O, st);
