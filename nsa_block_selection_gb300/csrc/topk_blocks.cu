@@ -684,11 +684,12 @@ __global__ void __launch_bounds__(kTopkWarps * 32, topk_ctas_per_sm<J>())
     const int64_t r1 = row + stride;
     const bool more = r1 < p.rows;
     const TopkRow next = more ? topk_row_info(p, r1) : r;
-    if (!topk_wait(p, bar, parity)) {
-      report_timeout();  // the row's scores never arrived: stop (outputs undefined)
+    // decided warp-wide: the selection below is warp-collective
+    if (!__all_sync(kFull, topk_wait(p, bar, parity))) {
+      if (lane == 0) report_timeout();  // the row's scores never arrived: stop (outputs undefined)
       return;
     }
-    __syncwarp();
+    __syncwarp();  // (cp.async rows) every lane's copies are visible to the others
     bool pending = more;
     if (!topk_select_fast<J>(p, r, next, pending, lane, sbuf, bar, sm))
       topk_general<J>(&p, r, lane, &sm);

@@ -34,12 +34,12 @@ def test_records_by_hand():
     idx = _rows(M, 4, lambda m: [1, 0, 2])
     rec = records_ref(idx, N, bs)[0, 0]
     # tiles of 16 queries: m0 = 0, 16, 32, 48, 64; a block qualifies when its
-    # last key (e + 1) * 32 - 1 is <= m0
-    assert rec[0].tolist() == [0] + [-1] * 7               # m0 = 0: nothing whole
-    assert rec[1].tolist() == [0] + [-1] * 7               # m0 = 16: block 0 ends at 31
-    assert rec[2].tolist() == [1, 0] + [-1] * 6            # m0 = 32: block 0
-    assert rec[3].tolist() == [1, 0] + [-1] * 6            # m0 = 48
-    assert rec[4].tolist() == [2, 1, 0] + [-1] * 5         # m0 = 64: blocks 1, 0 (first row's order)
+    # first key e * 32 is <= m0 and its keys end by min(M, N) = 80
+    assert rec[0].tolist() == [1, 0] + [-1] * 6            # m0 = 0: block 0 (the tile's own)
+    assert rec[1].tolist() == [1, 0] + [-1] * 6            # m0 = 16: block 0 still
+    assert rec[2].tolist() == [2, 1, 0] + [-1] * 5         # m0 = 32: blocks 1, 0 (first row's order)
+    assert rec[3].tolist() == [2, 1, 0] + [-1] * 5         # m0 = 48
+    assert rec[4].tolist() == [2, 1, 0] + [-1] * 5         # m0 = 64: block 2 runs to key 95 >= M
 
 
 def test_records_need_every_query_and_skip_padding_and_repeats():
