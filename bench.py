@@ -767,7 +767,8 @@ def run_variants(w, q, k, v, idx, work, flush, args):
 def run_two_pass(w, q, k, v, idx, work, flush, args, t_one_ms):
     """nsa_sel_attn_fwd_shared on the headline inputs, timed like the headline
     run (three kernels per step: per-tile lists of the blocks every query of
-    a 16-query tile lists and sees whole; their softmax on tcgen05; the gather
+    a 16-query tile lists, the tile's own block included; their softmax on
+    tcgen05, masked per row; the gather
     kernel over the remaining blocks). FLOPs and gathered bytes are those of
     the operation, as for the headline, so the numbers compare directly."""
     import torch

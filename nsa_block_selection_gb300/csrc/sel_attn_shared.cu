@@ -128,7 +128,8 @@ struct ListProblem {
 };
 
 // One warp per (b, g, tile): the record of the blocks every query of the tile
-// lists and sees whole.
+// lists whose first key the tile's first query sees and whose keys all lie
+// below M and N.
 __global__ void __launch_bounds__(128) shared_blocks_kernel(const ListProblem p) {
   const int lane = threadIdx.x & 31;
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);

@@ -52,7 +52,7 @@ def test_records_need_every_query_and_skip_padding_and_repeats():
     assert records_ref(idx, N, bs)[0, 0, 2].tolist() == [1, 0] + [-1] * 6
     # ids past N: nblk = ceil(N / bs) bounds them
     assert records_ref(idx, 40, bs)[0, 0, 2].tolist() == [1, 0] + [-1] * 6
-    # a block whose keys run past N is not whole (queries past N, M > N)
+    # a block whose keys run past N is not recorded (queries past N, M > N)
     idx = _rows(80, 2, lambda m: [0, 1])
     assert records_ref(idx, 160, bs)[0, 0, 4].tolist() == [2, 0, 1] + [-1] * 5
     assert records_ref(idx, 40, bs)[0, 0, 4].tolist() == [1, 0] + [-1] * 6
@@ -63,7 +63,7 @@ def test_records_cap():
     idx = gen.dense_causal_indices(1, M, 1, M // bs, bs)
     rec = records_ref(idx, M, bs)[0, 0]
     assert rec[:, 0].max() == MAXREC
-    last = rec[-1]  # m0 = 496: blocks 0..14 are whole; the first 7 in row order
+    last = rec[-1]  # m0 = 496: blocks 0..15 qualify; the first 7 in row order
     assert last.tolist() == [MAXREC] + list(range(MAXREC))
 
 
