@@ -197,3 +197,56 @@ def test_bwd_bf16_matches_oracle(B, M, N, D, bs, T, rule):
         bound = KAPPA * U_BF16 * mg
         assert np.all(err <= bound), \
             f"bf16 {name}: {int((err > bound).sum())} elements beyond 4u|terms|"
+
+
+def test_bwd_bf16_full_size():
+    """m64k_bs64 with bf16 inputs: dQ on sampled rows and dK/dV of sampled
+    blocks against the oracle on the same bf16 values, per element under
+    4 u |terms| with the bf16 unit roundoff; the dV and dK column identities."""
+    import torch
+
+    from nsa_block_selection_gb300 import inputs as gen
+    from nsa_block_selection_gb300 import sel_attn_fwd
+    from nsa_block_selection_gb300._lib import sel_attn_bwd
+    from _parity import sample_rows
+
+    w = gen.workload("m64k_bs64")
+    seed = gen.default_seed(w.name)
+    q, k, v = gen.make_qkv(w, seed, "bf16")
+    idx = gen.make_block_indices(w, seed)
+    dO = np.random.default_rng(2).standard_normal(q.shape, dtype=np.float32)
+    tq, tk, tv = (torch.from_numpy(x).cuda().to(torch.bfloat16) for x in (q, k, v))
+    ti, tdo = to_dev(idx, dO)
+    f32 = torch.float32
+    O, L = sel_attn_fwd(tq, tk, tv, ti, w.block_size, out=poisoned(tuple(tq.shape), f32),
+                        lse=poisoned((w.B, w.H, w.M), f32))
+    dq, dk, dv = sel_attn_bwd(tq, tk, tv, ti, O, L, tdo, w.block_size,
+                              dq=poisoned(tuple(tq.shape), f32), dk=poisoned(tuple(tk.shape), f32),
+                              dv=poisoned(tuple(tv.shape), f32))
+    torch.cuda.synchronize()
+    del O, L, tq, tk, tv, ti, tdo
+    dq, dk, dv = (x.cpu().numpy().astype(np.float64) for x in (dq, dk, dv))
+    hpg = w.H // w.G
+    rows = sample_rows(w.B, w.M, w.G, w.block_size, seed=9, n_random=256)
+    ex = oracle.sel_attn_bwd_dq_rows(q, k, v, idx, dO, rows, w.block_size)
+    mg = oracle.sel_attn_bwd_dq_rows(q, k, v, idx, dO, rows, w.block_size, magnitudes=True)
+    got = np.stack([dq[b, m, g * hpg:(g + 1) * hpg] for b, m, g in rows])
+
+    def check(name, g, e, m):
+        assert np.isfinite(g).all(), f"bf16 {name}: non-finite"
+        bad = np.abs(g - e) > KAPPA * U_BF16 * m
+        assert not bad.any(), f"bf16 {name}: {int(bad.sum())} elements beyond 4u|terms|"
+
+    check("dQ", got, ex, mg)
+    nblk = -(-w.N // w.block_size)
+    for b, g, t in ((0, 0, 1), (0, w.G - 1, nblk // 2), (0, w.G // 2, nblk - 1)):
+        ek, ev = oracle.sel_attn_bwd_block(q, k, v, idx, dO, b, g, t, w.block_size)
+        mk, mv = oracle.sel_attn_bwd_block(q, k, v, idx, dO, b, g, t, w.block_size,
+                                           magnitudes=True)
+        sl = slice(t * w.block_size, min((t + 1) * w.block_size, w.N))
+        check(f"dK block {t}", dk[b, sl, g], ek, mk)
+        check(f"dV block {t}", dv[b, sl, g], ev, mv)
+    # the same identities; bf16 rounds P and dS 8 times more coarsely than fp16
+    want = dO.astype(np.float64).reshape(w.B, w.M, w.G, hpg, w.D).sum(axis=(1, 3))
+    np.testing.assert_allclose(dv.sum(axis=1), want, rtol=8e-4, atol=8e-3 * np.abs(want).max())
+    assert np.abs(dk.sum(axis=1)).max() <= 8e-4 * np.abs(dk).sum(axis=1).max()
