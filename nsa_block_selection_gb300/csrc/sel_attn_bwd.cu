@@ -86,6 +86,7 @@ struct BwdProblem {
   const int* chunk_list;  // [chunks] the list of each chunk
   const int* chunk_order;  // [chunks] launch order of the chunks (D = 128), or null
   const int* lists;    // query ids, list by list
+  uint32_t* lmask;     // [B * M * G] entries taken by the local-block kernel (D = 128), or null
   int64_t B, M, N, H, G, T;
   int64_t units;       // B * G * nsub * M
   int hpg, nsub;       // heads per KV group, sub-groups of 8 heads
@@ -101,6 +102,16 @@ __device__ __forceinline__ void red_add_v4(float* p, float x, float y, float z, 
                : "memory");
 }
 
+
+// Bulk fp32 add of `bytes` (a multiple of 16) from shared memory into global
+// memory, both addresses 16-byte aligned; tracked by the issuing thread's
+// bulk group.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;\n" ::"l"(
+                   dst),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
 
 // Tensor-map element type of the inputs (fp16 or bf16).
 static inline CUtensorMapDataType map_dtype(bool bf16) {
@@ -418,8 +429,9 @@ __global__ void __launch_bounds__(256) sel_attn_bwd_prep_kernel(const BwdProblem
 // ---------------------------------------------------------------------------
 
 // Entry e of block_indices -> the list it belongs to, or -1 (padding, out of
-// range, or wholly in the query's future).
-__device__ __forceinline__ int entry_list(const BwdProblem& p, int64_t e, int64_t* m_out) {
+// range, or wholly in the query's future); *m_out = its query, *t_out = its block.
+__device__ __forceinline__ int entry_list(const BwdProblem& p, int64_t e, int64_t* m_out,
+                                          int* t_out) {
   const int64_t r = e / p.T;  // (b * M + m) * G + g
   const int g = static_cast<int>(r % p.G);
   const int64_t bm = r / p.G;
@@ -428,8 +440,30 @@ __device__ __forceinline__ int entry_list(const BwdProblem& p, int64_t e, int64_
   const int t = __ldg(p.idx + e);
   const int64_t lastkey = m < p.N - 1 ? m : p.N - 1;
   *m_out = m;
+  *t_out = t;
   if (t < 0 || t >= p.nblk || static_cast<int64_t>(t) * p.bs > lastkey) return -1;
   return static_cast<int>((b * p.G + g) * p.nblk + t);
+}
+
+// The local blocks of a query in block row c (queries c*bs .. c*bs + bs - 1):
+// slot 0 = its own block c, slot 1 = block c - 1; -1 for any other block.
+__device__ __forceinline__ int local_slot(int t, int c) {
+  if (t == c) return 0;
+  if (t == c - 1) return 1;
+  return -1;
+}
+
+// Whether the local-block kernel takes entry e (block t of query m): the
+// first of the row's entries in a local slot claims the slot's bit (bits
+// 0-1 in the count pass, 3-4 in the fill pass); a repeat of the block in
+// the row stays in the list, so both passes leave the same entries out.
+__device__ __forceinline__ bool taken_locally(const BwdProblem& p, int64_t e, int64_t m, int t,
+                                              int shift) {
+  if (p.lmask == nullptr) return false;
+  const int s = local_slot(t, static_cast<int>(m / p.bs));
+  if (s < 0) return false;
+  const uint32_t bit = 1u << (s + shift);
+  return (atomicOr(p.lmask + e / p.T, bit) & bit) == 0u;
 }
 
 __global__ void csr_count_kernel(const BwdProblem p, int* count) {
@@ -437,8 +471,9 @@ __global__ void csr_count_kernel(const BwdProblem p, int* count) {
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     int64_t m;
-    const int l = entry_list(p, e, &m);
-    if (l >= 0) atomicAdd(count + l, 1);
+    int t;
+    const int l = entry_list(p, e, &m, &t);
+    if (l >= 0 && !taken_locally(p, e, m, t, 0)) atomicAdd(count + l, 1);
   }
 }
 
@@ -559,8 +594,10 @@ __global__ void csr_fill_kernel(const BwdProblem p, int* cursor, int* lists) {
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     int64_t m;
-    const int l = entry_list(p, e, &m);
-    if (l >= 0) lists[p.offs[l] + atomicAdd(cursor + l, 1)] = static_cast<int>(m);
+    int t;
+    const int l = entry_list(p, e, &m, &t);
+    if (l >= 0 && !taken_locally(p, e, m, t, 3))
+      lists[p.offs[l] + atomicAdd(cursor + l, 1)] = static_cast<int>(m);
   }
 }
 
@@ -891,8 +928,9 @@ enum DkvBar : int {
   kPdsFree = 9,   // 2
   kAccDone = 11,
   kDqFull = 12,   // dQ of a batch is in tensor memory
-  kDqFree = 13,   // the softmax warps have read it
-  kDkvBars = 14
+  kDqFree = 13,   // the dQ warps have read it
+  kStaged = 14,   // the chunk's dV / dK staged in shared memory
+  kDkvBars = 15
 };
 
 // Q / dO tiles of a batch: item j's 8 head rows at j * 2048, dims 0-63 in
@@ -991,6 +1029,7 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
     mbar_init(bar(kAccDone), 1);
     mbar_init(bar(kDqFull), 1);
     mbar_init(bar(kDqFree), 4 * 32);
+    mbar_init(bar(kStaged), 4 * 32);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -1288,28 +1327,544 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(kPdsFull + s));
     }
-    // epilogue: lane = d; add the chunk's dV and dK (scaled) into global memory
+    // epilogue: the chunk's dV and dK (scaled) staged in a free Q / dO stage
+    // as key rows of D floats (lane = d), then added into global memory by
+    // one 512-byte bulk reduction per key row
     if (!failed && nbat > 0) {
       if (!wait_all(kAccDone, 0)) {
         failed = true;
       } else {
         tc_fence_after();
         const int d = r;
+        float* const stg_f = reinterpret_cast<float*>(gbase + C::kOffStage);  // dV rows, dK rows
         for (int half = 0; half < 2; ++half) {
           uint32_t vv[32], kv[32];
           tc_ld32(lane_addr + C::kColDv + 32 * half, vv);
           tc_ld32(lane_addr + C::kColDk + 32 * half, kv);
           tc_wait_ld();
+          float* const rv = stg_f + (32 * half) * D + d;
+          float* const rk = stg_f + (64 + 32 * half) * D + d;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int kidx = 32 * half + j;
-            const int n = n_blk + kidx;
-            if (kidx < p.bs && n < p.N) {
-              const int64_t at = ((b * p.N + n) * p.G + g) * D + d;
-              atomicAdd(p.dV + at, __uint_as_float(vv[j]));
-              atomicAdd(p.dK + at, __uint_as_float(kv[j]) * p.scale);
+            rv[j * D] = __uint_as_float(vv[j]);
+            rk[j * D] = __uint_as_float(kv[j]) * p.scale;
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kStaged));
+        if (!wait_all(kStaged, 0)) {
+          failed = true;
+        } else {
+          const int kidx = r & 63;  // thread r: key row kidx of dV (r < 64) or dK
+          const int n = n_blk + kidx;
+          if (kidx < p.bs && n < p.N) {
+            bulk_reduce_add_f32((r < 64 ? p.dV : p.dK) + ((b * p.N + n) * p.G + g) * D,
+                                base + C::kOffStage + static_cast<uint32_t>(r) * (D * 4), D * 4);
+            bulk_commit_group();
+            bulk_wait_group_read0();  // the staging row has been read
+          }
+        }
+      }
+    }
+  }
+
+  if (failed) report_timeout();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tc_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 3a (D = 128): the local blocks of every block row
+// ---------------------------------------------------------------------------
+//
+// The queries of block row c (positions c*bs .. c*bs + bs - 1) share their
+// two local blocks, block c and block c - 1 (local_slot). The list kernels
+// leave those entries out of the query lists and mark them per row in
+// lmask; this kernel takes them, one CTA per (b, block row, g). The CTA
+// owns the dQ rows of its queries: their contributions from both blocks
+// are summed in tensor memory and stored once (rows that take neither block
+// get zeros), so dQ needs no zeroing and the key-major kernel's fp32
+// reductions shrink by two of each row's blocks. The blocks' dK and dV
+// accumulate in tensor memory over the block row and are added with fp32
+// atomics at the end.
+//
+// Steps: (batch of 16 items, active slot), batch by batch. Per step the
+// MMA warp issues S = Q K^T and dP = dO V^T into 128 tensor-memory
+// columns; the softmax warps load them (which frees the columns for the
+// next step's S / dP) and write P and dS to shared memory; the MMA warp
+// then adds dQ_R += dS K into the batch's dQ columns and dV^T += dO^T P,
+// dK^T += Q^T dS into the slot's columns. After a batch's last slot the
+// dQ warps read its dQ_R out, scale it and store it. K / V of the two
+// blocks arrive once, the Q / dO tiles of each batch in two stages.
+enum LocBar : int {
+  kLKvFull = 0,    // 2: K / V of each active slot (loaded once)
+  kLQdFull = 2,    // 2 Q / dO stages
+  kLQdEmpty = 4,   // 2
+  kLSdFull = 6,    // S / dP of the step are in tensor memory
+  kLTFree = 7,     // the softmax warps have loaded them
+  kLPdsFull = 8,   // P / dS written
+  kLPdsFree = 9,   // the MMAs that read P / dS are done
+  kLDqFull = 10,   // dQ_R of a batch is complete
+  kLDqFree = 11,   // the dQ warps have read it
+  kLAccDone = 12,
+  kLStaged = 13,   // dV / dK of the block row staged in shared memory
+  kLocBars = 14
+};
+
+// Spin limit of the MMA issuer's polling loop, in SM clock cycles (about 2 s
+// at 2 GHz): the loop reads the SM clock, which is cheap, rather than the
+// global timer on every pass.
+constexpr long long kSpinLimitCycles = 4000000000LL;
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+struct LocalCfg {
+  static constexpr int kAtom = 128 * 128;    // 128 rows x 128 B
+  static constexpr int kItemBytes = 2048;    // 8 rows x 2 halves x 128 B
+  static constexpr int kBlkAtom = 64 * 128;  // 64 keys x 128 B
+  static constexpr int kKvBytes = 4 * kBlkAtom;  // K (2 atoms: d 0-63, 64-127), then V
+  static constexpr int kOffKv = 0;               // slot k at k * kKvBytes
+  static constexpr int kOffStage = kOffKv + 2 * kKvBytes;
+  static constexpr int kStageBytes = 4 * kAtom;  // Q tile (2 atoms), dO tile (2 atoms)
+  static constexpr int kOffPds = kOffStage + 2 * kStageBytes;
+  static constexpr int kPdsBytes = 2 * 128 * 128;  // P tile, dS tile (128 rows x 64 keys)
+  static constexpr int kOffBar = kOffPds + kPdsBytes;
+  static constexpr int kOffTmem = kOffBar + kLocBars * 8;
+  static constexpr int kSmemBytes = kOffTmem + 16 + 1024;
+  // slot k: dV^T at columns 128 k .. + 63, dK^T at 128 k + 64 .. + 127
+  static constexpr uint32_t kColT = 256;   // S (64 columns), dP (64)
+  static constexpr uint32_t kColDq = 384;  // dQ_R of the batch (128 rows x D)
+};
+static_assert(LocalCfg::kSmemBytes <= 232448, "one CTA per SM");
+
+template <bool SPLIT, bool BF16>
+__global__ void __launch_bounds__(kDkvTcThreads, 1)
+    sel_attn_bwd_local_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap tmK,
+                              const __grid_constant__ CUtensorMap tmV,
+                              const __grid_constant__ CUtensorMap tmQ,
+                              const __grid_constant__ CUtensorMap tmD) {
+  using C = LocalCfg;
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  const int nrow = static_cast<int>((p.M + p.bs - 1) / p.bs);
+  const int g = static_cast<int>(blockIdx.x % p.G);
+  const int64_t bc = blockIdx.x / p.G;
+  const int c = static_cast<int>(bc % nrow);
+  const int64_t b = bc / nrow;
+  const int m0 = c * p.bs;
+  const int nq = static_cast<int>(p.M - m0 < p.bs ? p.M - m0 : p.bs);
+  const int nsub = SPLIT ? p.nsub : 1;
+  const int nitems = nq * nsub;
+  const int nbat = (nitems + kTcBatch - 1) / kTcBatch;
+  const int64_t hgroup = static_cast<int64_t>(g) * p.hpg;
+  const int hw0 = p.hpg < kHeadsPerGroup ? p.hpg : kHeadsPerGroup;  // head rows per item
+  const int64_t mrow0 = (b * p.M + m0) * p.G + g;                  // lmask row of query m0
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  auto bar = [&](int i) { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+
+  if (threadIdx.x == 32) {  // the tensor maps' descriptors, while the CTA sets up
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmD);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  // the slots some query of the block row takes here, in slot order
+  uint32_t any = 0;
+  for (int q = threadIdx.x; q < nq; q += blockDim.x) any |= __ldg(p.lmask + mrow0 + q * p.G) & 3u;
+  const int act = (__syncthreads_or(any & 1u) ? 1 : 0) | (__syncthreads_or(any & 2u) ? 2 : 0);
+  const int nsl = __popc(act);
+  auto slot_at = [&](int k) { return act == 2 ? 1 : k; };  // k-th active slot
+  auto block_of = [&](int s) { return c - s; };
+  const int nsteps = nbat * nsl;
+
+  auto item_row = [&](int item, int& m, int& sub) {
+    m = m0 + (SPLIT ? item / nsub : item);
+    sub = SPLIT ? item % nsub : 0;
+  };
+
+  if (hw0 < kHeadsPerGroup) {
+    // head rows the copies never write: zero, so the padding rows multiply zeros
+    const int per = 2 * 2 * kTcBatch * 2 * (kHeadsPerGroup - hw0) * 8;
+    for (int e = threadIdx.x; e < per; e += blockDim.x) {
+      const int piece = e % 8, rr = e / 8;
+      const int row = hw0 + rr % (kHeadsPerGroup - hw0);
+      const int grp = rr / (kHeadsPerGroup - hw0);
+      st_shared_zero16(base + C::kOffStage + grp * 1024 + row * 128 + piece * 16);
+    }
+    fence_proxy_async_smem();
+  }
+  if (p.bs < 64) {
+    // 32-key blocks fill 32 rows of each K / V column half; the other rows stay zero
+    const int per = 2 * 4 * (64 - p.bs) * 8;  // (buffer, tensor, half) x rows x 16-byte pieces
+    for (int e = threadIdx.x; e < per; e += blockDim.x) {
+      const int piece = e % 8, rr = e / 8;
+      const int row = p.bs + rr % (64 - p.bs), atom = rr / (64 - p.bs);
+      st_shared_zero16(base + C::kOffKv + atom * C::kBlkAtom + row * 128 + piece * 16);
+    }
+    fence_proxy_async_smem();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kLKvFull + s), 1);
+      mbar_init(bar(kLQdFull + s), 1);
+      mbar_init(bar(kLQdEmpty + s), 1);
+    }
+    mbar_init(bar(kLSdFull), 1);
+    mbar_init(bar(kLTFree), 4 * 32);
+    mbar_init(bar(kLPdsFull), 4 * 32);
+    mbar_init(bar(kLPdsFree), 1);
+    mbar_init(bar(kLDqFull), 1);
+    mbar_init(bar(kLDqFree), 4 * 32);
+    mbar_init(bar(kLAccDone), 1);
+    mbar_init(bar(kLStaged), 4 * 32);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc_alloc(base + C::kOffTmem, 512);
+    tc_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kOffTmem);
+  bool failed = false;
+
+  if (warp == 0) {
+    // ---- producer: the K / V blocks of the active slots once (lane 0),
+    // per batch its Q / dO rows (lane j < 16: item j) ----
+    if (lane == 0) {
+      const uint64_t keep = l2_policy_evict_last();
+      for (int k = 0; k < nsl; ++k) {
+        const int n_blk = block_of(slot_at(k)) * p.bs;
+        const uint32_t kvb = base + C::kOffKv + k * C::kKvBytes;
+        mbar_arrive_expect_tx(bar(kLKvFull + k), 4 * p.bs * 128);
+        for (int a = 0; a < 2; ++a) {
+          tma_load_4d(kvb + a * C::kBlkAtom, &tmK, bar(kLKvFull + k), a * kBoxCols, g, n_blk,
+                      static_cast<int>(b), keep);
+          tma_load_4d(kvb + (2 + a) * C::kBlkAtom, &tmV, bar(kLKvFull + k), a * kBoxCols, g,
+                      n_blk, static_cast<int>(b), keep);
+        }
+      }
+    }
+    for (int i = 0; i < nbat && nsl > 0; ++i) {
+      const int s = i & 1;
+      if (i >= 2 &&
+          !__all_sync(kFull, wait_phase(bar(kLQdEmpty + s), ((i - 2) >> 1) & 1, kWaitLimitNs))) {
+        failed = true;
+        break;
+      }
+      const uint32_t st = base + C::kOffStage + s * C::kStageBytes;
+      if (lane == 0) mbar_arrive_expect_tx(bar(kLQdFull + s), kTcBatch * 4 * hw0 * 128);
+      __syncwarp();
+      if (lane < kTcBatch) {
+        // items past the block row repeat its last item (their rows are masked)
+        int m, sub;
+        item_row(min(i * kTcBatch + lane, nitems - 1), m, sub);
+        const int qrow = static_cast<int>((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup);
+        const uint32_t dq = st + lane * C::kItemBytes, dd = dq + 2 * C::kAtom;
+        if (hw0 == kHeadsPerGroup) {
+          tma_load_3d(dq, &tmQ, bar(kLQdFull + s), 0, qrow, 0);
+          tma_load_3d(dd, &tmD, bar(kLQdFull + s), 0, qrow, 0);
+        } else {
+          for (int a = 0; a < 2; ++a) {
+            tma_load_2d(dq + a * 1024, &tmQ, bar(kLQdFull + s), a * kBoxCols, qrow);
+            tma_load_2d(dd + a * 1024, &tmD, bar(kLQdFull + s), a * kBoxCols, qrow);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer: S / dP of a step as soon as the softmax warps have
+      // loaded the previous one (and its rows have landed); dQ_R, dV and dK
+      // of the oldest step whose P / dS are written (the first slot of a
+      // batch once the dQ warps have read the previous batch's dQ_R). One
+      // bounded wait: 1 s without progress fails. ----
+      constexpr uint32_t idesc_sd = umma_idesc_f16(128, 64, BF16, false);  // K-major A, B
+      constexpr uint32_t idesc_acc =
+          umma_idesc_f16(128, 64, BF16, true) | (1u << 15);  // MN-major A and B
+      constexpr uint32_t idesc_dq =
+          umma_idesc_f16(128, 128, BF16, true);  // dS K-major A, K MN-major B
+      const uint32_t pds = base + C::kOffPds;
+      auto issue_sd = [&](int j) {
+        const int i = j / nsl, k = j - i * nsl;
+        tc_fence_after();
+        const uint32_t st = base + C::kOffStage + (i & 1) * C::kStageBytes;
+        const uint32_t kvb = base + C::kOffKv + k * C::kKvBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offa = (kk >> 2) * 1024 + (kk & 3) * 32;  // column half, then 16 dims
+          const uint32_t offb = (kk >> 2) * C::kBlkAtom + (kk & 3) * 32;
+          tc_mma(tmem + C::kColT, umma_desc_sw128(st + offa, 16, C::kItemBytes),
+                 umma_desc_sw128(kvb + offb, 16), idesc_sd, kk > 0 ? 1u : 0u);
+          tc_mma(tmem + C::kColT + 64, umma_desc_sw128(st + 2 * C::kAtom + offa, 16, C::kItemBytes),
+                 umma_desc_sw128(kvb + 2 * C::kBlkAtom + offb, 16), idesc_sd, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(kLSdFull));
+      };
+      auto issue_acc = [&](int j) {
+        const int i = j / nsl, k = j - i * nsl;
+        tc_fence_after();
+        const uint32_t st = base + C::kOffStage + (i & 1) * C::kStageBytes;
+        const uint32_t kvb = base + C::kOffKv + k * C::kKvBytes;
+        // dQ_R (128 rows x D) += dS K: A = dS rows, 16 keys per step; B = the K
+        // tile read N-major, the two 64-column halves 8 KB apart
+#pragma unroll
+        for (int kk = 0; kk < 64 / 16; ++kk)
+          tc_mma(tmem + C::kColDq, umma_desc_sw128(pds + 128 * 128 + kk * 32, 16),
+                 umma_desc_sw128(kvb + kk * 2048, C::kBlkAtom), idesc_dq,
+                 (k > 0 || kk > 0) ? 1u : 0u);
+        const uint32_t cdv = tmem + 128u * static_cast<uint32_t>(k);
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk) {  // 16 rows (2 items) per step
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          tc_mma(cdv,
+                 umma_desc_sw128(st + 2 * C::kAtom + kk * 2 * C::kItemBytes, 1024, C::kItemBytes),
+                 umma_desc_sw128(pds + kk * 2048, 16), idesc_acc, acc);
+          tc_mma(cdv + 64, umma_desc_sw128(st + kk * 2 * C::kItemBytes, 1024, C::kItemBytes),
+                 umma_desc_sw128(pds + 128 * 128 + kk * 2048, 16), idesc_acc, acc);
+        }
+        tc_commit(bar(kLPdsFree));
+        if (k == nsl - 1) {
+          tc_commit(bar(kLQdEmpty + (i & 1)));
+          tc_commit(bar(kLDqFull));
+        }
+      };
+      bool ok = true;
+      int nsd = 0, nacc = 0;
+      long long t_last = clock64();
+      while (nacc < nsteps) {
+        bool progressed = false;
+        if (nsd < nsteps) {
+          const int i = nsd / nsl, k = nsd - i * nsl;
+          if ((nsd == 0 || mbar_test_wait(bar(kLTFree), (nsd - 1) & 1)) &&
+              (k != 0 || mbar_test_wait(bar(kLQdFull + (i & 1)), (i >> 1) & 1)) &&
+              mbar_test_wait(bar(kLKvFull + k), 0)) {
+            issue_sd(nsd++);
+            progressed = true;
+          }
+        }
+        if (nacc < nsd) {
+          const int i = nacc / nsl, k = nacc - i * nsl;
+          if (mbar_test_wait(bar(kLPdsFull), nacc & 1) &&
+              (k != 0 || i == 0 || mbar_test_wait(bar(kLDqFree), (i - 1) & 1))) {
+            issue_acc(nacc++);
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_last = clock64();
+        } else if (clock64() - t_last > kSpinLimitCycles) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok) tc_commit(bar(kLAccDone));
+      failed = !ok;
+    }
+  } else if (warp >= 6) {
+    // ---- dQ out (warps 6..9): each batch's dQ_R from tensor memory (the
+    // .16x256b layout: thread (g8 = lane / 4, c4 = lane % 4) gets columns
+    // 2 c4, 2 c4 + 1 (+ 8 per repetition) of rows g8 and g8 + 8 of a 16-row
+    // slice), scaled, regrouped by shuffles into 16-byte pieces of 4
+    // consecutive columns and stored. This thread: head g8 of items
+    // 16 i + 4 quarter + a. ----
+    const int quarter = warp & 3;
+    const int g8 = lane >> 2, c4 = lane & 3;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int src_lo = (lane & ~3) | (2 * (c4 & 1));  // holds columns 4 c4 % 8, + 1
+    const bool upper = c4 >= 2;                        // wants the odd repetition
+    for (int i = 0; i < nbat; ++i) {
+      uint32_t v[4][32];
+      if (nsl > 0) {
+        if (!__all_sync(kFull, wait_phase(bar(kLDqFull), i & 1, kWaitLimitNs))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int piece = 0; piece < 4; ++piece)
+          tc_ld_16x256b_x8(lane_addr + (static_cast<uint32_t>(16 * (piece >> 1)) << 16) +
+                               C::kColDq + 64 * (piece & 1),
+                           v[piece]);
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(kLDqFree));
+      } else {  // no local block in the block row: its rows start at zero
+#pragma unroll
+        for (int piece = 0; piece < 4; ++piece)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[piece][e] = 0u;
+      }
+      float* rowp[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int item = i * kTcBatch + quarter * 4 + a;
+        rowp[a] = nullptr;
+        if (item < nitems && g8 < hw0) {
+          int m, sub;
+          item_row(item, m, sub);
+          rowp[a] = p.dQ + ((b * p.M + m) * p.H + hgroup + sub * kHeadsPerGroup + g8) * D + 4 * c4;
+        }
+      }
+#pragma unroll
+      for (int piece = 0; piece < 4; ++piece) {
+        const int slice = piece >> 1, half = piece & 1;
+#pragma unroll
+        for (int up = 0; up < 2; ++up) {  // rows g8 and g8 + 8 of the slice: items a = 2 slice + up
+          float* const dst = rowp[2 * slice + up];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // columns 16k .. 16k + 15 of the half
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int src = src_lo + (e >> 1);
+              const float x =
+                  __shfl_sync(kFull, __uint_as_float(v[piece][8 * k + 2 * up + (e & 1)]), src);
+              const float y =
+                  __shfl_sync(kFull, __uint_as_float(v[piece][8 * k + 4 + 2 * up + (e & 1)]), src);
+              o[e] = (upper ? y : x) * p.scale;
+            }
+            if (dst)
+              *reinterpret_cast<float4*>(dst + 64 * half + 16 * k) = make_float4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+    }
+  } else if (warp >= 2) {
+    // ---- softmax (warps 2..5): thread <-> row (item r / 8, head r % 8) ----
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = p.sl2;
+    auto wait_all = [&](int bb, uint32_t parity) {
+      return __all_sync(kFull, wait_phase(bar(bb), parity, kWaitLimitNs));
+    };
+    for (int i = 0; i < nbat && !failed && nsl > 0; ++i) {
+      const int item = i * kTcBatch + r / 8;
+      int m = -1;
+      float lse2 = INFINITY, delta = 0.f;
+      uint32_t rmask = 0;
+      if (item < nitems) {
+        int sub;
+        item_row(item, m, sub);
+        const int64_t row = (b * p.M + m) * p.G + g;
+        const float* rec = p.rec + (row * nsub + sub) * 16;
+        lse2 = __ldg(rec + (r & 7));
+        delta = __ldg(rec + 8 + (r & 7));
+        rmask = __ldg(p.lmask + row);
+      }
+      const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
+      for (int k = 0; k < nsl; ++k) {
+        const int j = i * nsl + k;
+        const int sl = slot_at(k);
+        const int n_blk = block_of(sl) * p.bs;
+        // keys n_blk + jj visible: the row takes this block here, jj < block
+        // size and n_blk + jj <= lastkey
+        const bool valid = m >= 0 && ((rmask >> sl) & 1u);
+        const int nvis = valid ? min(p.bs, lastkey - n_blk + 1) : 0;
+        if (!wait_all(kLSdFull, j & 1)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[64], dv[64];
+        tc_ld32(lane_addr + C::kColT, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tc_ld32(lane_addr + C::kColT + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tc_ld32(lane_addr + C::kColT + 64, *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+        tc_ld32(lane_addr + C::kColT + 96, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(kLTFree));  // the next step's S / dP may go
+        // the P / dS tiles are free once the previous step's MMAs are done
+        if (j >= 1 && !wait_all(kLPdsFree, (j - 1) & 1)) {
+          failed = true;
+          break;
+        }
+        uint8_t* const prow = gbase + C::kOffPds + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t pw[4], dw[4];
+#pragma unroll
+          for (int h2 = 0; h2 < 4; ++h2) {
+            const int jj = 8 * cc + 2 * h2;
+            const bool v0 = jj < nvis, v1 = jj + 1 < nvis;
+            const float p0 = v0 ? ex2(fmaf(__uint_as_float(sv[jj]), sl2, -lse2)) : 0.f;
+            const float p1 = v1 ? ex2(fmaf(__uint_as_float(sv[jj + 1]), sl2, -lse2)) : 0.f;
+            const float d0 = v0 ? p0 * (__uint_as_float(dv[jj]) - delta) : 0.f;
+            const float d1 = v1 ? p1 * (__uint_as_float(dv[jj + 1]) - delta) : 0.f;
+            pw[h2] = pack2_t<BF16>(p0, p1);
+            dw[h2] = pack2_t<BF16>(d0, d1);
+          }
+          const uint32_t off = ((cc ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(prow + 128 * 128 + off) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kLPdsFull));
+      }
+    }
+    // epilogue: each slot's dV and dK (scaled) staged in the free Q / dO
+    // stages as key rows of D floats (lane = d), then added into global
+    // memory by one 512-byte bulk reduction per key row
+    if (!failed && nsteps > 0) {
+      if (!wait_all(kLAccDone, 0)) {
+        failed = true;
+      } else {
+        tc_fence_after();
+        const int d = r;
+        const uint32_t stg = base + C::kOffStage;  // (2 k + tensor) * 64 + key rows of 512 B
+        float* const stg_f = reinterpret_cast<float*>(gbase + C::kOffStage);
+        for (int k = 0; k < nsl; ++k) {
+          for (int half = 0; half < 2; ++half) {
+            uint32_t vv[32], kv[32];
+            tc_ld32(lane_addr + 128 * k + 32 * half, vv);
+            tc_ld32(lane_addr + 128 * k + 64 + 32 * half, kv);
+            tc_wait_ld();
+            float* const rv = stg_f + ((2 * k) * 64 + 32 * half) * D + d;
+            float* const rk = stg_f + ((2 * k + 1) * 64 + 32 * half) * D + d;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              rv[jj * D] = __uint_as_float(vv[jj]);
+              rk[jj * D] = __uint_as_float(kv[jj]) * p.scale;
             }
           }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kLStaged));
+        if (!wait_all(kLStaged, 0)) {
+          failed = true;
+        } else {
+          for (int q = r; q < 2 * nsl * 64; q += 128) {
+            const int tk = q >> 6, kidx = q & 63;  // tk = 2 k + tensor
+            const int n = block_of(slot_at(tk >> 1)) * p.bs + kidx;
+            if (kidx < p.bs && n < p.N)
+              bulk_reduce_add_f32((tk & 1 ? p.dK : p.dV) + ((b * p.N + n) * p.G + g) * D,
+                                  stg + static_cast<uint32_t>(q) * (D * 4), D * 4);
+          }
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the staging rows have been read
         }
       }
     }
@@ -1331,7 +1886,8 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
 
 struct BwdPlan {
   size_t off_do16, off_rec, off_count, off_cursor, off_offs, off_choffs, off_lists,
-      off_chunk_list, off_order, off_key, off_bcount, off_bcursor, off_boffs, off_bscratch, total;
+      off_chunk_list, off_order, off_key, off_bcount, off_bcursor, off_boffs, off_bscratch,
+      off_lmask, total;
   int64_t L, entries, max_chunks, nkeys, nbkt;
 };
 
@@ -1380,6 +1936,9 @@ static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, i
   at += align256(static_cast<size_t>(pl.nkeys + 1) * 4);
   pl.off_bscratch = at;
   at += align256(static_cast<size_t>(pl.nkeys + 1) * 4);
+  // per (b, m, g) row: the entries the local-block kernel takes (D = 128)
+  pl.off_lmask = at;
+  at += align256(static_cast<size_t>(B * M * G) * 4);
   pl.total = at;
   return pl;
 }
@@ -1434,6 +1993,8 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   int* chunk_list = reinterpret_cast<int*>(ws + pl.off_chunk_list);
   p.chunk_list = chunk_list;
   p.chunk_order = nullptr;
+  // D = 128: the local blocks of each block row go to their own kernel
+  p.lmask = D == 128 ? reinterpret_cast<uint32_t*>(ws + pl.off_lmask) : nullptr;
   const int64_t B = p.units / (p.M * p.G * p.nsub);
   if (p.N > 0 &&
       (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
@@ -1448,6 +2009,9 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   auto stage2 = [&](cudaStream_t s2) -> int {
     if (cudaMemsetAsync(count, 0, static_cast<size_t>(pl.L) * 4, s2) != cudaSuccess ||
         cudaMemsetAsync(cursor, 0, static_cast<size_t>(pl.L) * 4, s2) != cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    if (p.lmask != nullptr &&
+        cudaMemsetAsync(p.lmask, 0, static_cast<size_t>(B * p.M * p.G) * 4, s2) != cudaSuccess)
       return NSA_ERR_LAUNCH;
     // grid-stride: a few CTAs per SM are enough for atomics on small tables
     const int64_t grid_e =
@@ -1494,8 +2058,8 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   }
 
   if constexpr (D == 128) {
-    // stage 1: the key-major kernel accumulates dQ too; here only its
-    // per-row inputs (fp16 dO, LSE, delta) and a zeroed dQ
+    // stage 1: the per-row inputs of the stage-3 kernels (16-bit dO, LSE,
+    // delta); dQ needs no zeroing, the local-block kernel stores every row
     if (!have_keys || p.T == 0) {  // dQ = dK = dV = 0
       return cudaMemsetAsync(p.dQ, 0, static_cast<size_t>(B * p.M * p.H * D) * 4, st) ==
                      cudaSuccess
@@ -1503,10 +2067,9 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
                  : NSA_ERR_LAUNCH;
     }
     // Stage 2 runs beside stage 1 on a second stream: stage 1 streams dO and
-    // O through HBM (and zeroes dQ), stage 2 counts and files the index
-    // entries with atomics on small tables, and neither touches what the
-    // other writes. The caller's stream waits for both before the key-major
-    // kernel.
+    // O through HBM, stage 2 counts and files the index entries with atomics
+    // on small tables, and neither touches what the other writes. The
+    // caller's stream waits for both before the stage-3 kernels.
     SideStream side(second_stream);
     int rc2 = NSA_ERR_LAUNCH;
     if (side.ok && cudaEventRecord(side.fork, st) == cudaSuccess &&
@@ -1514,10 +2077,8 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
       rc2 = stage2(side.s);
     else
       rc2 = stage2(st);  // no second stream: in order on the caller's stream
-    bool rc1 =
-        cudaMemsetAsync(p.dQ, 0, static_cast<size_t>(B * p.M * p.H * D) * 4, st) == cudaSuccess;
     sel_attn_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((p.units + 7) / 8), 256, 0, st>>>(p);
-    rc1 = rc1 && cudaGetLastError() == cudaSuccess;
+    const bool rc1 = cudaGetLastError() == cudaSuccess;
     if (side.ok && !side.join_into(st)) return NSA_ERR_LAUNCH;
     if (rc2 != NSA_OK) return rc2;
     if (!rc1) return NSA_ERR_LAUNCH;
@@ -1571,6 +2132,16 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
                                   !encode_rows_halves_map(&tdo3, p.dO16, B * p.M * p.H, hw0,
                                                           map_dtype(BF16))))
       return NSA_ERR_LAUNCH;
+    // the local blocks of every block row first: it stores each dQ row once,
+    // then the key-major kernel adds the rest of the row's blocks
+    auto kl = split ? sel_attn_bwd_local_kernel<true, BF16> : sel_attn_bwd_local_kernel<false, BF16>;
+    if (cudaFuncSetAttribute(kl, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LocalCfg::kSmemBytes) != cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    const int64_t lgrid = B * p.G * ((p.M + p.bs - 1) / p.bs);  // < 2^31: B * M * G * T is
+    if (lgrid > 0)
+      kl<<<static_cast<unsigned>(lgrid), kDkvTcThreads, LocalCfg::kSmemBytes, st>>>(p, tk64, tv64,
+                                                                                   tq3, tdo3);
     p.chunk_order = order;  // written by stage 2
     auto kk = split ? sel_attn_bwd_dkv_tc_kernel<true, BF16> : sel_attn_bwd_dkv_tc_kernel<false, BF16>;
     if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
