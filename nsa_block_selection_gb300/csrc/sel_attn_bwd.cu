@@ -86,7 +86,9 @@ struct BwdProblem {
   const int* chunk_list;  // [chunks] the list of each chunk
   const int* chunk_order;  // [chunks] launch order of the chunks (D = 128), or null
   const int* lists;    // query ids, list by list
-  uint32_t* lmask;     // [B * M * G] entries taken by the local-block kernel (D = 128), or null
+  int2* lfirst;        // [B * M * G] per row, the entry index of its first entry of block c
+                       // and of block c - 1 (-1: none), taken by the local-block kernel
+                       // (D = 128); null otherwise
   int64_t B, M, N, H, G, T;
   int64_t units;       // B * G * nsub * M
   int hpg, nsub;       // heads per KV group, sub-groups of 8 heads
@@ -111,6 +113,23 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, ui
                    dst),
                "r"(src), "r"(bytes)
                : "memory");
+}
+
+// Spin limit of the MMA issuers' polling loops, in SM clock cycles (about 2 s
+// at 2 GHz): the loop reads the SM clock, which is cheap, rather than the
+// global timer on every pass.
+constexpr long long kSpinLimitCycles = 4000000000LL;
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // Tensor-map element type of the inputs (fp16 or bf16).
@@ -428,23 +447,6 @@ __global__ void __launch_bounds__(256) sel_attn_bwd_prep_kernel(const BwdProblem
 // Stage 2: transposed index (who selected each (b, g, block))
 // ---------------------------------------------------------------------------
 
-// Entry e of block_indices -> the list it belongs to, or -1 (padding, out of
-// range, or wholly in the query's future); *m_out = its query, *t_out = its block.
-__device__ __forceinline__ int entry_list(const BwdProblem& p, int64_t e, int64_t* m_out,
-                                          int* t_out) {
-  const int64_t r = e / p.T;  // (b * M + m) * G + g
-  const int g = static_cast<int>(r % p.G);
-  const int64_t bm = r / p.G;
-  const int64_t m = bm % p.M;
-  const int64_t b = bm / p.M;
-  const int t = __ldg(p.idx + e);
-  const int64_t lastkey = m < p.N - 1 ? m : p.N - 1;
-  *m_out = m;
-  *t_out = t;
-  if (t < 0 || t >= p.nblk || static_cast<int64_t>(t) * p.bs > lastkey) return -1;
-  return static_cast<int>((b * p.G + g) * p.nblk + t);
-}
-
 // The local blocks of a query in block row c (queries c*bs .. c*bs + bs - 1):
 // slot 0 = its own block c, slot 1 = block c - 1; -1 for any other block.
 __device__ __forceinline__ int local_slot(int t, int c) {
@@ -453,27 +455,58 @@ __device__ __forceinline__ int local_slot(int t, int c) {
   return -1;
 }
 
-// Whether the local-block kernel takes entry e (block t of query m): the
-// first of the row's entries in a local slot claims the slot's bit (bits
-// 0-1 in the count pass, 3-4 in the fill pass); a repeat of the block in
-// the row stays in the list, so both passes leave the same entries out.
-__device__ __forceinline__ bool taken_locally(const BwdProblem& p, int64_t e, int64_t m, int t,
-                                              int shift) {
-  if (p.lmask == nullptr) return false;
-  const int s = local_slot(t, static_cast<int>(m / p.bs));
-  if (s < 0) return false;
-  const uint32_t bit = 1u << (s + shift);
-  return (atomicOr(p.lmask + e / p.T, bit) & bit) == 0u;
-}
+// The count walks the index in units of (b, g, 32 consecutive queries):
+// lane l takes query m0 + l and its row's entries in order. Entry j -> the
+// list it files into, or -1: padding, out of range, wholly in the query's
+// future, or taken by the local-block kernel (with lfirst: the row's first
+// entry of each local block, recorded in `first`).
+struct RowWalk {
+  int64_t b, m, row;  // row = (b * M + m) * G + g
+  int g, c, lastkey;
+  bool live;
+  int first[2];
+  __device__ __forceinline__ RowWalk(const BwdProblem& p, int64_t unit, int lane) {
+    const int64_t nmw = (p.M + 31) / 32;
+    const int64_t bg = unit / nmw;
+    g = static_cast<int>(bg % p.G);
+    b = bg / p.G;
+    m = (unit % nmw) * 32 + lane;
+    live = m < p.M;
+    row = (b * p.M + m) * p.G + g;
+    c = static_cast<int>(m / p.bs);
+    lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
+    first[0] = first[1] = -1;
+  }
+  __device__ __forceinline__ int list_of(const BwdProblem& p, int j) {
+    if (!live) return -1;
+    const int t = __ldg(p.idx + row * p.T + j);
+    if (t < 0 || t >= p.nblk || static_cast<int64_t>(t) * p.bs > lastkey) return -1;
+    if (p.lfirst != nullptr) {
+      const int s = local_slot(t, c);
+      if (s >= 0 && first[s] < 0) {
+        first[s] = j;
+        return -1;
+      }
+    }
+    return static_cast<int>((b * p.G + g) * p.nblk + t);
+  }
+};
 
+// Per list, the number of entries it gets. Lanes filing into the same list
+// (block 0 and the local blocks, which neighbouring queries share) add with
+// one atomic. With lfirst, each row's local entries are recorded there.
 __global__ void csr_count_kernel(const BwdProblem p, int* count) {
-  const int64_t total = p.B * p.M * p.G * p.T;
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    int64_t m;
-    int t;
-    const int l = entry_list(p, e, &m, &t);
-    if (l >= 0 && !taken_locally(p, e, m, t, 0)) atomicAdd(count + l, 1);
+  const int lane = threadIdx.x & 31;
+  const int64_t nu = p.B * p.G * ((p.M + 31) / 32);
+  for (int64_t u = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; u < nu;
+       u += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+    RowWalk w(p, u, lane);
+    for (int j = 0; j < p.T; ++j) {
+      const int l = w.list_of(p, j);
+      const unsigned peers = __match_any_sync(kFull, l);
+      if (l >= 0 && lane == __ffs(peers) - 1) atomicAdd(count + l, __popc(peers));
+    }
+    if (w.live && p.lfirst != nullptr) p.lfirst[w.row] = make_int2(w.first[0], w.first[1]);
   }
 }
 
@@ -589,15 +622,31 @@ __global__ void chunk_order_fill_kernel(const BwdProblem p, const int* key, cons
   }
 }
 
+// Each list's entries (query ids). Threads take the index entries in order
+// (grid-stride), so the few hundred rows in flight at a time keep every
+// list in roughly increasing query order, which the chunks' launch order
+// relies on. Entries the count recorded in lfirst are left out.
 __global__ void csr_fill_kernel(const BwdProblem p, int* cursor, int* lists) {
   const int64_t total = p.B * p.M * p.G * p.T;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    int64_t m;
-    int t;
-    const int l = entry_list(p, e, &m, &t);
-    if (l >= 0 && !taken_locally(p, e, m, t, 3))
-      lists[p.offs[l] + atomicAdd(cursor + l, 1)] = static_cast<int>(m);
+    const int64_t r = e / p.T;  // (b * M + m) * G + g
+    const int j = static_cast<int>(e - r * p.T);
+    const int g = static_cast<int>(r % p.G);
+    const int64_t bm = r / p.G;
+    const int64_t m = bm % p.M, b = bm / p.M;
+    const int t = __ldg(p.idx + e);
+    const int64_t lastkey = m < p.N - 1 ? m : p.N - 1;
+    if (t < 0 || t >= p.nblk || static_cast<int64_t>(t) * p.bs > lastkey) continue;
+    if (p.lfirst != nullptr) {
+      const int s = local_slot(t, static_cast<int>(m / p.bs));
+      if (s >= 0) {
+        const int2 f = p.lfirst[r];
+        if ((s == 0 ? f.x : f.y) == j) continue;
+      }
+    }
+    const int l = static_cast<int>((b * p.G + g) * p.nblk + t);
+    lists[p.offs[l] + atomicAdd(cursor + l, 1)] = static_cast<int>(m);
   }
 }
 
@@ -1163,25 +1212,25 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
       // have landed (and the S / dP buffer is free: dV / dK of two batches
       // before issued), dV / dK / dQ of the oldest batch once its P / dS are
       // written and the previous dQ has been read -- so the dV / dK of batch
-      // i never waits for the rows of batch i + 1. One bounded wait: 1 s
-      // without progress fails.
+      // i never waits for the rows of batch i + 1. One bounded wait: about
+      // 2 s (kSpinLimitCycles) without progress fails.
       int nsd = 0, nacc = 0;
-      uint64_t t_last = globaltimer_ns();
+      long long t_last = clock64();
       while (ok && nacc < nbat) {
         bool progressed = false;
         if (nsd < nbat && nsd <= nacc + 1 &&
-            mbar_try_wait(bar(kQdFull + (nsd & 1)), (nsd >> 1) & 1)) {
+            mbar_test_wait(bar(kQdFull + (nsd & 1)), (nsd >> 1) & 1)) {
           issue_sd(nsd++);
           progressed = true;
         }
-        if (nacc < nsd && mbar_try_wait(bar(kPdsFull + (nacc & 1)), (nacc >> 1) & 1) &&
-            (nacc == 0 || mbar_try_wait(bar(kDqFree), (nacc - 1) & 1))) {
+        if (nacc < nsd && mbar_test_wait(bar(kPdsFull + (nacc & 1)), (nacc >> 1) & 1) &&
+            (nacc == 0 || mbar_test_wait(bar(kDqFree), (nacc - 1) & 1))) {
           issue_acc(nacc++);
           progressed = true;
         }
         if (progressed) {
-          t_last = globaltimer_ns();
-        } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
+          t_last = clock64();
+        } else if (clock64() - t_last > kSpinLimitCycles) {
           ok = false;
         }
       }
@@ -1384,8 +1433,8 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
 //
 // The queries of block row c (positions c*bs .. c*bs + bs - 1) share their
 // two local blocks, block c and block c - 1 (local_slot). The list kernels
-// leave those entries out of the query lists and mark them per row in
-// lmask; this kernel takes them, one CTA per (b, block row, g). The CTA
+// leave those entries out of the query lists and record them per row in
+// lfirst; this kernel takes them, one CTA per (b, block row, g). The CTA
 // owns the dQ rows of its queries: their contributions from both blocks
 // are summed in tensor memory and stored once (rows that take neither block
 // get zeros), so dQ needs no zeroing and the key-major kernel's fp32
@@ -1415,23 +1464,6 @@ enum LocBar : int {
   kLStaged = 13,   // dV / dK of the block row staged in shared memory
   kLocBars = 14
 };
-
-// Spin limit of the MMA issuer's polling loop, in SM clock cycles (about 2 s
-// at 2 GHz): the loop reads the SM clock, which is cheap, rather than the
-// global timer on every pass.
-constexpr long long kSpinLimitCycles = 4000000000LL;
-
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 struct LocalCfg {
   static constexpr int kAtom = 128 * 128;    // 128 rows x 128 B
@@ -1473,7 +1505,7 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
   const int nbat = (nitems + kTcBatch - 1) / kTcBatch;
   const int64_t hgroup = static_cast<int64_t>(g) * p.hpg;
   const int hw0 = p.hpg < kHeadsPerGroup ? p.hpg : kHeadsPerGroup;  // head rows per item
-  const int64_t mrow0 = (b * p.M + m0) * p.G + g;                  // lmask row of query m0
+  const int64_t mrow0 = (b * p.M + m0) * p.G + g;                  // row of query m0
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1490,7 +1522,10 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
   }
   // the slots some query of the block row takes here, in slot order
   uint32_t any = 0;
-  for (int q = threadIdx.x; q < nq; q += blockDim.x) any |= __ldg(p.lmask + mrow0 + q * p.G) & 3u;
+  for (int q = threadIdx.x; q < nq; q += blockDim.x) {
+    const int2 f = p.lfirst[mrow0 + q * p.G];
+    any |= (f.x >= 0 ? 1u : 0u) | (f.y >= 0 ? 2u : 0u);
+  }
   const int act = (__syncthreads_or(any & 1u) ? 1 : 0) | (__syncthreads_or(any & 2u) ? 2 : 0);
   const int nsl = __popc(act);
   auto slot_at = [&](int k) { return act == 2 ? 1 : k; };  // k-th active slot
@@ -1600,7 +1635,7 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
       // loaded the previous one (and its rows have landed); dQ_R, dV and dK
       // of the oldest step whose P / dS are written (the first slot of a
       // batch once the dQ warps have read the previous batch's dQ_R). One
-      // bounded wait: 1 s without progress fails. ----
+      // bounded wait: about 2 s (kSpinLimitCycles) without progress fails. ----
       constexpr uint32_t idesc_sd = umma_idesc_f16(128, 64, BF16, false);  // K-major A, B
       constexpr uint32_t idesc_acc =
           umma_idesc_f16(128, 64, BF16, true) | (1u << 15);  // MN-major A and B
@@ -1773,7 +1808,8 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
         const float* rec = p.rec + (row * nsub + sub) * 16;
         lse2 = __ldg(rec + (r & 7));
         delta = __ldg(rec + 8 + (r & 7));
-        rmask = __ldg(p.lmask + row);
+        const int2 f = p.lfirst[row];
+        rmask = (f.x >= 0 ? 1u : 0u) | (f.y >= 0 ? 2u : 0u);
       }
       const int lastkey = static_cast<int>(m < p.N - 1 ? m : p.N - 1);
       for (int k = 0; k < nsl; ++k) {
@@ -1887,7 +1923,7 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
 struct BwdPlan {
   size_t off_do16, off_rec, off_count, off_cursor, off_offs, off_choffs, off_lists,
       off_chunk_list, off_order, off_key, off_bcount, off_bcursor, off_boffs, off_bscratch,
-      off_lmask, total;
+      off_lfirst, total;
   int64_t L, entries, max_chunks, nkeys, nbkt;
 };
 
@@ -1937,8 +1973,8 @@ static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, i
   pl.off_bscratch = at;
   at += align256(static_cast<size_t>(pl.nkeys + 1) * 4);
   // per (b, m, g) row: the entries the local-block kernel takes (D = 128)
-  pl.off_lmask = at;
-  at += align256(static_cast<size_t>(B * M * G) * 4);
+  pl.off_lfirst = at;
+  at += align256(static_cast<size_t>(B * M * G) * 8);
   pl.total = at;
   return pl;
 }
@@ -1947,7 +1983,7 @@ static BwdPlan bwd_plan(int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, i
 // the call returns (CUDA defers the release until the queued work is done).
 struct SideStream {
   cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, mid = nullptr, back = nullptr;
   bool ok = false;
   explicit SideStream(bool wanted) {
     if (!wanted) return;  // ok stays false: everything runs on the caller's stream
@@ -1957,7 +1993,9 @@ struct SideStream {
     if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) hi = 0;
     ok = cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, hi) == cudaSuccess &&
          cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess;
+         cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&mid, cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&back, cudaEventDisableTiming) == cudaSuccess;
   }
   // `st` waits for everything queued on the side stream; if that cannot be
   // arranged, the side stream is waited for here, so no queued work outlives
@@ -1969,6 +2007,8 @@ struct SideStream {
     return false;
   }
   ~SideStream() {
+    if (back) cudaEventDestroy(back);
+    if (mid) cudaEventDestroy(mid);
     if (join) cudaEventDestroy(join);
     if (fork) cudaEventDestroy(fork);
     if (s) cudaStreamDestroy(s);
@@ -1994,31 +2034,43 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   p.chunk_list = chunk_list;
   p.chunk_order = nullptr;
   // D = 128: the local blocks of each block row go to their own kernel
-  p.lmask = D == 128 ? reinterpret_cast<uint32_t*>(ws + pl.off_lmask) : nullptr;
+  p.lfirst = D == 128 ? reinterpret_cast<int2*>(ws + pl.off_lfirst) : nullptr;
   const int64_t B = p.units / (p.M * p.G * p.nsub);
-  if (p.N > 0 &&
-      (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess ||
-       cudaMemsetAsync(p.dV, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, st) != cudaSuccess))
-    return NSA_ERR_LAUNCH;
+  // dK and dV start at zero (the stage-3 kernels add into them); with D =
+  // 128 and a query to process, stage 2 zeroes them on its stream
+  auto zero_dkv = [&](cudaStream_t s) {
+    return p.N <= 0 ||
+           (cudaMemsetAsync(p.dK, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, s) ==
+                cudaSuccess &&
+            cudaMemsetAsync(p.dV, 0, static_cast<size_t>(B * p.N * p.G * D) * 4, s) ==
+                cudaSuccess);
+  };
+  if ((D != 128 || p.N <= 0 || p.T == 0) && !zero_dkv(st)) return NSA_ERR_LAUNCH;
   const int64_t chunks = pl.max_chunks;
   int* order = reinterpret_cast<int*>(ws + pl.off_order);
 
-  // stage 2 on stream s2: the transposed index (count, scan, fill, chunk ->
-  // list table) and, with D = 128, the chunks' launch order. It reads only
-  // the index tensor.
-  auto stage2 = [&](cudaStream_t s2) -> int {
+  // stage 2 on stream s2: the transposed index and, with D = 128, the
+  // chunks' launch order. It reads only the index tensor. 2a: per list its
+  // count (and per row its local entries; with D = 128 also dK = dV = 0),
+  // which is all the local-block kernel needs; 2b: the scans, the lists,
+  // the chunk -> list table and the chunks' order.
+  auto stage2a = [&](cudaStream_t s2) -> int {
     if (cudaMemsetAsync(count, 0, static_cast<size_t>(pl.L) * 4, s2) != cudaSuccess ||
         cudaMemsetAsync(cursor, 0, static_cast<size_t>(pl.L) * 4, s2) != cudaSuccess)
       return NSA_ERR_LAUNCH;
-    if (p.lmask != nullptr &&
-        cudaMemsetAsync(p.lmask, 0, static_cast<size_t>(B * p.M * p.G) * 4, s2) != cudaSuccess)
-      return NSA_ERR_LAUNCH;
-    // grid-stride: a few CTAs per SM are enough for atomics on small tables
-    const int64_t grid_e =
-        (pl.entries + 255) / 256 < 152 * 4 ? (pl.entries + 255) / 256 : 152 * 4;
-    csr_count_kernel<<<static_cast<unsigned>(grid_e), 256, 0, s2>>>(p, count);
+    if (p.lfirst != nullptr && !zero_dkv(s2)) return NSA_ERR_LAUNCH;
+    // one warp per (b, g, 32 queries), grid-stride: a few CTAs per SM are
+    // enough for atomics on small tables
+    const int64_t units = B * p.G * ((p.M + 31) / 32);
+    const int64_t grid_u = (units + 7) / 8 < 152 * 4 ? (units + 7) / 8 : 152 * 4;
+    csr_count_kernel<<<static_cast<unsigned>(grid_u), 256, 0, s2>>>(p, count);
+    return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
+  };
+  auto stage2b = [&](cudaStream_t s2) -> int {
     csr_scan_kernel<<<1, 1024, 0, s2>>>(count, offs, choffs, static_cast<int>(pl.L),
                                         kQueriesPerChunk);
+    const int64_t grid_e =
+        (pl.entries + 255) / 256 < 152 * 4 ? (pl.entries + 255) / 256 : 152 * 4;
     csr_fill_kernel<<<static_cast<unsigned>(grid_e), 256, 0, s2>>>(p, cursor, lists);
     csr_chunk_list_kernel<<<static_cast<unsigned>((pl.L + 255) / 256), 256, 0, s2>>>(
         choffs, static_cast<int>(pl.L), chunk_list);
@@ -2056,32 +2108,81 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     memset(&tkb, 0, sizeof(tkb));
     memset(&tvb, 0, sizeof(tvb));
   }
+  // Q / dO rows of the stage-3 kernels
+  CUtensorMap tq, tdo;
+  const int hw0 = p.hpg < kHeadsPerGroup ? p.hpg : kHeadsPerGroup;
+  if (!encode_rows_map_t(&tq, p.Q, B * p.M * p.H, D, hw0, map_dtype(BF16)) ||
+      !encode_rows_map_t(&tdo, p.dO16, B * p.M * p.H, D, hw0, map_dtype(BF16)))
+    return NSA_ERR_LAUNCH;
+  const bool split = p.nsub > 1;
 
   if constexpr (D == 128) {
-    // stage 1: the per-row inputs of the stage-3 kernels (16-bit dO, LSE,
-    // delta); dQ needs no zeroing, the local-block kernel stores every row
     if (!have_keys || p.T == 0) {  // dQ = dK = dV = 0
       return cudaMemsetAsync(p.dQ, 0, static_cast<size_t>(B * p.M * p.H * D) * 4, st) ==
                      cudaSuccess
                  ? NSA_OK
                  : NSA_ERR_LAUNCH;
     }
-    // Stage 2 runs beside stage 1 on a second stream: stage 1 streams dO and
-    // O through HBM, stage 2 counts and files the index entries with atomics
-    // on small tables, and neither touches what the other writes. The
-    // caller's stream waits for both before the stage-3 kernels.
+    // the tensor-core (tcgen05) kernels: block K / V read as one box per
+    // column half, the Q / dO rows of an item as one 3-D box (both column
+    // halves)
+    CUtensorMap tk64, tv64, tq3 = tq, tdo3 = tdo;
+    if (!encode_kv_map(&tk64, K, B, p.N, p.G, D, p.bs, map_dtype(BF16)) ||
+        !encode_kv_map(&tv64, V, B, p.N, p.G, D, p.bs, map_dtype(BF16)))
+      return NSA_ERR_LAUNCH;
+    if (hw0 == kHeadsPerGroup &&
+        (!encode_rows_halves_map(&tq3, p.Q, B * p.M * p.H, hw0, map_dtype(BF16)) ||
+         !encode_rows_halves_map(&tdo3, p.dO16, B * p.M * p.H, hw0, map_dtype(BF16))))
+      return NSA_ERR_LAUNCH;
+    auto kl = split ? sel_attn_bwd_local_kernel<true, BF16> : sel_attn_bwd_local_kernel<false, BF16>;
+    auto kk = split ? sel_attn_bwd_dkv_tc_kernel<true, BF16> : sel_attn_bwd_dkv_tc_kernel<false, BF16>;
+    if (cudaFuncSetAttribute(kl, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LocalCfg::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkvTcCfg::kSmemBytes) != cudaSuccess)
+      return NSA_ERR_LAUNCH;
+    // Stage 2 runs on a second stream: 2a beside stage 1 (prep: 16-bit dO,
+    // LSE, delta), which streams dO and O through HBM; 2b after stage 1,
+    // beside the local-block kernel (one CTA of its fill fits beside each of
+    // that kernel's CTAs), so the prep has the SMs to itself but for 2a.
+    // Neither stage touches what the other writes. The local-block kernel
+    // waits for stage 1 and stage 2a; the key-major kernel for everything.
     SideStream side(second_stream);
-    int rc2 = NSA_ERR_LAUNCH;
-    if (side.ok && cudaEventRecord(side.fork, st) == cudaSuccess &&
-        cudaStreamWaitEvent(side.s, side.fork, 0) == cudaSuccess)
-      rc2 = stage2(side.s);
-    else
-      rc2 = stage2(st);  // no second stream: in order on the caller's stream
+    const bool on_side = side.ok && cudaEventRecord(side.fork, st) == cudaSuccess &&
+                         cudaStreamWaitEvent(side.s, side.fork, 0) == cudaSuccess;
+    cudaStream_t s2 = on_side ? side.s : st;  // no second stream: in order on st
+    int rc2 = stage2a(s2);
+    const bool mid_ok = on_side && rc2 == NSA_OK && cudaEventRecord(side.mid, s2) == cudaSuccess;
     sel_attn_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((p.units + 7) / 8), 256, 0, st>>>(p);
-    const bool rc1 = cudaGetLastError() == cudaSuccess;
-    if (side.ok && !side.join_into(st)) return NSA_ERR_LAUNCH;
-    if (rc2 != NSA_OK) return rc2;
+    bool rc1 = cudaGetLastError() == cudaSuccess;
+    // 2b after the prep (if that order cannot be arranged, 2b runs beside it)
+    if (on_side && cudaEventRecord(side.back, st) == cudaSuccess)
+      cudaStreamWaitEvent(s2, side.back, 0);
+    if (rc2 == NSA_OK) rc2 = stage2b(s2);
+    if (on_side) {
+      // the local-block kernel needs stage 2a only; if that wait cannot be
+      // arranged, it waits for all of stage 2
+      if (!(mid_ok && cudaStreamWaitEvent(st, side.mid, 0) == cudaSuccess) &&
+          !side.join_into(st))
+        return NSA_ERR_LAUNCH;
+    }
+    if (rc2 != NSA_OK || !rc1) {
+      if (on_side) side.join_into(st);  // no queued work outlives the call
+      return rc2 != NSA_OK ? rc2 : NSA_ERR_LAUNCH;
+    }
+    // the local blocks of every block row first: it stores each dQ row once,
+    // then the key-major kernel adds the rest of the row's blocks
+    const int64_t lgrid = B * p.G * ((p.M + p.bs - 1) / p.bs);  // < 2^31: B * M * G * T is
+    if (lgrid > 0)
+      kl<<<static_cast<unsigned>(lgrid), kDkvTcThreads, LocalCfg::kSmemBytes, st>>>(p, tk64, tv64,
+                                                                                   tq3, tdo3);
+    rc1 = cudaGetLastError() == cudaSuccess;
+    if (on_side && !side.join_into(st)) return NSA_ERR_LAUNCH;
     if (!rc1) return NSA_ERR_LAUNCH;
+    p.chunk_order = order;  // written by stage 2b
+    kk<<<static_cast<unsigned>(chunks), kDkvTcThreads, DkvTcCfg::kSmemBytes, st>>>(
+        p, tk64, tv64, tq3, tdo3);
+    return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
   } else {
     // stage 1: dQ and delta
     auto kq = sel_attn_bwd_dq_kernel<D, W, BF16>;
@@ -2091,73 +2192,34 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     kq<<<static_cast<unsigned>((p.units + W - 1) / W), W * 32, Cq::kSmemBytes, st>>>(p, tk, tv);
     if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
     if (!have_keys || p.T == 0) return NSA_OK;  // dK = dV = 0
-  }
-
-  if constexpr (D != 128) {
-    const int rc2 = stage2(st);  // after stage 1, on the caller's stream
+    // stage 2 after stage 1, on the caller's stream
+    int rc2 = stage2a(st);
+    if (rc2 == NSA_OK) rc2 = stage2b(st);
     if (rc2 != NSA_OK) return rc2;
-  }
-
-  // stage 3: dK, dV; grid bound: sum over lists of ceil(count / chunk)
-  CUtensorMap tq, tdo;
-  const int hw0 = p.hpg < kHeadsPerGroup ? p.hpg : kHeadsPerGroup;
-  if (!encode_rows_map_t(&tq, p.Q, B * p.M * p.H, D, hw0, map_dtype(BF16)) ||
-      !encode_rows_map_t(&tdo, p.dO16, B * p.M * p.H, D, hw0, map_dtype(BF16)))
-    return NSA_ERR_LAUNCH;
-  auto run = [&](auto kt, auto split) -> int {
-    constexpr int KT = decltype(kt)::value;
-    using Ck = DkvCfg<D, KT>;
-    auto kk = sel_attn_bwd_dkv_kernel<D, KT, decltype(split)::value, BF16>;
-    if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, Ck::kSmemBytes) !=
-        cudaSuccess)
-      return NSA_ERR_LAUNCH;
-    kk<<<static_cast<unsigned>(chunks), Ck::kWarps * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb, tq,
-                                                                             tdo);
-    return NSA_OK;
-  };
-  using I2 = std::integral_constant<int, 2>;
-  using I4 = std::integral_constant<int, 4>;
-  using Yes = std::true_type;
-  using No = std::false_type;
-  const bool split = p.nsub > 1;
-  if constexpr (D == 128) {
-    // the tensor-core (tcgen05) kernel, which also produces dQ; block K / V
-    // read as one box per column half, the Q / dO rows of an item as one 3-D
-    // box (both column halves)
-    CUtensorMap tk64, tv64, tq3 = tq, tdo3 = tdo;
-    if (!encode_kv_map(&tk64, K, B, p.N, p.G, D, p.bs, map_dtype(BF16)) ||
-        !encode_kv_map(&tv64, V, B, p.N, p.G, D, p.bs, map_dtype(BF16)))
-      return NSA_ERR_LAUNCH;
-    if (hw0 == kHeadsPerGroup && (!encode_rows_halves_map(&tq3, p.Q, B * p.M * p.H, hw0, map_dtype(BF16)) ||
-                                  !encode_rows_halves_map(&tdo3, p.dO16, B * p.M * p.H, hw0,
-                                                          map_dtype(BF16))))
-      return NSA_ERR_LAUNCH;
-    // the local blocks of every block row first: it stores each dQ row once,
-    // then the key-major kernel adds the rest of the row's blocks
-    auto kl = split ? sel_attn_bwd_local_kernel<true, BF16> : sel_attn_bwd_local_kernel<false, BF16>;
-    if (cudaFuncSetAttribute(kl, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             LocalCfg::kSmemBytes) != cudaSuccess)
-      return NSA_ERR_LAUNCH;
-    const int64_t lgrid = B * p.G * ((p.M + p.bs - 1) / p.bs);  // < 2^31: B * M * G * T is
-    if (lgrid > 0)
-      kl<<<static_cast<unsigned>(lgrid), kDkvTcThreads, LocalCfg::kSmemBytes, st>>>(p, tk64, tv64,
-                                                                                   tq3, tdo3);
-    p.chunk_order = order;  // written by stage 2
-    auto kk = split ? sel_attn_bwd_dkv_tc_kernel<true, BF16> : sel_attn_bwd_dkv_tc_kernel<false, BF16>;
-    if (cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DkvTcCfg::kSmemBytes) != cudaSuccess)
-      return NSA_ERR_LAUNCH;
-    kk<<<static_cast<unsigned>(chunks), kDkvTcThreads, DkvTcCfg::kSmemBytes, st>>>(
-        p, tk64, tv64, tq3, tdo3);
+    // stage 3: dK, dV; grid bound: sum over lists of ceil(count / chunk)
+    auto run = [&](auto kt, auto sp) -> int {
+      constexpr int KT = decltype(kt)::value;
+      using Ck = DkvCfg<D, KT>;
+      auto kd = sel_attn_bwd_dkv_kernel<D, KT, decltype(sp)::value, BF16>;
+      if (cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, Ck::kSmemBytes) !=
+          cudaSuccess)
+        return NSA_ERR_LAUNCH;
+      kd<<<static_cast<unsigned>(chunks), Ck::kWarps * 32, Ck::kSmemBytes, st>>>(p, tkb, tvb, tq,
+                                                                               tdo);
+      return NSA_OK;
+    };
+    using I2 = std::integral_constant<int, 2>;
+    using I4 = std::integral_constant<int, 4>;
+    using Yes = std::true_type;
+    using No = std::false_type;
+    int rc;
+    if (p.bs == 64)
+      rc = split ? run(I4{}, Yes{}) : run(I4{}, No{});
+    else
+      rc = split ? run(I2{}, Yes{}) : run(I2{}, No{});
+    if (rc != NSA_OK) return rc;
     return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
   }
-  int rc;
-  if (p.bs == 64)
-    rc = split ? run(I4{}, Yes{}) : run(I4{}, No{});
-  else
-    rc = split ? run(I2{}, Yes{}) : run(I2{}, No{});
-  if (rc != NSA_OK) return rc;
-  return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
 }
 
 int bwd_read_and_clear_status(unsigned int* value) { return read_and_clear_status(value); }
