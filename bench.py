@@ -801,6 +801,22 @@ def run_two_pass(w, q, k, v, idx, work, flush, args, t_one_ms):
     return res
 
 
+def local_entries(idx, w):
+    """(visible entries, entries of the query's own block c or of block
+    c - 1) of the index tensor [B, M, G, T]: the backward's dQ reductions
+    are the visible entries minus the local ones (rows list a block once)."""
+    import torch
+
+    m = torch.arange(w.M, device=idx.device).view(1, w.M, 1, 1)
+    c = m // w.block_size
+    nblk = (w.N + w.block_size - 1) // w.block_size
+    last = torch.clamp(m, max=w.N - 1)
+    t = idx.long()
+    vis = (t >= 0) & (t < nblk) & (t * w.block_size <= last)
+    loc = vis & ((t == c) | (t == c - 1))
+    return int(vis.sum()), int(loc.sum())
+
+
 def run_backward(w, q, k, v, idx, out, lse, work, flush, args):
     """nsa_sel_attn_bwd on the forward's outputs and a seeded fp32 dO.
     FLOPs: 10*D per (query, head, visible key) -- QK^T, dP, dQ, dK, dV."""
@@ -830,16 +846,24 @@ def run_backward(w, q, k, v, idx, out, lse, work, flush, args):
                           flush, steps, flops)
     if w.D == 128:
         # dQ = dS K per (query, selected block): every head of the group,
-        # D fp32 values each, added with reductions
-        red = work["gathered_bytes"] * (w.H // w.G) // w.block_size
+        # D fp32 values each. The entries of a query's own block c and of
+        # block c - 1 are summed inside the local-block kernel and stored
+        # once per row; the others are added with reductions.
+        per_entry = (w.H // w.G) * w.D * 4
+        n_entries, n_local = local_entries(idx, w)
+        red = (n_entries - n_local) * per_entry
         ceiling = run_leg(True, reduction_ceiling, dq, w)
         res.update({"dq_reduction_bytes": red, "dq_reduction_gbs": red / (t * 1e-3) / 1e9,
+                    "dq_local_entries": n_local, "dq_entries": n_entries,
                     "dq_reduction_ceiling": ceiling,
                     "dq_reduction_frac": (red / (t * 1e-3) / 1e9 / ceiling["gbs"]
                                           if ceiling and "gbs" in ceiling else None),
                     "kernels": "prep (fp16 dO, LSE, delta), index transpose (count, scan, "
-                               "fill), key-major tcgen05 kernel: dK, dV (fp32 atomics per "
-                               "chunk) and dQ = dS K (fp32 reductions per batch)"})
+                               "fill, chunk order; second stream), local-block tcgen05 kernel "
+                               "(blocks c and c - 1 of every block row: dQ stored once, dK / dV "
+                               "per block row), key-major tcgen05 kernel for the other entries: "
+                               "dK, dV (bulk fp32 reductions per chunk) and dQ = dS K (fp32 "
+                               "reductions per batch)"})
     else:
         res["kernels"] = ("dQ (query-major, mma.sync), index transpose (count, scan, fill), "
                           "dK/dV (key-major, mma.sync, fp32 atomics)")

@@ -283,8 +283,9 @@ int nsa_sel_attn_fwd_host_ex(const void* Q, const void* K, const void* V,
  * nsa_sel_attn_bwd_workspace_bytes -- device workspace nsa_sel_attn_bwd
  * needs: an fp16 copy of dO, one 64-byte (LSE, delta) record per (b, m, g,
  * 8-head sub-group), the per-(b, g, block) query lists (at most B*M*G*T
- * entries) and their counts and offsets. Negative nsa_status for
- * invalid sizes (B*M*G*T must stay below 2^31). Pure host arithmetic.
+ * entries) and their counts and offsets, and 8 bytes per (b, m, g) row
+ * for the row's local entries. Negative nsa_status for invalid sizes
+ * (B*M*G*T must stay below 2^31). Pure host arithmetic.
  */
 int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_t H,
                                          int64_t G, int64_t D, int64_t T, int block_size);
@@ -304,21 +305,27 @@ int64_t nsa_sel_attn_bwd_workspace_bytes(int64_t B, int64_t M, int64_t N, int64_
  *
  * With p = exp(scale q.k - LSE), dP = dO.v and delta = dO.O per row and head:
  * dS = p (dP - delta), dQ = scale sum dS k, dK += scale dS q, dV += p dO over
- * every visible (query, head, key). Three stages on `stream`: per-row
- * inputs (delta, an fp16 copy of dO; with D = 64 also dQ, from a
- * query-major kernel); a transposed index listing, per (b, g, block), the
- * queries that selected it; a key-major kernel that loads each block once
- * per chunk of its list and adds its dK / dV partial sums with fp32
- * atomics -- with D = 128 it also forms dQ = dS K on the tensor cores and
- * adds it with fp32 reductions. dK / dV (and dQ when D = 128) sum in an
- * order set by atomics (equal within rounding from run to run). With
- * D = 128 every key of a selected block enters dQ (with weight 0 where the
- * query does not see it), so K must be finite in the selected blocks,
- * including keys after a query's position. With D = 128 the index transpose
- * runs on a second stream that the call creates and releases, beside the
- * per-row stage; `stream` waits for it. Asynchronous, allocates no device
- * memory; errors as nsa_sel_attn_fwd plus NSA_ERR_WORKSPACE. Pointers must be
- * 16-byte aligned (LSE and block_indices 4-byte).
+ * every visible (query, head, key). Stages on `stream`: per-row inputs
+ * (delta, an fp16 copy of dO; with D = 64 also dQ, from a query-major
+ * kernel); a transposed index listing, per (b, g, block), the queries that
+ * selected it; a key-major kernel that loads each block once per chunk of
+ * its list and adds its dK / dV partial sums. With D = 128, the entries
+ * of each query's own block c and of block c - 1 go to a local-block
+ * kernel instead (one CTA per block row of 32 or 64 queries: their dQ rows
+ * summed on the tensor cores and stored once, dK / dV of the two blocks
+ * summed over the block row), and the key-major kernel also forms dQ =
+ * dS K for the other entries and adds it with fp32 reductions; dK / dV are
+ * added with fp32 atomics (D = 64) or bulk fp32 reductions (D = 128). dK /
+ * dV (and dQ when D = 128) sum in an order set by atomics (equal within
+ * rounding from run to run). With D = 128 every key of a block some query
+ * selects may enter the dQ of the queries that share its block row or its
+ * chunk (with weight 0 where a query does not select or see it), so K
+ * must be finite in every selected block, including keys after a query's
+ * position. With D = 128 the index transpose runs on a second stream that
+ * the call creates and releases, beside the per-row stage and the
+ * local-block kernel; `stream` waits for it. Asynchronous, allocates no
+ * device memory; errors as nsa_sel_attn_fwd plus NSA_ERR_WORKSPACE.
+ * Pointers must be 16-byte aligned (LSE and block_indices 4-byte).
  */
 int nsa_sel_attn_bwd(const void* Q, const void* K, const void* V,
                      const int32_t* block_indices, const float* O, const float* LSE,
