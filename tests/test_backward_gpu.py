@@ -74,6 +74,8 @@ def _check(got, q, k, v, idx, dO, bs, scale=None, what=""):
     (1, 500, 500, 128, 32, 6, "first_local"),
     (1, 300, 520, 128, 64, 3, "local"),
     (1, 520, 300, 64, 64, 3, "local"),
+    (1, 520, 300, 128, 64, 3, "local"),
+    (1, 410, 200, 128, 32, 5, "first_two_local"),
     (1, 640, 640, 128, 64, 10, "all_causal"),
 ])
 def test_bwd_matches_oracle(B, M, N, D, bs, T, rule):
@@ -94,6 +96,27 @@ def test_bwd_padding_out_of_range_future_and_empty_rows():
     got = _run(q, k, v, idx, dO, 64, scale=0.1)
     _check(got, q, k, v, idx, dO, 64, scale=0.1, what="padding")
     assert np.all(got[0][0, 5:9] == 0)  # dQ of empty rows
+
+
+@pytest.mark.parametrize("bs", [64, 32])
+def test_bwd_local_blocks_taken_by_some_rows_only(bs):
+    """The local-block kernel (D = 128) takes each row's entries of its own
+    block c and of block c - 1. Here rows of one block row differ: some
+    list both, some one, some neither, and one block row (queries 4 bs ..
+    5 bs - 1) lists neither anywhere, so its CTA runs no step and stores
+    zero dQ rows before the key-major kernel adds their other blocks."""
+    M = 9 * bs + 5
+    q, k, v, idx = small_inputs(1, M, M, 16, 2, 128, bs, 6, "first_two_local", seed=bs + 3)
+    rng = np.random.default_rng(bs)
+    c = (np.arange(M) // bs)[None, :, None, None]
+    drop_c = rng.random(idx.shape[:3])[..., None] < 0.3
+    drop_p = rng.random(idx.shape[:3])[..., None] < 0.3
+    row4 = (c == 4)
+    idx = np.where(((idx == c) & (drop_c | row4)) | ((idx == c - 1) & (drop_p | row4)), -1,
+                   idx).astype(np.int32)
+    dO = rng.standard_normal(q.shape).astype(np.float32)
+    got = _run(q, k, v, idx, dO, bs)
+    _check(got, q, k, v, idx, dO, bs, what=f"local rows bs{bs}")
 
 
 @pytest.mark.parametrize("T,N", [(0, 256), (3, 0)])
