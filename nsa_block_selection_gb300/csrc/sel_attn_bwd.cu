@@ -2054,23 +2054,25 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
   // count (and per row its local entries; with D = 128 also dK = dV = 0),
   // which is all the local-block kernel needs; 2b: the scans, the lists,
   // the chunk -> list table and the chunks' order.
-  auto stage2a = [&](cudaStream_t s2) -> int {
+  // Grids: grid-stride, `per_sm` CTAs per SM. Beside the prep and the
+  // local-block kernel one CTA per SM disturbs those least and still
+  // finishes in their shadow; run alone, four keep more atomics in flight.
+  auto stage2a = [&](cudaStream_t s2, int per_sm) -> int {
     if (cudaMemsetAsync(count, 0, static_cast<size_t>(pl.L) * 4, s2) != cudaSuccess ||
         cudaMemsetAsync(cursor, 0, static_cast<size_t>(pl.L) * 4, s2) != cudaSuccess)
       return NSA_ERR_LAUNCH;
     if (p.lfirst != nullptr && !zero_dkv(s2)) return NSA_ERR_LAUNCH;
-    // one warp per (b, g, 32 queries), grid-stride: a few CTAs per SM are
-    // enough for atomics on small tables
+    // one warp per (b, g, 32 queries)
     const int64_t units = B * p.G * ((p.M + 31) / 32);
-    const int64_t grid_u = (units + 7) / 8 < 152 * 4 ? (units + 7) / 8 : 152 * 4;
+    const int64_t grid_u = (units + 7) / 8 < 152 * per_sm ? (units + 7) / 8 : 152 * per_sm;
     csr_count_kernel<<<static_cast<unsigned>(grid_u), 256, 0, s2>>>(p, count);
     return cudaGetLastError() == cudaSuccess ? NSA_OK : NSA_ERR_LAUNCH;
   };
-  auto stage2b = [&](cudaStream_t s2) -> int {
+  auto stage2b = [&](cudaStream_t s2, int per_sm) -> int {
     csr_scan_kernel<<<1, 1024, 0, s2>>>(count, offs, choffs, static_cast<int>(pl.L),
                                         kQueriesPerChunk);
     const int64_t grid_e =
-        (pl.entries + 255) / 256 < 152 * 4 ? (pl.entries + 255) / 256 : 152 * 4;
+        (pl.entries + 255) / 256 < 152 * per_sm ? (pl.entries + 255) / 256 : 152 * per_sm;
     csr_fill_kernel<<<static_cast<unsigned>(grid_e), 256, 0, s2>>>(p, cursor, lists);
     csr_chunk_list_kernel<<<static_cast<unsigned>((pl.L + 255) / 256), 256, 0, s2>>>(
         choffs, static_cast<int>(pl.L), chunk_list);
@@ -2151,14 +2153,15 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     const bool on_side = side.ok && cudaEventRecord(side.fork, st) == cudaSuccess &&
                          cudaStreamWaitEvent(side.s, side.fork, 0) == cudaSuccess;
     cudaStream_t s2 = on_side ? side.s : st;  // no second stream: in order on st
-    int rc2 = stage2a(s2);
+    const int per_sm = on_side ? 1 : 4;
+    int rc2 = stage2a(s2, per_sm);
     const bool mid_ok = on_side && rc2 == NSA_OK && cudaEventRecord(side.mid, s2) == cudaSuccess;
     sel_attn_bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((p.units + 7) / 8), 256, 0, st>>>(p);
     bool rc1 = cudaGetLastError() == cudaSuccess;
     // 2b after the prep (if that order cannot be arranged, 2b runs beside it)
     if (on_side && cudaEventRecord(side.back, st) == cudaSuccess)
       cudaStreamWaitEvent(s2, side.back, 0);
-    if (rc2 == NSA_OK) rc2 = stage2b(s2);
+    if (rc2 == NSA_OK) rc2 = stage2b(s2, per_sm);
     if (on_side) {
       // the local-block kernel needs stage 2a only; if that wait cannot be
       // arranged, it waits for all of stage 2
@@ -2193,8 +2196,8 @@ static int launch_bwd(BwdProblem& p, const void* K, const void* V, uint8_t* ws,
     if (cudaGetLastError() != cudaSuccess) return NSA_ERR_LAUNCH;
     if (!have_keys || p.T == 0) return NSA_OK;  // dK = dV = 0
     // stage 2 after stage 1, on the caller's stream
-    int rc2 = stage2a(st);
-    if (rc2 == NSA_OK) rc2 = stage2b(st);
+    int rc2 = stage2a(st, 4);
+    if (rc2 == NSA_OK) rc2 = stage2b(st, 4);
     if (rc2 != NSA_OK) return rc2;
     // stage 3: dK, dV; grid bound: sum over lists of ceil(count / chunk)
     auto run = [&](auto kt, auto sp) -> int {
