@@ -8,29 +8,39 @@
 //   dS_n = p_n (dP_n - delta);  dQ = scale sum_n dS_n k_n;
 //   dK[n] += scale dS_n q;      dV[n] += p_n dO.
 //
-// Three stages, all on the caller's stream:
+// Stages:
 //  1. D = 64: query-major kernel (one warp per (b, m, g), same TMA tile
 //     gather as the forward): recomputes S^T = K Q^T, P, dP^T = V dO^T and dS
 //     on the tensor cores (mma.sync m16n8k16, fp16 operands, fp32
 //     accumulate) and accumulates dQ^T += K^T dS^T in registers; it also
 //     writes delta. D = 128: a small kernel writes only the per-row inputs of
-//     stage 3 (fp16 dO, LSE, delta) and dQ is zeroed.
+//     the tensor-core kernels (16-bit dO, LSE, delta).
 //  2. transposed index: for every (b, g, block) the list of queries whose row
-//     selects it (count with atomics, one-CTA scan, fill with atomics). The
-//     order inside a list follows atomic order.
+//     selects it (count: warp row walks with combined atomics; one-CTA scan;
+//     fill with atomics in index order, so lists keep rough query order).
+//     With D = 128 the entries of each query's own block c and of block
+//     c - 1 stay out of the lists (recorded per row for stage 3a), and the
+//     stage runs on a second stream of the call beside stage 1 and 3a.
+//  3a. D = 128: local-block kernel, one CTA per (b, block row, g): the two
+//     blocks a block row shares, loaded once; each dQ row summed over both
+//     on the tensor cores (tcgen05) and stored once, so dQ needs no zeroing;
+//     dK / dV of both blocks summed over the block row.
 //  3. key-major kernel: one CTA per chunk of <= kQueriesPerChunk queries of a
 //     list; the block's K / V are loaded once and each query's S, P, dP, dS
 //     recomputed against them. D = 64: bs/16 warps each own 16 keys and use
 //     mma.sync m16n8k8 (the C layout of S^T is already the A layout of that
-//     MMA) for dV += P^T dO and dK += dS^T Q. D = 128: tcgen05 MMAs with
-//     tensor-memory accumulators on 128-row batches of (query, head) rows,
-//     which also give dQ = dS K per batch; dQ is added into global memory
-//     with fp32 reductions. dK / dV partial sums are added with fp32 atomics
-//     at the end of a chunk. Summation orders follow the atomics.
+//     MMA) for dV += P^T dO and dK += dS^T Q, added with fp32 atomics at the
+//     end of a chunk. D = 128: tcgen05 MMAs with tensor-memory accumulators
+//     on 128-row batches of (query, head) rows, which also give dQ = dS K per
+//     batch, added into global memory with fp32 reductions; dK / dV are
+//     staged in shared memory at the end of a chunk (and of a block row in
+//     3a) and added by 512-byte bulk reductions. Summation orders follow the
+//     atomics and reductions.
 // Masked keys get exact zero weights by select (never multiplied through).
 // In stage 1 (D = 64), K / V rows past a query's last visible key are zeroed
 // in shared memory before they enter a product; with D = 128 the whole
-// block's K rows enter dQ = dS K with dS = 0 for masked keys, so those rows
+// block's K rows enter dQ = dS K with dS = 0 for masked keys (and, in 3a,
+// for queries of the block row that do not take the block), so those rows
 // must hold finite values.
 
 #include <cuda.h>
@@ -2282,7 +2292,7 @@ static int bwd_check_pointers(const void* Q, const void* K, const void* V, const
 }
 
 // Validated arguments -> the kernels' problem description, then the launch
-// of the three stages with `ws` as scratch.
+// of the stages with `ws` as scratch.
 static int run_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                    const float* O, const float* LSE, const float* dO, float* dQ, float* dK,
                    float* dV, int64_t B, int64_t M, int64_t N, int64_t H, int64_t G, int64_t D,
