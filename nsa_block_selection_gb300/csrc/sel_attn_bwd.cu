@@ -59,7 +59,12 @@
 
 namespace nsa {
 
-constexpr int kQueriesPerChunk = 256;
+// Queries per chunk of a list (the key-major kernels' unit of work): larger
+// chunks mean fewer block loads and dK / dV epilogues per list (m64k_bs64
+// backward: 64 / 128 / 256 / 384 / 448 queries measured 19.4 / 15.4 / 12.37
+// / 11.93 / 11.79 ms). 448 keeps the tensor-core kernel's shared memory
+// (query ids included) within 227 KB.
+constexpr int kQueriesPerChunk = 448;
 
 // D = A(16x8, row) * B(8x8, col) + D, bf16 inputs, fp32 accumulate: the
 // bf16 twin of mma_1688, used only by the key-major dK / dV products.
@@ -1011,6 +1016,7 @@ struct DkvTcCfg {
   static constexpr int kSmemBytes = kOffList + kQueriesPerChunk * 4 + 1024;
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 320, kColDq = 384;
 };
+static_assert(DkvTcCfg::kSmemBytes <= 232448, "one CTA per SM within 227 KB");
 
 constexpr int kDkvTcThreads = 320;
 
