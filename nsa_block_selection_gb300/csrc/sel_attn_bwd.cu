@@ -1455,8 +1455,8 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
 // are summed in tensor memory and stored once (rows that take neither block
 // get zeros), so dQ needs no zeroing and the key-major kernel's fp32
 // reductions shrink by two of each row's blocks. The blocks' dK and dV
-// accumulate in tensor memory over the block row and are added with fp32
-// atomics at the end.
+// accumulate in tensor memory over the block row; at the end they are
+// staged in shared memory and added by 512-byte bulk fp32 reductions.
 //
 // Steps: (batch of 16 items, active slot), batch by batch. Per step the
 // MMA warp issues S = Q K^T and dP = dO V^T into 128 tensor-memory
@@ -1476,7 +1476,7 @@ enum LocBar : int {
   kLPdsFree = 9,   // the MMAs that read P / dS are done
   kLDqFull = 10,   // dQ_R of a batch is complete
   kLDqFree = 11,   // the dQ warps have read it
-  kLAccDone = 12,
+  kLAccDone = 12,  // every MMA of the CTA is done
   kLStaged = 13,   // dV / dK of the block row staged in shared memory
   kLocBars = 14
 };
