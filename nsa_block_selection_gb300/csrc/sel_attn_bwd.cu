@@ -1137,11 +1137,10 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
         }
       }
     };
-    prefetch(0);
-    prefetch(1);
+    // batch i's copies first, then the L2 prefetches of the batches two
+    // ahead, so the chunk's first copies do not queue behind prefetches
     for (int i = 0; i < nbat && !failed; ++i) {
       const int s = i & 1;
-      prefetch(i + 2);
       if (i >= 2 &&
           !__all_sync(kFull, wait_phase(bar(kQdEmpty + s), ((i - 2) >> 1) & 1, kWaitLimitNs))) {
         failed = true;
@@ -1167,6 +1166,8 @@ __global__ void __launch_bounds__(kDkvTcThreads, 1)
           }
         }
       }
+      if (i == 0) prefetch(1);
+      prefetch(i + 2);
     }
   } else if (warp == 1) {
     if (lane == 0) {
